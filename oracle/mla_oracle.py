@@ -1,0 +1,320 @@
+"""fp64 CPU oracle for the Multi-head Latent Attention (MLA) forward.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import or run this module.  The product
+path (the CUDA library and its Python binding) never calls it; it shares no
+code, table or helper with that path.
+
+What it computes is the plain definition, written out step by step, in fp64
+(numpy), on the bf16 values the caller holds (inputs are decoded exactly):
+
+  for each query row r and its key set J(r):
+      s_j   = scale * <q_r, k_j>                      (all dk columns)
+      m     = max_j s_j ;  l = sum_j exp(s_j - m)
+      O_r   = sum_j exp(s_j - m) * v_j / l            (v_j = value row of key j)
+      lse_r = m + ln l                                (natural log)
+  an empty J(r) gives O_r = 0 and lse_r = -inf.
+  With a previous pair (O_p, lse_p):
+      m' = max(lse_p, lse_r); m' = -inf -> (0, -inf)
+      O  = (e^(lse_p-m') O_p + e^(lse_r-m') O_r) / (e^(lse_p-m') + e^(lse_r-m'))
+      lse = m' + ln(e^(lse_p-m') + e^(lse_r-m'))
+
+Passages followed (pages by title, with their sections):
+  * Tenstorrent "ttnn.transformer.ring_mla": one shared KV head; QK^T over the
+    full KV width; the first head_dim_v columns of KV are V; causal; outputs
+    the attention output and streaming statistics.
+  * Huawei Ascend "RingMLAOperation", parameter table: split q/k (128 no-PE +
+    64 RoPE), value 128, seqLen [batch] or [2, batch], kvHeadNum (0 = headNum),
+    qkScale, maskType NO_MASK/TRIU, prevOut/prevLse in, softmaxLse [headNum,
+    qNTokens] float out, calcType (first ring step passes no prev).
+  * NVIDIA TensorRT-LLM "mla.py": forward_context_with_chunked_prefill (cached
+    chunks with a FULL mask, current chunk CAUSAL, each partial merged into the
+    running output and softmax statistics by merge_attention_for_mla);
+    _attn_forward_gen (a fully masked row must not poison a combine with NaN).
+  * Modular Mojo "mha_single_batch_pipelined": token generation, seqlen = 1,
+    split-K over keys needs a separate reduction.
+  * AWS NKI "MLA Sparse Attention CTE Kernel API Reference": per query,
+    absorbed latent + RoPE attention over the top-k selected cache rows.
+
+Readings where the pages are silent (each also listed in the design doc):
+  * lse is the natural log of sum exp(scale * q.k) (Ascend: "exp, sum, and log
+    ... in sequence"); prev_lse is fp32 (the page's "float16" for prevLse
+    contradicts its float softmaxLse output).
+  * Split layout causal alignment is bottom-right: query i of a sequence with
+    q_len queries and kv_len keys sits at position kv_len - q_len + i.
+  * Sparse: indices outside [0, S_kv) are padding and skipped; a repeated
+    index counts once per occurrence; no causal mask beyond the list itself.
+  * Decode: the single query sees all len keys of its request.
+
+Pins: every function here is checked in tests/test_oracle_pins.py against
+closed forms, a pure-Python brute force, library routines and identities of
+the mathematics (see that file).  No function is "parity unpinned".
+"""
+from __future__ import annotations
+
+from typing import Optional, Sequence
+
+import numpy as np
+
+NEG_INF = -np.inf
+
+
+def _f64(x) -> np.ndarray:
+    """Decode a tensor/array (bf16, fp32, ...) exactly into float64."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            return x.detach().to("cpu").to(torch.float64).numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.asarray(x, dtype=np.float64)
+
+
+def _i64(x) -> np.ndarray:
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            return x.detach().to("cpu").to(torch.int64).numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.asarray(x, dtype=np.int64)
+
+
+# ---------------------------------------------------------------------------
+# the core definition
+# ---------------------------------------------------------------------------
+def attend(q_rows: np.ndarray, keys: np.ndarray, values: np.ndarray, scale: float):
+    """Softmax attention of R query rows over one key set J.
+
+    q_rows [R, dk], keys [|J|, dk], values [|J|, dv] (fp64).
+    Returns (O [R, dv], lse [R]).  |J| = 0 gives O = 0, lse = -inf.
+    """
+    R = q_rows.shape[0]
+    dv = values.shape[1]
+    if keys.shape[0] == 0:
+        return np.zeros((R, dv)), np.full((R,), NEG_INF)
+    s = scale * (q_rows @ keys.T)                  # [R, |J|]
+    m = s.max(axis=1, keepdims=True)               # row max
+    p = np.exp(s - m)                              # unnormalised weights
+    l = p.sum(axis=1, keepdims=True)               # row sum
+    out = (p @ values) / l
+    lse = (m + np.log(l))[:, 0]
+    return out, lse
+
+
+def attend_rowwise(q_rows: np.ndarray, keys_per_row: Sequence[np.ndarray],
+                   values_per_row: Sequence[np.ndarray], scale: float):
+    """attend() where each row has its own key set."""
+    R = q_rows.shape[0]
+    dv = values_per_row[0].shape[1] if len(values_per_row) else 0
+    out = np.zeros((R, dv))
+    lse = np.full((R,), NEG_INF)
+    for r in range(R):
+        o, l_ = attend(q_rows[r:r + 1], keys_per_row[r], values_per_row[r], scale)
+        out[r], lse[r] = o[0], l_[0]
+    return out, lse
+
+
+def merge(out_a: np.ndarray, lse_a: np.ndarray, out_b: np.ndarray, lse_b: np.ndarray):
+    """Merge two partial results of the same rows by their log-sum-exp.
+
+    out_* [..., dv], lse_* [...] (matching leading shape).  A side with
+    lse = -inf contributes nothing; both -inf gives (0, -inf), never NaN.
+    This is the combine of merge_attention_for_mla / Ascend prevOut+prevLse.
+    """
+    out_a = np.asarray(out_a, dtype=np.float64)
+    out_b = np.asarray(out_b, dtype=np.float64)
+    lse_a = np.asarray(lse_a, dtype=np.float64)
+    lse_b = np.asarray(lse_b, dtype=np.float64)
+    m = np.maximum(lse_a, lse_b)
+    empty = np.isneginf(m)
+    m_safe = np.where(empty, 0.0, m)
+    w_a = np.where(np.isneginf(lse_a), 0.0, np.exp(lse_a - m_safe))
+    w_b = np.where(np.isneginf(lse_b), 0.0, np.exp(lse_b - m_safe))
+    w = w_a + w_b
+    w_div = np.where(empty, 1.0, w)
+    out = (w_a[..., None] * out_a + w_b[..., None] * out_b) / w_div[..., None]
+    out = np.where(empty[..., None], 0.0, out)
+    lse = np.where(empty, NEG_INF, m_safe + np.log(np.where(empty, 1.0, w)))
+    return out, lse
+
+
+# ---------------------------------------------------------------------------
+# absorbed dense prefill: many heads over one shared KV head
+# ---------------------------------------------------------------------------
+def prefill_key_set(t: int, Tkv: int, causal: bool, q_pos0: int, kv_pos0: int, kv_valid: int) -> np.ndarray:
+    """Keys visible to query token t: j < kv_valid and (causal: kv_pos0 + j <= q_pos0 + t)."""
+    n = min(Tkv, kv_valid)
+    if causal:
+        n = min(n, q_pos0 + t - kv_pos0 + 1)
+    return np.arange(max(0, n))
+
+
+def mla_prefill(q, kv, scale: float, dv: int = 512, causal: bool = True,
+                q_pos0: int = 0, kv_pos0: int = 0, kv_valid: Optional[int] = None,
+                prev_out=None, prev_lse=None, tokens: Optional[Sequence[int]] = None):
+    """Absorbed causal MLA prefill over one shared KV head (ring_mla semantics).
+
+    q [T, H, dk], kv [Tkv, dk]; V = kv[:, :dv].  Query token t sits at global
+    position q_pos0 + t, key j at kv_pos0 + j; only keys j < kv_valid exist.
+    Returns out [n, H, dv] and lse [H, n] for the requested tokens (all by
+    default).  With prev_out [T, H, dv] / prev_lse [H, T] the result is merged
+    with the previous pair (ring step / chunked prefill).
+    """
+    q = _f64(q)
+    kv = _f64(kv)
+    T, H, dk = q.shape
+    Tkv = kv.shape[0]
+    if kv_valid is None:
+        kv_valid = Tkv
+    toks = list(range(T)) if tokens is None else [int(t) for t in tokens]
+    out = np.zeros((len(toks), H, dv))
+    lse = np.full((H, len(toks)), NEG_INF)
+    for i, t in enumerate(toks):
+        J = prefill_key_set(t, Tkv, causal, q_pos0, kv_pos0, kv_valid)
+        o, l_ = attend(q[t], kv[J], kv[J, :dv], scale)
+        out[i], lse[:, i] = o, l_
+    if prev_out is not None:
+        po = _f64(prev_out)[toks]
+        pl = _f64(prev_lse)[:, toks]
+        mo, ml = merge(po, pl.T, out, lse.T)
+        out, lse = mo, ml.T
+    return out, lse
+
+
+# ---------------------------------------------------------------------------
+# Ascend split layout (non-absorbed), varlen, GQA, NO_MASK / TRIU
+# ---------------------------------------------------------------------------
+def mla_prefill_split(q_nope, q_pe, k_nope, k_pe, v, seq_len, head_num: int, kv_head_num: int,
+                      scale: float, mask_type: int, prev_out=None, prev_lse=None,
+                      tokens: Optional[Sequence[int]] = None):
+    """Ascend RingMLAOperation forward on the BSND split layout.
+
+    q_nope [Nq,H,128], q_pe [Nq,H,64], k_nope/k_pe/v [Nkv,Hkv,*]; seq_len
+    [batch] (q = kv lengths) or [2, batch].  Head h reads KV head
+    h // (H / Hkv); kv_head_num 0 means head_num.  mask_type 0 = NO_MASK,
+    1 = TRIU (query i of a sequence sees keys j <= kv_len - q_len + i).
+    Returns out [n, H, 128], lse [H, n] for the requested global query tokens.
+    """
+    qn, qp = _f64(q_nope), _f64(q_pe)
+    kn, kp, vv = _f64(k_nope), _f64(k_pe), _f64(v)
+    sl = _i64(seq_len)
+    if sl.ndim == 1:
+        q_lens, kv_lens = sl, sl
+    else:
+        q_lens, kv_lens = sl[0], sl[1]
+    H = int(head_num)
+    Hkv = int(kv_head_num) if kv_head_num else H
+    group = H // Hkv
+    Nq = qn.shape[0]
+    dv = vv.shape[2]
+    q_off = np.concatenate([[0], np.cumsum(q_lens)])
+    kv_off = np.concatenate([[0], np.cumsum(kv_lens)])
+    toks = list(range(Nq)) if tokens is None else [int(t) for t in tokens]
+    out = np.zeros((len(toks), H, dv))
+    lse = np.full((H, len(toks)), NEG_INF)
+    for i, t in enumerate(toks):
+        b = int(np.searchsorted(q_off, t, side="right") - 1)
+        qi = t - q_off[b]
+        ql, kl = int(q_lens[b]), int(kv_lens[b])
+        n = kl if mask_type == 0 else max(0, min(kl, kl - ql + qi + 1))
+        ks = slice(kv_off[b], kv_off[b] + n)
+        for h in range(H):
+            g = h // group
+            qrow = np.concatenate([qn[t, h], qp[t, h]])[None, :]
+            keys = np.concatenate([kn[ks, g], kp[ks, g]], axis=1)
+            o, l_ = attend(qrow, keys, vv[ks, g], scale)
+            out[i, h], lse[h, i] = o[0], l_[0]
+    if prev_out is not None:
+        po = _f64(prev_out)[toks]
+        pl = _f64(prev_lse)[:, toks]
+        mo, ml = merge(po, pl.T, out, lse.T)
+        out, lse = mo, ml.T
+    return out, lse
+
+
+# ---------------------------------------------------------------------------
+# decode: one query token per request over a paged latent cache
+# ---------------------------------------------------------------------------
+def gather_pages(cache, block_table_row, n: int, page_size: int) -> np.ndarray:
+    """Rows 0..n-1 of one request: row j lives at cache[block_table[j // P], j % P]."""
+    cache = _f64(cache) if not isinstance(cache, np.ndarray) else cache
+    bt = _i64(block_table_row)
+    j = np.arange(n)
+    return cache[bt[j // page_size], j % page_size]
+
+
+def mla_decode(q, cache, block_table, lens, scale: float, dv: int = 512,
+               requests: Optional[Sequence[int]] = None):
+    """Absorbed MLA decode (seqlen = 1): each request's query sees all its len keys.
+
+    q [B, H, dk], cache [pages, page_size, dk], block_table [B, max_pages],
+    lens [B].  Returns out [n, H, dv] and lse [n, H].
+    """
+    qq = _f64(q)
+    cc = _f64(cache)
+    bt = _i64(block_table)
+    ln = _i64(lens)
+    B, H, dk = qq.shape
+    P = cc.shape[1]
+    reqs = list(range(B)) if requests is None else [int(b) for b in requests]
+    out = np.zeros((len(reqs), H, dv))
+    lse = np.full((len(reqs), H), NEG_INF)
+    for i, b in enumerate(reqs):
+        rows = gather_pages(cc, bt[b], int(ln[b]), P)
+        o, l_ = attend(qq[b], rows, rows[:, :dv], scale)
+        out[i], lse[i] = o, l_
+    return out, lse
+
+
+# ---------------------------------------------------------------------------
+# top-k sparse latent + RoPE attention
+# ---------------------------------------------------------------------------
+def mla_sparse(q_lift, q_pe, c_kv, k_pe, topk, scale: float,
+               tokens: Optional[Sequence[int]] = None):
+    """NKI sparse MLA: query (b, s) attends the cache rows listed in topk[b, s].
+
+    q_lift [B,S,H,L], q_pe [B,S,H,R], c_kv [B,S_kv,L], k_pe [B,S_kv,R],
+    topk [B,S,K] int.  Indices outside [0, S_kv) are skipped; each listed
+    occurrence counts.  Output in natural order: out [B, n, H*L], lse [B, n, H].
+    """
+    ql, qp = _f64(q_lift), _f64(q_pe)
+    ck, kp = _f64(c_kv), _f64(k_pe)
+    tk = _i64(topk)
+    B, S, H, L = ql.shape
+    S_kv = ck.shape[1]
+    toks = list(range(S)) if tokens is None else [int(t) for t in tokens]
+    out = np.zeros((B, len(toks), H * L))
+    lse = np.full((B, len(toks), H), NEG_INF)
+    for b in range(B):
+        for i, s in enumerate(toks):
+            idx = tk[b, s]
+            idx = idx[(idx >= 0) & (idx < S_kv)]
+            keys = np.concatenate([ck[b, idx], kp[b, idx]], axis=1)
+            qrows = np.concatenate([ql[b, s], qp[b, s]], axis=1)     # [H, L+R]
+            o, l_ = attend(qrows, keys, ck[b, idx], scale)
+            out[b, i] = o.reshape(-1)
+            lse[b, i] = l_
+    return out, lse
+
+
+def attention_flops(pairs: int, H: int, dk: int, dv: int) -> float:
+    """Algorithmic FLOPs of attention over `pairs` unmasked (query token, key) pairs."""
+    return 2.0 * float(pairs) * H * (dk + dv)
+
+
+def causal_pairs(T: int, Tkv: int, q_pos0: int, kv_pos0: int, kv_valid: Optional[int] = None) -> int:
+    """Number of unmasked (token, key) pairs of a causal dense prefill call."""
+    if kv_valid is None:
+        kv_valid = Tkv
+    tot = 0
+    n_cap = min(Tkv, kv_valid)
+    for t in range(T):
+        tot += max(0, min(n_cap, q_pos0 + t - kv_pos0 + 1))
+    return tot
+
+
+__all__ = [
+    "attend", "attend_rowwise", "merge", "prefill_key_set", "mla_prefill", "mla_prefill_split",
+    "gather_pages", "mla_decode", "mla_sparse", "attention_flops", "causal_pairs", "NEG_INF",
+]
