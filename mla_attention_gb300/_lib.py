@@ -1,0 +1,244 @@
+"""ctypes binding of libmla.so: argument marshalling only.
+
+Every function here turns torch tensors into pointers and sizes, calls the C
+entry point of the same name, and raises MLAError on a non-OK status.  No
+attention arithmetic happens in Python; there is no fallback path: if the
+library is missing, loading fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmla.so")
+
+MLA_OK = 0
+STATUS_NAMES = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "MLA_ERR_CUDA",
+                4: "MLA_ERR_TIMEOUT", 5: "MLA_ERR_DEVICE_RANGE", 6: "MLA_ERR_WORKSPACE"}
+
+
+class MLAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+_lock = threading.Lock()
+
+c_void_p, c_int, c_int64, c_float, c_size_t, c_uint32 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                                          ctypes.c_float, ctypes.c_size_t, ctypes.c_uint32)
+
+_SIGNATURES = {
+    "mla_version": ([], c_int),
+    "mla_last_error_string": ([], ctypes.c_char_p),
+    "mla_status_string": ([c_int], ctypes.c_char_p),
+    "mla_check_device_status": ([c_void_p, c_void_p, ctypes.POINTER(c_uint32)], c_int),
+    "mla_set_spin_limit": ([c_uint32], None),
+    "mla_prefill_workspace_size": ([c_int, c_int], c_size_t),
+    "mla_prefill": ([c_void_p, c_int64, c_int64, c_void_p, c_int64, c_int, c_int, c_int, c_int, c_int, c_float, c_int,
+                     c_int64, c_int64, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p],
+                    c_int),
+    "mla_prefill_split_workspace_size": ([c_int, c_int], c_size_t),
+    "mla_prefill_split": ([c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
+                           c_float, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p],
+                          c_int),
+    "mla_decode_workspace_size": ([c_int, c_int, c_int], c_size_t),
+    "mla_decode": ([c_void_p, c_void_p, c_int64, c_int, c_void_p, c_int, c_void_p, c_int, c_int, c_float, c_int,
+                    c_void_p, c_void_p, c_void_p, c_size_t, c_void_p], c_int),
+    "mla_sparse_workspace_size": ([c_int, c_int], c_size_t),
+    "mla_sparse": ([c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_float,
+                    c_void_p, c_void_p, c_void_p, c_size_t, c_void_p], c_int),
+    "mla_merge_lse": ([c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int, c_int, c_void_p],
+                      c_int),
+}
+
+
+def lib():
+    """Load libmla.so once (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libmla.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+            handle = ctypes.CDLL(LIB_PATH)
+            for name, (args, res) in _SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = handle
+    return _lib
+
+
+def exported_symbols():
+    return sorted(_SIGNATURES)
+
+
+def _check(status: int):
+    if status != MLA_OK:
+        msg = lib().mla_last_error_string().decode(errors="replace")
+        raise MLAError(status, msg)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need(t: torch.Tensor, name: str, dtype, device=None):
+    if t.dtype != dtype:
+        raise MLAError(1, f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise MLAError(1, f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise MLAError(1, f"{name} is on {t.device}, expected {device}")
+
+
+# ---------------------------------------------------------------------------
+# workspace: caller-owned scratch, cached per device; first bytes = status word
+# ---------------------------------------------------------------------------
+_ws_cache = {}
+
+
+def workspace(nbytes: int, device: torch.device) -> torch.Tensor:
+    key = (device.type, device.index)
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws
+
+
+def check_device_status(ws: Optional[torch.Tensor] = None, device=None, stream=None) -> int:
+    """Read and clear the device status word; raise MLAError if a kernel reported a fault."""
+    if ws is None:
+        device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        ws = workspace(256, device)
+    detail = c_uint32(0)
+    s = lib().mla_check_device_status(_ptr(ws), _stream(stream), ctypes.byref(detail))
+    _check(s)
+    return detail.value
+
+
+def set_spin_limit(limit: int):
+    lib().mla_set_spin_limit(int(limit))
+
+
+# ---------------------------------------------------------------------------
+# the calls
+# ---------------------------------------------------------------------------
+def mla_prefill(q: torch.Tensor, kv: torch.Tensor, scale: float, causal: bool = True, q_pos0: int = 0,
+                kv_pos0: int = 0, kv_valid: int = -1, prev_out: Optional[torch.Tensor] = None,
+                prev_lse: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                lse: Optional[torch.Tensor] = None, dv: int = 512, ws: Optional[torch.Tensor] = None, stream=None):
+    """Absorbed causal MLA prefill: q [T,H,576], kv [Tkv,576] -> out [T,H,dv], lse [H,T]."""
+    _need(q, "q", torch.bfloat16)
+    _need(kv, "kv", torch.bfloat16, q.device)
+    T, H, dk = q.shape
+    Tkv = kv.shape[0]
+    if q.stride(2) != 1 or kv.stride(1) != 1:
+        raise MLAError(1, "q and kv need contiguous last dimensions")
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    nbytes = lib().mla_prefill_workspace_size(T, H)
+    ws = workspace(nbytes, q.device) if ws is None else ws
+    s = lib().mla_prefill(_ptr(q), q.stride(0), q.stride(1), _ptr(kv), kv.stride(0), T, H, Tkv, dk, dv, float(scale),
+                          int(bool(causal)), int(q_pos0), int(kv_pos0), int(kv_valid), _ptr(prev_out),
+                          _ptr(prev_lse), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+    _check(s)
+    return out, lse
+
+
+def mla_prefill_split(q_nope, q_pe, k_nope, k_pe, v, seq_len: torch.Tensor, head_num: int, kv_head_num: int,
+                      qk_scale: float, mask_type: int = 1, prev_out=None, prev_lse=None, out=None, lse=None,
+                      ws=None, stream=None):
+    """Ascend split-layout prefill: returns out [Nq,H,128], lse [H,Nq]. seq_len is a HOST int32 tensor."""
+    for name, t in (("q_nope", q_nope), ("q_pe", q_pe), ("k_nope", k_nope), ("k_pe", k_pe), ("v", v)):
+        _need(t, name, torch.bfloat16, q_nope.device)
+        if not t.is_contiguous():
+            raise MLAError(1, f"{name} must be contiguous")
+    sl = seq_len.to("cpu", torch.int32).contiguous()
+    rows = 1 if sl.dim() == 1 else 2
+    batch = sl.shape[-1]
+    Nq, H = q_nope.shape[0], q_nope.shape[1]
+    if out is None:
+        out = torch.empty((Nq, H, 128), dtype=torch.bfloat16, device=q_nope.device)
+    if lse is None:
+        lse = torch.empty((H, Nq), dtype=torch.float32, device=q_nope.device)
+    nbytes = lib().mla_prefill_split_workspace_size(Nq, H)
+    ws = workspace(nbytes, q_nope.device) if ws is None else ws
+    s = lib().mla_prefill_split(_ptr(q_nope), _ptr(q_pe), _ptr(k_nope), _ptr(k_pe), _ptr(v),
+                                ctypes.c_void_p(sl.data_ptr()), rows, batch, int(head_num), int(kv_head_num),
+                                float(qk_scale), int(mask_type), _ptr(prev_out), _ptr(prev_lse), _ptr(out), _ptr(lse),
+                                _ptr(ws), ws.numel(), _stream(stream))
+    _check(s)
+    return out, lse
+
+
+def mla_decode(q, kv_cache, block_table, lens, scale: float, num_splits: int = 0, out=None, lse=None, ws=None,
+               stream=None):
+    """Paged absorbed decode: q [B,H,576], kv_cache [pages,page,576] -> out [B,H,512], lse [B,H]."""
+    _need(q, "q", torch.bfloat16)
+    _need(kv_cache, "kv_cache", torch.bfloat16, q.device)
+    _need(block_table, "block_table", torch.int32, q.device)
+    _need(lens, "lens", torch.int32, q.device)
+    B, H, _ = q.shape
+    num_pages, page_size, _ = kv_cache.shape
+    if out is None:
+        out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    nbytes = lib().mla_decode_workspace_size(B, H, int(num_splits))
+    ws = workspace(nbytes, q.device) if ws is None else ws
+    s = lib().mla_decode(_ptr(q), _ptr(kv_cache), num_pages, page_size, _ptr(block_table), block_table.shape[1],
+                         _ptr(lens), B, H, float(scale), int(num_splits), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
+                         _stream(stream))
+    _check(s)
+    return out, lse
+
+
+def mla_sparse(q_lift, q_pe, c_kv, k_pe, topk, softmax_scale: float, out=None, lse=None, ws=None, stream=None):
+    """Top-k sparse MLA: returns out [B,S,H*512] (natural order), lse [B,S,H]."""
+    for name, t in (("q_lift", q_lift), ("q_pe", q_pe), ("c_kv", c_kv), ("k_pe", k_pe)):
+        _need(t, name, torch.bfloat16, q_lift.device)
+    _need(topk, "topk", torch.int32, q_lift.device)
+    B, S, H, L = q_lift.shape
+    S_kv = c_kv.shape[1]
+    K = topk.shape[-1]
+    if out is None:
+        out = torch.empty((B, S, H * L), dtype=torch.bfloat16, device=q_lift.device)
+    if lse is None:
+        lse = torch.empty((B, S, H), dtype=torch.float32, device=q_lift.device)
+    nbytes = lib().mla_sparse_workspace_size(S, H)
+    ws = workspace(nbytes, q_lift.device) if ws is None else ws
+    s = lib().mla_sparse(_ptr(q_lift), _ptr(q_pe), _ptr(c_kv), _ptr(k_pe), _ptr(topk), B, S, S_kv, H, K,
+                         float(softmax_scale), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+    _check(s)
+    return out, lse
+
+
+def mla_merge_lse(out_a, lse_a, out_b, lse_b, out=None, lse=None, stream=None):
+    """Merge two partial results by LSE: out_* [rows,H,dv] bf16, lse_* [H,rows] fp32."""
+    rows, H, dv = out_a.shape
+    if out is None:
+        out = torch.empty_like(out_a)
+    if lse is None:
+        lse = torch.empty_like(lse_a)
+    s = lib().mla_merge_lse(_ptr(out_a), _ptr(lse_a), _ptr(out_b), _ptr(lse_b), _ptr(out), _ptr(lse), rows, H, dv,
+                            _stream(stream))
+    _check(s)
+    return out, lse

@@ -1,0 +1,863 @@
+// Absorbed MLA tile engine for sm_103a: one shared KV head whose rows are
+// [512 latent | 64 RoPE]; QK^T over all 576 columns; V = the first 512
+// columns of the same rows (Tenstorrent "ttnn.transformer.ring_mla": "QK uses
+// the full KV head dimension and QKT@V uses the first head_dim_v columns").
+//
+// One tile = 128 query rows against the KV rows in tiles of 64 keys.  An
+// fp32 O tile of 128 x 512 fills the whole 512-column tensor memory of one
+// SM, so each tile is handled by a cluster of two CTAs on two SMs:
+//
+//   S-CTA (cluster rank 0)                 O-CTA (cluster rank 1)
+//   TMEM: Q [128 x 576 bf16] (288 cols)    TMEM: O [128 x 512 fp32] (512 cols)
+//         S double buffer (2 x 64 cols)
+//   warp 4: TMA K tiles (9 col boxes)      warp 4: TMA V tiles (8 col boxes)
+//   warp 5: S = Q K^T (A from TMEM)        warp 5: O += P V (P, V from smem)
+//   warps 0-3: online softmax, one row     warps 0-3: pull P from the S-CTA's
+//     per thread; P (bf16) and the           shared memory, lazy O rescale,
+//     rescale factor into shared memory      epilogue (normalise, prev merge)
+//
+// The two CTAs hand P over through distributed shared memory with cluster-
+// scope mbarrier arrivals.  The online softmax keeps a stale row maximum and
+// only rescales O when the maximum grows by more than 2^8, so O rescales are
+// rare.  Every wait is bounded; on a timeout a CTA records the wait site in
+// the device status word, stops issuing work, lets in-flight copies and MMAs
+// drain, and exits through the same cluster barrier as the normal path.
+//
+// Three sources of KV tiles share the engine:
+//   prefill - dense [Tkv, 576] rows (TMA tile boxes); causal by global position
+//   decode  - a paged latent cache; split-K: each CTA pair owns an equal share
+//             of all requests' key tiles and writes per-request partials that
+//             a reduction kernel merges (Mojo "mha_single_batch_pipelined")
+//   sparse  - the top-k rows of each query, gathered with TMA tile::gather4
+//             (AWS NKI "MLA Sparse Attention CTE Kernel API Reference")
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include "mla_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kThreads = 192;  // warps 0-3 rows, warp 4 TMA, warp 5 MMA
+constexpr int kStagesS = 2;
+constexpr int kStagesO = 3;
+constexpr int kBoxBytes = kKeys * 128;                 // 64 rows x 128 B
+constexpr int kStageBytesS = kKBoxes * kBoxBytes;      // 73728
+constexpr int kStageBytesO = kVBoxes * kBoxBytes;      // 65536
+constexpr int kPBytes = kRows * kKeys * 2;             // 16384
+
+// shared memory map (offsets from a 1024-aligned base; identical in both CTAs)
+constexpr int kOffStages = 0;
+constexpr int kOffPS = kStagesS * kStageBytesS;        // S-CTA: P buffers (147456)
+constexpr int kOffAlpha = kOffPS + 2 * kPBytes;        // S-CTA: rescale factors [2][128]
+constexpr int kOffStats = kOffAlpha + 2 * kRows * 4;   // S-CTA: (m, l) [128][2]
+constexpr int kOffPO = kStagesO * kStageBytesO;        // O-CTA: local P buffers (196608)
+constexpr int kOffBars = kOffPO + 2 * kPBytes;         // both: barriers (229376)
+constexpr int kSmemUsed = kOffBars + 512;
+constexpr int kSmemAlloc = kSmemUsed + 1024;
+static_assert(kOffStats + kRows * 8 <= kOffBars, "S-CTA layout overlaps the barriers");
+static_assert(kSmemAlloc <= 232448, "shared memory over the sm_103a limit");
+
+constexpr uint32_t kTmemQ = 0;          // S-CTA: Q columns [0, 288)
+constexpr uint32_t kTmemS = 288;        // S-CTA: S buffers [288, 416)
+constexpr float kRescaleLog2 = 8.0f;    // rescale O only when the max grows by > 2^8
+
+struct Bars {
+  // S-CTA
+  uint64_t s_kv_full[kStagesS], s_kv_empty[kStagesS];
+  uint64_t s_full[2], s_free[2];
+  uint64_t q_full;
+  uint64_t p_free[2];       // arrived remotely by the O-CTA rows
+  uint64_t stats_free;      // arrived remotely by the O-CTA rows
+  // O-CTA
+  uint64_t o_kv_full[kStagesO], o_kv_empty[kStagesO];
+  uint64_t p_full[2];       // arrived remotely by the S-CTA rows
+  uint64_t pb_free[2], p_ready[2];
+  uint64_t pv_done;
+  uint64_t stats_full;      // arrived remotely by the S-CTA rows
+  uint64_t o_free;
+  uint32_t tmem_base;
+  uint32_t abort_flag;
+};
+static_assert(sizeof(Bars) <= 512, "barrier block too large");
+
+// wait-site ids (device status word detail)
+enum : uint32_t {
+  W_S_KV_EMPTY = 1, W_S_KV_FULL, W_S_SFREE, W_S_QFULL, W_S_SFULL, W_S_PFREE, W_S_STATSFREE,
+  W_O_KV_EMPTY, W_O_KV_FULL, W_O_PREADY, W_O_PFULL, W_O_PBFREE, W_O_PVDONE, W_O_STATSFULL, W_O_OFREE,
+  R_PAGE = 0x40, R_LEN = 0x41,
+};
+
+// ---------------------------------------------------------------------------
+// the work list of one CTA pair
+// ---------------------------------------------------------------------------
+struct Item {
+  int id;          // prefill: row tile; decode: request; sparse: token
+  int J;           // KV tiles
+  int64_t k0;      // decode: first key (within the request) of this segment
+  int64_t k1;      // decode: end key of this segment
+  int slot;        // decode: partial slot
+};
+
+__device__ __forceinline__ int64_t prefill_keys_for_token(const CoreParams& p, int64_t t) {
+  int64_t n = p.kv_valid;
+  if (p.causal) {
+    int64_t c = p.q_pos0 + t - p.kv_pos0 + 1;
+    if (c < n) n = c;
+  }
+  return n < 0 ? 0 : n;
+}
+
+__device__ __forceinline__ int decode_len(const CoreParams& p, int b) {
+  int n = p.lens[b];
+  if (n < 0) n = 0;
+  const int64_t cap = (int64_t)p.max_pages * p.page_size;
+  if (n > cap) n = (int)cap;
+  return n;
+}
+
+struct ItemIter {
+  const CoreParams* p;
+  int pair;
+  int64_t k;        // prefill / sparse: running index
+  // decode state
+  int b;
+  int64_t pre;
+  int64_t lo, hi;
+
+  __device__ void init(const CoreParams& prm, int pair_id) {
+    p = &prm;
+    pair = pair_id;
+    k = pair_id;
+    b = 0;
+    pre = 0;
+    if (prm.mode == MODE_DECODE) {
+      int64_t tot = 0;
+      for (int i = 0; i < prm.B; ++i) tot += (decode_len(prm, i) + kKeys - 1) / kKeys;
+      lo = tot * pair_id / prm.num_pairs;
+      hi = tot * (pair_id + 1) / prm.num_pairs;
+    }
+  }
+
+  __device__ bool next(Item& it) {
+    const CoreParams& P = *p;
+    if (P.mode == MODE_PREFILL) {
+      const int64_t rows = (int64_t)P.T * P.H;
+      const int64_t n_items = (rows + kRows - 1) / kRows;
+      if (k >= n_items) return false;
+      const int64_t id = n_items - 1 - k;  // longest causal rows first
+      k += P.num_pairs;
+      int64_t last = id * kRows + kRows - 1;
+      if (last >= rows) last = rows - 1;
+      const int64_t n = prefill_keys_for_token(P, last / P.H);
+      it.id = (int)id;
+      it.J = (int)((n + kKeys - 1) / kKeys);
+      return true;
+    }
+    if (P.mode == MODE_SPARSE) {
+      if (k >= P.T) return false;
+      it.id = (int)k;
+      it.J = (P.K + kKeys - 1) / kKeys;
+      k += P.num_pairs;
+      return true;
+    }
+    // decode: segments of requests overlapping [lo, hi)
+    while (b < P.B) {
+      const int len = decode_len(P, b);
+      const int64_t nt = (len + kKeys - 1) / kKeys;
+      const int64_t s = pre, e = pre + nt;
+      const int cur = b;
+      pre = e;
+      ++b;
+      if (nt == 0 || e <= lo) continue;  // no key, or wholly before this pair's share
+      if (s >= hi) {
+        b = P.B;
+        return false;
+      }
+      const int64_t t0 = (s > lo ? s : lo) - s, t1 = (e < hi ? e : hi) - s;
+      it.id = cur;
+      it.J = (int)(t1 - t0);
+      it.k0 = t0 * kKeys;
+      it.k1 = t1 * kKeys < len ? t1 * kKeys : len;
+      it.slot = cur + pair;
+      return true;
+    }
+    return false;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// KV tile loaders (producer warp).  `dst` is a stage base; boxes [b0, b1).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void gather4(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y0, int32_t y1,
+                                        int32_t y2, int32_t y3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// rows[i] for i in 0..63 held by lanes: lane l holds rows 2l and 2l+1
+__device__ __forceinline__ void issue_gather_tile(uint32_t dst, const CUtensorMap* map_lat, const CUtensorMap* map_pe,
+                                                  int nboxes, int32_t r_even, int32_t r_odd, uint64_t* bar) {
+  const int lane = threadIdx.x & 31;
+  // lane g (0..15) issues rows 4g..4g+3 = lanes 2g, 2g+1 (even/odd each)
+  const int32_t a0 = __shfl_sync(0xffffffffu, r_even, (2 * lane) & 31);
+  const int32_t a1 = __shfl_sync(0xffffffffu, r_odd, (2 * lane) & 31);
+  const int32_t a2 = __shfl_sync(0xffffffffu, r_even, (2 * lane + 1) & 31);
+  const int32_t a3 = __shfl_sync(0xffffffffu, r_odd, (2 * lane + 1) & 31);
+  if (lane < 16) {
+    for (int bx = 0; bx < nboxes; ++bx) {
+      const CUtensorMap* m = (bx < kVBoxes) ? map_lat : map_pe;
+      const int32_t x = (bx < kVBoxes) ? bx * kBoxCols : 0;
+      gather4(dst + bx * kBoxBytes + lane * 512, m, x, a0, a1, a2, a3, bar);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    mla_core_kernel(const __grid_constant__ CoreParams p, const __grid_constant__ CUtensorMap map_kv,
+                    const __grid_constant__ CUtensorMap map_row, const __grid_constant__ CUtensorMap map_pe) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars& bars = *reinterpret_cast<Bars*>(smem + kOffBars);
+  const uint32_t rank = cluster_ctarank();
+  const bool is_s = (rank == 0);
+  const int pair = blockIdx.x >> 1;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const uint32_t lim = p.spin_limit;
+  uint32_t* err = p.err;
+  const uint32_t peer = rank ^ 1u;
+
+  // ---- setup ----
+  if (tid == 0) {
+    if (is_s) {
+      for (int i = 0; i < kStagesS; ++i) {
+        mbar_init(&bars.s_kv_full[i], 1);
+        mbar_init(&bars.s_kv_empty[i], 1);
+      }
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&bars.s_full[i], 1);
+        mbar_init(&bars.s_free[i], kRows);
+        mbar_init(&bars.p_free[i], kRows);
+      }
+      mbar_init(&bars.q_full, kRows);
+      mbar_init(&bars.stats_free, kRows);
+    } else {
+      for (int i = 0; i < kStagesO; ++i) {
+        mbar_init(&bars.o_kv_full[i], 1);
+        mbar_init(&bars.o_kv_empty[i], 1);
+      }
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&bars.p_full[i], kRows);
+        mbar_init(&bars.pb_free[i], 1);
+        mbar_init(&bars.p_ready[i], kRows);
+      }
+      mbar_init(&bars.pv_done, 1);
+      mbar_init(&bars.stats_full, kRows);
+      mbar_init(&bars.o_free, kRows);
+    }
+    bars.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&bars.tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&map_kv);
+    tma_prefetch_desc(&map_row);
+    tma_prefetch_desc(&map_pe);
+  }
+  // decode: publish the per-request tile prefix for the reduction kernel
+  if (p.mode == MODE_DECODE && blockIdx.x == 0 && warp == 0) {
+    int64_t run = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+      const int b = b0 + lane;
+      int n = 0;
+      if (b < p.B) {
+        const int raw = p.lens[b];
+        const int64_t cap = (int64_t)p.max_pages * p.page_size;
+        if (raw < 0 || raw > cap) record_error(err, DEV_RANGE_BASE | R_LEN);
+        n = (decode_len(p, b) + kKeys - 1) / kKeys;
+      }
+      int incl = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (b < p.B) p.tile_prefix[b] = (int32_t)(run + incl - n);
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) p.tile_prefix[p.B] = (int32_t)run;
+  }
+  tc_fence_before();
+  cluster_sync();  // barriers of both CTAs initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tbase = bars.tmem_base;
+  volatile uint32_t* abort_flag = &bars.abort_flag;
+  // Every wait is made by a whole warp and its outcome is warp-uniform, so no
+  // warp reaches a warp-collective tcgen05 instruction with some lanes gone.
+  auto waitb = [&](uint64_t* bar, uint32_t parity, uint32_t site, bool cl) -> bool {
+    bool ok = (*abort_flag == 0) && mbar_wait(bar, parity, err, site, lim, cl);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) *abort_flag = 1;
+    return ok;
+  };
+
+  ItemIter iter;
+  iter.init(p, pair);
+  Item it;
+
+  if (is_s) {
+    // =====================================================================
+    // S-CTA
+    // =====================================================================
+    if (warp == 4) {
+      // ---------------- TMA producer: K tiles (all 576 columns) ----------------
+      uint32_t g = 0;
+      bool live = true;
+      while (live && iter.next(it)) {
+        for (int j = 0; j < it.J && live; ++j, ++g) {
+          const int s = g % kStagesS;
+          if (!waitb(&bars.s_kv_empty[s], ((g / kStagesS) & 1) ^ 1, W_S_KV_EMPTY, false)) { live = false; break; }
+          const uint32_t dst = smem_u32(smem + kOffStages + s * kStageBytesS);
+          if (p.mode == MODE_PREFILL) {
+            if (lane == 0) {
+              mbar_arrive_expect_tx(&bars.s_kv_full[s], kStageBytesS);
+              for (int bx = 0; bx < kKBoxes; ++bx)
+                tma_load_2d(dst + bx * kBoxBytes, &map_kv, bx * kBoxCols, j * kKeys, &bars.s_kv_full[s]);
+            }
+          } else {
+            int32_t re, ro;
+            bool tiled = false;
+            int32_t ytile = 0;
+            if (p.mode == MODE_DECODE) {
+              const int64_t kb = it.k0 + (int64_t)j * kKeys;  // first key of the tile
+              const int len = decode_len(p, it.id);
+              const int32_t* bt = p.block_table + (int64_t)it.id * p.max_pages;
+              auto row_of = [&](int64_t key) -> int32_t {
+                if (key >= len) return -1;
+                const int32_t pg = bt[key / p.page_size];
+                if (pg < 0 || pg >= p.num_pages) {
+                  record_error(err, DEV_RANGE_BASE | R_PAGE);
+                  return -1;
+                }
+                return (int32_t)(pg * (int64_t)p.page_size + key % p.page_size);
+              };
+              if (p.page_size % kKeys == 0 && kb + kKeys <= len) {
+                const int32_t pg = bt[kb / p.page_size];
+                if (pg >= 0 && pg < p.num_pages) {
+                  tiled = true;
+                  ytile = (int32_t)(pg * (int64_t)p.page_size + kb % p.page_size);
+                }
+              }
+              re = row_of(kb + 2 * lane);
+              ro = row_of(kb + 2 * lane + 1);
+            } else {
+              const int32_t* tk = p.topk + (int64_t)it.id * p.K;
+              const int c0 = j * kKeys + 2 * lane;
+              re = (c0 < p.K) ? tk[c0] : -1;
+              ro = (c0 + 1 < p.K) ? tk[c0 + 1] : -1;
+              if (re < 0 || re >= p.S_kv) re = -1;
+              if (ro < 0 || ro >= p.S_kv) ro = -1;
+            }
+            if (lane == 0) mbar_arrive_expect_tx(&bars.s_kv_full[s], kStageBytesS);
+            __syncwarp();
+            if (tiled) {
+              if (lane == 0)
+                for (int bx = 0; bx < kKBoxes; ++bx)
+                  tma_load_2d(dst + bx * kBoxBytes, &map_kv, bx * kBoxCols, ytile, &bars.s_kv_full[s]);
+            } else {
+              issue_gather_tile(dst, &map_row, &map_pe, kKBoxes, re, ro, &bars.s_kv_full[s]);
+            }
+          }
+          __syncwarp();
+        }
+      }
+    } else if (warp == 5) {
+      // ---------------- MMA issuer: S = Q K^T ----------------
+      const uint32_t idesc = idesc_bf16_f32(kRows, kKeys, false, false);
+      uint32_t g = 0, i = 0;
+      bool live = true;
+      while (live && iter.next(it)) {
+        if (!waitb(&bars.q_full, i & 1, W_S_QFULL, false)) break;
+        for (int j = 0; j < it.J; ++j, ++g) {
+          const int s = g % kStagesS;
+          const int sb = g & 1;
+          if (!waitb(&bars.s_kv_full[s], (g / kStagesS) & 1, W_S_KV_FULL, false) ||
+              !waitb(&bars.s_free[sb], ((g >> 1) & 1) ^ 1, W_S_SFREE, false)) {
+            live = false;
+            break;
+          }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t stage = smem_u32(smem + kOffStages + s * kStageBytesS);
+            const uint32_t d = tbase + kTmemS + sb * kKeys;
+#pragma unroll 4
+            for (int ks = 0; ks < kDk / 16; ++ks) {
+              const uint64_t bdesc = sdesc_sw128(stage + (ks >> 2) * kBoxBytes + (ks & 3) * 32, 16, 1024);
+              mma_ts(d, tbase + kTmemQ + ks * 8, bdesc, idesc, ks > 0 ? 1u : 0u);
+            }
+            mma_commit(&bars.s_kv_empty[s]);
+            mma_commit(&bars.s_full[sb]);
+          }
+          __syncwarp();
+        }
+        ++i;
+      }
+    } else {
+      // ---------------- rows: Q load, online softmax, P hand-over ----------------
+      const int r = tid;  // row within the tile = TMEM lane
+      const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+      uint8_t* pbuf = smem + kOffPS;
+      float* alpha = reinterpret_cast<float*>(smem + kOffAlpha);
+      float* stats = reinterpret_cast<float*>(smem + kOffStats);
+      const uint32_t rem_p_full0 = map_to_rank(smem_u32(&bars.p_full[0]), peer);
+      const uint32_t rem_p_full1 = map_to_rank(smem_u32(&bars.p_full[1]), peer);
+      const uint32_t rem_stats_full = map_to_rank(smem_u32(&bars.stats_full), peer);
+      uint32_t g = 0, i = 0;
+      bool live = true;
+      while (live && iter.next(it)) {
+        // ---- this row's query and key limit ----
+        const __nv_bfloat16* qrow = nullptr;
+        const __nv_bfloat16* qpe = nullptr;
+        int64_t nkeys = 0;  // prefill: keys visible to the row
+        bool row_ok = false;
+        if (p.mode == MODE_PREFILL) {
+          const int64_t f = (int64_t)it.id * kRows + r;
+          if (f < (int64_t)p.T * p.H) {
+            const int64_t t = f / p.H, h = f - t * p.H;
+            qrow = p.q + t * p.q_stride_t + h * p.q_stride_h;
+            nkeys = prefill_keys_for_token(p, t);
+            row_ok = true;
+          }
+        } else if (p.mode == MODE_DECODE) {
+          if (r < p.H) {
+            qrow = p.q + ((int64_t)it.id * p.H + r) * kDk;
+            row_ok = true;
+          }
+        } else {
+          if (r < p.H) {
+            qrow = p.q + ((int64_t)it.id * p.H + r) * kLatent;
+            qpe = p.q_pe + ((int64_t)it.id * p.H + r) * kRope;
+            row_ok = true;
+          }
+        }
+        // ---- Q -> TMEM (bf16 pairs, K-contiguous): 9 chunks of 64 columns ----
+#pragma unroll 1
+        for (int c = 0; c < kDk / 64; ++c) {
+          uint32_t v[32];
+          const uint4* src = nullptr;
+          if (row_ok) {
+            if (p.mode == MODE_SPARSE)
+              src = (c < 8) ? reinterpret_cast<const uint4*>(qrow + c * 64) : reinterpret_cast<const uint4*>(qpe);
+            else
+              src = reinterpret_cast<const uint4*>(qrow + c * 64);
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            uint4 x = src ? __ldg(src + u) : make_uint4(0, 0, 0, 0);
+            v[4 * u + 0] = x.x;
+            v[4 * u + 1] = x.y;
+            v[4 * u + 2] = x.z;
+            v[4 * u + 3] = x.w;
+          }
+          tmem_st32(tbase + lane_base + kTmemQ + c * 32, v);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars.q_full);
+
+        float m_used = -CUDART_INF_F;  // log2-domain offset of the exponentials
+        float l = 0.f;                 // running row sum (relative to m_used)
+        for (int j = 0; j < it.J; ++j, ++g) {
+          const int sb = g & 1;
+          // ---- per-tile key validity mask ----
+          uint64_t vmask;
+          if (p.mode == MODE_PREFILL) {
+            int64_t nv = nkeys - (int64_t)j * kKeys;
+            nv = nv < 0 ? 0 : (nv > 64 ? 64 : nv);
+            vmask = (nv == 64) ? ~0ull : ((1ull << nv) - 1ull);
+          } else if (p.mode == MODE_DECODE) {
+            int64_t nv = it.k1 - (it.k0 + (int64_t)j * kKeys);
+            nv = nv < 0 ? 0 : (nv > 64 ? 64 : nv);
+            vmask = (nv == 64) ? ~0ull : ((1ull << nv) - 1ull);
+          } else {
+            const int32_t* tk = p.topk + (int64_t)it.id * p.K;
+            const int c0 = j * kKeys + lane, c1 = c0 + 32;
+            const int32_t i0 = (c0 < p.K) ? tk[c0] : -1;
+            const int32_t i1 = (c1 < p.K) ? tk[c1] : -1;
+            const uint32_t lo = __ballot_sync(0xffffffffu, i0 >= 0 && i0 < p.S_kv);
+            const uint32_t hi = __ballot_sync(0xffffffffu, i1 >= 0 && i1 < p.S_kv);
+            vmask = ((uint64_t)hi << 32) | lo;
+          }
+          if (!row_ok) vmask = 0;
+
+          if (!waitb(&bars.s_full[sb], (g >> 1) & 1, W_S_SFULL, false)) { live = false; break; }
+          tc_fence_after();
+          uint32_t sraw[64];
+          {
+            uint32_t (&a)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sraw[0]);
+            uint32_t (&b)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sraw[32]);
+            tmem_ld32(tbase + lane_base + kTmemS + sb * kKeys, a);
+            tmem_ld32(tbase + lane_base + kTmemS + sb * kKeys + 32, b);
+          }
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(&bars.s_free[sb]);
+
+          float x[64];
+          float mt = -CUDART_INF_F;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            x[c] = ((vmask >> c) & 1ull) ? __uint_as_float(sraw[c]) * p.scale_log2 : -CUDART_INF_F;
+            mt = fmaxf(mt, x[c]);
+          }
+          float a = 1.f;
+          if (mt > m_used + kRescaleLog2) {
+            if (l > 0.f) a = ex2_approx(m_used - mt);
+            l *= a;
+            m_used = mt;
+          }
+          if (j == 0) a = 1.f;  // the first P V overwrites O
+          const float msub = (m_used == -CUDART_INF_F) ? 0.f : m_used;
+          uint32_t pk[32];
+          float rs = 0.f;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float e0 = ex2_approx(x[2 * c] - msub);
+            const float e1 = ex2_approx(x[2 * c + 1] - msub);
+            rs += e0 + e1;
+            pk[c] = pack_bf16x2(e0, e1);
+          }
+          l += rs;
+
+          // ---- hand P and the rescale factor to the O-CTA ----
+          if (!waitb(&bars.p_free[sb], ((g >> 1) & 1) ^ 1, W_S_PFREE, true)) { live = false; break; }
+          uint8_t* prow = pbuf + sb * kPBytes + r * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint4 v4 = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = v4;
+          }
+          alpha[sb * kRows + r] = a;
+          mbar_arrive_remote(sb ? rem_p_full1 : rem_p_full0);
+        }
+        if (!live) break;
+        // ---- row statistics for the epilogue ----
+        if (!waitb(&bars.stats_free, (i & 1) ^ 1, W_S_STATSFREE, true)) break;
+        stats[2 * r] = m_used;
+        stats[2 * r + 1] = l;
+        mbar_arrive_remote(rem_stats_full);
+        ++i;
+      }
+    }
+  } else {
+    // =====================================================================
+    // O-CTA
+    // =====================================================================
+    if (warp == 4) {
+      // ---------------- TMA producer: V tiles (first 512 columns) ----------------
+      uint32_t g = 0;
+      bool live = true;
+      while (live && iter.next(it)) {
+        for (int j = 0; j < it.J && live; ++j, ++g) {
+          const int s = g % kStagesO;
+          if (!waitb(&bars.o_kv_empty[s], ((g / kStagesO) & 1) ^ 1, W_O_KV_EMPTY, false)) { live = false; break; }
+          const uint32_t dst = smem_u32(smem + kOffStages + s * kStageBytesO);
+          if (p.mode == MODE_PREFILL) {
+            if (lane == 0) {
+              mbar_arrive_expect_tx(&bars.o_kv_full[s], kStageBytesO);
+              for (int bx = 0; bx < kVBoxes; ++bx)
+                tma_load_2d(dst + bx * kBoxBytes, &map_kv, bx * kBoxCols, j * kKeys, &bars.o_kv_full[s]);
+            }
+          } else {
+            int32_t re, ro;
+            bool tiled = false;
+            int32_t ytile = 0;
+            if (p.mode == MODE_DECODE) {
+              const int64_t kb = it.k0 + (int64_t)j * kKeys;
+              const int len = decode_len(p, it.id);
+              const int32_t* bt = p.block_table + (int64_t)it.id * p.max_pages;
+              auto row_of = [&](int64_t key) -> int32_t {
+                if (key >= len) return -1;
+                const int32_t pg = bt[key / p.page_size];
+                if (pg < 0 || pg >= p.num_pages) return -1;
+                return (int32_t)(pg * (int64_t)p.page_size + key % p.page_size);
+              };
+              if (p.page_size % kKeys == 0 && kb + kKeys <= len) {
+                const int32_t pg = bt[kb / p.page_size];
+                if (pg >= 0 && pg < p.num_pages) {
+                  tiled = true;
+                  ytile = (int32_t)(pg * (int64_t)p.page_size + kb % p.page_size);
+                }
+              }
+              re = row_of(kb + 2 * lane);
+              ro = row_of(kb + 2 * lane + 1);
+            } else {
+              const int32_t* tk = p.topk + (int64_t)it.id * p.K;
+              const int c0 = j * kKeys + 2 * lane;
+              re = (c0 < p.K) ? tk[c0] : -1;
+              ro = (c0 + 1 < p.K) ? tk[c0 + 1] : -1;
+              if (re < 0 || re >= p.S_kv) re = -1;
+              if (ro < 0 || ro >= p.S_kv) ro = -1;
+            }
+            if (lane == 0) mbar_arrive_expect_tx(&bars.o_kv_full[s], kStageBytesO);
+            __syncwarp();
+            if (tiled) {
+              if (lane == 0)
+                for (int bx = 0; bx < kVBoxes; ++bx)
+                  tma_load_2d(dst + bx * kBoxBytes, &map_kv, bx * kBoxCols, ytile, &bars.o_kv_full[s]);
+            } else {
+              issue_gather_tile(dst, &map_row, &map_pe, kVBoxes, re, ro, &bars.o_kv_full[s]);
+            }
+          }
+          __syncwarp();
+        }
+      }
+    } else if (warp == 5) {
+      // ---------------- MMA issuer: O += P V ----------------
+      const uint32_t idesc = idesc_bf16_f32(kRows, 256, false, true);
+      uint32_t g = 0, i = 0;
+      bool live = true;
+      while (live && iter.next(it)) {
+        if (i > 0 && !waitb(&bars.o_free, (i - 1) & 1, W_O_OFREE, false)) break;
+        for (int j = 0; j < it.J; ++j, ++g) {
+          const int s = g % kStagesO;
+          const int pb = g & 1;
+          if (!waitb(&bars.o_kv_full[s], (g / kStagesO) & 1, W_O_KV_FULL, false) ||
+              !waitb(&bars.p_ready[pb], (g >> 1) & 1, W_O_PREADY, false)) {
+            live = false;
+            break;
+          }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t vst = smem_u32(smem + kOffStages + s * kStageBytesO);
+            const uint32_t pst = smem_u32(smem + kOffPO + pb * kPBytes);
+#pragma unroll
+            for (int ks = 0; ks < kKeys / 16; ++ks) {
+              const uint64_t adesc = sdesc_sw128(pst + ks * 32, 16, 1024);
+#pragma unroll
+              for (int half = 0; half < 2; ++half) {
+                const uint64_t bdesc = sdesc_sw128(vst + half * 4 * kBoxBytes + ks * 2048, kBoxBytes, 1024);
+                mma_ss(tbase + half * 256, adesc, bdesc, idesc, (j > 0 || ks > 0) ? 1u : 0u);
+              }
+            }
+            mma_commit(&bars.o_kv_empty[s]);
+            mma_commit(&bars.pb_free[pb]);
+            mma_commit(&bars.pv_done);
+          }
+          __syncwarp();
+        }
+        ++i;
+      }
+    } else {
+      // ---------------- rows: P pull, lazy rescale, epilogue ----------------
+      const int r = tid;
+      const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+      const uint32_t rem_pbuf = map_to_rank(smem_u32(smem + kOffPS), peer);
+      const uint32_t rem_alpha = map_to_rank(smem_u32(smem + kOffAlpha), peer);
+      const uint32_t rem_stats = map_to_rank(smem_u32(smem + kOffStats), peer);
+      const uint32_t rem_p_free0 = map_to_rank(smem_u32(&bars.p_free[0]), peer);
+      const uint32_t rem_p_free1 = map_to_rank(smem_u32(&bars.p_free[1]), peer);
+      const uint32_t rem_stats_free = map_to_rank(smem_u32(&bars.stats_free), peer);
+      uint8_t* plocal = smem + kOffPO;
+      uint32_t g = 0, i = 0;
+      bool live = true;
+      while (live && iter.next(it)) {
+        for (int j = 0; j < it.J; ++j, ++g) {
+          const int pb = g & 1;
+          if (!waitb(&bars.p_full[pb], (g >> 1) & 1, W_O_PFULL, true) ||
+              !waitb(&bars.pb_free[pb], ((g >> 1) & 1) ^ 1, W_O_PBFREE, false)) {
+            live = false;
+            break;
+          }
+          // copy this row's 128 bytes of P (already in the swizzled K-major layout)
+          const uint32_t src = rem_pbuf + pb * kPBytes + r * 128;
+          uint8_t* dst = plocal + pb * kPBytes + r * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint4 v;
+            asm volatile("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                         : "r"(src + c * 16));
+            *reinterpret_cast<uint4*>(dst + c * 16) = v;
+          }
+          float a;
+          asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(a) : "r"(rem_alpha + (pb * kRows + r) * 4));
+          fence_proxy_async_smem();
+          mbar_arrive_remote(pb ? rem_p_free1 : rem_p_free0);
+          // tcgen05.ld/st are warp-collective: rescale when any row of the warp needs it
+          if (__any_sync(0xffffffffu, a != 1.f)) {
+            // O must hold every earlier P V before it is rescaled
+            if (!waitb(&bars.pv_done, (g - 1) & 1, W_O_PVDONE, false)) { live = false; break; }
+            tc_fence_after();
+#pragma unroll 1
+            for (int c0 = 0; c0 < kLatent; c0 += 32) {
+              uint32_t v[32];
+              tmem_ld32(tbase + lane_base + c0, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * a);
+              tmem_st32(tbase + lane_base + c0, v);
+            }
+            tmem_wait_st();
+          }
+          tc_fence_before();
+          mbar_arrive(&bars.p_ready[pb]);
+        }
+        if (!live) break;
+        // ---- epilogue ----
+        if (!waitb(&bars.stats_full, i & 1, W_O_STATSFULL, true)) break;
+        float m_used, l;
+        asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(m_used) : "r"(rem_stats + r * 8));
+        asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(l) : "r"(rem_stats + r * 8 + 4));
+        mbar_arrive_remote(rem_stats_free);
+        if (it.J > 0) {
+          if (!waitb(&bars.pv_done, (g - 1) & 1, W_O_PVDONE, false)) break;
+          tc_fence_after();
+        }
+        const bool has = (it.J > 0) && (l > 0.f);
+        const float inv_l = has ? 1.f / l : 0.f;
+        const float lse_new = has ? (m_used + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+
+        // destination of this row
+        bool row_ok = false;
+        float prev_l = -CUDART_INF_F;
+        const __nv_bfloat16* prev_row = nullptr;
+        __nv_bfloat16* orow = nullptr;
+        float* orow_f = nullptr;
+        float* lse_dst = nullptr;
+        if (p.mode == MODE_PREFILL) {
+          const int64_t f = (int64_t)it.id * kRows + r;
+          if (f < (int64_t)p.T * p.H) {
+            const int64_t t = f / p.H, h = f - t * p.H;
+            row_ok = true;
+            orow = p.out + f * kLatent;
+            lse_dst = p.lse + h * p.T + t;
+            if (p.prev_out) {
+              prev_row = p.prev_out + f * kLatent;
+              prev_l = p.prev_lse[h * p.T + t];
+            }
+          }
+        } else if (p.mode == MODE_DECODE) {
+          if (r < p.H) {
+            row_ok = true;
+            orow_f = p.part_o + ((int64_t)it.slot * p.H + r) * kLatent;
+            lse_dst = p.part_lse + (int64_t)it.slot * p.H + r;
+          }
+        } else {
+          if (r < p.H) {
+            row_ok = true;
+            orow = p.out + ((int64_t)it.id * p.H + r) * kLatent;
+            lse_dst = p.lse ? p.lse + (int64_t)it.id * p.H + r : nullptr;
+          }
+        }
+        {
+          // merge weights with the previous pair (weight 0 for an empty side)
+          float wn = has ? 1.f : 0.f, wp = 0.f, lse_out = lse_new;
+          if (row_ok && prev_row) {
+            const float m = fmaxf(prev_l, lse_new);
+            if (m == -CUDART_INF_F) {
+              wn = 0.f;
+              wp = 0.f;
+              lse_out = -CUDART_INF_F;
+            } else {
+              wp = (prev_l == -CUDART_INF_F) ? 0.f : expf(prev_l - m);
+              wn = has ? expf(lse_new - m) : 0.f;
+              const float ws = wp + wn;
+              lse_out = m + logf(ws);
+              wp /= ws;
+              wn /= ws;
+            }
+          }
+          const float cn = wn * inv_l;
+#pragma unroll 1
+          for (int c0 = 0; c0 < kLatent; c0 += 32) {
+            float o[32];
+            if (it.J > 0) {  // uniform over the CTA: every lane takes part in the TMEM load
+              uint32_t v[32];
+              tmem_ld32(tbase + lane_base + c0, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int c = 0; c < 32; ++c) o[c] = __uint_as_float(v[c]) * cn;
+            } else {
+#pragma unroll
+              for (int c = 0; c < 32; ++c) o[c] = 0.f;
+            }
+            if (!row_ok) continue;
+            if (prev_row && wp > 0.f) {
+              const uint4* pr = reinterpret_cast<const uint4*>(prev_row + c0);
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                uint4 x = pr[u];
+                const __nv_bfloat162* hx = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  float2 f2 = __bfloat1622float2(hx[k]);
+                  o[8 * u + 2 * k] += wp * f2.x;
+                  o[8 * u + 2 * k + 1] += wp * f2.y;
+                }
+              }
+            }
+            if (orow) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                dst[u] = make_uint4(pack_bf16x2(o[8 * u], o[8 * u + 1]), pack_bf16x2(o[8 * u + 2], o[8 * u + 3]),
+                                    pack_bf16x2(o[8 * u + 4], o[8 * u + 5]), pack_bf16x2(o[8 * u + 6], o[8 * u + 7]));
+            } else {
+              float4* dst = reinterpret_cast<float4*>(orow_f + c0);
+#pragma unroll
+              for (int u = 0; u < 8; ++u) dst[u] = make_float4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+            }
+          }
+          if (row_ok && lse_dst) *lse_dst = lse_out;
+        }
+        tc_fence_before();
+        mbar_arrive(&bars.o_free);
+        ++i;
+      }
+    }
+  }
+
+  // ---- teardown: drain on abort, then leave together ----
+  __syncwarp();
+  if (*abort_flag) {
+    // let copies and MMAs already in flight land before the CTA exits
+    for (int k = 0; k < 200; ++k) __nanosleep(1000);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 5) tmem_dealloc(tbase, 512);
+}
+
+}  // namespace
+
+size_t core_smem_bytes() { return kSmemAlloc; }
+
+cudaError_t launch_core(const CoreParams& p, const CUtensorMap& map_kv, const CUtensorMap& map_row,
+                        const CUtensorMap& map_pe, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(mla_core_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  if (p.num_pairs <= 0) return cudaSuccess;
+  mla_core_kernel<<<dim3(2 * p.num_pairs), dim3(kThreads), kSmemAlloc, stream>>>(p, map_kv, map_row, map_pe);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

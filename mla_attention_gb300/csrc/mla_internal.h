@@ -1,0 +1,124 @@
+// Internal interfaces between the C-ABI layer (mla_api.cu) and the kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/mla.h"
+#include "mla_device_status.h"
+
+namespace mla {
+
+// ---------------------------------------------------------------------------
+// geometry of the absorbed (latent) path
+// ---------------------------------------------------------------------------
+constexpr int kLatent = 512;            // V width = latent width
+constexpr int kRope = 64;               // RoPE columns
+constexpr int kDk = kLatent + kRope;    // 576
+constexpr int kRows = 128;              // query rows per tile (MMA M)
+constexpr int kKeys = 64;               // keys per KV tile (MMA N of QK^T, K of PV)
+constexpr int kBoxCols = 64;            // 64 bf16 = 128 B: one 128B-swizzle row
+constexpr int kKBoxes = kDk / kBoxCols;       // 9 column boxes for K (576 columns)
+constexpr int kVBoxes = kLatent / kBoxCols;   // 8 column boxes for V (512 columns)
+
+// ---------------------------------------------------------------------------
+// workspace layout (shared by every call): a 256-byte header first
+// ---------------------------------------------------------------------------
+constexpr size_t kWsHeader = 256;       // [0]: device status word
+constexpr uint32_t kDefaultSpinLimit = 1u << 25;
+
+uint32_t spin_limit();                  // process-wide bound for device waits
+
+// kinds of work the absorbed tile engine runs
+enum CoreMode : int { MODE_PREFILL = 0, MODE_DECODE = 1, MODE_SPARSE = 2 };
+
+struct CoreParams {
+  int mode;
+  int num_pairs;          // CTA pairs in the grid (cluster of 2 per pair)
+  float scale_log2;       // scale * log2(e)
+  uint32_t spin_limit;
+  uint32_t* err;          // device status word
+
+  // ---- query rows ----
+  const __nv_bfloat16* q;        // prefill / decode: [.., 576] rows; sparse: q_lift [.., 512]
+  const __nv_bfloat16* q_pe;     // sparse: q_pe [.., 64]
+  int64_t q_stride_t;            // prefill: token stride (elements)
+  int64_t q_stride_h;            // prefill: head stride (elements)
+  int T;                         // prefill: tokens; sparse: S
+  int H;                         // heads
+
+  // ---- prefill ----
+  int64_t q_pos0, kv_pos0;
+  int kv_valid;
+  int causal;
+  const __nv_bfloat16* prev_out; // [T,H,512] or null
+  const float* prev_lse;         // [H,T] or null
+  __nv_bfloat16* out;            // prefill: [T,H,512]; sparse: [S,H*512]
+  float* lse;                    // prefill: [H,T]; sparse: [S,H] (nullable)
+
+  // ---- decode ----
+  const int32_t* block_table;    // [B, max_pages]
+  const int32_t* lens;           // [B]
+  int B;
+  int max_pages;
+  int page_size;
+  int64_t num_pages;
+  int32_t* tile_prefix;          // ws: [B+1] tiles before request b (written by CTA 0)
+  float* part_o;                 // ws: [slots, H, 512]
+  float* part_lse;               // ws: [slots, H]
+
+  // ---- sparse ----
+  const int32_t* topk;           // [S, K]
+  int K;
+  int S_kv;
+};
+
+// kernels' host launchers (return cudaError_t of the launch)
+cudaError_t launch_core(const CoreParams& p, const CUtensorMap& map_kv, const CUtensorMap& map_row,
+                        const CUtensorMap& map_pe, cudaStream_t stream);
+size_t core_smem_bytes();
+
+cudaError_t launch_merge(const __nv_bfloat16* out_a, const float* lse_a, const __nv_bfloat16* out_b,
+                         const float* lse_b, __nv_bfloat16* out, float* lse, int64_t rows, int H, int dv,
+                         cudaStream_t stream);
+
+cudaError_t launch_decode_reduce(const CoreParams& p, __nv_bfloat16* out, float* lse, cudaStream_t stream);
+
+// non-absorbed split layout
+struct SplitParams {
+  int batch;
+  int H, Hkv;
+  int Nq, Nkv;
+  float scale_log2;
+  int causal;
+  uint32_t spin_limit;
+  uint32_t* err;
+  int total_q_tiles;           // sum over sequences of ceil(q_len / 128)
+  const __nv_bfloat16* prev_out;
+  const float* prev_lse;
+  __nv_bfloat16* out;
+  float* lse;
+  // per-sequence tables (kernel parameters; batch <= kMaxBatch)
+  int q_off[257];
+  int kv_off[257];
+  int tile_off[257];
+};
+constexpr int kSplitMaxBatch = 256;
+
+cudaError_t launch_split(const SplitParams& p, const CUtensorMap& mq_nope, const CUtensorMap& mq_pe,
+                         const CUtensorMap& mk_nope, const CUtensorMap& mk_pe, const CUtensorMap& mv,
+                         cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// host helpers
+// ---------------------------------------------------------------------------
+// cuTensorMapEncodeTiled through the runtime's driver entry point
+CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, const void* base,
+                      const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                      CUtensorMapSwizzle swizzle);
+
+int device_sm_count();
+
+}  // namespace mla

@@ -185,6 +185,25 @@ def mla_prefill(q, kv, scale: float, dv: int = 512, causal: bool = True,
 # ---------------------------------------------------------------------------
 # Ascend split layout (non-absorbed), varlen, GQA, NO_MASK / TRIU
 # ---------------------------------------------------------------------------
+def attend_masked(q_rows: np.ndarray, keys: np.ndarray, values: np.ndarray, scale: float, visible: np.ndarray):
+    """attend() where row r sees only the keys with visible[r, j] true (a row may see none)."""
+    R, dv = q_rows.shape[0], values.shape[1]
+    out = np.zeros((R, dv))
+    lse = np.full((R,), NEG_INF)
+    if keys.shape[0] == 0:
+        return out, lse
+    s = scale * (q_rows @ keys.T)
+    s = np.where(visible, s, NEG_INF)
+    has = visible.any(axis=1)
+    m = np.where(has, s.max(axis=1), 0.0)[:, None]
+    p = np.where(visible, np.exp(s - m), 0.0)
+    l = p.sum(axis=1, keepdims=True)
+    l_safe = np.where(l > 0, l, 1.0)
+    out = np.where(has[:, None], (p @ values) / l_safe, 0.0)
+    lse = np.where(has, (m + np.log(l_safe))[:, 0], NEG_INF)
+    return out, lse
+
+
 def mla_prefill_split(q_nope, q_pe, k_nope, k_pe, v, seq_len, head_num: int, kv_head_num: int,
                       scale: float, mask_type: int, prev_out=None, prev_lse=None,
                       tokens: Optional[Sequence[int]] = None):
@@ -210,21 +229,29 @@ def mla_prefill_split(q_nope, q_pe, k_nope, k_pe, v, seq_len, head_num: int, kv_
     dv = vv.shape[2]
     q_off = np.concatenate([[0], np.cumsum(q_lens)])
     kv_off = np.concatenate([[0], np.cumsum(kv_lens)])
-    toks = list(range(Nq)) if tokens is None else [int(t) for t in tokens]
+    toks = np.arange(Nq) if tokens is None else np.asarray([int(t) for t in tokens], dtype=np.int64)
     out = np.zeros((len(toks), H, dv))
     lse = np.full((H, len(toks)), NEG_INF)
-    for i, t in enumerate(toks):
-        b = int(np.searchsorted(q_off, t, side="right") - 1)
-        qi = t - q_off[b]
+    seq_of = np.searchsorted(q_off, toks, side="right") - 1
+    for b in range(len(q_lens)):
+        sel = np.nonzero(seq_of == b)[0]               # positions in `toks` of this sequence
+        if len(sel) == 0:
+            continue
         ql, kl = int(q_lens[b]), int(kv_lens[b])
-        n = kl if mask_type == 0 else max(0, min(kl, kl - ql + qi + 1))
-        ks = slice(kv_off[b], kv_off[b] + n)
+        qi = toks[sel] - q_off[b]                       # query index inside the sequence
+        j = np.arange(kl)
+        if mask_type == 0:
+            visible = np.ones((len(sel), kl), dtype=bool)
+        else:
+            visible = j[None, :] <= (kl - ql + qi)[:, None]
+        ks = slice(kv_off[b], kv_off[b] + kl)
         for h in range(H):
             g = h // group
-            qrow = np.concatenate([qn[t, h], qp[t, h]])[None, :]
+            qrows = np.concatenate([qn[toks[sel], h], qp[toks[sel], h]], axis=1)
             keys = np.concatenate([kn[ks, g], kp[ks, g]], axis=1)
-            o, l_ = attend(qrow, keys, vv[ks, g], scale)
-            out[i, h], lse[h, i] = o[0], l_[0]
+            o, l_ = attend_masked(qrows, keys, vv[ks, g], scale, visible)
+            out[sel, h] = o
+            lse[h, sel] = l_
     if prev_out is not None:
         po = _f64(prev_out)[toks]
         pl = _f64(prev_lse)[:, toks]
@@ -315,6 +342,6 @@ def causal_pairs(T: int, Tkv: int, q_pos0: int, kv_pos0: int, kv_valid: Optional
 
 
 __all__ = [
-    "attend", "attend_rowwise", "merge", "prefill_key_set", "mla_prefill", "mla_prefill_split",
+    "attend", "attend_rowwise", "attend_masked", "merge", "prefill_key_set", "mla_prefill", "mla_prefill_split",
     "gather_pages", "mla_decode", "mla_sparse", "attention_flops", "causal_pairs", "NEG_INF",
 ]

@@ -1,0 +1,121 @@
+"""Parity of mla_prefill (absorbed causal MLA, CUDA path through the C ABI) with the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.mla_oracle as mo
+from mla_attention_gb300 import inputs as gen
+from mla_attention_gb300 import mla_prefill, check_device_status
+from tests.helpers import assert_lse_close, assert_out_close, dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(P, **kw):
+    q = P.q.to(dev())
+    kv = P.kv.to(dev())
+    out, lse = mla_prefill(q, kv, P.scale, **kw)
+    torch.cuda.synchronize()
+    check_device_status()
+    return out, lse
+
+
+def test_tiny_config_full_parity():
+    """B=1, H=16, T=Tkv=256 causal, every row (rows pack 8 tokens x 16 heads per tile)."""
+    P = gen.prefill_inputs(T=256, H=16, Tkv=256, seed=1)
+    out, lse = _run(P)
+    ro, rl = mo.mla_prefill(P.q, P.kv, P.scale, causal=True)
+    assert_out_close(out, ro)
+    assert_lse_close(lse, rl)
+
+
+@pytest.mark.parametrize("T,H,Tkv,q_pos0,kv_pos0,kv_valid,causal", [
+    (100, 7, 77, 50, 20, 70, True),       # ragged rows/tiles, padded chunk, offsets
+    (37, 128, 200, 0, 10, 200, True),     # tokens 0..9 see no key: O = 0, lse = -inf
+    (64, 3, 130, 0, 0, 130, False),       # FULL mask (a cached chunk)
+    (5, 128, 1, 0, 0, 1, True),           # a single key
+    (130, 128, 64, 1000, 0, 64, True),    # every token sees the whole chunk
+])
+def test_ragged_and_edge_cases(T, H, Tkv, q_pos0, kv_pos0, kv_valid, causal):
+    P = gen.prefill_inputs(T=T, H=H, Tkv=Tkv, seed=T + H)
+    out, lse = _run(P, causal=causal, q_pos0=q_pos0, kv_pos0=kv_pos0, kv_valid=kv_valid)
+    ro, rl = mo.mla_prefill(P.q, P.kv, P.scale, causal=causal, q_pos0=q_pos0, kv_pos0=kv_pos0, kv_valid=kv_valid)
+    assert_out_close(out, ro)
+    assert_lse_close(lse, rl)
+
+
+def test_empty_rows_are_zero_and_neg_inf():
+    P = gen.prefill_inputs(T=20, H=16, Tkv=64, seed=3)
+    out, lse = _run(P, q_pos0=0, kv_pos0=100)   # no token reaches the chunk
+    assert torch.all(out == 0)
+    assert torch.all(torch.isneginf(lse))
+
+
+def test_prev_merge_and_in_place():
+    T, H = 96, 128
+    P = gen.prefill_inputs(T=T, H=H, Tkv=96, seed=4)
+    prev_out, prev_lse = gen.prev_inputs(T, H, 512, seed=44, lse_lo=1.0, lse_hi=6.0)
+    prev_lse[:, :5] = -float("inf")           # rows with an empty previous part
+    ro, rl = mo.mla_prefill(P.q, P.kv, P.scale, causal=True, q_pos0=40, kv_pos0=0, prev_out=prev_out,
+                            prev_lse=prev_lse)
+    po = prev_out.to(dev())
+    pl = prev_lse.to(dev())
+    out, lse = _run(P, q_pos0=40, kv_pos0=0, prev_out=po, prev_lse=pl, out=po, lse=pl)   # in place
+    assert out.data_ptr() == po.data_ptr()
+    assert_out_close(out, ro)
+    assert_lse_close(lse, rl)
+
+
+def test_chunked_ring_equals_one_pass():
+    """4 KV chunks in sequence, each merged in place into (out, lse), equal one causal pass."""
+    T, H, C = 512, 128, 128
+    P = gen.prefill_inputs(T=T, H=H, Tkv=T, seed=2)
+    q = P.q.to(dev())
+    kv = P.kv.to(dev())
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev())
+    lse = torch.empty((H, T), dtype=torch.float32, device=dev())
+    for j in range(T // C):
+        prev = (out, lse) if j > 0 else (None, None)
+        mla_prefill(q, kv[j * C:(j + 1) * C], P.scale, causal=True, q_pos0=0, kv_pos0=j * C,
+                    prev_out=prev[0], prev_lse=prev[1], out=out, lse=lse)
+    torch.cuda.synchronize()
+    check_device_status()
+    toks = gen.sample_rows(T, 96, seed=7, must=[0, 127, 128, 255, 256, 383, 384, 511])
+    ro, rl = mo.mla_prefill(P.q, P.kv, P.scale, causal=True, tokens=toks)
+    assert_out_close(out[toks], ro)
+    assert_lse_close(lse[:, toks], rl)
+
+
+def test_strided_q():
+    T, H = 40, 16
+    P = gen.prefill_inputs(T=T, H=H, Tkv=50, seed=6)
+    big = torch.zeros((T, H, 640), dtype=torch.bfloat16)
+    big[:, :, :576] = P.q
+    qv = big.to(dev())[:, :, :576]
+    out, lse = mla_prefill(qv, P.kv.to(dev()), P.scale, causal=True, q_pos0=10)
+    torch.cuda.synchronize()
+    ro, rl = mo.mla_prefill(P.q, P.kv, P.scale, causal=True, q_pos0=10)
+    assert_out_close(out, ro)
+    assert_lse_close(lse, rl)
+
+
+@pytest.mark.full
+def test_full_size_chunked_config_sampled():
+    """H=128, 8192 tokens, 4 chunks of 2048 keys in sequence with prev merge in place;
+    256 sampled tokens x all heads (every chunk boundary included) against the oracle."""
+    T, H, C = 8192, 128, 2048
+    P = gen.prefill_inputs(T=T, H=H, Tkv=T, seed=2)
+    q = P.q.to(dev())
+    kv = P.kv.to(dev())
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev())
+    lse = torch.empty((H, T), dtype=torch.float32, device=dev())
+    for j in range(4):
+        prev = (out, lse) if j > 0 else (None, None)
+        mla_prefill(q, kv[j * C:(j + 1) * C], P.scale, causal=True, q_pos0=0, kv_pos0=j * C,
+                    prev_out=prev[0], prev_lse=prev[1], out=out, lse=lse)
+    torch.cuda.synchronize()
+    check_device_status()
+    toks = gen.sample_rows(T, 256, seed=2, must=[0, 2047, 2048, 4095, 4096, 6143, 6144, 8191])
+    ro, rl = mo.mla_prefill(P.q, P.kv, P.scale, causal=True, tokens=toks)
+    assert_out_close(out[toks], ro)
+    assert_lse_close(lse[:, toks], rl)

@@ -15,9 +15,15 @@ import oracle.mla_oracle as mo
 import tests.test_oracle_pins as pins
 
 MUTANTS = {
-    "scores drop the last column": ("s = scale * (q_rows @ keys.T)",
+    "scores drop the last column": ("s = scale * (q_rows @ keys.T)                  # [R, |J|]",
                                     "s = scale * (q_rows[:, :-1] @ keys[:, :-1].T)"),
-    "scale applied twice": ("s = scale * (q_rows @ keys.T)", "s = scale * scale * (q_rows @ keys.T)"),
+    "scale applied twice": ("s = scale * (q_rows @ keys.T)                  # [R, |J|]",
+                            "s = scale * scale * (q_rows @ keys.T)"),
+    "masked scores drop the RoPE part": ("    s = scale * (q_rows @ keys.T)\n    s = np.where(visible, s, NEG_INF)",
+                                         "    s = scale * (q_rows[:, :128] @ keys[:, :128].T)\n"
+                                         "    s = np.where(visible, s, NEG_INF)"),
+    "masked lse in base 2": ("lse = np.where(has, (m + np.log(l_safe))[:, 0], NEG_INF)",
+                             "lse = np.where(has, (m + np.log2(l_safe))[:, 0], NEG_INF)"),
     "lse in base 2": ("lse = (m + np.log(l))[:, 0]", "lse = (m + np.log2(l))[:, 0]"),
     "lse without the max": ("lse = (m + np.log(l))[:, 0]", "lse = (np.log(l))[:, 0]"),
     "softmax not normalised": ("out = (p @ values) / l", "out = (p @ values)"),
@@ -40,10 +46,12 @@ MUTANTS = {
     "decode page index transposed": ("return cache[bt[j // page_size], j % page_size]",
                                      "return cache[bt[j % page_size], j // page_size]"),
     "split GQA head map": ("g = h // group", "g = h % Hkv"),
-    "split causal top-left": ("n = kl if mask_type == 0 else max(0, min(kl, kl - ql + qi + 1))",
-                              "n = kl if mask_type == 0 else max(0, min(kl, qi + 1))"),
-    "split rope/nope swapped in q": ("qrow = np.concatenate([qn[t, h], qp[t, h]])[None, :]",
-                                     "qrow = np.concatenate([qp[t, h], qn[t, h]])[None, :]"),
+    "split causal top-left": ("visible = j[None, :] <= (kl - ql + qi)[:, None]",
+                              "visible = j[None, :] <= qi[:, None]"),
+    "split rope/nope swapped in q": ("qrows = np.concatenate([qn[toks[sel], h], qp[toks[sel], h]], axis=1)",
+                                     "qrows = np.concatenate([qp[toks[sel], h], qn[toks[sel], h]], axis=1)"),
+    "masked softmax keeps hidden keys": [("s = np.where(visible, s, NEG_INF)", "pass"),
+                                         ("p = np.where(visible, np.exp(s - m), 0.0)", "p = np.exp(s - m)")],
 }
 
 
