@@ -1,0 +1,443 @@
+"""Benchmark of the MLA attention forward on GB300 (libmla, C ABI).
+
+One step = the chunked ring-style absorbed causal prefill: q [8192, 128, 576]
+against 4 KV chunks of 2048 rows [512 latent | 64 RoPE], processed in sequence,
+each call merging in place with the previous (out, lse).  The metric is
+attention TFLOP/s over unmasked (query, key) pairs, H x 2 x (576 + 512) FLOP
+per pair.  The same JSON line carries the paged decode figure (GB/s against
+HBM), and the top-k sparse and split-layout prefill figures, each timed on its
+own workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl libmla|reference]
+
+With --impl reference the fp64 CPU oracle is timed on a bounded sample of the
+same workload (host cores); it is a reported baseline, not a target.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+H, DK, DV, T_TOTAL, CHUNK = 128, 576, 512, 8192, 2048
+SCALE = 192.0 ** -0.5
+FLOP_PER_PAIR = 2.0 * H * (DK + DV)
+METRIC = "MLA prefill TFLOP/s & % BF16 peak; decode HBM GB/s & % of peak (1xGB300)"
+
+
+def causal_pairs(T, Tkv, q_pos0, kv_pos0):
+    tot = 0
+    for t in range(T):
+        tot += max(0, min(Tkv, q_pos0 + t - kv_pos0 + 1))
+    return tot
+
+
+def chunk_pairs():
+    return [causal_pairs(T_TOTAL, CHUNK, 0, CHUNK * j) for j in range(T_TOTAL // CHUNK)]
+
+
+def load_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas: every rank runs the same workload)
+# ---------------------------------------------------------------------------
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the libmla arm
+# ---------------------------------------------------------------------------
+def prefill_step(lib, q, kv, out, lse, events=None):
+    n = 0
+    for j in range(T_TOTAL // CHUNK):
+        prev = (out, lse) if j > 0 else (None, None)
+        if events is not None:
+            events.append(torch.cuda.Event(enable_timing=True))
+            events[-1].record()
+        lib.mla_prefill(q, kv[j * CHUNK:(j + 1) * CHUNK], SCALE, causal=True, q_pos0=0, kv_pos0=j * CHUNK,
+                        prev_out=prev[0], prev_lse=prev[1], out=out, lse=lse)
+        if events is not None:
+            events.append(torch.cuda.Event(enable_timing=True))
+            events[-1].record()
+        n += 1
+    return n
+
+
+def time_region(fn, steps):
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def measure_decode(lib, dev, peaks, steps=10, warmup=3):
+    from mla_attention_gb300 import inputs as gen
+    lens = gen.decode_lens(64, 4096, 32768, seed=4)
+    page = 64
+    pages_per = [(n + page - 1) // page for n in lens]
+    num_pages = sum(pages_per)
+    g = torch.Generator().manual_seed(4)
+    perm = torch.randperm(num_pages, generator=g).to(torch.int32)
+    bt = torch.full((64, max(pages_per)), -1, dtype=torch.int32)
+    o = 0
+    for b, n in enumerate(pages_per):
+        bt[b, :n] = perm[o:o + n]
+        o += n
+    q = gen.randn_bf16_device((64, H, DK), 41, dev)
+    cache = gen.randn_bf16_device((num_pages, page, DK), 42, dev)
+    bt_d, lens_d = bt.to(dev), torch.tensor(lens, dtype=torch.int32, device=dev)
+    out = torch.empty((64, H, DV), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((64, H), dtype=torch.float32, device=dev)
+    fn = lambda: lib.mla_decode(q, cache, bt_d, lens_d, SCALE, out=out, lse=lse)  # noqa: E731
+    for _ in range(warmup):
+        fn()
+    ms = time_region(fn, steps)
+    kv_bytes = sum(lens) * DK * 2
+    moved = kv_bytes + q.numel() * 2 + out.numel() * 2
+    gbs = moved / (ms * 1e-3) / 1e9
+    flops = 2.0 * sum(lens) * H * (DK + DV)
+    return {"workload": "decode B=64 H=128 lens U[4096,32768] 64-token pages", "ms": round(ms, 4),
+            "GB_per_s": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+            "TFLOP_per_s": round(flops / (ms * 1e-3) / 1e12, 1), "kv_bytes": kv_bytes,
+            "note": "algorithmic bytes = sum(lens) x 1152 B of latent cache + q + out; cache larger than L2"}
+
+
+def measure_sparse(lib, dev, peaks, steps=5, warmup=3):
+    from mla_attention_gb300 import inputs as gen
+    S, S_kv, K = 4096, 32768, 2048
+    q_lift = gen.randn_bf16_device((1, S, H, 512), 51, dev)
+    q_pe = gen.randn_bf16_device((1, S, H, 64), 52, dev)
+    c_kv = gen.randn_bf16_device((1, S_kv, 512), 53, dev)
+    k_pe = gen.randn_bf16_device((1, S_kv, 64), 54, dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(55)
+    pos = torch.arange(28672, 28672 + S, device=dev)
+    keys = torch.rand((S, S_kv), generator=g, device=dev)
+    keys = torch.where(torch.arange(S_kv, device=dev)[None, :] <= pos[:, None], keys, torch.full_like(keys, 2.0))
+    topk = torch.topk(keys, K, dim=1, largest=False).indices.to(torch.int32).view(1, S, K).contiguous()
+    del keys
+    out = torch.empty((1, S, H * 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((1, S, H), dtype=torch.float32, device=dev)
+    fn = lambda: lib.mla_sparse(q_lift, q_pe, c_kv, k_pe, topk, SCALE, out=out, lse=lse)  # noqa: E731
+    for _ in range(warmup):
+        fn()
+    ms = time_region(fn, steps)
+    flops = 2.0 * S * K * H * (DK + DV)
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"workload": "sparse S=4096 S_kv=32768 H=128 K=2048", "ms": round(ms, 4), "TFLOP_per_s": round(tf, 1),
+            "tensor_frac": round(tf / peaks["bf16_tflops"], 4)}
+
+
+def measure_split(lib, dev, peaks, steps=5, warmup=3):
+    from mla_attention_gb300 import inputs as gen
+    lens = gen.split_lens(4, 1024, 8192, seed=3)
+    N = sum(lens)
+    t = {k: gen.randn_bf16_device(s, 60 + i, dev) for i, (k, s) in enumerate(
+        [("qn", (N, H, 128)), ("qp", (N, H, 64)), ("kn", (N, H, 128)), ("kp", (N, H, 64)), ("v", (N, H, 128)),
+         ("po", (N, H, 128))])}
+    g = torch.Generator(device=dev)
+    g.manual_seed(66)
+    pl = 7.4 + 2.1 * torch.rand((H, N), generator=g, device=dev)
+    seq = torch.tensor([lens, lens], dtype=torch.int32)
+    out = torch.empty((N, H, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((H, N), dtype=torch.float32, device=dev)
+    fn = lambda: lib.mla_prefill_split(t["qn"], t["qp"], t["kn"], t["kp"], t["v"], seq, H, H, SCALE, 1,  # noqa
+                                       prev_out=t["po"], prev_lse=pl, out=out, lse=lse)
+    for _ in range(warmup):
+        fn()
+    ms = time_region(fn, steps)
+    flops = 2.0 * H * (192 + 128) * sum(L * (L + 1) // 2 for L in lens)
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"workload": f"split layout batch 4 lens {lens} H=Hkv=128 TRIU + prev", "ms": round(ms, 4),
+            "TFLOP_per_s": round(tf, 1), "tensor_frac": round(tf / peaks["bf16_tflops"], 4)}
+
+
+def cpu_baseline_sample(budget_s=20.0):
+    """The oracle, as it stands, on a bounded sample of the prefill workload (host cores)."""
+    import numpy as np
+    import oracle.mla_oracle as mo
+    from mla_attention_gb300 import inputs as gen
+    # token t of the 8192-token sequence sees t + 1 keys; sample late tokens (the costly ones)
+    n_tok = 4
+    P = gen.prefill_inputs(T=1, H=H, Tkv=T_TOTAL, seed=2)
+    q = P.q.double().numpy()
+    kv = P.kv.double().numpy()
+    done = pairs = 0
+    t0 = time.perf_counter()
+    while True:
+        for _ in range(n_tok):
+            mo.attend(q[0], kv, kv[:, :DV], SCALE)
+            pairs += T_TOTAL
+        done += n_tok
+        if time.perf_counter() - t0 > budget_s or done >= 256:
+            break
+    dt = time.perf_counter() - t0
+    cores = os.cpu_count()
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        if info:
+            cores = max(int(i.get("num_threads", 1)) for i in info)
+    except Exception:
+        pass
+    tflops = pairs * FLOP_PER_PAIR / dt / 1e12
+    return {"value": tflops, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} query tokens x 128 heads x 8192 keys of the 8192-token causal prefill "
+                      f"(the longest rows), fp64 numpy, {dt:.1f} s"}
+
+
+def run_libmla(args, world, rank, local):
+    import mla_attention_gb300 as lib
+    from mla_attention_gb300 import inputs as gen
+    from mla_attention_gb300 import _lib
+    _lib.lib()  # fail loudly if the library is missing
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks, peak_kind = load_peaks()
+
+    q = gen.randn_bf16_device((T_TOTAL, H, DK), 21, dev)
+    kv = gen.randn_bf16_device((T_TOTAL, DK), 22, dev)
+    out = torch.empty((T_TOTAL, H, DV), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((H, T_TOTAL), dtype=torch.float32, device=dev)
+    pairs = chunk_pairs()
+    flops_step = sum(pairs) * FLOP_PER_PAIR
+
+    for _ in range(args.warmup):
+        prefill_step(lib, q, kv, out, lse)
+    torch.cuda.synchronize()
+    lib.check_device_status()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    events = []
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record()
+    launches = 0
+    for _ in range(args.steps):
+        launches += prefill_step(lib, q, kv, out, lse, events)
+    stop.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms_total = start.elapsed_time(stop)
+    ms_total = max_over_ranks(ms_total, world)
+    ms_step = ms_total / args.steps
+    lib.check_device_status()
+    value = world * flops_step / (ms_step * 1e-3) / 1e12
+
+    # dominant kernel: per-launch durations from the events around each launch
+    durs = [events[2 * i].elapsed_time(events[2 * i + 1]) for i in range(len(events) // 2)]
+    kflops = [pairs[i % len(pairs)] * FLOP_PER_PAIR for i in range(len(durs))]
+    achieved = sum(kflops) / (sum(durs) * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+
+    # end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    hq = q.cpu().pin_memory()
+    hkv = kv.cpu().pin_memory()
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    hlse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    dq = torch.empty_like(q)
+    dkv = torch.empty_like(kv)
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dkv.copy_(hkv, non_blocking=True)
+        prefill_step(lib, dq, dkv, out, lse)
+        hout.copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    e2e_steps = max(2, args.steps // 2)
+    e2e_ms = time_region(e2e_step, e2e_steps)
+    e2e_ms = max_over_ranks(e2e_ms, world)
+    e2e_val = world * flops_step / (e2e_ms * 1e-3) / 1e12
+    h2d = hq.numel() * 2 + hkv.numel() * 2
+    d2h = hout.numel() * 2 + hlse.numel() * 4
+    del hq, hkv, hout, hlse, dq, dkv
+
+    extra = {}
+    if not args.no_extra:
+        for name, fn in (("decode", measure_decode), ("sparse", measure_sparse), ("split", measure_split)):
+            try:
+                extra[name] = fn(lib, dev, peaks)
+                torch.cuda.empty_cache()
+            except Exception as e:  # reported, never silently dropped
+                extra[name] = {"error": repr(e)[:300]}
+        lib.check_device_status()
+
+    traffic = None
+    try:
+        prof = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+        traffic = prof.get("mla_core_kernel_prefill_bytes_per_launch")
+    except Exception:
+        pass
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "chunked ring-style causal absorbed MLA prefill: B=1, H=128, dk=576, dv=512, "
+                               "8192 tokens, 4 KV chunks of 2048 in sequence with in-place prev merge",
+                   "tflop_per_step": round(flops_step / 1e12, 4), "unmasked_pairs": sum(pairs),
+                   "l2": "inputs larger than L2 (q 1.2 GB, out 1.07 GB per step)", "parallelism": f"replicas x{world}",
+                   "inputs": "seeded N(0,1) bf16 drawn on the device"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "mla_core_kernel (prefill mode)", "peak_kind": f"bf16 burst ({peak_kind})"},
+        "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "decode": extra.get("decode"), "sparse": extra.get("sparse"), "split": extra.get("split"),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_sample(args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args, world, rank):
+    """The oracle on the host cores: each step is a bounded sample of the same workload."""
+    if rank != 0:
+        return
+    steps, warmup = args.steps, args.warmup
+    budget = max(1.0, min(8.0, 150.0 / max(1, steps + warmup)))
+    for _ in range(warmup):
+        cpu_baseline_sample(budget)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        vals.append(cpu_baseline_sample(budget))
+    dt = time.perf_counter() - t0
+    v = statistics.median(x["value"] for x in vals)
+    cb = dict(vals[-1])
+    cb["value"] = v
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": steps, "warmup": warmup, "ms_per_step": round(dt / steps * 1e3, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "chunked ring-style causal absorbed MLA prefill: B=1, H=128, dk=576, dv=512, "
+                                   "8192 tokens (oracle on a bounded sample of the rows)"},
+            "cpu_baseline": cb,
+            "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["libmla", "reference"], default="libmla")
+    ap.add_argument("--no-extra", action="store_true", help="skip the decode/sparse/split lines")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_libmla(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -77,6 +77,14 @@ mla_status mla_check_device_status(void* workspace, void* stream, uint32_t* deta
  */
 void mla_set_spin_limit(uint32_t spin_limit);
 
+/*
+ * Fault injection for tests (host-side switch, process-wide): when enabled,
+ * the MMA warp of every CTA launched afterwards first waits on a barrier that
+ * nothing arrives on, so that wait runs out of its bound and the call reports
+ * MLA_ERR_TIMEOUT through mla_check_device_status.  Off by default.
+ */
+void mla_debug_inject_stall(int enable);
+
 /* ------------------------------------------------------------------------- */
 /* Absorbed causal MLA prefill (one shared KV head)                          */
 /* ------------------------------------------------------------------------- */

@@ -40,6 +40,7 @@ _SIGNATURES = {
     "mla_status_string": ([c_int], ctypes.c_char_p),
     "mla_check_device_status": ([c_void_p, c_void_p, ctypes.POINTER(c_uint32)], c_int),
     "mla_set_spin_limit": ([c_uint32], None),
+    "mla_debug_inject_stall": ([c_int], None),
     "mla_prefill_workspace_size": ([c_int, c_int], c_size_t),
     "mla_prefill": ([c_void_p, c_int64, c_int64, c_void_p, c_int64, c_int, c_int, c_int, c_int, c_int, c_float, c_int,
                      c_int64, c_int64, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p],
@@ -134,6 +135,11 @@ def check_device_status(ws: Optional[torch.Tensor] = None, device=None, stream=N
 
 def set_spin_limit(limit: int):
     lib().mla_set_spin_limit(int(limit))
+
+
+def inject_stall(enable: bool):
+    """Tests only: make every later launch wait on a barrier nothing arrives on."""
+    lib().mla_debug_inject_stall(1 if enable else 0)
 
 
 # ---------------------------------------------------------------------------

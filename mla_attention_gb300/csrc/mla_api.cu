@@ -20,6 +20,7 @@ namespace {
 
 thread_local char g_err[512] = {0};
 std::atomic<uint32_t> g_spin_limit{kDefaultSpinLimit};
+std::atomic<uint32_t> g_debug_stall{0};
 
 mla_status fail(mla_status s, const char* fmt, ...) {
   va_list ap;
@@ -51,6 +52,7 @@ std::once_flag g_encode_once;
 }  // namespace
 
 uint32_t spin_limit() { return g_spin_limit.load(std::memory_order_relaxed); }
+uint32_t debug_stall() { return g_debug_stall.load(std::memory_order_relaxed); }
 
 CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, const void* base,
                       const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
@@ -138,6 +140,8 @@ const char* mla_status_string(mla_status s) {
 
 void mla_set_spin_limit(uint32_t limit) { g_spin_limit.store(limit ? limit : kDefaultSpinLimit); }
 
+void mla_debug_inject_stall(int enable) { g_debug_stall.store(enable ? 1u : 0u); }
+
 mla_status mla_check_device_status(void* workspace, void* stream, uint32_t* detail) {
   if (!workspace) return fail(MLA_ERR_INVALID_ARG, "mla_check_device_status: workspace is NULL");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -180,7 +184,7 @@ mla_status mla_prefill(const void* q, int64_t q_stride_t, int64_t q_stride_h, co
   MLA_REQUIRE(q && out && lse, "mla_prefill: q, out and lse are required");
   MLA_REQUIRE(aligned16(q) && aligned16(out) && (!prev_out || aligned16(prev_out)),
               "mla_prefill: q, out, prev_out must be 16-byte aligned");
-  MLA_REQUIRE(q_stride_h >= kDk && q_stride_t >= (int64_t)H * 0 && (q_stride_h % 8) == 0 && (q_stride_t % 8) == 0,
+  MLA_REQUIRE(q_stride_h >= kDk && q_stride_t >= 0 && (q_stride_h % 8) == 0 && (q_stride_t % 8) == 0,
               "mla_prefill: q strides must be multiples of 8 elements with q_stride_h >= 576");
   if (kv_valid > 0) {
     MLA_REQUIRE(kv != nullptr, "mla_prefill: kv is NULL");
@@ -200,6 +204,7 @@ mla_status mla_prefill(const void* q, int64_t q_stride_t, int64_t q_stride_h, co
   p.num_pairs = default_pairs();
   p.scale_log2 = scale * 1.4426950408889634f;
   p.spin_limit = spin_limit();
+  p.debug_stall = debug_stall();
   p.err = ws_err(workspace);
   p.q = reinterpret_cast<const __nv_bfloat16*>(q);
   p.q_stride_t = q_stride_t;
@@ -261,6 +266,7 @@ mla_status mla_decode(const void* q, const void* kv_cache, int64_t num_pages, in
   p.num_pairs = num_splits > 0 ? num_splits : default_pairs();
   p.scale_log2 = scale * 1.4426950408889634f;
   p.spin_limit = spin_limit();
+  p.debug_stall = debug_stall();
   p.err = ws_err(workspace);
   p.q = reinterpret_cast<const __nv_bfloat16*>(q);
   p.H = H;
@@ -317,6 +323,7 @@ mla_status mla_sparse(const void* q_lift, const void* q_pe, const void* c_kv, co
   if (S < p.num_pairs) p.num_pairs = S;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.spin_limit = spin_limit();
+  p.debug_stall = debug_stall();
   p.err = ws_err(workspace);
   p.q = reinterpret_cast<const __nv_bfloat16*>(q_lift);
   p.q_pe = reinterpret_cast<const __nv_bfloat16*>(q_pe);
@@ -410,6 +417,7 @@ mla_status mla_prefill_split(const void* q_nope, const void* q_pe, const void* k
   p.scale_log2 = qk_scale * 1.4426950408889634f;
   p.causal = mask_type;
   p.spin_limit = spin_limit();
+  p.debug_stall = debug_stall();
   p.err = ws_err(workspace);
   p.total_q_tiles = (int)tiles;
   p.prev_out = reinterpret_cast<const __nv_bfloat16*>(prev_out);

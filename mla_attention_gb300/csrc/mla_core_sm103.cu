@@ -74,10 +74,10 @@ struct Bars {
   // O-CTA
   uint64_t o_kv_full[kStagesO], o_kv_empty[kStagesO];
   uint64_t p_full[2];       // arrived remotely by the S-CTA rows
-  uint64_t pb_free[2], p_ready[2];
-  uint64_t pv_done;
+  uint64_t pb_free[2], p_ready[2];  // pb_free[b]: the P V that read local P buffer b is complete
   uint64_t stats_full;      // arrived remotely by the S-CTA rows
   uint64_t o_free;
+  uint64_t stall;           // fault injection: never arrived on
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
@@ -86,7 +86,7 @@ static_assert(sizeof(Bars) <= 512, "barrier block too large");
 // wait-site ids (device status word detail)
 enum : uint32_t {
   W_S_KV_EMPTY = 1, W_S_KV_FULL, W_S_SFREE, W_S_QFULL, W_S_SFULL, W_S_PFREE, W_S_STATSFREE,
-  W_O_KV_EMPTY, W_O_KV_FULL, W_O_PREADY, W_O_PFULL, W_O_PBFREE, W_O_PVDONE, W_O_STATSFULL, W_O_OFREE,
+  W_O_KV_EMPTY, W_O_KV_FULL, W_O_PREADY, W_O_PFULL, W_O_PBFREE, W_O_PVDONE, W_O_STATSFULL, W_O_OFREE, W_STALL,
   R_PAGE = 0x40, R_LEN = 0x41,
 };
 
@@ -200,9 +200,12 @@ __device__ __forceinline__ void gather4(uint32_t dst, const CUtensorMap* map, in
       : "memory");
 }
 
-// rows[i] for i in 0..63 held by lanes: lane l holds rows 2l and 2l+1
+// rows[i] for i in 0..63 held by lanes: lane l holds rows 2l and 2l+1.  Column
+// boxes 0..7 come from map_lat at x = 64*box; box 8 (the RoPE columns) from
+// map_pe at x = pe_x (512 on a [rows, 576] cache, 0 on a separate [rows, 64] tensor).
 __device__ __forceinline__ void issue_gather_tile(uint32_t dst, const CUtensorMap* map_lat, const CUtensorMap* map_pe,
-                                                  int nboxes, int32_t r_even, int32_t r_odd, uint64_t* bar) {
+                                                  int32_t pe_x, int nboxes, int32_t r_even, int32_t r_odd,
+                                                  uint64_t* bar) {
   const int lane = threadIdx.x & 31;
   // lane g (0..15) issues rows 4g..4g+3 = lanes 2g, 2g+1 (even/odd each)
   const int32_t a0 = __shfl_sync(0xffffffffu, r_even, (2 * lane) & 31);
@@ -212,7 +215,7 @@ __device__ __forceinline__ void issue_gather_tile(uint32_t dst, const CUtensorMa
   if (lane < 16) {
     for (int bx = 0; bx < nboxes; ++bx) {
       const CUtensorMap* m = (bx < kVBoxes) ? map_lat : map_pe;
-      const int32_t x = (bx < kVBoxes) ? bx * kBoxCols : 0;
+      const int32_t x = (bx < kVBoxes) ? bx * kBoxCols : pe_x;
       gather4(dst + bx * kBoxBytes + lane * 512, m, x, a0, a1, a2, a3, bar);
     }
   }
@@ -261,10 +264,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(&bars.pb_free[i], 1);
         mbar_init(&bars.p_ready[i], kRows);
       }
-      mbar_init(&bars.pv_done, 1);
       mbar_init(&bars.stats_full, kRows);
       mbar_init(&bars.o_free, kRows);
     }
+    mbar_init(&bars.stall, 1);
     bars.abort_flag = 0;
     fence_mbar_init();
   }
@@ -317,6 +320,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   ItemIter iter;
   iter.init(p, pair);
   Item it;
+  if (p.debug_stall && warp == 5) waitb(&bars.stall, 0, W_STALL, false);  // runs out: injected fault
 
   if (is_s) {
     // =====================================================================
@@ -378,7 +382,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int bx = 0; bx < kKBoxes; ++bx)
                   tma_load_2d(dst + bx * kBoxBytes, &map_kv, bx * kBoxCols, ytile, &bars.s_kv_full[s]);
             } else {
-              issue_gather_tile(dst, &map_row, &map_pe, kKBoxes, re, ro, &bars.s_kv_full[s]);
+              issue_gather_tile(dst, &map_row, &map_pe, p.mode == MODE_DECODE ? kLatent : 0, kKBoxes, re, ro,
+                                &bars.s_kv_full[s]);
             }
           }
           __syncwarp();
@@ -387,9 +392,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp == 5) {
       // ---------------- MMA issuer: S = Q K^T ----------------
       const uint32_t idesc = idesc_bf16_f32(kRows, kKeys, false, false);
-      uint32_t g = 0, i = 0;
+      uint32_t g = 0, i = 0;  // i counts items that have KV tiles
       bool live = true;
       while (live && iter.next(it)) {
+        if (it.J == 0) continue;  // no key: the O-CTA writes these rows on its own
         if (!waitb(&bars.q_full, i & 1, W_S_QFULL, false)) break;
         for (int j = 0; j < it.J; ++j, ++g) {
           const int s = g % kStagesS;
@@ -425,9 +431,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t rem_p_full0 = map_to_rank(smem_u32(&bars.p_full[0]), peer);
       const uint32_t rem_p_full1 = map_to_rank(smem_u32(&bars.p_full[1]), peer);
       const uint32_t rem_stats_full = map_to_rank(smem_u32(&bars.stats_full), peer);
-      uint32_t g = 0, i = 0;
+      uint32_t g = 0, i = 0;  // i counts items that have KV tiles
       bool live = true;
       while (live && iter.next(it)) {
+        if (it.J == 0) continue;  // no key: the O-CTA writes these rows on its own
         // ---- this row's query and key limit ----
         const __nv_bfloat16* qrow = nullptr;
         const __nv_bfloat16* qpe = nullptr;
@@ -619,7 +626,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int bx = 0; bx < kVBoxes; ++bx)
                   tma_load_2d(dst + bx * kBoxBytes, &map_kv, bx * kBoxCols, ytile, &bars.o_kv_full[s]);
             } else {
-              issue_gather_tile(dst, &map_row, &map_pe, kVBoxes, re, ro, &bars.o_kv_full[s]);
+              issue_gather_tile(dst, &map_row, &map_pe, 0, kVBoxes, re, ro, &bars.o_kv_full[s]);
             }
           }
           __syncwarp();
@@ -628,9 +635,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp == 5) {
       // ---------------- MMA issuer: O += P V ----------------
       const uint32_t idesc = idesc_bf16_f32(kRows, 256, false, true);
-      uint32_t g = 0, i = 0;
+      uint32_t g = 0, i = 0;  // i counts items that have KV tiles
       bool live = true;
       while (live && iter.next(it)) {
+        if (it.J == 0) continue;
         if (i > 0 && !waitb(&bars.o_free, (i - 1) & 1, W_O_OFREE, false)) break;
         for (int j = 0; j < it.J; ++j, ++g) {
           const int s = g % kStagesO;
@@ -655,7 +663,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             mma_commit(&bars.o_kv_empty[s]);
             mma_commit(&bars.pb_free[pb]);
-            mma_commit(&bars.pv_done);
           }
           __syncwarp();
         }
@@ -699,8 +706,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           mbar_arrive_remote(pb ? rem_p_free1 : rem_p_free0);
           // tcgen05.ld/st are warp-collective: rescale when any row of the warp needs it
           if (__any_sync(0xffffffffu, a != 1.f)) {
-            // O must hold every earlier P V before it is rescaled
-            if (!waitb(&bars.pv_done, (g - 1) & 1, W_O_PVDONE, false)) { live = false; break; }
+            // O must hold every earlier P V before it is rescaled: PV(g-1) is use
+            // (g-1)/2 of P buffer (g-1)%2, and no later use of that buffer can start yet
+            if (!waitb(&bars.pb_free[(g - 1) & 1], ((g - 1) >> 1) & 1, W_O_PVDONE, false)) { live = false; break; }
             tc_fence_after();
 #pragma unroll 1
             for (int c0 = 0; c0 < kLatent; c0 += 32) {
@@ -718,13 +726,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (!live) break;
         // ---- epilogue ----
-        if (!waitb(&bars.stats_full, i & 1, W_O_STATSFULL, true)) break;
-        float m_used, l;
-        asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(m_used) : "r"(rem_stats + r * 8));
-        asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(l) : "r"(rem_stats + r * 8 + 4));
-        mbar_arrive_remote(rem_stats_free);
+        float m_used = -CUDART_INF_F, l = 0.f;
         if (it.J > 0) {
-          if (!waitb(&bars.pv_done, (g - 1) & 1, W_O_PVDONE, false)) break;
+          if (!waitb(&bars.stats_full, i & 1, W_O_STATSFULL, true)) break;
+          asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(m_used) : "r"(rem_stats + r * 8));
+          asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(l) : "r"(rem_stats + r * 8 + 4));
+          mbar_arrive_remote(rem_stats_free);
+          // the last P V of the item: use (g-1)/2 of P buffer (g-1)%2
+          if (!waitb(&bars.pb_free[(g - 1) & 1], ((g - 1) >> 1) & 1, W_O_PVDONE, false)) break;
           tc_fence_after();
         }
         const bool has = (it.J > 0) && (l > 0.f);
@@ -824,9 +833,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           if (row_ok && lse_dst) *lse_dst = lse_out;
         }
-        tc_fence_before();
-        mbar_arrive(&bars.o_free);
-        ++i;
+        if (it.J > 0) {
+          tc_fence_before();
+          mbar_arrive(&bars.o_free);
+          ++i;
+        }
       }
     }
   }

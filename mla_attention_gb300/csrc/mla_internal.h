@@ -30,6 +30,7 @@ constexpr size_t kWsHeader = 256;       // [0]: device status word
 constexpr uint32_t kDefaultSpinLimit = 1u << 25;
 
 uint32_t spin_limit();                  // process-wide bound for device waits
+uint32_t debug_stall();                 // 1: kernels wait on a barrier nothing arrives on (tests)
 
 // kinds of work the absorbed tile engine runs
 enum CoreMode : int { MODE_PREFILL = 0, MODE_DECODE = 1, MODE_SPARSE = 2 };
@@ -39,6 +40,7 @@ struct CoreParams {
   int num_pairs;          // CTA pairs in the grid (cluster of 2 per pair)
   float scale_log2;       // scale * log2(e)
   uint32_t spin_limit;
+  uint32_t debug_stall;   // tests: the MMA warps wait on a barrier that is never arrived on
   uint32_t* err;          // device status word
 
   // ---- query rows ----
@@ -94,6 +96,7 @@ struct SplitParams {
   float scale_log2;
   int causal;
   uint32_t spin_limit;
+  uint32_t debug_stall;
   uint32_t* err;
   int total_q_tiles;           // sum over sequences of ceil(q_len / 128)
   const __nv_bfloat16* prev_out;

@@ -48,12 +48,13 @@ struct Bars {
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t s_full[2];
   uint64_t p_full[2];
-  uint64_t o_done;
+  uint64_t pv_done[2];  // pv_done[b]: the P V that read P from S buffer b is complete
+  uint64_t stall;  // fault injection: never arrived on
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
 
-enum : uint32_t { W_QFULL = 0x20, W_KVEMPTY, W_KVFULL, W_SFULL, W_PFULL, W_ODONE };
+enum : uint32_t { W_QFULL = 0x20, W_KVEMPTY, W_KVFULL, W_SFULL, W_PFULL, W_ODONE, W_STALL };
 
 struct TileInfo {
   int seq, tile, h, hk;
@@ -112,7 +113,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.s_full[i], 1);
       mbar_init(&bars.p_full[i], kTile);
     }
-    mbar_init(&bars.o_done, 1);
+    mbar_init(&bars.pv_done[0], 1);
+    mbar_init(&bars.pv_done[1], 1);
+    mbar_init(&bars.stall, 1);
     bars.abort_flag = 0;
     fence_mbar_init();
   }
@@ -134,6 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     return ok;
   };
   const int qz = ti.q0 + ti.tile * kTile;  // first query token of the tile
+  if (p.debug_stall && warp == 5) waitb(&bars.stall, 0, W_STALL);  // runs out: injected fault
 
   if (warp == 4) {
     // ---------------- TMA producer ----------------
@@ -196,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts(tbase + kTmemO, pa + ks * 8, sdesc_sw128(vst + ks * 2048, kBox, 1024), idesc_o,
                  (j > 0 || ks > 0) ? 1u : 0u);
         mma_commit(&bars.kv_empty[s]);
-        mma_commit(&bars.o_done);
+        mma_commit(&bars.pv_done[j & 1]);
       }
       __syncwarp();
     }
@@ -237,8 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // tcgen05.ld/st are warp-collective: rescale when any row of the warp needs it
       if (__any_sync(0xffffffffu, a != 1.f)) {
-        // O must hold P V of every earlier tile before it is rescaled
-        if (!waitb(&bars.o_done, (j - 1) & 1, W_ODONE)) { live = false; break; }
+        // O must hold P V of every earlier tile before it is rescaled: PV(j-1) is
+        // use (j-1)/2 of buffer (j-1)%2 and the next use of that buffer needs P(j+1)
+        if (!waitb(&bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, W_ODONE)) { live = false; break; }
         tc_fence_after();
         const uint32_t oa = tbase + lane_base + kTmemO;
 #pragma unroll 1
@@ -272,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ---- epilogue ----
     if (live && ti.J > 0) {
-      live = waitb(&bars.o_done, (ti.J - 1) & 1, W_ODONE);
+      live = waitb(&bars.pv_done[(ti.J - 1) & 1], ((ti.J - 1) >> 1) & 1, W_ODONE);
       tc_fence_after();
     }
     if (live) {

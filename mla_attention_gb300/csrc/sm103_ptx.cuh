@@ -100,20 +100,38 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t addr, uint32_t pa
   return ok != 0;
 }
 
-// Bounded wait.  Returns false (and records `site`) when the bound is hit or
-// when another thread already raised an error.
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Longest any single wait may last, whatever the spin bound (2 s).
+constexpr uint64_t kWaitWallNs = 2000000000ull;
+
+// Bounded wait.  Returns false (and records `site`) when `spin_limit` tries
+// or kWaitWallNs of wall time have passed, or when another thread already
+// raised an error.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t site,
                                           uint32_t spin_limit, bool cluster_scope = false) {
   const uint32_t a = smem_u32(bar);
   uint32_t n = 0;
+  uint64_t t0 = 0;
   while (true) {
     bool ok = cluster_scope ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity);
     if (ok) return true;
-    if (++n >= spin_limit) {
+    ++n;
+    bool expired = n >= spin_limit;
+    if ((n & 255u) == 1u) {
+      const uint64_t now = global_ns();
+      if (n == 1u) t0 = now;
+      else if (now - t0 > kWaitWallNs) expired = true;
+      if (n > 1u && error_raised(err)) return false;
+    }
+    if (expired) {
       record_error(err, DEV_TIMEOUT_BASE | site);
       return false;
     }
-    if ((n & 1023u) == 0 && error_raised(err)) return false;
   }
 }
 

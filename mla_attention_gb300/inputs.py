@@ -215,3 +215,14 @@ def sample_rows(n: int, count: int, seed: int, must=()) -> list:
         return list(range(n))
     extra = torch.randperm(n, generator=g)[: max(0, count - len(base))].tolist()
     return sorted(base.union(int(x) for x in extra))
+
+
+def randn_bf16_device(shape, seed: int, device) -> torch.Tensor:
+    """fp32 N(0,1) rounded to bf16, drawn on the device by a seeded CUDA generator.
+
+    Same distribution as randn_bf16, used for full-size timing inputs that the
+    CPU generator would take tens of seconds to draw.
+    """
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)

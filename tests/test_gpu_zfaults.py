@@ -1,45 +1,54 @@
-"""Failure detection without a GPU fault: a bound on every device wait turns a wait that
-cannot finish into MLA_ERR_TIMEOUT, and the context stays usable afterwards."""
+"""Failure detection without a GPU fault.  A wait that cannot finish (a barrier that
+nothing arrives on, switched on from the host) runs out of its bound; the kernel
+records MLA_ERR_TIMEOUT, drains and exits; the context stays usable afterwards."""
 import pytest
 import torch
 
 from mla_attention_gb300 import inputs as gen
-from mla_attention_gb300 import MLAError, check_device_status, mla_prefill, mla_prefill_split, set_spin_limit
+from mla_attention_gb300 import (MLAError, check_device_status, inject_stall, mla_decode, mla_prefill,
+                                 mla_prefill_split, set_spin_limit)
 from tests.helpers import dev
 
 pytestmark = pytest.mark.gpu
 
 
-def test_wait_bound_reports_timeout_and_context_survives():
-    P = gen.prefill_inputs(T=64, H=128, Tkv=256, seed=1)
-    q, kv = P.q.to(dev()), P.kv.to(dev())
+def _expect_timeout(run):
     check_device_status()
-    set_spin_limit(1)
+    set_spin_limit(4096)
+    inject_stall(True)
     try:
-        mla_prefill(q, kv, P.scale, q_pos0=192)
+        run()
         torch.cuda.synchronize()
     finally:
+        inject_stall(False)
         set_spin_limit(0)
     with pytest.raises(MLAError) as e:
         check_device_status()
     assert e.value.status == 4
-    # the same call with the default bound succeeds on the same context
+    check_device_status()   # the word was cleared
+
+
+def test_core_kernel_timeout_and_context_survives():
+    P = gen.prefill_inputs(T=64, H=128, Tkv=256, seed=1)
+    q, kv = P.q.to(dev()), P.kv.to(dev())
+    _expect_timeout(lambda: mla_prefill(q, kv, P.scale, q_pos0=192))
     out, lse = mla_prefill(q, kv, P.scale, q_pos0=192)
     torch.cuda.synchronize()
     check_device_status()
     assert torch.isfinite(out.float()).all()
 
 
-def test_split_wait_bound_reports_timeout():
+def test_split_kernel_timeout():
     si = gen.split_inputs([300], [300], 2, 2, seed=2)
     d = dev()
-    set_spin_limit(1)
-    try:
-        mla_prefill_split(si.q_nope.to(d), si.q_pe.to(d), si.k_nope.to(d), si.k_pe.to(d), si.v.to(d), si.seq_len,
-                          2, 2, si.scale, 1)
-        torch.cuda.synchronize()
-    finally:
-        set_spin_limit(0)
-    with pytest.raises(MLAError) as e:
-        check_device_status()
-    assert e.value.status == 4
+    args = [si.q_nope.to(d), si.q_pe.to(d), si.k_nope.to(d), si.k_pe.to(d), si.v.to(d), si.seq_len, 2, 2, si.scale, 1]
+    _expect_timeout(lambda: mla_prefill_split(*args))
+    mla_prefill_split(*args)
+    torch.cuda.synchronize()
+    check_device_status()
+
+
+def test_decode_timeout():
+    D = gen.decode_inputs([200, 70], H=16, seed=3)
+    a = [D.q.to(dev()), D.cache.to(dev()), D.block_table.to(dev()), D.lens.to(dev()), D.scale]
+    _expect_timeout(lambda: mla_decode(*a))
