@@ -417,6 +417,47 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_profile_case(kind: str):
+    """Small cases for ncu (inputs larger than L2, a few GB at most): one warm-up launch, then one launch."""
+    import mla_attention_gb300 as lib
+    from mla_attention_gb300 import inputs as gen
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if kind == "prefill":
+        T = 2048
+        q = gen.randn_bf16_device((T, H, DK), 71, dev)
+        kv = gen.randn_bf16_device((T, DK), 72, dev)
+        po = gen.randn_bf16_device((T, H, DV), 73, dev)
+        pl = torch.full((H, T), 5.0, device=dev)
+        fn = lambda: lib.mla_prefill(q, kv, SCALE, causal=True, q_pos0=T, kv_pos0=0,  # noqa: E731
+                                     prev_out=po, prev_lse=pl, out=po, lse=pl)
+    elif kind == "decode":
+        measure_decode(lib, dev, load_peaks()[0], steps=1, warmup=1)
+        return
+    elif kind == "sparse":
+        S, S_kv, K = 512, 32768, 2048
+        q_lift = gen.randn_bf16_device((1, S, H, 512), 51, dev)
+        q_pe = gen.randn_bf16_device((1, S, H, 64), 52, dev)
+        c_kv = gen.randn_bf16_device((1, S_kv, 512), 53, dev)
+        k_pe = gen.randn_bf16_device((1, S_kv, 64), 54, dev)
+        g = torch.Generator(device=dev)
+        g.manual_seed(55)
+        topk = torch.randint(0, S_kv, (1, S, K), generator=g, device=dev, dtype=torch.int32)
+        fn = lambda: lib.mla_sparse(q_lift, q_pe, c_kv, k_pe, topk, SCALE)  # noqa: E731
+    else:
+        lens = [4096, 4096]
+        N = sum(lens)
+        t = [gen.randn_bf16_device(s, 80 + i, dev) for i, s in enumerate(
+            [(N, H, 128), (N, H, 64), (N, H, 128), (N, H, 64), (N, H, 128)])]
+        seq = torch.tensor([lens, lens], dtype=torch.int32)
+        fn = lambda: lib.mla_prefill_split(*t, seq, H, H, SCALE, 1)  # noqa: E731
+    fn()
+    torch.cuda.synchronize()
+    fn()
+    torch.cuda.synchronize()
+    lib.check_device_status()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -426,7 +467,12 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the decode/sparse/split lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--profile", choices=["prefill", "decode", "sparse", "split"], default=None,
+                    help="run one small case of a kernel for ncu and exit (prints no JSON)")
     args = ap.parse_args()
+    if args.profile:
+        run_profile_case(args.profile)
+        return
     if args.warmup < 3:
         args.warmup = 3
     world, rank, local = dist_setup()

@@ -188,6 +188,34 @@ struct ItemIter {
   }
 };
 
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
+// The query row (and for sparse its RoPE part) that row r of item `it` reads.
+__device__ __forceinline__ bool query_row(const CoreParams& p, const Item& it, int r, const __nv_bfloat16*& qrow,
+                                          const __nv_bfloat16*& qpe, int64_t& nkeys) {
+  qrow = nullptr;
+  qpe = nullptr;
+  nkeys = 0;
+  if (p.mode == MODE_PREFILL) {
+    const int64_t f = (int64_t)it.id * kRows + r;
+    if (f >= (int64_t)p.T * p.H) return false;
+    const int64_t t = f / p.H, h = f - t * p.H;
+    qrow = p.q + t * p.q_stride_t + h * p.q_stride_h;
+    nkeys = prefill_keys_for_token(p, t);
+    return true;
+  }
+  if (r >= p.H) return false;
+  if (p.mode == MODE_DECODE) {
+    qrow = p.q + ((int64_t)it.id * p.H + r) * kDk;
+  } else {
+    qrow = p.q + ((int64_t)it.id * p.H + r) * kLatent;
+    qpe = p.q_pe + ((int64_t)it.id * p.H + r) * kRope;
+  }
+  return true;
+}
+
 // ---------------------------------------------------------------------------
 // KV tile loaders (producer warp).  `dst` is a stage base; boxes [b0, b1).
 // ---------------------------------------------------------------------------
@@ -436,50 +464,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       while (live && iter.next(it)) {
         if (it.J == 0) continue;  // no key: the O-CTA writes these rows on its own
         // ---- this row's query and key limit ----
-        const __nv_bfloat16* qrow = nullptr;
-        const __nv_bfloat16* qpe = nullptr;
-        int64_t nkeys = 0;  // prefill: keys visible to the row
-        bool row_ok = false;
-        if (p.mode == MODE_PREFILL) {
-          const int64_t f = (int64_t)it.id * kRows + r;
-          if (f < (int64_t)p.T * p.H) {
-            const int64_t t = f / p.H, h = f - t * p.H;
-            qrow = p.q + t * p.q_stride_t + h * p.q_stride_h;
-            nkeys = prefill_keys_for_token(p, t);
-            row_ok = true;
+        const __nv_bfloat16* qrow;
+        const __nv_bfloat16* qpe;
+        int64_t nkeys;  // prefill: keys visible to the row
+        const bool row_ok = query_row(p, it, r, qrow, qpe, nkeys);
+        // warm L2 with the next item's query row while this item runs
+        {
+          ItemIter peek = iter;
+          Item nx;
+          bool found = false;
+          while (peek.next(nx)) {
+            if (nx.J > 0) {
+              found = true;
+              break;
+            }
           }
-        } else if (p.mode == MODE_DECODE) {
-          if (r < p.H) {
-            qrow = p.q + ((int64_t)it.id * p.H + r) * kDk;
-            row_ok = true;
-          }
-        } else {
-          if (r < p.H) {
-            qrow = p.q + ((int64_t)it.id * p.H + r) * kLatent;
-            qpe = p.q_pe + ((int64_t)it.id * p.H + r) * kRope;
-            row_ok = true;
+          const __nv_bfloat16 *nq, *npe;
+          int64_t nk;
+          if (found && query_row(p, nx, r, nq, npe, nk)) {
+            const char* b = reinterpret_cast<const char*>(nq);
+            const int nbytes = (p.mode == MODE_SPARSE) ? kLatent * 2 : kDk * 2;
+            for (int o = 0; o < nbytes; o += 128) prefetch_l2(b + o);
+            if (npe) prefetch_l2(npe);
           }
         }
-        // ---- Q -> TMEM (bf16 pairs, K-contiguous): 9 chunks of 64 columns ----
+        // ---- Q -> TMEM (bf16 pairs, K-contiguous): 9 chunks of 64 columns, 3 in flight ----
 #pragma unroll 1
-        for (int c = 0; c < kDk / 64; ++c) {
-          uint32_t v[32];
-          const uint4* src = nullptr;
-          if (row_ok) {
-            if (p.mode == MODE_SPARSE)
-              src = (c < 8) ? reinterpret_cast<const uint4*>(qrow + c * 64) : reinterpret_cast<const uint4*>(qpe);
-            else
-              src = reinterpret_cast<const uint4*>(qrow + c * 64);
+        for (int c0 = 0; c0 < kDk / 64; c0 += 3) {
+          uint4 x[3][8];
+#pragma unroll
+          for (int cc = 0; cc < 3; ++cc) {
+            const int c = c0 + cc;
+            const uint4* src = nullptr;
+            if (row_ok) {
+              if (p.mode == MODE_SPARSE)
+                src = (c < 8) ? reinterpret_cast<const uint4*>(qrow + c * 64) : reinterpret_cast<const uint4*>(qpe);
+              else
+                src = reinterpret_cast<const uint4*>(qrow + c * 64);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) x[cc][u] = src ? __ldg(src + u) : make_uint4(0, 0, 0, 0);
           }
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            uint4 x = src ? __ldg(src + u) : make_uint4(0, 0, 0, 0);
-            v[4 * u + 0] = x.x;
-            v[4 * u + 1] = x.y;
-            v[4 * u + 2] = x.z;
-            v[4 * u + 3] = x.w;
+          for (int cc = 0; cc < 3; ++cc) {
+            uint32_t v[32];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              v[4 * u + 0] = x[cc][u].x;
+              v[4 * u + 1] = x[cc][u].y;
+              v[4 * u + 2] = x[cc][u].z;
+              v[4 * u + 3] = x[cc][u].w;
+            }
+            tmem_st32(tbase + lane_base + kTmemQ + (c0 + cc) * 32, v);
           }
-          tmem_st32(tbase + lane_base + kTmemQ + c * 32, v);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -682,6 +719,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t g = 0, i = 0;
       bool live = true;
       while (live && iter.next(it)) {
+        if (p.mode == MODE_PREFILL && p.prev_out) {  // warm L2 with this row's previous output
+          const int64_t f = (int64_t)it.id * kRows + r;
+          if (f < (int64_t)p.T * p.H) {
+            const char* b = reinterpret_cast<const char*>(p.prev_out + f * kLatent);
+            for (int o = 0; o < kLatent * 2; o += 128) prefetch_l2(b + o);
+          }
+        }
         for (int j = 0; j < it.J; ++j, ++g) {
           const int pb = g & 1;
           if (!waitb(&bars.p_full[pb], (g >> 1) & 1, W_O_PFULL, true) ||
@@ -791,8 +835,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
           }
           const float cn = wn * inv_l;
+          const bool use_prev = row_ok && prev_row && wp > 0.f;
 #pragma unroll 1
-          for (int c0 = 0; c0 < kLatent; c0 += 32) {
+          for (int c1 = 0; c1 < kLatent; c1 += 128) {
+            // the previous output for 128 columns: 16 loads in flight
+            uint4 pv[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+              pv[u] = use_prev ? reinterpret_cast<const uint4*>(prev_row + c1)[u] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int c2 = 0; c2 < 128; c2 += 32) {
+            const int c0 = c1 + c2;
             float o[32];
             if (it.J > 0) {  // uniform over the CTA: every lane takes part in the TMEM load
               uint32_t v[32];
@@ -805,11 +858,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               for (int c = 0; c < 32; ++c) o[c] = 0.f;
             }
             if (!row_ok) continue;
-            if (prev_row && wp > 0.f) {
-              const uint4* pr = reinterpret_cast<const uint4*>(prev_row + c0);
+            if (use_prev) {
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
-                uint4 x = pr[u];
+                const uint4 x = pv[(c2 >> 3) + u];
                 const __nv_bfloat162* hx = reinterpret_cast<const __nv_bfloat162*>(&x);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
@@ -830,6 +882,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int u = 0; u < 8; ++u) dst[u] = make_float4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
             }
+          }
           }
           if (row_ok && lse_dst) *lse_dst = lse_out;
         }
