@@ -192,10 +192,16 @@ mla_status mla_prefill(const void* q, int64_t q_stride_t, int64_t q_stride_h, co
                 "mla_prefill: kv must be 16-byte aligned with kv_stride a multiple of 8 and >= 576");
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  CUtensorMap mkv;
-  memset(&mkv, 0, sizeof(mkv));
+  CoreMaps maps;
+  memset(&maps, 0, sizeof(maps));
   if (kv_valid > 0) {
-    mla_status s = map2d(&mkv, kv, kDk, (uint64_t)kv_valid, (uint64_t)kv_stride, kKeys, "kv");
+    mla_status s = map2d(&maps.kv, kv, kDk, (uint64_t)kv_valid, (uint64_t)kv_stride, kKeys, "kv");
+    if (s != MLA_OK) return s;
+  }
+  {
+    const uint64_t rows = (uint64_t)T * (uint64_t)H;
+    mla_status s = map2d(&maps.out, out, kLatent, rows, kLatent, 64, "out");
+    if (s == MLA_OK && prev_out) s = map2d(&maps.prev, prev_out, kLatent, rows, kLatent, 64, "prev_out");
     if (s != MLA_OK) return s;
   }
   CoreParams p;
@@ -221,7 +227,7 @@ mla_status mla_prefill(const void* q, int64_t q_stride_t, int64_t q_stride_h, co
   p.lse = lse;
   const int64_t items = ((int64_t)T * H + kRows - 1) / kRows;
   if (items < p.num_pairs) p.num_pairs = (int)items;
-  cudaError_t e = launch_core(p, mkv, mkv, mkv, st);
+  cudaError_t e = launch_core(p, maps, st);
   if (e != cudaSuccess) return cuda_fail(e, "mla_prefill launch");
   return ok();
 }
@@ -254,12 +260,14 @@ mla_status mla_decode(const void* q, const void* kv_cache, int64_t num_pages, in
   MLA_REQUIRE(aligned16(q) && aligned16(kv_cache) && aligned16(out), "mla_decode: q, kv_cache, out 16-byte aligned");
   MLA_REQUIRE(num_pages >= 1 && max_pages >= 1, "mla_decode: need at least one page");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  CUtensorMap mtile, mrow;
+  CoreMaps maps;
+  memset(&maps, 0, sizeof(maps));
   const uint64_t rows = (uint64_t)num_pages * (uint64_t)page_size;
-  mla_status s = map2d(&mtile, kv_cache, kDk, rows, kDk, page_size >= kKeys ? kKeys : (uint32_t)page_size, "cache");
+  mla_status s = map2d(&maps.kv, kv_cache, kDk, rows, kDk, page_size >= kKeys ? kKeys : (uint32_t)page_size, "cache");
   if (s != MLA_OK) return s;
-  s = map2d(&mrow, kv_cache, kDk, rows, kDk, 1, "cache rows");
+  s = map2d(&maps.row, kv_cache, kDk, rows, kDk, 1, "cache rows");
   if (s != MLA_OK) return s;
+  maps.pe = maps.row;
   CoreParams p;
   memset(&p, 0, sizeof(p));
   p.mode = MODE_DECODE;
@@ -283,7 +291,7 @@ mla_status mla_decode(const void* q, const void* kv_cache, int64_t num_pages, in
   p.part_lse = reinterpret_cast<float*>(w);
   w += align_up(sizeof(float) * slots * (size_t)H, 256);
   p.part_o = reinterpret_cast<float*>(w);
-  cudaError_t e = launch_core(p, mtile, mrow, mrow, st);
+  cudaError_t e = launch_core(p, maps, st);
   if (e != cudaSuccess) return cuda_fail(e, "mla_decode launch");
   e = launch_decode_reduce(p, reinterpret_cast<__nv_bfloat16*>(out), lse, st);
   if (e != cudaSuccess) return cuda_fail(e, "mla_decode reduce launch");
@@ -311,11 +319,15 @@ mla_status mla_sparse(const void* q_lift, const void* q_pe, const void* c_kv, co
   MLA_REQUIRE(aligned16(q_lift) && aligned16(q_pe) && aligned16(c_kv) && aligned16(k_pe) && aligned16(out),
               "mla_sparse: tensors must be 16-byte aligned");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  CUtensorMap mlat, mpe;
-  mla_status s = map2d(&mlat, c_kv, kLatent, (uint64_t)S_kv, kLatent, 1, "c_kv");
+  CoreMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  mla_status s = map2d(&maps.row, c_kv, kLatent, (uint64_t)S_kv, kLatent, 1, "c_kv");
   if (s != MLA_OK) return s;
-  s = map2d(&mpe, k_pe, kRope, (uint64_t)S_kv, kRope, 1, "k_pe");
+  s = map2d(&maps.pe, k_pe, kRope, (uint64_t)S_kv, kRope, 1, "k_pe");
   if (s != MLA_OK) return s;
+  s = map2d(&maps.out, out, kLatent, (uint64_t)S * (uint64_t)H, kLatent, 64, "out");
+  if (s != MLA_OK) return s;
+  maps.kv = maps.row;
   CoreParams p;
   memset(&p, 0, sizeof(p));
   p.mode = MODE_SPARSE;
@@ -334,7 +346,7 @@ mla_status mla_sparse(const void* q_lift, const void* q_pe, const void* c_kv, co
   p.topk = topk;
   p.K = K;
   p.S_kv = S_kv;
-  cudaError_t e = launch_core(p, mlat, mlat, mpe, st);
+  cudaError_t e = launch_core(p, maps, st);
   if (e != cudaSuccess) return cuda_fail(e, "mla_sparse launch");
   return ok();
 }

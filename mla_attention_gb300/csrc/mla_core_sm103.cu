@@ -154,6 +154,11 @@ struct ItemIter {
       const int64_t n = prefill_keys_for_token(P, last / P.H);
       it.id = (int)id;
       it.J = (int)((n + kKeys - 1) / kKeys);
+      // In place, a row that sees no key keeps its previous (out, lse) exactly; J only
+      // falls along this order (causal) or is constant, so the rest of the list is done.
+      if (it.J == 0 && P.prev_out && (const void*)P.prev_out == (const void*)P.out &&
+          (const void*)P.prev_lse == (const void*)P.lse)
+        return false;
       return true;
     }
     if (P.mode == MODE_SPARSE) {
@@ -163,7 +168,8 @@ struct ItemIter {
       k += P.num_pairs;
       return true;
     }
-    // decode: segments of requests overlapping [lo, hi)
+    // decode: segments of requests overlapping [lo, hi); an empty share has none
+    if (hi <= lo) return false;
     while (b < P.B) {
       const int len = decode_len(P, b);
       const int64_t nt = (len + kKeys - 1) / kKeys;
@@ -177,6 +183,7 @@ struct ItemIter {
         return false;
       }
       const int64_t t0 = (s > lo ? s : lo) - s, t1 = (e < hi ? e : hi) - s;
+      if (t1 <= t0) continue;
       it.id = cur;
       it.J = (int)(t1 - t0);
       it.k0 = t0 * kKeys;
@@ -187,6 +194,21 @@ struct ItemIter {
     return false;
   }
 };
+
+__device__ __forceinline__ void tma_store_2d(const void* tmap, int32_t x, int32_t y, uint32_t src_smem) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(x), "r"(y), "r"(src_smem)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 
 __device__ __forceinline__ void prefetch_l2(const void* ptr) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
@@ -253,8 +275,17 @@ __device__ __forceinline__ void issue_gather_tile(uint32_t dst, const CUtensorMa
 // the kernel
 // ---------------------------------------------------------------------------
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mla_core_kernel(const __grid_constant__ CoreParams p, const __grid_constant__ CUtensorMap map_kv,
-                    const __grid_constant__ CUtensorMap map_row, const __grid_constant__ CUtensorMap map_pe) {
+    mla_core_kernel(const __grid_constant__ CoreParams p, const __grid_constant__ CoreMaps maps) {
+  const CUtensorMap& map_kv = maps.kv;
+  const CUtensorMap& map_row = maps.row;
+  const CUtensorMap& map_pe = maps.pe;
+  const CUtensorMap& map_out = maps.out;
+  const CUtensorMap& map_prev = maps.prev;
+  // Prefill (128 flat rows per tile) and sparse with H a multiple of 64 stage
+  // their output (and the previous output) through two V stages and TMA; decode
+  // writes fp32 partials directly, and other head counts write bf16 rows directly.
+  const bool staged = (p.mode == MODE_PREFILL) || (p.mode == MODE_SPARSE && (p.H % 64) == 0);
+  const int rows_per_item = (p.mode == MODE_PREFILL) ? kRows : p.H;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars& bars = *reinterpret_cast<Bars*>(smem + kOffBars);
@@ -307,6 +338,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&map_kv);
     tma_prefetch_desc(&map_row);
     tma_prefetch_desc(&map_pe);
+    if (staged) tma_prefetch_desc(&map_out);
+    if (staged && p.prev_out) tma_prefetch_desc(&map_prev);
   }
   // decode: publish the per-request tile prefix for the reduction kernel
   if (p.mode == MODE_DECODE && blockIdx.x == 0 && warp == 0) {
@@ -612,7 +645,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // =====================================================================
     if (warp == 4) {
       // ---------------- TMA producer: V tiles (first 512 columns) ----------------
-      uint32_t g = 0;
+      uint32_t g = 0;  // position in the stage ring
       bool live = true;
       while (live && iter.next(it)) {
         for (int j = 0; j < it.J && live; ++j, ++g) {
@@ -668,19 +701,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
         }
+        // two more ring stages stage the epilogue of this item: rows 0-63 and 64-127,
+        // holding the previous output when there is one
+        if (staged && it.J > 0) {
+          for (int hh = 0; hh < 2 && live; ++hh, ++g) {
+            const int s = g % kStagesO;
+            if (!waitb(&bars.o_kv_empty[s], ((g / kStagesO) & 1) ^ 1, W_O_KV_EMPTY, false)) { live = false; break; }
+            if (lane == 0) {
+              const int64_t row0 = (int64_t)it.id * kRows + hh * 64;
+              if (p.prev_out && row0 < (int64_t)p.T * p.H) {
+                const uint32_t dst = smem_u32(smem + kOffStages + s * kStageBytesO);
+                mbar_arrive_expect_tx(&bars.o_kv_full[s], kStageBytesO);
+                for (int bx = 0; bx < kVBoxes; ++bx)
+                  tma_load_2d(dst + bx * kBoxBytes, &map_prev, bx * kBoxCols, (int32_t)row0, &bars.o_kv_full[s]);
+              } else {
+                mbar_arrive(&bars.o_kv_full[s]);
+              }
+            }
+            __syncwarp();
+          }
+        }
       }
     } else if (warp == 5) {
       // ---------------- MMA issuer: O += P V ----------------
       const uint32_t idesc = idesc_bf16_f32(kRows, 256, false, true);
-      uint32_t g = 0, i = 0;  // i counts items that have KV tiles
+      uint32_t g = 0, gs = 0, i = 0;  // P tiles, stage ring position, items that have KV tiles
       bool live = true;
       while (live && iter.next(it)) {
         if (it.J == 0) continue;
         if (i > 0 && !waitb(&bars.o_free, (i - 1) & 1, W_O_OFREE, false)) break;
-        for (int j = 0; j < it.J; ++j, ++g) {
-          const int s = g % kStagesO;
+        for (int j = 0; j < it.J; ++j, ++g, ++gs) {
+          const int s = gs % kStagesO;
           const int pb = g & 1;
-          if (!waitb(&bars.o_kv_full[s], (g / kStagesO) & 1, W_O_KV_FULL, false) ||
+          if (!waitb(&bars.o_kv_full[s], (gs / kStagesO) & 1, W_O_KV_FULL, false) ||
               !waitb(&bars.p_ready[pb], (g >> 1) & 1, W_O_PREADY, false)) {
             live = false;
             break;
@@ -703,11 +756,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
         }
+        if (staged) gs += 2;  // the epilogue's two stages
         ++i;
       }
     } else {
       // ---------------- rows: P pull, lazy rescale, epilogue ----------------
       const int r = tid;
+      const int half = r >> 6;   // warps 0-1: rows 0-63, warps 2-3: rows 64-127
+      const int rr = r & 63;
       const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
       const uint32_t rem_pbuf = map_to_rank(smem_u32(smem + kOffPS), peer);
       const uint32_t rem_alpha = map_to_rank(smem_u32(smem + kOffAlpha), peer);
@@ -716,75 +772,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t rem_p_free1 = map_to_rank(smem_u32(&bars.p_free[1]), peer);
       const uint32_t rem_stats_free = map_to_rank(smem_u32(&bars.stats_free), peer);
       uint8_t* plocal = smem + kOffPO;
-      uint32_t g = 0, i = 0;
+      uint32_t g = 0, gs = 0, i = 0;  // P tiles, stage ring position, items that have KV tiles
       bool live = true;
+      bool stored = false;            // this thread issued TMA stores that must finish before exit
       while (live && iter.next(it)) {
-        if (p.mode == MODE_PREFILL && p.prev_out) {  // warm L2 with this row's previous output
-          const int64_t f = (int64_t)it.id * kRows + r;
-          if (f < (int64_t)p.T * p.H) {
-            const char* b = reinterpret_cast<const char*>(p.prev_out + f * kLatent);
-            for (int o = 0; o < kLatent * 2; o += 128) prefetch_l2(b + o);
-          }
-        }
-        for (int j = 0; j < it.J; ++j, ++g) {
-          const int pb = g & 1;
-          if (!waitb(&bars.p_full[pb], (g >> 1) & 1, W_O_PFULL, true) ||
-              !waitb(&bars.pb_free[pb], ((g >> 1) & 1) ^ 1, W_O_PBFREE, false)) {
-            live = false;
-            break;
-          }
-          // copy this row's 128 bytes of P (already in the swizzled K-major layout)
-          const uint32_t src = rem_pbuf + pb * kPBytes + r * 128;
-          uint8_t* dst = plocal + pb * kPBytes + r * 128;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint4 v;
-            asm volatile("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                         : "r"(src + c * 16));
-            *reinterpret_cast<uint4*>(dst + c * 16) = v;
-          }
-          float a;
-          asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(a) : "r"(rem_alpha + (pb * kRows + r) * 4));
-          fence_proxy_async_smem();
-          mbar_arrive_remote(pb ? rem_p_free1 : rem_p_free0);
-          // tcgen05.ld/st are warp-collective: rescale when any row of the warp needs it
-          if (__any_sync(0xffffffffu, a != 1.f)) {
-            // O must hold every earlier P V before it is rescaled: PV(g-1) is use
-            // (g-1)/2 of P buffer (g-1)%2, and no later use of that buffer can start yet
-            if (!waitb(&bars.pb_free[(g - 1) & 1], ((g - 1) >> 1) & 1, W_O_PVDONE, false)) { live = false; break; }
-            tc_fence_after();
-#pragma unroll 1
-            for (int c0 = 0; c0 < kLatent; c0 += 32) {
-              uint32_t v[32];
-              tmem_ld32(tbase + lane_base + c0, v);
-              tmem_wait_ld();
-#pragma unroll
-              for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * a);
-              tmem_st32(tbase + lane_base + c0, v);
-            }
-            tmem_wait_st();
-          }
-          tc_fence_before();
-          mbar_arrive(&bars.p_ready[pb]);
-        }
-        if (!live) break;
-        // ---- epilogue ----
-        float m_used = -CUDART_INF_F, l = 0.f;
-        if (it.J > 0) {
-          if (!waitb(&bars.stats_full, i & 1, W_O_STATSFULL, true)) break;
-          asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(m_used) : "r"(rem_stats + r * 8));
-          asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(l) : "r"(rem_stats + r * 8 + 4));
-          mbar_arrive_remote(rem_stats_free);
-          // the last P V of the item: use (g-1)/2 of P buffer (g-1)%2
-          if (!waitb(&bars.pb_free[(g - 1) & 1], ((g - 1) >> 1) & 1, W_O_PVDONE, false)) break;
-          tc_fence_after();
-        }
-        const bool has = (it.J > 0) && (l > 0.f);
-        const float inv_l = has ? 1.f / l : 0.f;
-        const float lse_new = has ? (m_used + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
-
-        // destination of this row
+        // ---- destination of this row ----
         bool row_ok = false;
         float prev_l = -CUDART_INF_F;
         const __nv_bfloat16* prev_row = nullptr;
@@ -816,82 +808,194 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             lse_dst = p.lse ? p.lse + (int64_t)it.id * p.H + r : nullptr;
           }
         }
-        {
-          // merge weights with the previous pair (weight 0 for an empty side)
-          float wn = has ? 1.f : 0.f, wp = 0.f, lse_out = lse_new;
-          if (row_ok && prev_row) {
-            const float m = fmaxf(prev_l, lse_new);
-            if (m == -CUDART_INF_F) {
-              wn = 0.f;
-              wp = 0.f;
-              lse_out = -CUDART_INF_F;
-            } else {
-              wp = (prev_l == -CUDART_INF_F) ? 0.f : expf(prev_l - m);
-              wn = has ? expf(lse_new - m) : 0.f;
-              const float ws = wp + wn;
-              lse_out = m + logf(ws);
-              wp /= ws;
-              wn /= ws;
+
+        if (it.J == 0) {
+          // no key reaches these rows: out = prev (or 0), lse = prev_lse (or -inf).
+          // Only prefill and sparse produce such items; decode segments always hold keys.
+          if (row_ok && orow) {
+            for (int c = 0; c < kLatent; c += 8) {
+              uint4 v = prev_row ? *reinterpret_cast<const uint4*>(prev_row + c) : make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(orow + c) = v;
             }
+            if (lse_dst) *lse_dst = prev_row ? prev_l : -CUDART_INF_F;
           }
-          const float cn = wn * inv_l;
-          const bool use_prev = row_ok && prev_row && wp > 0.f;
+          continue;
+        }
+
+        for (int j = 0; j < it.J; ++j, ++g, ++gs) {
+          const int pb = g & 1;
+          if (!waitb(&bars.p_full[pb], (g >> 1) & 1, W_O_PFULL, true) ||
+              !waitb(&bars.pb_free[pb], ((g >> 1) & 1) ^ 1, W_O_PBFREE, false)) {
+            live = false;
+            break;
+          }
+          // copy this row's 128 bytes of P (already in the swizzled K-major layout) and its
+          // rescale factor: all nine remote loads are in flight before the first use
+          const uint32_t src = rem_pbuf + pb * kPBytes + r * 128;
+          uint8_t* dst = plocal + pb * kPBytes + r * 128;
+          uint4 pv[8];
+          float a;
+          asm volatile(
+              "ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%33];\n\t"
+              "ld.shared::cluster.v4.u32 {%4,%5,%6,%7}, [%33+16];\n\t"
+              "ld.shared::cluster.v4.u32 {%8,%9,%10,%11}, [%33+32];\n\t"
+              "ld.shared::cluster.v4.u32 {%12,%13,%14,%15}, [%33+48];\n\t"
+              "ld.shared::cluster.v4.u32 {%16,%17,%18,%19}, [%33+64];\n\t"
+              "ld.shared::cluster.v4.u32 {%20,%21,%22,%23}, [%33+80];\n\t"
+              "ld.shared::cluster.v4.u32 {%24,%25,%26,%27}, [%33+96];\n\t"
+              "ld.shared::cluster.v4.u32 {%28,%29,%30,%31}, [%33+112];\n\t"
+              "ld.shared::cluster.f32 %32, [%34];"
+              : "=r"(pv[0].x), "=r"(pv[0].y), "=r"(pv[0].z), "=r"(pv[0].w), "=r"(pv[1].x), "=r"(pv[1].y),
+                "=r"(pv[1].z), "=r"(pv[1].w), "=r"(pv[2].x), "=r"(pv[2].y), "=r"(pv[2].z), "=r"(pv[2].w),
+                "=r"(pv[3].x), "=r"(pv[3].y), "=r"(pv[3].z), "=r"(pv[3].w), "=r"(pv[4].x), "=r"(pv[4].y),
+                "=r"(pv[4].z), "=r"(pv[4].w), "=r"(pv[5].x), "=r"(pv[5].y), "=r"(pv[5].z), "=r"(pv[5].w),
+                "=r"(pv[6].x), "=r"(pv[6].y), "=r"(pv[6].z), "=r"(pv[6].w), "=r"(pv[7].x), "=r"(pv[7].y),
+                "=r"(pv[7].z), "=r"(pv[7].w), "=f"(a)
+              : "r"(src), "r"(rem_alpha + (pb * kRows + r) * 4)
+              : "memory");
+#pragma unroll
+          for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(dst + c * 16) = pv[c];
+          fence_proxy_async_smem();
+          mbar_arrive_remote(pb ? rem_p_free1 : rem_p_free0);
+          // tcgen05.ld/st are warp-collective: rescale when any row of the warp needs it
+          if (__any_sync(0xffffffffu, a != 1.f)) {
+            // O must hold every earlier P V before it is rescaled: PV(g-1) is use
+            // (g-1)/2 of P buffer (g-1)%2, and no later use of that buffer can start yet
+            if (!waitb(&bars.pb_free[(g - 1) & 1], ((g - 1) >> 1) & 1, W_O_PVDONE, false)) { live = false; break; }
+            tc_fence_after();
 #pragma unroll 1
-          for (int c1 = 0; c1 < kLatent; c1 += 128) {
-            // the previous output for 128 columns: 16 loads in flight
-            uint4 pv[16];
-#pragma unroll
-            for (int u = 0; u < 16; ++u)
-              pv[u] = use_prev ? reinterpret_cast<const uint4*>(prev_row + c1)[u] : make_uint4(0, 0, 0, 0);
-#pragma unroll
-          for (int c2 = 0; c2 < 128; c2 += 32) {
-            const int c0 = c1 + c2;
-            float o[32];
-            if (it.J > 0) {  // uniform over the CTA: every lane takes part in the TMEM load
+            for (int c0 = 0; c0 < kLatent; c0 += 32) {
               uint32_t v[32];
               tmem_ld32(tbase + lane_base + c0, v);
               tmem_wait_ld();
 #pragma unroll
-              for (int c = 0; c < 32; ++c) o[c] = __uint_as_float(v[c]) * cn;
-            } else {
-#pragma unroll
-              for (int c = 0; c < 32; ++c) o[c] = 0.f;
+              for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * a);
+              tmem_st32(tbase + lane_base + c0, v);
             }
-            if (!row_ok) continue;
-            if (use_prev) {
+            tmem_wait_st();
+          }
+          tc_fence_before();
+          mbar_arrive(&bars.p_ready[pb]);
+        }
+        if (!live) break;
+
+        // ---- epilogue ----
+        if (!waitb(&bars.stats_full, i & 1, W_O_STATSFULL, true)) break;
+        float m_used, l;
+        asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(m_used) : "r"(rem_stats + r * 8));
+        asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(l) : "r"(rem_stats + r * 8 + 4));
+        mbar_arrive_remote(rem_stats_free);
+        // the last P V of the item: use (g-1)/2 of P buffer (g-1)%2
+        if (!waitb(&bars.pb_free[(g - 1) & 1], ((g - 1) >> 1) & 1, W_O_PVDONE, false)) break;
+        tc_fence_after();
+        const bool has = l > 0.f;
+        const float inv_l = has ? 1.f / l : 0.f;
+        const float lse_new = has ? (m_used + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+        // merge weights with the previous pair (weight 0 for an empty side)
+        float wn = has ? 1.f : 0.f, wp = 0.f, lse_out = lse_new;
+        if (row_ok && prev_row) {
+          const float m = fmaxf(prev_l, lse_new);
+          if (m == -CUDART_INF_F) {
+            wn = 0.f;
+            wp = 0.f;
+            lse_out = -CUDART_INF_F;
+          } else {
+            wp = (prev_l == -CUDART_INF_F) ? 0.f : expf(prev_l - m);
+            wn = has ? expf(lse_new - m) : 0.f;
+            const float ws = wp + wn;
+            lse_out = m + logf(ws);
+            wp /= ws;
+            wn /= ws;
+          }
+        }
+        const float cn = wn * inv_l;
+
+        if (staged) {
+          // rows of this half live in ring stage gs + half, [8 column boxes][64 rows][128 B] swizzled
+          const uint32_t sidx = gs + half;
+          const int s = sidx % kStagesO;
+          if (!waitb(&bars.o_kv_full[s], (sidx / kStagesO) & 1, W_O_KV_FULL, false)) break;
+          uint8_t* stage = smem + kOffStages + s * kStageBytesO;
+          const bool use_prev = (prev_row != nullptr) && wp > 0.f;
+#pragma unroll 1
+          for (int c0 = 0; c0 < kLatent; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tbase + lane_base + c0, v);
+            tmem_wait_ld();
+            uint8_t* rowp = stage + (c0 >> 6) * kBoxBytes + rr * 128;
+            const int g0 = (c0 & 63) >> 3;
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const uint4 x = pv[(c2 >> 3) + u];
+            for (int u = 0; u < 4; ++u) {
+              uint4* cell = reinterpret_cast<uint4*>(rowp + (((g0 + u) ^ (rr & 7)) << 4));
+              float o[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) o[k] = __uint_as_float(v[8 * u + k]) * cn;
+              if (use_prev) {
+                const uint4 x = *cell;
                 const __nv_bfloat162* hx = reinterpret_cast<const __nv_bfloat162*>(&x);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                  float2 f2 = __bfloat1622float2(hx[k]);
-                  o[8 * u + 2 * k] += wp * f2.x;
-                  o[8 * u + 2 * k + 1] += wp * f2.y;
+                  const float2 f2 = __bfloat1622float2(hx[k]);
+                  o[2 * k] += wp * f2.x;
+                  o[2 * k + 1] += wp * f2.y;
                 }
               }
-            }
-            if (orow) {
-              uint4* dst = reinterpret_cast<uint4*>(orow + c0);
-#pragma unroll
-              for (int u = 0; u < 4; ++u)
-                dst[u] = make_uint4(pack_bf16x2(o[8 * u], o[8 * u + 1]), pack_bf16x2(o[8 * u + 2], o[8 * u + 3]),
-                                    pack_bf16x2(o[8 * u + 4], o[8 * u + 5]), pack_bf16x2(o[8 * u + 6], o[8 * u + 7]));
-            } else {
-              float4* dst = reinterpret_cast<float4*>(orow_f + c0);
-#pragma unroll
-              for (int u = 0; u < 8; ++u) dst[u] = make_float4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+              *cell = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
+                                 pack_bf16x2(o[6], o[7]));
             }
           }
-          }
-          if (row_ok && lse_dst) *lse_dst = lse_out;
-        }
-        if (it.J > 0) {
+          // O has been read: the next item's P V may start
           tc_fence_before();
           mbar_arrive(&bars.o_free);
-          ++i;
+          if (row_ok && lse_dst) *lse_dst = lse_out;
+          // the 64 rows of this half go out with TMA (rows past the end are clipped)
+          fence_proxy_async_smem();
+          named_barrier(1 + half, 64);
+          if (rr == 0) {
+            if (half * 64 < rows_per_item) {
+              const int32_t row0 = it.id * rows_per_item + half * 64;
+              const uint32_t sbase = smem_u32(stage);
+              for (int bx = 0; bx < kVBoxes; ++bx)
+                tma_store_2d(&map_out, bx * kBoxCols, row0, sbase + bx * kBoxBytes);
+              bulk_commit();
+              bulk_wait_read_all();
+              stored = true;
+            }
+            mbar_arrive(&bars.o_kv_empty[s]);
+          }
+          gs += 2;
+        } else {
+          // decode: fp32 partial rows to the workspace; sparse with other head counts: bf16 rows
+#pragma unroll 1
+          for (int c0 = 0; c0 < kLatent; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tbase + lane_base + c0, v);
+            tmem_wait_ld();
+            if (!row_ok) continue;
+            if (orow_f) {
+              float4* dst = reinterpret_cast<float4*>(orow_f + c0);
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                dst[u] = make_float4(__uint_as_float(v[4 * u]) * cn, __uint_as_float(v[4 * u + 1]) * cn,
+                                     __uint_as_float(v[4 * u + 2]) * cn, __uint_as_float(v[4 * u + 3]) * cn);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                dst[u] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * u]) * cn, __uint_as_float(v[8 * u + 1]) * cn),
+                                    pack_bf16x2(__uint_as_float(v[8 * u + 2]) * cn, __uint_as_float(v[8 * u + 3]) * cn),
+                                    pack_bf16x2(__uint_as_float(v[8 * u + 4]) * cn, __uint_as_float(v[8 * u + 5]) * cn),
+                                    pack_bf16x2(__uint_as_float(v[8 * u + 6]) * cn, __uint_as_float(v[8 * u + 7]) * cn));
+              }
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(&bars.o_free);
+          if (row_ok && lse_dst) *lse_dst = lse_out;
         }
+        ++i;
       }
+      if (stored) bulk_wait_all();
     }
   }
 
@@ -911,8 +1015,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 size_t core_smem_bytes() { return kSmemAlloc; }
 
-cudaError_t launch_core(const CoreParams& p, const CUtensorMap& map_kv, const CUtensorMap& map_row,
-                        const CUtensorMap& map_pe, cudaStream_t stream) {
+cudaError_t launch_core(const CoreParams& p, const CoreMaps& maps, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(mla_core_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
@@ -920,7 +1023,7 @@ cudaError_t launch_core(const CoreParams& p, const CUtensorMap& map_kv, const CU
     attr_set = true;
   }
   if (p.num_pairs <= 0) return cudaSuccess;
-  mla_core_kernel<<<dim3(2 * p.num_pairs), dim3(kThreads), kSmemAlloc, stream>>>(p, map_kv, map_row, map_pe);
+  mla_core_kernel<<<dim3(2 * p.num_pairs), dim3(kThreads), kSmemAlloc, stream>>>(p, maps);
   return cudaGetLastError();
 }
 

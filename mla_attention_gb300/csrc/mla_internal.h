@@ -77,9 +77,17 @@ struct CoreParams {
   int S_kv;
 };
 
+// TMA descriptors of one launch of the absorbed engine
+struct CoreMaps {
+  CUtensorMap kv;    // K/V rows [rows, 576] (prefill: the chunk; decode: the cache), box {64, 64 or page}
+  CUtensorMap row;   // gather rows, box {64, 1} (decode: the cache; sparse: c_kv [S_kv, 512])
+  CUtensorMap pe;    // sparse: k_pe [S_kv, 64], box {64, 1}
+  CUtensorMap out;   // prefill / sparse output rows [rows, 512], box {64, 64}
+  CUtensorMap prev;  // prefill previous output rows [rows, 512], box {64, 64}
+};
+
 // kernels' host launchers (return cudaError_t of the launch)
-cudaError_t launch_core(const CoreParams& p, const CUtensorMap& map_kv, const CUtensorMap& map_row,
-                        const CUtensorMap& map_pe, cudaStream_t stream);
+cudaError_t launch_core(const CoreParams& p, const CoreMaps& maps, cudaStream_t stream);
 size_t core_smem_bytes();
 
 cudaError_t launch_merge(const __nv_bfloat16* out_a, const float* lse_a, const __nv_bfloat16* out_b,

@@ -99,14 +99,18 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const float* __restr
     // pair owning tile t: the largest p with floor(p * total / P) <= t
     const int p_first = (int)(((t0 + 1) * (int64_t)num_pairs - 1) / total);
     const int p_last = (int)(((t1) * (int64_t)num_pairs - 1) / total);
+    // a pair whose share of the tiles is empty wrote no partial: skip it
+    auto owns = [&](int p) { return (int64_t)p * total / num_pairs < (int64_t)(p + 1) * total / num_pairs; };
     float m = -CUDART_INF_F;
-    for (int p = p_first; p <= p_last; ++p) m = fmaxf(m, part_lse[(int64_t)(b + p) * H + h]);
+    for (int p = p_first; p <= p_last; ++p)
+      if (owns(p)) m = fmaxf(m, part_lse[(int64_t)(b + p) * H + h]);
     float acc[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i] = 0.f;
     float wsum = 0.f;
     if (m != -CUDART_INF_F) {
       for (int p = p_first; p <= p_last; ++p) {
+        if (!owns(p)) continue;
         const int64_t slot = (int64_t)(b + p) * H + h;
         const float l = part_lse[slot];
         if (l == -CUDART_INF_F) continue;
