@@ -172,6 +172,26 @@ mla_status mla_decode(const void* q, const void* kv_cache, int64_t num_pages, in
                       const int32_t* block_table, int max_pages, const int32_t* lens, int B, int H, float scale,
                       int num_splits, void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * mla_decode without a workspace, for callers that cannot allocate device
+ * memory (the pages have no counterpart of this call): plug-ins handed only
+ * their input and output buffers by a framework that owns every device
+ * allocation, processes that forbid device allocation after start-up, and
+ * callers whose memory pool cannot grow from inside the call.  Arguments as
+ * mla_decode minus the workspace.  The split-K scratch is a fixed array inside
+ * this library (50,446,848 bytes, about 48.1 MiB, held by every GPU that loads the library until
+ * exit); limits: B <= 4096 and (B + CTA pairs) * H <= 24576, where the pairs
+ * are num_splits, or half the SM count when num_splits = 0; beyond them the
+ * call returns MLA_ERR_INVALID_ARG and launches nothing.  Allocates nothing.
+ * The first call on a device (with it current) looks up the array's address;
+ * make it before any stream capture.  Every call shares the array: calls that
+ * overlap on the GPU race.  Device-side index faults are zero-filled as in
+ * mla_decode but have no workspace to be read back from.
+ */
+mla_status mla_decode_noalloc(const void* q, const void* kv_cache, int64_t num_pages, int page_size,
+                              const int32_t* block_table, int max_pages, const int32_t* lens, int B, int H,
+                              float scale, int num_splits, void* out, float* lse, void* stream);
+
 /* ------------------------------------------------------------------------- */
 /* Top-k sparse latent + RoPE attention                                       */
 /* ------------------------------------------------------------------------- */

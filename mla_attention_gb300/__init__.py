@@ -6,8 +6,10 @@ ABI (include/mla.h) plus the seeded input generators used by tests and the
 bench.  Importing the package does not load the library; the first call does,
 and fails loudly if it was not built.
 """
-from ._lib import (MLAError, check_device_status, exported_symbols, inject_stall, lib, mla_decode, mla_merge_lse,
+from ._lib import (MLAError, check_device_status, exported_symbols, inject_stall, lib, mla_decode,
+                   mla_decode_noalloc, mla_merge_lse,
                    mla_prefill, mla_prefill_split, mla_sparse, set_spin_limit, workspace)
 
-__all__ = ["MLAError", "check_device_status", "exported_symbols", "inject_stall", "lib", "mla_decode", "mla_merge_lse",
+__all__ = ["MLAError", "check_device_status", "exported_symbols", "inject_stall", "lib", "mla_decode",
+           "mla_decode_noalloc", "mla_merge_lse",
            "mla_prefill", "mla_prefill_split", "mla_sparse", "set_spin_limit", "workspace"]

@@ -52,6 +52,8 @@ _SIGNATURES = {
     "mla_decode_workspace_size": ([c_int, c_int, c_int], c_size_t),
     "mla_decode": ([c_void_p, c_void_p, c_int64, c_int, c_void_p, c_int, c_void_p, c_int, c_int, c_float, c_int,
                     c_void_p, c_void_p, c_void_p, c_size_t, c_void_p], c_int),
+    "mla_decode_noalloc": ([c_void_p, c_void_p, c_int64, c_int, c_void_p, c_int, c_void_p, c_int, c_int, c_float,
+                            c_int, c_void_p, c_void_p, c_void_p], c_int),
     "mla_sparse_workspace_size": ([c_int, c_int], c_size_t),
     "mla_sparse": ([c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_float,
                     c_void_p, c_void_p, c_void_p, c_size_t, c_void_p], c_int),
@@ -213,6 +215,26 @@ def mla_decode(q, kv_cache, block_table, lens, scale: float, num_splits: int = 0
     s = lib().mla_decode(_ptr(q), _ptr(kv_cache), num_pages, page_size, _ptr(block_table), block_table.shape[1],
                          _ptr(lens), B, H, float(scale), int(num_splits), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
                          _stream(stream))
+    _check(s)
+    return out, lse
+
+
+def mla_decode_noalloc(q, kv_cache, block_table, lens, scale: float, num_splits: int = 0, out=None, lse=None,
+                       stream=None):
+    """mla_decode with its scratch in the library's fixed device array (no workspace, no allocation)."""
+    _need(q, "q", torch.bfloat16)
+    _need(kv_cache, "kv_cache", torch.bfloat16, q.device)
+    _need(block_table, "block_table", torch.int32, q.device)
+    _need(lens, "lens", torch.int32, q.device)
+    B, H, _ = q.shape
+    num_pages, page_size, _ = kv_cache.shape
+    if out is None:
+        out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    s = lib().mla_decode_noalloc(_ptr(q), _ptr(kv_cache), num_pages, page_size, _ptr(block_table),
+                                 block_table.shape[1], _ptr(lens), B, H, float(scale), int(num_splits), _ptr(out),
+                                 _ptr(lse), _stream(stream))
     _check(s)
     return out, lse
 

@@ -54,6 +54,8 @@ std::once_flag g_encode_once;
 uint32_t spin_limit() { return g_spin_limit.load(std::memory_order_relaxed); }
 uint32_t debug_stall() { return g_debug_stall.load(std::memory_order_relaxed); }
 
+mla_status set_last_error(mla_status s, const char* msg) { return fail(s, "%s", msg); }
+
 CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, const void* base,
                       const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
                       CUtensorMapSwizzle swizzle) {

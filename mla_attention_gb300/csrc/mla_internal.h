@@ -132,4 +132,7 @@ CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank
 
 int device_sm_count();
 
+// Record `msg` as the calling thread's last error and return `s`.
+mla_status set_last_error(mla_status s, const char* msg);
+
 }  // namespace mla
