@@ -54,7 +54,8 @@ constexpr int kOffPS = kStagesS * kStageBytesS;        // S-CTA: P buffers (1474
 constexpr int kOffAlpha = kOffPS + 2 * kPBytes;        // S-CTA: rescale factors [2][128]
 constexpr int kOffStats = kOffAlpha + 2 * kRows * 4;   // S-CTA: (m, l) [128][2]
 constexpr int kOffPO = kStagesO * kStageBytesO;        // O-CTA: local P buffers (196608)
-constexpr int kOffBars = kOffPO + 2 * kPBytes;         // both: barriers (229376)
+constexpr int kOffAlphaO = kOffPO + 2 * kPBytes;       // O-CTA: rescale factors [2][128] (229376)
+constexpr int kOffBars = kOffAlphaO + 2 * kRows * 4;   // both: barriers (230400)
 constexpr int kSmemUsed = kOffBars + 512;
 constexpr int kSmemAlloc = kSmemUsed + 1024;
 static_assert(kOffStats + kRows * 8 <= kOffBars, "S-CTA layout overlaps the barriers");
@@ -69,12 +70,17 @@ struct Bars {
   uint64_t s_kv_full[kStagesS], s_kv_empty[kStagesS];
   uint64_t s_full[2], s_free[2];
   uint64_t q_full;
-  uint64_t p_free[2];       // arrived remotely by the O-CTA rows
   uint64_t stats_free;      // arrived remotely by the O-CTA rows
+  uint64_t pwritten[2];     // S-CTA: all 128 rows wrote P tile b into the local buffer
+  uint64_t pbuf_free[2];    // S-CTA: the bulk copy out of local P buffer b has been read
   // O-CTA
   uint64_t o_kv_full[kStagesO], o_kv_empty[kStagesO];
-  uint64_t p_full[2];       // arrived remotely by the S-CTA rows
-  uint64_t pb_free[2], p_ready[2];  // pb_free[b]: the P V that read local P buffer b is complete
+  uint64_t p_full[2];       // O-CTA: P tile b landed (bulk copy from the S-CTA, with its tx bytes)
+  uint64_t p_ready[2];
+  // both CTAs: pb_free[b] completes when the P V that read the O-CTA's P buffer b is
+  // done (one multicast commit arrives on both copies; the S-CTA's copy gates the next
+  // bulk copy into that buffer)
+  uint64_t pb_free[2];
   uint64_t stats_full;      // arrived remotely by the S-CTA rows
   uint64_t o_free;
   uint64_t stall;           // fault injection: never arrived on
@@ -85,7 +91,8 @@ static_assert(sizeof(Bars) <= 512, "barrier block too large");
 
 // wait-site ids (device status word detail)
 enum : uint32_t {
-  W_S_KV_EMPTY = 1, W_S_KV_FULL, W_S_SFREE, W_S_QFULL, W_S_SFULL, W_S_PFREE, W_S_STATSFREE,
+  W_S_KV_EMPTY = 1, W_S_KV_FULL, W_S_SFREE, W_S_QFULL, W_S_SFULL, W_S_PFREE, W_S_STATSFREE, W_S_PWRITTEN,
+  W_S_PBOFREE,
   W_O_KV_EMPTY, W_O_KV_FULL, W_O_PREADY, W_O_PFULL, W_O_PBFREE, W_O_PVDONE, W_O_STATSFULL, W_O_OFREE, W_STALL,
   R_PAGE = 0x40, R_LEN = 0x41,
 };
@@ -210,6 +217,30 @@ __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// shared::cta -> shared::cluster bulk copy, completing tx bytes on a barrier of the destination CTA
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                                  uint32_t bar_cluster) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst_cluster),
+               "r"(src_cta), "r"(bytes), "r"(bar_cluster)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t bar_cluster, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(bar_cluster),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_le1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// commit that arrives on the barrier at this offset in every CTA of `mask`
+__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
+                   "r"(smem_u32(bar)),
+               "h"(mask)
+               : "memory");
+}
+
 __device__ __forceinline__ void prefetch_l2(const void* ptr) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
 }
@@ -309,17 +340,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 2; ++i) {
         mbar_init(&bars.s_full[i], 1);
         mbar_init(&bars.s_free[i], kRows);
-        mbar_init(&bars.p_free[i], kRows);
+        mbar_init(&bars.pb_free[i], 1);
       }
       mbar_init(&bars.q_full, kRows);
       mbar_init(&bars.stats_free, kRows);
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&bars.pwritten[i], kRows);
+        mbar_init(&bars.pbuf_free[i], 1);
+      }
     } else {
       for (int i = 0; i < kStagesO; ++i) {
         mbar_init(&bars.o_kv_full[i], 1);
         mbar_init(&bars.o_kv_empty[i], 1);
       }
       for (int i = 0; i < 2; ++i) {
-        mbar_init(&bars.p_full[i], kRows);
+        mbar_init(&bars.p_full[i], 1);
         mbar_init(&bars.pb_free[i], 1);
         mbar_init(&bars.p_ready[i], kRows);
       }
@@ -492,6 +527,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t rem_p_full0 = map_to_rank(smem_u32(&bars.p_full[0]), peer);
       const uint32_t rem_p_full1 = map_to_rank(smem_u32(&bars.p_full[1]), peer);
       const uint32_t rem_stats_full = map_to_rank(smem_u32(&bars.stats_full), peer);
+      const uint32_t rem_p_o = map_to_rank(smem_u32(smem + kOffPO), peer);          // O-CTA P buffers
+      const uint32_t rem_alpha_o = map_to_rank(smem_u32(smem + kOffAlphaO), peer);  // O-CTA factors
       uint32_t g = 0, i = 0;  // i counts items that have KV tiles
       bool live = true;
       while (live && iter.next(it)) {
@@ -593,13 +630,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tc_fence_before();
           mbar_arrive(&bars.s_free[sb]);
 
-          float x[64];
-          float mt = -CUDART_INF_F;
+          // scores in the log2 domain: t = s * scale * log2(e); the row maximum is taken on
+          // the raw dot products (their largest, or their smallest when the scale is negative)
+          const float sl2 = p.scale_log2;
+          const bool full = (vmask == ~0ull);
+          float hi_raw = -CUDART_INF_F, lo_raw = CUDART_INF_F;
+          if (full) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            x[c] = ((vmask >> c) & 1ull) ? __uint_as_float(sraw[c]) * p.scale_log2 : -CUDART_INF_F;
-            mt = fmaxf(mt, x[c]);
+            for (int c = 0; c < 64; ++c) {
+              const float v = __uint_as_float(sraw[c]);
+              hi_raw = fmaxf(hi_raw, v);
+              lo_raw = fminf(lo_raw, v);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+              const bool ok = (vmask >> c) & 1ull;
+              const float v = __uint_as_float(sraw[c]);
+              hi_raw = ok ? fmaxf(hi_raw, v) : hi_raw;
+              lo_raw = ok ? fminf(lo_raw, v) : lo_raw;
+            }
           }
+          const float mt = (vmask == 0ull) ? -CUDART_INF_F : (sl2 >= 0.f ? hi_raw : lo_raw) * sl2;
           float a = 1.f;
           if (mt > m_used + kRescaleLog2) {
             if (l > 0.f) a = ex2_approx(m_used - mt);
@@ -612,15 +664,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           float rs = 0.f;
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const float e0 = ex2_approx(x[2 * c] - msub);
-            const float e1 = ex2_approx(x[2 * c + 1] - msub);
+            float e0 = ex2_approx(fmaf(__uint_as_float(sraw[2 * c]), sl2, -msub));
+            float e1 = ex2_approx(fmaf(__uint_as_float(sraw[2 * c + 1]), sl2, -msub));
+            if (!full) {
+              e0 = ((vmask >> (2 * c)) & 1ull) ? e0 : 0.f;
+              e1 = ((vmask >> (2 * c + 1)) & 1ull) ? e1 : 0.f;
+            }
             rs += e0 + e1;
             pk[c] = pack_bf16x2(e0, e1);
           }
           l += rs;
 
-          // ---- hand P and the rescale factor to the O-CTA ----
-          if (!waitb(&bars.p_free[sb], ((g >> 1) & 1) ^ 1, W_S_PFREE, true)) { live = false; break; }
+          // ---- hand P and the rescale factor to the O-CTA: one bulk copy per tile ----
+          // local buffer sb was last read by the copy of tile g-2
+          if (!waitb(&bars.pbuf_free[sb], ((g >> 1) & 1) ^ 1, W_S_PFREE, false)) { live = false; break; }
           uint8_t* prow = pbuf + sb * kPBytes + r * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
@@ -628,7 +685,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = v4;
           }
           alpha[sb * kRows + r] = a;
-          mbar_arrive_remote(sb ? rem_p_full1 : rem_p_full0);
+          fence_proxy_async_smem();  // the bulk copy reads through the async proxy
+          mbar_arrive(&bars.pwritten[sb]);
+          if (warp == 0) {
+            // every row is written, and the O-CTA's buffer sb is free (its P V of tile g-2 is done)
+            if (!waitb(&bars.pwritten[sb], (g >> 1) & 1, W_S_PWRITTEN, false) ||
+                !waitb(&bars.pb_free[sb], ((g >> 1) & 1) ^ 1, W_S_PBOFREE, true)) {
+              live = false;
+              break;
+            }
+            if (lane == 0) {
+              const uint32_t bar = sb ? rem_p_full1 : rem_p_full0;
+              mbar_arrive_expect_tx_remote(bar, kPBytes + kRows * 4);
+              bulk_copy_to_peer(rem_p_o + sb * kPBytes, smem_u32(pbuf + sb * kPBytes), kPBytes, bar);
+              bulk_copy_to_peer(rem_alpha_o + sb * kRows * 4, smem_u32(alpha + sb * kRows), kRows * 4, bar);
+              bulk_commit();
+              // the copy of tile g-1 has been read: its local buffer may be rewritten
+              if (g > 0) {
+                bulk_wait_read_le1();
+                mbar_arrive(&bars.pbuf_free[(g - 1) & 1]);
+              }
+            }
+            __syncwarp();
+          }
         }
         if (!live) break;
         // ---- row statistics for the epilogue ----
@@ -638,6 +717,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_arrive_remote(rem_stats_full);
         ++i;
       }
+      if (warp == 0 && lane == 0) bulk_wait_all();  // our shared memory is read until the copies end
     }
   } else {
     // =====================================================================
@@ -752,7 +832,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               }
             }
             mma_commit(&bars.o_kv_empty[s]);
-            mma_commit(&bars.pb_free[pb]);
+            mma_commit_multicast(&bars.pb_free[pb], 0x3);  // this CTA and the S-CTA
           }
           __syncwarp();
         }
@@ -765,13 +845,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int half = r >> 6;   // warps 0-1: rows 0-63, warps 2-3: rows 64-127
       const int rr = r & 63;
       const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-      const uint32_t rem_pbuf = map_to_rank(smem_u32(smem + kOffPS), peer);
-      const uint32_t rem_alpha = map_to_rank(smem_u32(smem + kOffAlpha), peer);
       const uint32_t rem_stats = map_to_rank(smem_u32(smem + kOffStats), peer);
-      const uint32_t rem_p_free0 = map_to_rank(smem_u32(&bars.p_free[0]), peer);
-      const uint32_t rem_p_free1 = map_to_rank(smem_u32(&bars.p_free[1]), peer);
       const uint32_t rem_stats_free = map_to_rank(smem_u32(&bars.stats_free), peer);
-      uint8_t* plocal = smem + kOffPO;
+      const float* alpha_o = reinterpret_cast<const float*>(smem + kOffAlphaO);
       uint32_t g = 0, gs = 0, i = 0;  // P tiles, stage ring position, items that have KV tiles
       bool live = true;
       bool stored = false;            // this thread issued TMA stores that must finish before exit
@@ -824,39 +900,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
         for (int j = 0; j < it.J; ++j, ++g, ++gs) {
           const int pb = g & 1;
-          if (!waitb(&bars.p_full[pb], (g >> 1) & 1, W_O_PFULL, true) ||
-              !waitb(&bars.pb_free[pb], ((g >> 1) & 1) ^ 1, W_O_PBFREE, false)) {
+          // P tile g and its rescale factors landed in the local buffer pb (bulk copy)
+          if (!waitb(&bars.p_full[pb], (g >> 1) & 1, W_O_PFULL, true)) {
             live = false;
             break;
           }
-          // copy this row's 128 bytes of P (already in the swizzled K-major layout) and its
-          // rescale factor: all nine remote loads are in flight before the first use
-          const uint32_t src = rem_pbuf + pb * kPBytes + r * 128;
-          uint8_t* dst = plocal + pb * kPBytes + r * 128;
-          uint4 pv[8];
-          float a;
-          asm volatile(
-              "ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%33];\n\t"
-              "ld.shared::cluster.v4.u32 {%4,%5,%6,%7}, [%33+16];\n\t"
-              "ld.shared::cluster.v4.u32 {%8,%9,%10,%11}, [%33+32];\n\t"
-              "ld.shared::cluster.v4.u32 {%12,%13,%14,%15}, [%33+48];\n\t"
-              "ld.shared::cluster.v4.u32 {%16,%17,%18,%19}, [%33+64];\n\t"
-              "ld.shared::cluster.v4.u32 {%20,%21,%22,%23}, [%33+80];\n\t"
-              "ld.shared::cluster.v4.u32 {%24,%25,%26,%27}, [%33+96];\n\t"
-              "ld.shared::cluster.v4.u32 {%28,%29,%30,%31}, [%33+112];\n\t"
-              "ld.shared::cluster.f32 %32, [%34];"
-              : "=r"(pv[0].x), "=r"(pv[0].y), "=r"(pv[0].z), "=r"(pv[0].w), "=r"(pv[1].x), "=r"(pv[1].y),
-                "=r"(pv[1].z), "=r"(pv[1].w), "=r"(pv[2].x), "=r"(pv[2].y), "=r"(pv[2].z), "=r"(pv[2].w),
-                "=r"(pv[3].x), "=r"(pv[3].y), "=r"(pv[3].z), "=r"(pv[3].w), "=r"(pv[4].x), "=r"(pv[4].y),
-                "=r"(pv[4].z), "=r"(pv[4].w), "=r"(pv[5].x), "=r"(pv[5].y), "=r"(pv[5].z), "=r"(pv[5].w),
-                "=r"(pv[6].x), "=r"(pv[6].y), "=r"(pv[6].z), "=r"(pv[6].w), "=r"(pv[7].x), "=r"(pv[7].y),
-                "=r"(pv[7].z), "=r"(pv[7].w), "=f"(a)
-              : "r"(src), "r"(rem_alpha + (pb * kRows + r) * 4)
-              : "memory");
-#pragma unroll
-          for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(dst + c * 16) = pv[c];
-          fence_proxy_async_smem();
-          mbar_arrive_remote(pb ? rem_p_free1 : rem_p_free0);
+          const float a = alpha_o[pb * kRows + r];
           // tcgen05.ld/st are warp-collective: rescale when any row of the warp needs it
           if (__any_sync(0xffffffffu, a != 1.f)) {
             // O must hold every earlier P V before it is rescaled: PV(g-1) is use
