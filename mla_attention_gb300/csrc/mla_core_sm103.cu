@@ -12,9 +12,10 @@
 //         S double buffer (2 x 64 cols)
 //   warp 4: TMA K tiles (9 col boxes)      warp 4: TMA V tiles (8 col boxes)
 //   warp 5: S = Q K^T (A from TMEM)        warp 5: O += P V (P, V from smem)
-//   warps 0-3: online softmax, one row     warps 0-3: pull P from the S-CTA's
-//     per thread; P (bf16) and the           shared memory, lazy O rescale,
-//     rescale factor into shared memory      epilogue (normalise, prev merge)
+//   warps 0-3: online softmax, one row     warps 0-3: lazy O rescale, epilogue
+//     per thread; P (bf16) and the           (normalise, prev merge)
+//     rescale factor into shared memory
+//   warp 6: one bulk copy of P and the factors into the O-CTA per tile
 //
 // The two CTAs hand P over through distributed shared memory with cluster-
 // scope mbarrier arrivals.  The online softmax keeps a stale row maximum and
@@ -35,12 +36,13 @@
 #include <math_constants.h>
 
 #include "mla_internal.h"
+#include "mma_seq.cuh"
 #include "sm103_ptx.cuh"
 
 namespace mla {
 namespace {
 
-constexpr int kThreads = 192;  // warps 0-3 rows, warp 4 TMA, warp 5 MMA
+constexpr int kThreads = 224;  // warps 0-3 rows, warp 4 TMA, warp 5 MMA, warp 6 P copies (S-CTA)
 constexpr int kStagesS = 2;
 constexpr int kStagesO = 3;
 constexpr int kBoxBytes = kKeys * 128;                 // 64 rows x 128 B
@@ -504,12 +506,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tc_fence_after();
           if (lane == 0) {
             const uint32_t stage = smem_u32(smem + kOffStages + s * kStageBytesS);
-            const uint32_t d = tbase + kTmemS + sb * kKeys;
-#pragma unroll 4
-            for (int ks = 0; ks < kDk / 16; ++ks) {
-              const uint64_t bdesc = sdesc_sw128(stage + (ks >> 2) * kBoxBytes + (ks & 3) * 32, 16, 1024);
-              mma_ts(d, tbase + kTmemQ + ks * 8, bdesc, idesc, ks > 0 ? 1u : 0u);
-            }
+            mma_s_q576_n64(tbase + kTmemS + sb * kKeys, tbase + kTmemQ, sdesc_sw128(stage, 16, 1024), idesc);
             mma_commit(&bars.s_kv_empty[s]);
             mma_commit(&bars.s_full[sb]);
           }
@@ -517,18 +514,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         ++i;
       }
-    } else {
+    } else if (warp == 6) {
+      // ---------------- P hand-over: one bulk copy per tile into the O-CTA ----------------
+      // Kept off the softmax warps: waiting for a copy to be read would otherwise delay
+      // one row warp, and every S tile waits for all 128 rows.
+      uint8_t* pbuf = smem + kOffPS;
+      float* alpha = reinterpret_cast<float*>(smem + kOffAlpha);
+      const uint32_t rem_p_full0 = map_to_rank(smem_u32(&bars.p_full[0]), peer);
+      const uint32_t rem_p_full1 = map_to_rank(smem_u32(&bars.p_full[1]), peer);
+      const uint32_t rem_p_o = map_to_rank(smem_u32(smem + kOffPO), peer);          // O-CTA P buffers
+      const uint32_t rem_alpha_o = map_to_rank(smem_u32(smem + kOffAlphaO), peer);  // O-CTA factors
+      uint32_t g = 0;
+      bool live = true;
+      while (live && iter.next(it)) {
+        for (int j = 0; j < it.J; ++j, ++g) {
+          const int sb = g & 1;
+          // every row wrote P tile g, and the O-CTA's buffer sb is free (its P V of tile g-2 is done)
+          if (!waitb(&bars.pwritten[sb], (g >> 1) & 1, W_S_PWRITTEN, false) ||
+              !waitb(&bars.pb_free[sb], ((g >> 1) & 1) ^ 1, W_S_PBOFREE, true)) {
+            live = false;
+            break;
+          }
+          if (lane == 0) {
+            const uint32_t bar = sb ? rem_p_full1 : rem_p_full0;
+            mbar_arrive_expect_tx_remote(bar, kPBytes + kRows * 4);
+            bulk_copy_to_peer(rem_p_o + sb * kPBytes, smem_u32(pbuf + sb * kPBytes), kPBytes, bar);
+            bulk_copy_to_peer(rem_alpha_o + sb * kRows * 4, smem_u32(alpha + sb * kRows), kRows * 4, bar);
+            bulk_commit();
+            bulk_wait_read_all();                 // local buffer sb has been read
+            mbar_arrive(&bars.pbuf_free[sb]);
+          }
+          __syncwarp();
+        }
+      }
+      if (lane == 0) bulk_wait_all();  // our shared memory is read until the copies end
+    } else if (warp < 4) {
       // ---------------- rows: Q load, online softmax, P hand-over ----------------
       const int r = tid;  // row within the tile = TMEM lane
       const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
       uint8_t* pbuf = smem + kOffPS;
       float* alpha = reinterpret_cast<float*>(smem + kOffAlpha);
       float* stats = reinterpret_cast<float*>(smem + kOffStats);
-      const uint32_t rem_p_full0 = map_to_rank(smem_u32(&bars.p_full[0]), peer);
-      const uint32_t rem_p_full1 = map_to_rank(smem_u32(&bars.p_full[1]), peer);
       const uint32_t rem_stats_full = map_to_rank(smem_u32(&bars.stats_full), peer);
-      const uint32_t rem_p_o = map_to_rank(smem_u32(smem + kOffPO), peer);          // O-CTA P buffers
-      const uint32_t rem_alpha_o = map_to_rank(smem_u32(smem + kOffAlphaO), peer);  // O-CTA factors
       uint32_t g = 0, i = 0;  // i counts items that have KV tiles
       bool live = true;
       while (live && iter.next(it)) {
@@ -687,27 +714,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           alpha[sb * kRows + r] = a;
           fence_proxy_async_smem();  // the bulk copy reads through the async proxy
           mbar_arrive(&bars.pwritten[sb]);
-          if (warp == 0) {
-            // every row is written, and the O-CTA's buffer sb is free (its P V of tile g-2 is done)
-            if (!waitb(&bars.pwritten[sb], (g >> 1) & 1, W_S_PWRITTEN, false) ||
-                !waitb(&bars.pb_free[sb], ((g >> 1) & 1) ^ 1, W_S_PBOFREE, true)) {
-              live = false;
-              break;
-            }
-            if (lane == 0) {
-              const uint32_t bar = sb ? rem_p_full1 : rem_p_full0;
-              mbar_arrive_expect_tx_remote(bar, kPBytes + kRows * 4);
-              bulk_copy_to_peer(rem_p_o + sb * kPBytes, smem_u32(pbuf + sb * kPBytes), kPBytes, bar);
-              bulk_copy_to_peer(rem_alpha_o + sb * kRows * 4, smem_u32(alpha + sb * kRows), kRows * 4, bar);
-              bulk_commit();
-              // the copy of tile g-1 has been read: its local buffer may be rewritten
-              if (g > 0) {
-                bulk_wait_read_le1();
-                mbar_arrive(&bars.pbuf_free[(g - 1) & 1]);
-              }
-            }
-            __syncwarp();
-          }
         }
         if (!live) break;
         // ---- row statistics for the epilogue ----
@@ -717,7 +723,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_arrive_remote(rem_stats_full);
         ++i;
       }
-      if (warp == 0 && lane == 0) bulk_wait_all();  // our shared memory is read until the copies end
     }
   } else {
     // =====================================================================
@@ -822,15 +827,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             const uint32_t vst = smem_u32(smem + kOffStages + s * kStageBytesO);
             const uint32_t pst = smem_u32(smem + kOffPO + pb * kPBytes);
-#pragma unroll
-            for (int ks = 0; ks < kKeys / 16; ++ks) {
-              const uint64_t adesc = sdesc_sw128(pst + ks * 32, 16, 1024);
-#pragma unroll
-              for (int half = 0; half < 2; ++half) {
-                const uint64_t bdesc = sdesc_sw128(vst + half * 4 * kBoxBytes + ks * 2048, kBoxBytes, 1024);
-                mma_ss(tbase + half * 256, adesc, bdesc, idesc, (j > 0 || ks > 0) ? 1u : 0u);
-              }
-            }
+            mma_pv_k64_n512(tbase, tbase + 256, sdesc_sw128(pst, 16, 1024), sdesc_sw128(vst, kBoxBytes, 1024),
+                            sdesc_sw128(vst + 4 * kBoxBytes, kBoxBytes, 1024), idesc, j > 0 ? 1u : 0u);
             mma_commit(&bars.o_kv_empty[s]);
             mma_commit_multicast(&bars.pb_free[pb], 0x3);  // this CTA and the S-CTA
           }
@@ -839,8 +837,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (staged) gs += 2;  // the epilogue's two stages
         ++i;
       }
-    } else {
-      // ---------------- rows: P pull, lazy rescale, epilogue ----------------
+    } else if (warp < 4) {
+      // ---------------- rows: lazy rescale, epilogue ----------------
       const int r = tid;
       const int half = r >> 6;   // warps 0-1: rows 0-63, warps 2-3: rows 64-127
       const int rr = r & 63;

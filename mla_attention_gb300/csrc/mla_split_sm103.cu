@@ -20,6 +20,7 @@
 #include <math_constants.h>
 
 #include "mla_internal.h"
+#include "mma_seq.cuh"
 #include "sm103_ptx.cuh"
 
 namespace mla {
@@ -174,12 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       if (lane == 0) {
         const uint32_t st = smem_u32(smem + kOffStage + s * kStageBytes);
-        const uint32_t d = tbase + kTmemS + (j & 1) * kTile;
-#pragma unroll
-        for (int ks = 0; ks < 12; ++ks) {
-          const uint32_t off = (ks >> 2) * kBox + (ks & 3) * 32;
-          mma_ss(d, sdesc_sw128(sq + off, 16, 1024), sdesc_sw128(st + off, 16, 1024), idesc_s, ks > 0 ? 1u : 0u);
-        }
+        mma_s_k192_n128(tbase + kTmemS + (j & 1) * kTile, sdesc_sw128(sq, 16, 1024), sdesc_sw128(st, 16, 1024),
+                        idesc_s);
         mma_commit(&bars.s_full[j & 1]);
       }
       __syncwarp();
@@ -194,11 +191,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         const int s = j % kStages;
         const uint32_t vst = smem_u32(smem + kOffStage + s * kStageBytes + kKBytes);
-        const uint32_t pa = tbase + kTmemS + (j & 1) * kTile;
-#pragma unroll
-        for (int ks = 0; ks < kTile / 16; ++ks)
-          mma_ts(tbase + kTmemO, pa + ks * 8, sdesc_sw128(vst + ks * 2048, kBox, 1024), idesc_o,
-                 (j > 0 || ks > 0) ? 1u : 0u);
+        mma_pv_tmem_k128_n128(tbase + kTmemO, tbase + kTmemS + (j & 1) * kTile, sdesc_sw128(vst, kBox, 1024), idesc_o,
+                              j > 0 ? 1u : 0u);
         mma_commit(&bars.kv_empty[s]);
         mma_commit(&bars.pv_done[j & 1]);
       }
