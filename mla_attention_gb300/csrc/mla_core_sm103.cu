@@ -42,8 +42,10 @@
 namespace mla {
 namespace {
 
-constexpr int kThreads = 224;  // warps 0-3 rows, warp 4 TMA, warp 5 MMA, warp 6 P copies (S-CTA)
-constexpr int kStagesS = 2;
+// warps 0-3 rows, warp 4 TMA; S-CTA: warps 5 and 7 issue the S MMAs of even and odd tiles,
+// warp 6 copies P out.  O-CTA: warp 5 issues P V.
+constexpr int kThreads = 256;
+constexpr int kStagesS = 2;  // stage g % 2 pairs with S buffer g % 2
 constexpr int kStagesO = 3;
 constexpr int kBoxBytes = kKeys * 128;                 // 64 rows x 128 B
 constexpr int kStageBytesS = kKBoxes * kBoxBytes;      // 73728
@@ -69,9 +71,13 @@ constexpr float kRescaleLog2 = 8.0f;    // rescale O only when the max grows by 
 
 struct Bars {
   // S-CTA
-  uint64_t s_kv_full[kStagesS], s_kv_empty[kStagesS];
-  uint64_t s_full[2], s_free[2];
+  // s_go[b]: K tile g (b = g % 2) landed AND every row read S tile g-2 out of buffer b
+  // (128 row arrivals + the producer's expect_tx), so the MMA warp waits once per tile.
+  // s_full[b]: the S MMA of tile g is done: S is ready, and stage b may be refilled.
+  uint64_t s_go[2];
+  uint64_t s_full[2];
   uint64_t q_full;
+  uint64_t q_taken;         // both S issuers passed q_full of the current item (count 2)
   uint64_t stats_free;      // arrived remotely by the O-CTA rows
   uint64_t pwritten[2];     // S-CTA: all 128 rows wrote P tile b into the local buffer
   uint64_t pbuf_free[2];    // S-CTA: the bulk copy out of local P buffer b has been read
@@ -335,16 +341,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // ---- setup ----
   if (tid == 0) {
     if (is_s) {
-      for (int i = 0; i < kStagesS; ++i) {
-        mbar_init(&bars.s_kv_full[i], 1);
-        mbar_init(&bars.s_kv_empty[i], 1);
-      }
       for (int i = 0; i < 2; ++i) {
+        mbar_init(&bars.s_go[i], kRows + 1);
         mbar_init(&bars.s_full[i], 1);
-        mbar_init(&bars.s_free[i], kRows);
         mbar_init(&bars.pb_free[i], 1);
       }
       mbar_init(&bars.q_full, kRows);
+      mbar_init(&bars.q_taken, 2);
       mbar_init(&bars.stats_free, kRows);
       for (int i = 0; i < 2; ++i) {
         mbar_init(&bars.pwritten[i], kRows);
@@ -430,14 +433,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool live = true;
       while (live && iter.next(it)) {
         for (int j = 0; j < it.J && live; ++j, ++g) {
-          const int s = g % kStagesS;
-          if (!waitb(&bars.s_kv_empty[s], ((g / kStagesS) & 1) ^ 1, W_S_KV_EMPTY, false)) { live = false; break; }
+          const int s = g & 1;
+          // stage s was last read by the S MMA of tile g-2
+          if (!waitb(&bars.s_full[s], ((g >> 1) & 1) ^ 1, W_S_KV_EMPTY, false)) { live = false; break; }
           const uint32_t dst = smem_u32(smem + kOffStages + s * kStageBytesS);
           if (p.mode == MODE_PREFILL) {
             if (lane == 0) {
-              mbar_arrive_expect_tx(&bars.s_kv_full[s], kStageBytesS);
+              mbar_arrive_expect_tx(&bars.s_go[s], kStageBytesS);
               for (int bx = 0; bx < kKBoxes; ++bx)
-                tma_load_2d(dst + bx * kBoxBytes, &map_kv, bx * kBoxCols, j * kKeys, &bars.s_kv_full[s]);
+                tma_load_2d(dst + bx * kBoxBytes, &map_kv, bx * kBoxCols, j * kKeys, &bars.s_go[s]);
             }
           } else {
             int32_t re, ro;
@@ -473,47 +477,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               if (re < 0 || re >= p.S_kv) re = -1;
               if (ro < 0 || ro >= p.S_kv) ro = -1;
             }
-            if (lane == 0) mbar_arrive_expect_tx(&bars.s_kv_full[s], kStageBytesS);
+            if (lane == 0) mbar_arrive_expect_tx(&bars.s_go[s], kStageBytesS);
             __syncwarp();
             if (tiled) {
               if (lane == 0)
                 for (int bx = 0; bx < kKBoxes; ++bx)
-                  tma_load_2d(dst + bx * kBoxBytes, &map_kv, bx * kBoxCols, ytile, &bars.s_kv_full[s]);
+                  tma_load_2d(dst + bx * kBoxBytes, &map_kv, bx * kBoxCols, ytile, &bars.s_go[s]);
             } else {
               issue_gather_tile(dst, &map_row, &map_pe, p.mode == MODE_DECODE ? kLatent : 0, kKBoxes, re, ro,
-                                &bars.s_kv_full[s]);
+                                &bars.s_go[s]);
             }
           }
           __syncwarp();
         }
       }
-    } else if (warp == 5) {
-      // ---------------- MMA issuer: S = Q K^T ----------------
-      const uint32_t idesc = idesc_bf16_f32(kRows, kKeys, false, false);
-      uint32_t g = 0, i = 0;  // i counts items that have KV tiles
-      bool live = true;
-      while (live && iter.next(it)) {
-        if (it.J == 0) continue;  // no key: the O-CTA writes these rows on its own
-        if (!waitb(&bars.q_full, i & 1, W_S_QFULL, false)) break;
-        for (int j = 0; j < it.J; ++j, ++g) {
-          const int s = g % kStagesS;
-          const int sb = g & 1;
-          if (!waitb(&bars.s_kv_full[s], (g / kStagesS) & 1, W_S_KV_FULL, false) ||
-              !waitb(&bars.s_free[sb], ((g >> 1) & 1) ^ 1, W_S_SFREE, false)) {
-            live = false;
-            break;
+    } else if (warp == 5 || warp == 7) {
+      // ---------------- MMA issuers: S = Q K^T ----------------
+      // Two warps take turns, warp 5 the even tiles and warp 7 the odd ones; each owns one K
+      // stage and one S buffer (index g % 2).  A barrier wait by the thread that issued MMAs
+      // stalls until its queued MMAs drain, so with one issuer the tensor pipe idles at every
+      // tile boundary; the second issuer's queued tile covers that gap.  One thread per warp
+      // runs the loop (these warps issue no warp-collective tcgen05 instruction here).
+      if (lane == 0) {
+        const uint32_t b = (warp == 5) ? 0u : 1u;
+        const uint32_t idesc = idesc_bf16_f32(kRows, kKeys, false, false);
+        auto wait1 = [&](uint64_t* bar, uint32_t parity, uint32_t site) -> bool {
+          const bool ok = (*abort_flag == 0) && mbar_wait(bar, parity, err, site, lim, false);
+          if (!ok) *abort_flag = 1;
+          return ok;
+        };
+        const uint32_t stage = smem_u32(smem + kOffStages + b * kStageBytesS);
+        const uint64_t bdesc = sdesc_sw128(stage, 16, 1024);
+        const uint32_t d_tmem = tbase + kTmemS + b * kKeys;
+        uint32_t g = 0, i = 0;  // i counts items that have KV tiles
+        bool live = true;
+        while (live && iter.next(it)) {
+          if (it.J == 0) continue;  // no key: the O-CTA writes these rows on its own
+          // every item's Q is waited for by both issuers, so neither can read q_full a phase
+          // ahead: the rows write the next item's Q only after both have arrived on q_taken
+          if (!wait1(&bars.q_full, i & 1, W_S_QFULL)) break;
+          mbar_arrive(&bars.q_taken);
+          for (int j = 0; j < it.J; ++j, ++g) {
+            if ((g & 1u) != b) continue;
+            if (!wait1(&bars.s_go[b], (g >> 1) & 1, W_S_KV_FULL)) {
+              live = false;
+              break;
+            }
+            tc_fence_after();
+            mma_s_q576_n64(d_tmem, tbase + kTmemQ, bdesc, idesc);
+            mma_commit(&bars.s_full[b]);
           }
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t stage = smem_u32(smem + kOffStages + s * kStageBytesS);
-            mma_s_q576_n64(tbase + kTmemS + sb * kKeys, tbase + kTmemQ, sdesc_sw128(stage, 16, 1024), idesc);
-            mma_commit(&bars.s_kv_empty[s]);
-            mma_commit(&bars.s_full[sb]);
-          }
-          __syncwarp();
+          ++i;
         }
-        ++i;
       }
+      __syncwarp();
     } else if (warp == 6) {
       // ---------------- P hand-over: one bulk copy per tile into the O-CTA ----------------
       // Kept off the softmax warps: waiting for a copy to be read would otherwise delay
@@ -558,6 +575,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t rem_stats_full = map_to_rank(smem_u32(&bars.stats_full), peer);
       uint32_t g = 0, i = 0;  // i counts items that have KV tiles
       bool live = true;
+      // both S buffers start free (the row arrivals of tiles 0 and 1)
+      mbar_arrive(&bars.s_go[0]);
+      mbar_arrive(&bars.s_go[1]);
       while (live && iter.next(it)) {
         if (it.J == 0) continue;  // no key: the O-CTA writes these rows on its own
         // ---- this row's query and key limit ----
@@ -586,6 +606,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         // ---- Q -> TMEM (bf16 pairs, K-contiguous): 9 chunks of 64 columns, 3 in flight ----
+        // (both issuers took the previous item's Q signal; its MMAs are done, since every S
+        // tile of that item has been read)
+        if (i > 0 && !waitb(&bars.q_taken, (i - 1) & 1, W_S_QFULL, false)) break;
 #pragma unroll 1
         for (int c0 = 0; c0 < kDk / 64; c0 += 3) {
           uint4 x[3][8];
@@ -655,7 +678,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           tmem_wait_ld();
           tc_fence_before();
-          mbar_arrive(&bars.s_free[sb]);
+          mbar_arrive(&bars.s_go[sb]);  // S buffer sb may take tile g+2
 
           // scores in the log2 domain: t = s * scale * log2(e); the row maximum is taken on
           // the raw dot products (their largest, or their smallest when the scale is negative)
