@@ -684,23 +684,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // the raw dot products (their largest, or their smallest when the scale is negative)
           const float sl2 = p.scale_log2;
           const bool full = (vmask == ~0ull);
-          float hi_raw = -CUDART_INF_F, lo_raw = CUDART_INF_F;
+          // four independent chains each for the max, the min and the sum: one row warp per
+          // sub-partition has no other warp to hide a 64-long dependent chain behind
+          float hq[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+          float lq[4] = {CUDART_INF_F, CUDART_INF_F, CUDART_INF_F, CUDART_INF_F};
           if (full) {
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
               const float v = __uint_as_float(sraw[c]);
-              hi_raw = fmaxf(hi_raw, v);
-              lo_raw = fminf(lo_raw, v);
+              hq[c & 3] = fmaxf(hq[c & 3], v);
+              lq[c & 3] = fminf(lq[c & 3], v);
             }
           } else {
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
               const bool ok = (vmask >> c) & 1ull;
               const float v = __uint_as_float(sraw[c]);
-              hi_raw = ok ? fmaxf(hi_raw, v) : hi_raw;
-              lo_raw = ok ? fminf(lo_raw, v) : lo_raw;
+              hq[c & 3] = ok ? fmaxf(hq[c & 3], v) : hq[c & 3];
+              lq[c & 3] = ok ? fminf(lq[c & 3], v) : lq[c & 3];
             }
           }
+          const float hi_raw = fmaxf(fmaxf(hq[0], hq[1]), fmaxf(hq[2], hq[3]));
+          const float lo_raw = fminf(fminf(lq[0], lq[1]), fminf(lq[2], lq[3]));
           const float mt = (vmask == 0ull) ? -CUDART_INF_F : (sl2 >= 0.f ? hi_raw : lo_raw) * sl2;
           float a = 1.f;
           if (mt > m_used + kRescaleLog2) {
@@ -711,7 +716,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (j == 0) a = 1.f;  // the first P V overwrites O
           const float msub = (m_used == -CUDART_INF_F) ? 0.f : m_used;
           uint32_t pk[32];
-          float rs = 0.f;
+          float rsq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             float e0 = ex2_approx(fmaf(__uint_as_float(sraw[2 * c]), sl2, -msub));
@@ -720,10 +725,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               e0 = ((vmask >> (2 * c)) & 1ull) ? e0 : 0.f;
               e1 = ((vmask >> (2 * c + 1)) & 1ull) ? e1 : 0.f;
             }
-            rs += e0 + e1;
+            rsq[c & 3] += e0 + e1;
             pk[c] = pack_bf16x2(e0, e1);
           }
-          l += rs;
+          l += (rsq[0] + rsq[1]) + (rsq[2] + rsq[3]);
 
           // ---- hand P and the rescale factor to the O-CTA: one bulk copy per tile ----
           // local buffer sb was last read by the copy of tile g-2
