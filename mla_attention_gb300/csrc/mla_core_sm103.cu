@@ -72,7 +72,7 @@ constexpr float kRescaleLog2 = 8.0f;    // rescale O only when the max grows by 
 struct Bars {
   // S-CTA
   // s_go[b]: K tile g (b = g % 2) landed AND every row read S tile g-2 out of buffer b
-  // (128 row arrivals + the producer's expect_tx), so the MMA warp waits once per tile.
+  // (one arrival per row warp + the producer's expect_tx), so the MMA warp waits once per tile.
   // s_full[b]: the S MMA of tile g is done: S is ready, and stage b may be refilled.
   uint64_t s_go[2];
   uint64_t s_full[2];
@@ -253,6 +253,19 @@ __device__ __forceinline__ void prefetch_l2(const void* ptr) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
 }
 
+// One arrival per warp: the lanes' earlier writes are ordered before lane 0's arrival by
+// the warp barrier, and 32 threads arriving one by one on the same word cost 32 serial
+// shared-memory atomics.  Row barriers therefore count warps, not threads.
+constexpr int kRowWarps = kRows / 32;
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+__device__ __forceinline__ void warp_arrive_remote(uint32_t bar_cluster) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive_remote(bar_cluster);
+}
+
 // The query row (and for sparse its RoPE part) that row r of item `it` reads.
 __device__ __forceinline__ bool query_row(const CoreParams& p, const Item& it, int r, const __nv_bfloat16*& qrow,
                                           const __nv_bfloat16*& qpe, int64_t& nkeys) {
@@ -342,15 +355,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     if (is_s) {
       for (int i = 0; i < 2; ++i) {
-        mbar_init(&bars.s_go[i], kRows + 1);
+        mbar_init(&bars.s_go[i], kRowWarps + 1);
         mbar_init(&bars.s_full[i], 1);
         mbar_init(&bars.pb_free[i], 1);
       }
-      mbar_init(&bars.q_full, kRows);
+      mbar_init(&bars.q_full, kRowWarps);
       mbar_init(&bars.q_taken, 2);
-      mbar_init(&bars.stats_free, kRows);
+      mbar_init(&bars.stats_free, kRowWarps);
       for (int i = 0; i < 2; ++i) {
-        mbar_init(&bars.pwritten[i], kRows);
+        mbar_init(&bars.pwritten[i], kRowWarps);
         mbar_init(&bars.pbuf_free[i], 1);
       }
     } else {
@@ -361,10 +374,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 2; ++i) {
         mbar_init(&bars.p_full[i], 1);
         mbar_init(&bars.pb_free[i], 1);
-        mbar_init(&bars.p_ready[i], kRows);
+        mbar_init(&bars.p_ready[i], kRowWarps);
       }
-      mbar_init(&bars.stats_full, kRows);
-      mbar_init(&bars.o_free, kRows);
+      mbar_init(&bars.stats_full, kRowWarps);
+      mbar_init(&bars.o_free, kRowWarps);
     }
     mbar_init(&bars.stall, 1);
     bars.abort_flag = 0;
@@ -576,8 +589,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t g = 0, i = 0;  // i counts items that have KV tiles
       bool live = true;
       // both S buffers start free (the row arrivals of tiles 0 and 1)
-      mbar_arrive(&bars.s_go[0]);
-      mbar_arrive(&bars.s_go[1]);
+      warp_arrive(&bars.s_go[0]);
+      warp_arrive(&bars.s_go[1]);
       while (live && iter.next(it)) {
         if (it.J == 0) continue;  // no key: the O-CTA writes these rows on its own
         // ---- this row's query and key limit ----
@@ -640,7 +653,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars.q_full);
+        warp_arrive(&bars.q_full);
 
         float m_used = -CUDART_INF_F;  // log2-domain offset of the exponentials
         float l = 0.f;                 // running row sum (relative to m_used)
@@ -678,7 +691,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           tmem_wait_ld();
           tc_fence_before();
-          mbar_arrive(&bars.s_go[sb]);  // S buffer sb may take tile g+2
+          warp_arrive(&bars.s_go[sb]);  // S buffer sb may take tile g+2
 
           // scores in the log2 domain: t = s * scale * log2(e); the row maximum is taken on
           // the raw dot products (their largest, or their smallest when the scale is negative)
@@ -741,14 +754,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           alpha[sb * kRows + r] = a;
           fence_proxy_async_smem();  // the bulk copy reads through the async proxy
-          mbar_arrive(&bars.pwritten[sb]);
+          warp_arrive(&bars.pwritten[sb]);
         }
         if (!live) break;
         // ---- row statistics for the epilogue ----
         if (!waitb(&bars.stats_free, (i & 1) ^ 1, W_S_STATSFREE, true)) break;
         stats[2 * r] = m_used;
         stats[2 * r + 1] = l;
-        mbar_arrive_remote(rem_stats_full);
+        warp_arrive_remote(rem_stats_full);
         ++i;
       }
     }
@@ -950,7 +963,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tmem_wait_st();
           }
           tc_fence_before();
-          mbar_arrive(&bars.p_ready[pb]);
+          warp_arrive(&bars.p_ready[pb]);
         }
         if (!live) break;
 
@@ -959,7 +972,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         float m_used, l;
         asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(m_used) : "r"(rem_stats + r * 8));
         asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(l) : "r"(rem_stats + r * 8 + 4));
-        mbar_arrive_remote(rem_stats_free);
+        warp_arrive_remote(rem_stats_free);
         // the last P V of the item: use (g-1)/2 of P buffer (g-1)%2
         if (!waitb(&bars.pb_free[(g - 1) & 1], ((g - 1) >> 1) & 1, W_O_PVDONE, false)) break;
         tc_fence_after();
@@ -1021,7 +1034,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           // O has been read: the next item's P V may start
           tc_fence_before();
-          mbar_arrive(&bars.o_free);
+          warp_arrive(&bars.o_free);
           if (row_ok && lse_dst) *lse_dst = lse_out;
           // the 64 rows of this half go out with TMA (rows past the end are clipped)
           fence_proxy_async_smem();
@@ -1065,7 +1078,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
           }
           tc_fence_before();
-          mbar_arrive(&bars.o_free);
+          warp_arrive(&bars.o_free);
           if (row_ok && lse_dst) *lse_dst = lse_out;
         }
         ++i;
