@@ -571,13 +571,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             bulk_copy_to_peer(rem_p_o + sb * kPBytes, smem_u32(pbuf + sb * kPBytes), kPBytes, bar);
             bulk_copy_to_peer(rem_alpha_o + sb * kRows * 4, smem_u32(alpha + sb * kRows), kRows * 4, bar);
             bulk_commit();
-            bulk_wait_read_all();                 // local buffer sb has been read
-            mbar_arrive(&bars.pbuf_free[sb]);
+            // two copies in flight: once every group but this one has been read, the local
+            // buffer of tile g-1 is free
+            bulk_wait_read_le1();
+            if (g > 0) mbar_arrive(&bars.pbuf_free[sb ^ 1]);
           }
           __syncwarp();
         }
       }
-      if (lane == 0) bulk_wait_all();  // our shared memory is read until the copies end
+      if (lane == 0) {
+        bulk_wait_all();  // our shared memory is read until the copies end
+        if (g > 0) mbar_arrive(&bars.pbuf_free[(g - 1) & 1]);
+      }
     } else if (warp < 4) {
       // ---------------- rows: Q load, online softmax, P hand-over ----------------
       const int r = tid;  // row within the tile = TMEM lane
