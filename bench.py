@@ -16,6 +16,7 @@ same workload (host cores); it is a reported baseline, not a target.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -43,6 +44,25 @@ def causal_pairs(T, Tkv, q_pos0, kv_pos0):
 
 def chunk_pairs():
     return [causal_pairs(T_TOTAL, CHUNK, 0, CHUNK * j) for j in range(T_TOTAL // CHUNK)]
+
+
+def kernel_source_digest(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the prefill kernel from the committed ncu capture, or None when the
+    kernel sources changed since that capture (the counters would describe another kernel)."""
+    try:
+        prof = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+        if kernel_source_digest(prof["kernel_sources"]) != prof["kernel_source_sha256"]:
+            return None
+        return prof.get("mla_core_kernel_prefill_bytes_per_launch")
+    except Exception:
+        return None
 
 
 def load_peaks():
@@ -361,12 +381,7 @@ def run_libmla(args, world, rank, local):
                 extra[name] = {"error": repr(e)[:300]}
         lib.check_device_status()
 
-    traffic = None
-    try:
-        prof = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
-        traffic = prof.get("mla_core_kernel_prefill_bytes_per_launch")
-    except Exception:
-        pass
+    traffic = recorded_traffic()
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
