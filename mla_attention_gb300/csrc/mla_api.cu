@@ -9,6 +9,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -111,6 +112,16 @@ uint32_t* ws_err(void* ws) { return reinterpret_cast<uint32_t*>(ws); }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Keys per score tile of the dense prefill: 128 (mla_prefill128_kernel) unless the
+// environment variable MLA_PREFILL_TILE_KEYS is 64 (mla_core_kernel), read once.
+int prefill_tile_keys() {
+  static const int keys = [] {
+    const char* v = getenv("MLA_PREFILL_TILE_KEYS");
+    return (v && atoi(v) == 64) ? 64 : 128;
+  }();
+  return keys;
+}
+
 int default_pairs() {
   int p = device_sm_count() / 2;
   return p < 1 ? 1 : p;
@@ -196,8 +207,10 @@ mla_status mla_prefill(const void* q, int64_t q_stride_t, int64_t q_stride_h, co
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   CoreMaps maps;
   memset(&maps, 0, sizeof(maps));
+  const bool tile128 = prefill_tile_keys() == 128;
   if (kv_valid > 0) {
     mla_status s = map2d(&maps.kv, kv, kDk, (uint64_t)kv_valid, (uint64_t)kv_stride, kKeys, "kv");
+    if (s == MLA_OK && tile128) s = map2d(&maps.row, kv, kDk, (uint64_t)kv_valid, (uint64_t)kv_stride, 128, "kv");
     if (s != MLA_OK) return s;
   }
   {
@@ -229,7 +242,7 @@ mla_status mla_prefill(const void* q, int64_t q_stride_t, int64_t q_stride_h, co
   p.lse = lse;
   const int64_t items = ((int64_t)T * H + kRows - 1) / kRows;
   if (items < p.num_pairs) p.num_pairs = (int)items;
-  cudaError_t e = launch_core(p, maps, st);
+  cudaError_t e = tile128 ? launch_prefill128(p, maps, st) : launch_core(p, maps, st);
   if (e != cudaSuccess) return cuda_fail(e, "mla_prefill launch");
   return ok();
 }

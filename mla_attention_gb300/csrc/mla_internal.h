@@ -88,6 +88,9 @@ struct CoreMaps {
 
 // kernels' host launchers (return cudaError_t of the launch)
 cudaError_t launch_core(const CoreParams& p, const CoreMaps& maps, cudaStream_t stream);
+// prefill with 128-key score tiles: maps.row holds the K rows with box {64, 128}, maps.kv
+// the V rows with box {64, 64}
+cudaError_t launch_prefill128(const CoreParams& p, const CoreMaps& maps, cudaStream_t stream);
 size_t core_smem_bytes();
 
 cudaError_t launch_merge(const __nv_bfloat16* out_a, const float* lse_a, const __nv_bfloat16* out_b,

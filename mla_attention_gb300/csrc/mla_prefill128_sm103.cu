@@ -1,0 +1,717 @@
+// Absorbed causal MLA prefill with 128-key score tiles (sm_103a: tcgen05, TMEM, TMA).
+//
+// What it computes is the prefill of mla_core_kernel (pages: Tenstorrent ring_mla and
+// Ascend RingMLA "prefill" sections -- scores over all 576 columns of the shared KV row,
+// V = its first 512 columns, causal mask by global position, output plus natural-log LSE,
+// merged with (prev_out, prev_lse) when given).  The tiling differs: a score tile is
+// 128 query rows x 128 keys, which the tensor core runs at about 90% of its N=256 rate
+// where the 64-key tile of mla_core_kernel runs at about 55%.
+//
+// Cluster of two CTAs per 128-row item, as in mla_core_kernel (an fp32 O tile of
+// 128 x 512 fills one SM's TMEM):
+//   S-CTA  TMEM: Q latent part (512 bf16 = 256 columns) + two S buffers of 128 columns.
+//          smem: K ring of three 48 KB groups (64-column boxes 0-2, 3-5, 6-8 of 128 rows),
+//          Q RoPE part (128 x 64, SW128), two local P buffers (128 x 128 bf16) and factors.
+//          warps 0-3: softmax, one row per thread (the 128 scores of a tile in registers,
+//          read with one TMEM wait); warp 4: TMA; warps 5, 6: S MMAs of even / odd tiles;
+//          warp 7: P copies.
+//   O-CTA  TMEM: O (512 columns).  smem: V ring of two 64-key halves (64 KB each), two P
+//          buffers and factors, the row statistics.
+//          warps 0-3: rescale and epilogue rows; warp 4: TMA; warp 5: P V MMAs.
+// Every wait is bounded (see mbar_wait); a timeout sets the abort flag, the CTA lets its
+// copies and MMAs land and leaves through the cluster barrier.
+#include <math_constants.h>
+
+#include "mla_internal.h"
+#include "mma_seq.cuh"
+#include "sm103_ptx.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kThreadsT = 256;
+constexpr int kKeysT = 128;                           // keys per score tile
+constexpr int kGroups = 3;                            // K groups per tile
+constexpr int kBoxBytesK = kKeysT * 128;              // 128 rows x 128 B
+constexpr int kGroupBytes = 3 * kBoxBytesK;           // 49152
+constexpr int kBoxBytesV = 64 * 128;                  // 64 rows x 128 B
+constexpr int kHalfBytesV = kVBoxes * kBoxBytesV;     // 65536: 64 keys x 512 columns
+constexpr int kPBytesT = kRows * kKeysT * 2;          // 32768
+constexpr int kPBoxBytes = kRows * 128;               // 16384: P for 64 keys
+constexpr int kRowWarpsS = 4;
+constexpr int kRowWarpsO = 4;
+
+// shared memory (offsets from the dynamic base, which is 1024-byte aligned; the barrier
+// block sits at the same offset in both CTAs)
+constexpr int kOffK = 0;                              // S: 3 K groups
+constexpr int kOffQpe = kGroups * kGroupBytes;        // S: Q RoPE part (147456)
+constexpr int kOffPS = kOffQpe + kRows * 128;         // S: P buffers (163840)
+constexpr int kOffAlphaS = kOffPS + 2 * kPBytesT;     // S: factors [2][128] (229376)
+constexpr int kOffV = 0;                              // O: 2 V halves
+constexpr int kOffPO = 2 * kHalfBytesV;               // O: P buffers (131072)
+constexpr int kOffAlphaO = kOffPO + 2 * kPBytesT;     // O: factors [2][128] (196608)
+constexpr int kOffStatsO = kOffAlphaO + 2 * kRows * 4;  // O: (m, l) [128][2] from the S-CTA (197632)
+constexpr int kOffBarsT = kOffAlphaS + 2 * kRows * 4;   // both (230400)
+constexpr int kSmemT = kOffBarsT + 512;               // 231936
+static_assert(kOffStatsO + kRows * 8 <= kOffBarsT, "O-CTA layout overlaps the barriers");
+static_assert(kSmemT <= 232448, "shared memory over the sm_103a limit");
+static_assert(kOffPS % 1024 == 0 && kOffPO % 1024 == 0 && kOffQpe % 1024 == 0, "SW128 operands need 1 KB");
+
+constexpr uint32_t kTmemQ = 0;      // S: Q latent part [0, 256)
+constexpr uint32_t kTmemS = 256;    // S: S buffers [256, 384), [384, 512)
+constexpr float kRescaleLog2 = 8.0f;
+
+struct BarsT {
+  // S-CTA
+  uint64_t kfull[kGroups][2];  // group k of tile t landed (index t % 2: one consumer per barrier)
+  uint64_t kempty[kGroups];    // the MMAs of group k of the last tile are done
+  uint64_t s_full[2];          // S tile of issuer b done
+  uint64_t s_free[2];          // every row warp read S buffer b
+  uint64_t q_full;             // Q of the item in TMEM / smem
+  uint64_t q_taken;            // both issuers passed q_full (count 2)
+  uint64_t pwritten[2];        // rows wrote local P buffer b
+  uint64_t pbuf_free[2];       // the copy out of local P buffer b has been read
+  uint64_t stats_free;         // the O-CTA read the row statistics (remote)
+  // O-CTA
+  uint64_t vfull[2], vempty[2];
+  uint64_t p_full[2];          // P tile and factors landed (bulk copy with its tx bytes)
+  uint64_t p_ready[2];         // rows rescaled O for P tile b
+  uint64_t stats_full;         // row statistics stored here by the S-CTA (remote)
+  uint64_t o_free;             // the epilogue read O
+  uint64_t ep_half[2];         // both warps of an epilogue half staged their rows (count 2)
+  // both
+  uint64_t pb_free[2];         // P V of O-CTA buffer b done (multicast commit)
+  uint64_t stall;              // fault injection: never arrived on
+  uint32_t tmem_base;
+  uint32_t abort_flag;
+};
+static_assert(sizeof(BarsT) <= 512, "barrier block too large");
+
+enum : uint32_t {
+  X_K_EMPTY = 0x40, X_K_FULL, X_S_FREE, X_S_FULL, X_Q_FULL, X_Q_TAKEN, X_P_WRITTEN, X_PBUF_FREE, X_PB_FREE,
+  X_STATS_FREE, X_V_EMPTY, X_V_FULL, X_P_FULL, X_P_READY, X_PV_DONE, X_STATS_FULL, X_O_FREE, X_STALL, X_EP_HALF,
+  X_ALIGN = 0x4F,
+};
+
+struct ItemT {
+  int id;  // row tile
+  int J;   // 128-key tiles
+};
+
+__device__ __forceinline__ int64_t keys_for_token(const CoreParams& p, int64_t t) {
+  int64_t n = p.kv_valid;
+  if (p.causal) {
+    const int64_t c = p.q_pos0 + t - p.kv_pos0 + 1;
+    if (c < n) n = c;
+  }
+  return n < 0 ? 0 : n;
+}
+
+// Row tiles in longest-first order, dealt round robin to the CTA pairs.  In place, a row
+// that sees no key keeps its previous (out, lse); J only falls along this order (causal)
+// or is constant, so the first key-less item ends the list.
+struct ItemIterT {
+  const CoreParams* p;
+  int64_t k;
+  __device__ void init(const CoreParams& prm, int pair) {
+    p = &prm;
+    k = pair;
+  }
+  __device__ bool next(ItemT& it) {
+    const CoreParams& P = *p;
+    const int64_t rows = (int64_t)P.T * P.H;
+    const int64_t n_items = (rows + kRows - 1) / kRows;
+    if (k >= n_items) return false;
+    const int64_t id = n_items - 1 - k;
+    k += P.num_pairs;
+    int64_t last = id * kRows + kRows - 1;
+    if (last >= rows) last = rows - 1;
+    const int64_t n = keys_for_token(P, last / P.H);
+    it.id = (int)id;
+    it.J = (int)((n + kKeysT - 1) / kKeysT);
+    if (it.J == 0 && P.prev_out && (const void*)P.prev_out == (const void*)P.out &&
+        (const void*)P.prev_lse == (const void*)P.lse)
+      return false;
+    return true;
+  }
+};
+
+__device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float a, float b) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
+    mla_prefill128_kernel(const __grid_constant__ CoreParams p, const __grid_constant__ CoreMaps maps) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  BarsT& bars = *reinterpret_cast<BarsT*>(smem + kOffBarsT);
+  const uint32_t rank = cluster_ctarank();
+  const bool is_s = (rank == 0);
+  const uint32_t peer = rank ^ 1u;
+  const int pair = blockIdx.x >> 1;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const uint32_t lim = p.spin_limit;
+  uint32_t* err = p.err;
+  // The layout assumes a 1 KB aligned dynamic base (true when the kernel has no static
+  // shared memory); anything else is refused before any barrier is touched.
+  if (smem_u32(smem) & 1023u) {
+    if (tid == 0) record_error(err, DEV_RANGE_BASE | X_ALIGN);
+    return;
+  }
+
+  // ---- setup ----
+  if (tid == 0) {
+    if (is_s) {
+      for (int k = 0; k < kGroups; ++k) {
+        mbar_init(&bars.kfull[k][0], 1);
+        mbar_init(&bars.kfull[k][1], 1);
+        mbar_init(&bars.kempty[k], 1);
+      }
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&bars.s_full[b], 1);
+        mbar_init(&bars.s_free[b], kRowWarpsS);
+        mbar_init(&bars.pwritten[b], kRowWarpsS);
+        mbar_init(&bars.pbuf_free[b], 1);
+        mbar_init(&bars.pb_free[b], 1);
+      }
+      mbar_init(&bars.q_full, kRowWarpsS);
+      mbar_init(&bars.q_taken, 2);
+      mbar_init(&bars.stats_free, kRowWarpsO);
+    } else {
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&bars.vfull[b], 1);
+        mbar_init(&bars.vempty[b], 1);
+        mbar_init(&bars.p_full[b], 1);
+        mbar_init(&bars.p_ready[b], kRowWarpsO);
+        mbar_init(&bars.pb_free[b], 1);
+      }
+      mbar_init(&bars.stats_full, kRowWarpsS);
+      mbar_init(&bars.o_free, kRowWarpsO);
+      mbar_init(&bars.ep_half[0], 2);
+      mbar_init(&bars.ep_half[1], 2);
+    }
+    mbar_init(&bars.stall, 1);
+    bars.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&bars.tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&maps.kv);
+    tma_prefetch_desc(&maps.row);
+    tma_prefetch_desc(&maps.out);
+    if (p.prev_out) tma_prefetch_desc(&maps.prev);
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tbase = bars.tmem_base;
+  volatile uint32_t* abort_flag = &bars.abort_flag;
+  auto waitb = [&](uint64_t* bar, uint32_t parity, uint32_t site, bool cl) -> bool {
+    bool ok = (*abort_flag == 0) && mbar_wait(bar, parity, err, site, lim, cl);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) *abort_flag = 1;
+    return ok;
+  };
+  // single-thread wait for the MMA issuers (no warp-collective tcgen05 instruction follows)
+  auto wait1 = [&](uint64_t* bar, uint32_t parity, uint32_t site, bool cl) -> bool {
+    const bool ok = (*abort_flag == 0) && mbar_wait(bar, parity, err, site, lim, cl);
+    if (!ok) *abort_flag = 1;
+    return ok;
+  };
+  if (p.debug_stall && warp == 5) waitb(&bars.stall, 0, X_STALL, false);  // runs out: injected fault
+
+  ItemIterT iter;
+  iter.init(p, pair);
+  ItemT it;
+  const CUtensorMap& map_k = maps.row;   // K rows, box {64, 128}
+  const CUtensorMap& map_v = maps.kv;    // V rows, box {64, 64}
+
+  if (is_s) {
+    // =====================================================================
+    // S-CTA
+    // =====================================================================
+    if (warp == 4) {
+      // ---------------- TMA producer: K groups ----------------
+      // Group k of every tile goes to slot k once the MMAs of group k of the previous tile
+      // are done; its landing barrier alternates with the tile's parity, so each issuer
+      // waits only on the barriers of its own tiles.
+      uint32_t t = 0;
+      bool live = true;
+      while (live && iter.next(it)) {
+        for (int j = 0; j < it.J && live; ++j, ++t) {
+          const uint32_t par = t & 1;
+          for (int k = 0; k < kGroups; ++k) {
+            if (!waitb(&bars.kempty[k], par ^ 1, X_K_EMPTY, false)) { live = false; break; }
+            if (lane == 0) {
+              uint64_t* fb = &bars.kfull[k][par];
+              mbar_arrive_expect_tx(fb, kGroupBytes);
+              const uint32_t dst = smem_u32(smem + kOffK + k * kGroupBytes);
+              for (int i = 0; i < 3; ++i)
+                tma_load_2d(dst + i * kBoxBytesK, &map_k, (3 * k + i) * kBoxCols, j * kKeysT, fb);
+            }
+            __syncwarp();
+          }
+        }
+      }
+    } else if (warp == 5 || warp == 6) {
+      // ---------------- S MMA issuers: even tiles (warp 5), odd tiles (warp 6) ----------------
+      // A barrier wait by the thread that issued MMAs stalls until its queued MMAs drain;
+      // the other issuer's queued tile keeps the tensor pipe busy meanwhile.
+      if (lane == 0) {
+        const uint32_t b = (uint32_t)(warp - 5);
+        const uint32_t idesc = idesc_bf16_f32(kRows, kKeysT, false, false);
+        const uint64_t a_rope = sdesc_sw128(smem_u32(smem + kOffQpe), 16, 1024);
+        const uint32_t d_tmem = tbase + kTmemS + b * kKeysT;
+        uint32_t t = 0, i = 0, nb = 0;  // all tiles, items with keys, this issuer's tiles
+        bool live = true;
+        while (live && iter.next(it)) {
+          if (it.J == 0) continue;
+          if (!wait1(&bars.q_full, i & 1, X_Q_FULL, false)) break;
+          mbar_arrive(&bars.q_taken);
+          for (int j = 0; j < it.J && live; ++j, ++t) {
+            if ((t & 1u) != b) continue;
+            // S buffer b was read by the rows (this issuer's previous tile)
+            if (!wait1(&bars.s_free[b], (nb & 1) ^ 1, X_S_FREE, false)) { live = false; break; }
+            for (int k = 0; k < kGroups; ++k) {
+              if (!wait1(&bars.kfull[k][b], nb & 1, X_K_FULL, false)) { live = false; break; }
+              tc_fence_after();
+              const uint64_t bd = sdesc_sw128(smem_u32(smem + kOffK + k * kGroupBytes), 16, 1024);
+              if (k < 2) mma_s_grp3_n128(d_tmem, tbase + kTmemQ + 96 * k, bd, idesc, (uint32_t)k);
+              else mma_s_grp2r_n128(d_tmem, tbase + kTmemQ + 192, bd, a_rope, idesc);
+              mma_commit(&bars.kempty[k]);
+            }
+            if (!live) break;
+            mma_commit(&bars.s_full[b]);
+            ++nb;
+          }
+          ++i;
+        }
+      }
+      __syncwarp();
+    } else if (warp == 7) {
+      // ---------------- P copies into the O-CTA, two in flight ----------------
+      const uint8_t* pbuf = smem + kOffPS;
+      const float* alpha = reinterpret_cast<const float*>(smem + kOffAlphaS);
+      const uint32_t rem_p_full0 = map_to_rank(smem_u32(&bars.p_full[0]), peer);
+      const uint32_t rem_p_full1 = map_to_rank(smem_u32(&bars.p_full[1]), peer);
+      const uint32_t rem_p_o = map_to_rank(smem_u32(smem + kOffPO), peer);
+      const uint32_t rem_alpha_o = map_to_rank(smem_u32(smem + kOffAlphaO), peer);
+      uint32_t t = 0;
+      bool live = true;
+      while (live && iter.next(it)) {
+        for (int j = 0; j < it.J; ++j, ++t) {
+          const int sb = t & 1;
+          if (!waitb(&bars.pwritten[sb], (t >> 1) & 1, X_P_WRITTEN, false) ||
+              !waitb(&bars.pb_free[sb], ((t >> 1) & 1) ^ 1, X_PB_FREE, true)) {
+            live = false;
+            break;
+          }
+          if (lane == 0) {
+            const uint32_t bar = sb ? rem_p_full1 : rem_p_full0;
+            mbar_arrive_expect_tx_remote(bar, kPBytesT + kRows * 4);
+            bulk_copy_to_peer(rem_p_o + sb * kPBytesT, smem_u32(pbuf + sb * kPBytesT), kPBytesT, bar);
+            bulk_copy_to_peer(rem_alpha_o + sb * kRows * 4, smem_u32(alpha + sb * kRows), kRows * 4, bar);
+            bulk_commit();
+            bulk_wait_read_le1();  // every copy but this one has been read
+            if (t > 0) mbar_arrive(&bars.pbuf_free[sb ^ 1]);
+          }
+          __syncwarp();
+        }
+      }
+      if (lane == 0) {
+        bulk_wait_all();
+        if (t > 0) mbar_arrive(&bars.pbuf_free[(t - 1) & 1]);
+      }
+    } else if (warp < kRowWarpsS) {
+      // ---------------- rows: Q load, online softmax, one row per thread ----------------
+      const int r = tid;  // row within the item = TMEM lane
+      const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+      float* alpha = reinterpret_cast<float*>(smem + kOffAlphaS);
+      const uint32_t rem_stats = map_to_rank(smem_u32(smem + kOffStatsO), peer);
+      const uint32_t rem_stats_full = map_to_rank(smem_u32(&bars.stats_full), peer);
+      const float sl2 = p.scale_log2;
+      const bool up = sl2 >= 0.f;  // the row extreme is the largest raw score, or the smallest
+      uint32_t t = 0, i = 0;
+      bool live = true;
+      while (live && iter.next(it)) {
+        if (it.J == 0) continue;  // no key: the O-CTA writes these rows on its own
+        const int64_t f = (int64_t)it.id * kRows + r;
+        const bool row_ok = f < (int64_t)p.T * p.H;
+        const __nv_bfloat16* qrow = nullptr;
+        int64_t nkeys = 0;
+        if (row_ok) {
+          const int64_t tt = f / p.H, hh = f - tt * p.H;
+          qrow = p.q + tt * p.q_stride_t + hh * p.q_stride_h;
+          nkeys = keys_for_token(p, tt);
+        }
+        // ---- Q: latent part -> TMEM (256 columns), RoPE part -> smem (SW128 K-major) ----
+        if (i > 0 && !waitb(&bars.q_taken, (i - 1) & 1, X_Q_TAKEN, false)) break;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 8; c0 += 2) {
+          uint4 x[2][8];
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const uint4* src = row_ok ? reinterpret_cast<const uint4*>(qrow + 64 * (c0 + cc)) : nullptr;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) x[cc][u] = src ? __ldg(src + u) : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t v[32];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              v[4 * u + 0] = x[cc][u].x;
+              v[4 * u + 1] = x[cc][u].y;
+              v[4 * u + 2] = x[cc][u].z;
+              v[4 * u + 3] = x[cc][u].w;
+            }
+            tmem_st32(tbase + lane_base + kTmemQ + 32 * (c0 + cc), v);
+          }
+        }
+        {
+          uint8_t* qpe_row = smem + kOffQpe + r * 128;
+          const uint4* src = row_ok ? reinterpret_cast<const uint4*>(qrow + kLatent) : nullptr;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v = src ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(qpe_row + ((c ^ (r & 7)) << 4)) = v;
+          }
+          fence_proxy_async_smem();  // read by the MMA through the async proxy
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        warp_arrive(&bars.q_full);
+
+        float m_used = -CUDART_INF_F;  // log2-domain offset of the exponentials
+        float l = 0.f;                 // running row sum (relative to m_used)
+        for (int j = 0; j < it.J; ++j, ++t) {
+          const int sb = t & 1;
+          int64_t nv64 = nkeys - (int64_t)j * kKeysT;  // keys of this tile visible to the row
+          const int nv = (int)(nv64 < 0 ? 0 : (nv64 > kKeysT ? kKeysT : nv64));
+
+          if (!waitb(&bars.s_full[sb], (t >> 1) & 1, X_S_FULL, false)) { live = false; break; }
+          tc_fence_after();
+          // Two passes over the tile in 32-column pieces read from TMEM (a rolled loop each,
+          // so the loop body stays small): the row extreme first, then the exponentials.
+          const uint32_t scol = tbase + lane_base + kTmemS + sb * kKeysT;
+          float eq[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) eq[k] = up ? -CUDART_INF_F : CUDART_INF_F;
+#pragma unroll 1
+          for (int p32 = 0; p32 < kKeysT / 32; ++p32) {
+            uint32_t sr[32];
+            tmem_ld32(scol + 32 * p32, sr);
+            tmem_wait_ld();
+            const int lim = nv - 32 * p32;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const float v = __uint_as_float(sr[c]);
+              eq[c & 3] = (c >= lim) ? eq[c & 3] : (up ? fmaxf(eq[c & 3], v) : fminf(eq[c & 3], v));
+            }
+          }
+          const float e = up ? fmaxf(fmaxf(eq[0], eq[1]), fmaxf(eq[2], eq[3]))
+                             : fminf(fminf(eq[0], eq[1]), fminf(eq[2], eq[3]));
+          const float mt = (nv == 0) ? -CUDART_INF_F : e * sl2;
+          float a = 1.f;
+          if (mt > m_used + kRescaleLog2) {
+            a = ex2_approx(m_used - mt);  // 0 while nothing was accumulated (m_used = -inf)
+            l *= a;
+            m_used = mt;
+          }
+          if (j == 0) a = 1.f;  // the first P V overwrites O
+          const float msub = (m_used == -CUDART_INF_F) ? 0.f : m_used;
+
+          // ---- P (two K-major boxes of 64 keys) and the rescale factor ----
+          if (!waitb(&bars.pbuf_free[sb], ((t >> 1) & 1) ^ 1, X_PBUF_FREE, false)) { live = false; break; }
+          uint8_t* prow = smem + kOffPS + sb * kPBytesT + r * 128;
+          float rsq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+          for (int p32 = 0; p32 < kKeysT / 32; ++p32) {
+            uint32_t sr[32];
+            tmem_ld32(scol + 32 * p32, sr);
+            tmem_wait_ld();
+            const int lim = nv - 32 * p32;
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) {  // 8 keys -> one 16-byte chunk of P
+              uint32_t w[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int c = 8 * c8 + 2 * u;
+                float e0 = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -msub));
+                float e1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), sl2, -msub));
+                e0 = (c < lim) ? e0 : 0.f;
+                e1 = (c + 1 < lim) ? e1 : 0.f;
+                rsq[u] += e0 + e1;
+                w[u] = pack_bf16x2(e0, e1);
+              }
+              const int kc = 4 * p32 + c8;  // 16-byte chunk of the 128-key row
+              const int box = kc >> 3, chunk = kc & 7;
+              *reinterpret_cast<uint4*>(prow + box * kPBoxBytes + ((chunk ^ (r & 7)) << 4)) =
+                  make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+          tc_fence_before();
+          warp_arrive(&bars.s_free[sb]);  // S buffer sb has been read
+          l += (rsq[0] + rsq[1]) + (rsq[2] + rsq[3]);
+          alpha[sb * kRows + r] = a;
+          fence_proxy_async_smem();  // the bulk copy reads through the async proxy
+          warp_arrive(&bars.pwritten[sb]);
+        }
+        if (!live) break;
+        // ---- row statistics into the O-CTA ----
+        if (!waitb(&bars.stats_free, (i & 1) ^ 1, X_STATS_FREE, false)) break;
+        st_cluster_f32x2(rem_stats + r * 8, m_used, l);
+        warp_arrive_remote(rem_stats_full);
+        ++i;
+      }
+    }
+  } else {
+    // =====================================================================
+    // O-CTA
+    // =====================================================================
+    if (warp == 4) {
+      // ---------------- TMA producer: V halves (64 keys x 512 columns), epilogue stages ----------------
+      uint32_t u = 0;  // position in the two-slot ring
+      bool live = true;
+      while (live && iter.next(it)) {
+        for (int j = 0; j < it.J && live; ++j) {
+          for (int h = 0; h < 2; ++h, ++u) {
+            const int s = u & 1;
+            if (!waitb(&bars.vempty[s], ((u >> 1) & 1) ^ 1, X_V_EMPTY, false)) { live = false; break; }
+            if (lane == 0) {
+              const uint32_t dst = smem_u32(smem + kOffV + s * kHalfBytesV);
+              mbar_arrive_expect_tx(&bars.vfull[s], kHalfBytesV);
+              for (int bx = 0; bx < kVBoxes; ++bx)
+                tma_load_2d(dst + bx * kBoxBytesV, &map_v, bx * kBoxCols, j * kKeysT + 64 * h, &bars.vfull[s]);
+            }
+            __syncwarp();
+          }
+        }
+        // the two ring slots then stage the epilogue: rows 0-63 and 64-127 (with prev)
+        if (it.J > 0) {
+          for (int h = 0; h < 2 && live; ++h, ++u) {
+            const int s = u & 1;
+            if (!waitb(&bars.vempty[s], ((u >> 1) & 1) ^ 1, X_V_EMPTY, false)) { live = false; break; }
+            if (lane == 0) {
+              const int64_t row0 = (int64_t)it.id * kRows + h * 64;
+              if (p.prev_out && row0 < (int64_t)p.T * p.H) {
+                const uint32_t dst = smem_u32(smem + kOffV + s * kHalfBytesV);
+                mbar_arrive_expect_tx(&bars.vfull[s], kHalfBytesV);
+                for (int bx = 0; bx < kVBoxes; ++bx)
+                  tma_load_2d(dst + bx * kBoxBytesV, &maps.prev, bx * kBoxCols, (int32_t)row0, &bars.vfull[s]);
+              } else {
+                mbar_arrive(&bars.vfull[s]);
+              }
+            }
+            __syncwarp();
+          }
+        }
+      }
+    } else if (warp == 5) {
+      // ---------------- P V issuer ----------------
+      if (lane == 0) {
+        const uint32_t idesc = idesc_bf16_f32(kRows, 256, false, true);
+        uint32_t t = 0, u = 0, i = 0;
+        bool live = true;
+        while (live && iter.next(it)) {
+          if (it.J == 0) continue;
+          if (i > 0 && !wait1(&bars.o_free, (i - 1) & 1, X_O_FREE, false)) break;
+          for (int j = 0; j < it.J && live; ++j, ++t) {
+            const int pb = t & 1;
+            if (!wait1(&bars.p_ready[pb], (t >> 1) & 1, X_P_READY, false)) { live = false; break; }
+            for (int h = 0; h < 2; ++h, ++u) {
+              const int s = u & 1;
+              if (!wait1(&bars.vfull[s], (u >> 1) & 1, X_V_FULL, false)) { live = false; break; }
+              tc_fence_after();
+              const uint32_t vst = smem_u32(smem + kOffV + s * kHalfBytesV);
+              const uint32_t pst = smem_u32(smem + kOffPO + pb * kPBytesT + h * kPBoxBytes);
+              mma_pv_k64_n512(tbase, tbase + 256, sdesc_sw128(pst, 16, 1024), sdesc_sw128(vst, kBoxBytesV, 1024),
+                              sdesc_sw128(vst + 4 * kBoxBytesV, kBoxBytesV, 1024), idesc,
+                              (j > 0 || h > 0) ? 1u : 0u);
+              mma_commit(&bars.vempty[s]);
+            }
+            if (!live) break;
+            mma_commit_multicast(&bars.pb_free[pb], 0x3);  // this CTA and the S-CTA
+          }
+          u += 2;  // the epilogue's stages
+          ++i;
+        }
+      }
+      __syncwarp();
+    } else if (warp < kRowWarpsO) {
+      // ---------------- rows: lazy rescale, epilogue ----------------
+      const int r = tid;
+      const int half = r >> 6;
+      const int rr = r & 63;
+      const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+      const uint32_t rem_stats_free = map_to_rank(smem_u32(&bars.stats_free), peer);
+      const float* alpha_o = reinterpret_cast<const float*>(smem + kOffAlphaO);
+      const float* stats = reinterpret_cast<const float*>(smem + kOffStatsO);
+      uint32_t t = 0, u = 0, i = 0;
+      bool live = true;
+      bool stored = false;
+      while (live && iter.next(it)) {
+        const int64_t f = (int64_t)it.id * kRows + r;
+        const bool row_ok = f < (int64_t)p.T * p.H;
+        float prev_l = -CUDART_INF_F;
+        const __nv_bfloat16* prev_row = nullptr;
+        __nv_bfloat16* orow = nullptr;
+        float* lse_dst = nullptr;
+        if (row_ok) {
+          const int64_t tt = f / p.H, hh = f - tt * p.H;
+          orow = p.out + f * kLatent;
+          lse_dst = p.lse + hh * p.T + tt;
+          if (p.prev_out) {
+            prev_row = p.prev_out + f * kLatent;
+            prev_l = p.prev_lse[hh * p.T + tt];
+          }
+        }
+        if (it.J == 0) {
+          // no key reaches these rows: out = prev (or 0), lse = prev_lse (or -inf)
+          if (row_ok) {
+            for (int c = 0; c < kLatent; c += 8) {
+              uint4 v = prev_row ? *reinterpret_cast<const uint4*>(prev_row + c) : make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(orow + c) = v;
+            }
+            *lse_dst = prev_row ? prev_l : -CUDART_INF_F;
+          }
+          continue;
+        }
+        for (int j = 0; j < it.J; ++j, ++t) {
+          const int pb = t & 1;
+          if (!waitb(&bars.p_full[pb], (t >> 1) & 1, X_P_FULL, true)) { live = false; break; }
+          const float a = alpha_o[pb * kRows + r];
+          if (__any_sync(0xffffffffu, a != 1.f)) {
+            // O holds every earlier P V before it is rescaled (P V of tile t-1 is done)
+            if (!waitb(&bars.pb_free[(t - 1) & 1], ((t - 1) >> 1) & 1, X_PV_DONE, false)) { live = false; break; }
+            tc_fence_after();
+#pragma unroll 1
+            for (int c0 = 0; c0 < kLatent; c0 += 32) {
+              uint32_t v[32];
+              tmem_ld32(tbase + lane_base + c0, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * a);
+              tmem_st32(tbase + lane_base + c0, v);
+            }
+            tmem_wait_st();
+          }
+          tc_fence_before();
+          warp_arrive(&bars.p_ready[pb]);
+        }
+        if (!live) break;
+        u += 2 * it.J;
+
+        // ---- epilogue ----
+        if (!waitb(&bars.stats_full, i & 1, X_STATS_FULL, true)) break;
+        const float m_used = stats[2 * r];
+        const float l = stats[2 * r + 1];
+        warp_arrive_remote(rem_stats_free);
+        if (!waitb(&bars.pb_free[(t - 1) & 1], ((t - 1) >> 1) & 1, X_PV_DONE, false)) break;
+        tc_fence_after();
+        const bool has = l > 0.f;
+        const float inv_l = has ? 1.f / l : 0.f;
+        const float lse_new = has ? (m_used + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+        float wn = has ? 1.f : 0.f, wp = 0.f, lse_out = lse_new;
+        if (row_ok && prev_row) {
+          const float m = fmaxf(prev_l, lse_new);
+          if (m == -CUDART_INF_F) {
+            wn = 0.f;
+            wp = 0.f;
+            lse_out = -CUDART_INF_F;
+          } else {
+            wp = (prev_l == -CUDART_INF_F) ? 0.f : expf(prev_l - m);
+            wn = has ? expf(lse_new - m) : 0.f;
+            const float ws = wp + wn;
+            lse_out = m + logf(ws);
+            wp /= ws;
+            wn /= ws;
+          }
+        }
+        const float cn = wn * inv_l;
+        // rows of this half live in ring slot (u + half), [8 column boxes][64 rows][128 B] swizzled
+        const uint32_t sidx = u + half;
+        const int s = sidx & 1;
+        if (!waitb(&bars.vfull[s], (sidx >> 1) & 1, X_V_FULL, false)) break;
+        uint8_t* stage = smem + kOffV + s * kHalfBytesV;
+        const bool use_prev = (prev_row != nullptr) && wp > 0.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kLatent; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(tbase + lane_base + c0, v);
+          tmem_wait_ld();
+          uint8_t* rowp = stage + (c0 >> 6) * kBoxBytesV + rr * 128;
+          const int g0 = (c0 & 63) >> 3;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4* cell = reinterpret_cast<uint4*>(rowp + (((g0 + q) ^ (rr & 7)) << 4));
+            float o[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) o[k] = __uint_as_float(v[8 * q + k]) * cn;
+            if (use_prev) {
+              const uint4 x = *cell;
+              const __nv_bfloat162* hx = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float2 f2 = __bfloat1622float2(hx[k]);
+                o[2 * k] += wp * f2.x;
+                o[2 * k + 1] += wp * f2.y;
+              }
+            }
+            *cell = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
+                               pack_bf16x2(o[6], o[7]));
+          }
+        }
+        tc_fence_before();
+        warp_arrive(&bars.o_free);  // O has been read: the next item's P V may start
+        if (row_ok) *lse_dst = lse_out;
+        fence_proxy_async_smem();
+        // both warps of this half staged their rows (a bounded wait, unlike a named barrier)
+        warp_arrive(&bars.ep_half[half]);
+        if (!waitb(&bars.ep_half[half], i & 1, X_EP_HALF, false)) break;
+        if (rr == 0) {
+          const int32_t row0 = it.id * kRows + half * 64;
+          const uint32_t sbase = smem_u32(stage);
+          for (int bx = 0; bx < kVBoxes; ++bx) tma_store_2d(&maps.out, bx * kBoxCols, row0, sbase + bx * kBoxBytesV);
+          bulk_commit();
+          bulk_wait_read_all();
+          stored = true;
+          mbar_arrive(&bars.vempty[s]);
+        }
+        u += 2;
+        ++i;
+      }
+      if (stored) bulk_wait_all();
+    }
+  }
+
+  // ---- teardown: drain on abort, then leave together ----
+  __syncwarp();
+  if (*abort_flag) {
+    for (int k = 0; k < 200; ++k) __nanosleep(1000);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 5) tmem_dealloc(tbase, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill128(const CoreParams& p, const CoreMaps& maps, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(mla_prefill128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemT);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  if (p.num_pairs <= 0) return cudaSuccess;
+  mla_prefill128_kernel<<<dim3(2 * p.num_pairs), dim3(kThreadsT), kSmemT, stream>>>(p, maps);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -30,6 +30,39 @@ __device__ __forceinline__ void mma_s_q576_n64(uint32_t d_tmem, uint32_t a_tmem,
       : "memory");
 }
 
+// ---- 128-key score tiles: M128 N128, K streamed in groups of three 64-column boxes of
+// 128 rows (16 KB each, 1024 units) ----
+#define MLA_TS128(P, BINC) \
+  "tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %3, " P ";\n\tadd.u32 at, at, 8;\n\tadd.s64 bd, bd, " #BINC ";\n\t"
+#define MLA_TS128_BOX(P0) MLA_TS128(P0, 2) MLA_TS128("pt", 2) MLA_TS128("pt", 2) MLA_TS128("pt", 1018)
+#define MLA_SS128(P) \
+  "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, " P ";\n\tadd.s64 ad, ad, 2;\n\tadd.s64 bd, bd, 2;\n\t"
+
+// S[128 x 128] (+)= Q[:, three latent boxes] (TMEM, 96 columns from a_tmem) * K_group^T.
+// accumulate = 0 overwrites S (the first group of a tile).
+__device__ __forceinline__ void mma_s_grp3_n128(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred pa, pt;\n\t.reg .b64 bd;\n\t.reg .b32 at;\n\t"
+      "setp.ne.u32 pa, %4, 0;\n\tsetp.eq.u32 pt, %3, %3;\n\tmov.b64 bd, %2;\n\tmov.b32 at, %1;\n\t"
+      MLA_TS128_BOX("pa") MLA_TS128_BOX("pt") MLA_TS128_BOX("pt")
+      "}" ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// S[128 x 128] += Q[:, two latent boxes] (TMEM) * K_group[boxes 0, 1]^T + Q_rope (smem, 128 x 64)
+// * K_group[box 2]^T.
+__device__ __forceinline__ void mma_s_grp2r_n128(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                 uint64_t a_rope_desc, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred pt;\n\t.reg .b64 bd, ad;\n\t.reg .b32 at;\n\t"
+      "setp.eq.u32 pt, %3, %3;\n\tmov.b64 bd, %2;\n\tmov.b32 at, %1;\n\tmov.b64 ad, %4;\n\t"
+      MLA_TS128_BOX("pt") MLA_TS128_BOX("pt")
+      MLA_SS128("pt") MLA_SS128("pt") MLA_SS128("pt") MLA_SS128("pt")
+      "}" ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "l"(a_rope_desc)
+      : "memory");
+}
+
 #define MLA_PV256(ACC) \
   "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd0, %4, " ACC ";\n\t" \
   "tcgen05.mma.cta_group::1.kind::f16 [%1], ad, bd1, %4, " ACC ";\n\t" \
@@ -85,5 +118,8 @@ __device__ __forceinline__ void mma_pv_tmem_k128_n128(uint32_t d_tmem, uint32_t 
 #undef MLA_SS
 #undef MLA_SS_BOX128
 #undef MLA_TSV
+#undef MLA_TS128
+#undef MLA_TS128_BOX
+#undef MLA_SS128
 
 }  // namespace mla
