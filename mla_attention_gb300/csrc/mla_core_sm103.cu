@@ -633,44 +633,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
           if (!waitb(&bars.s_full[sb], (g >> 1) & 1, W_S_SFULL, false)) { live = false; break; }
           tc_fence_after();
-          uint32_t sraw[64];
-          {
-            uint32_t (&a)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sraw[0]);
-            uint32_t (&b)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sraw[32]);
-            tmem_ld32(tbase + lane_base + kTmemS + sb * kKeys, a);
-            tmem_ld32(tbase + lane_base + kTmemS + sb * kKeys + 32, b);
-          }
-          tmem_wait_ld();
-          tc_fence_before();
-          warp_arrive(&bars.s_go[sb]);  // S buffer sb may take tile g+2
-
-          // scores in the log2 domain: t = s * scale * log2(e); the row maximum is taken on
-          // the raw dot products (their largest, or their smallest when the scale is negative)
+          // Scores in the log2 domain: t = s * scale * log2(e); the row maximum is taken on the
+          // raw dot products (their largest, or their smallest when the scale is negative).
+          // Two passes over the tile in 32-column pieces read from TMEM, each a rolled loop:
+          // fully unrolled 64-column loops made the row loop too large for the instruction
+          // cache, which slowed these warps several times over.
+          const uint32_t scol = tbase + lane_base + kTmemS + sb * kKeys;
           const float sl2 = p.scale_log2;
-          const bool full = (vmask == ~0ull);
-          // four independent chains each for the max, the min and the sum: one row warp per
-          // sub-partition has no other warp to hide a 64-long dependent chain behind
-          float hq[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
-          float lq[4] = {CUDART_INF_F, CUDART_INF_F, CUDART_INF_F, CUDART_INF_F};
-          if (full) {
+          const bool up = sl2 >= 0.f;
+          float eq[4];
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-              const float v = __uint_as_float(sraw[c]);
-              hq[c & 3] = fmaxf(hq[c & 3], v);
-              lq[c & 3] = fminf(lq[c & 3], v);
-            }
-          } else {
+          for (int k = 0; k < 4; ++k) eq[k] = up ? -CUDART_INF_F : CUDART_INF_F;
+#pragma unroll 1
+          for (int p32 = 0; p32 < kKeys / 32; ++p32) {
+            uint32_t sr[32];
+            tmem_ld32(scol + 32 * p32, sr);
+            tmem_wait_ld();
+            const uint32_t vm = (uint32_t)(vmask >> (32 * p32));
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-              const bool ok = (vmask >> c) & 1ull;
-              const float v = __uint_as_float(sraw[c]);
-              hq[c & 3] = ok ? fmaxf(hq[c & 3], v) : hq[c & 3];
-              lq[c & 3] = ok ? fminf(lq[c & 3], v) : lq[c & 3];
+            for (int c = 0; c < 32; ++c) {
+              const float v = __uint_as_float(sr[c]);
+              const bool ok = (vm >> c) & 1u;
+              eq[c & 3] = !ok ? eq[c & 3] : (up ? fmaxf(eq[c & 3], v) : fminf(eq[c & 3], v));
             }
           }
-          const float hi_raw = fmaxf(fmaxf(hq[0], hq[1]), fmaxf(hq[2], hq[3]));
-          const float lo_raw = fminf(fminf(lq[0], lq[1]), fminf(lq[2], lq[3]));
-          const float mt = (vmask == 0ull) ? -CUDART_INF_F : (sl2 >= 0.f ? hi_raw : lo_raw) * sl2;
+          const float ext = up ? fmaxf(fmaxf(eq[0], eq[1]), fmaxf(eq[2], eq[3]))
+                               : fminf(fminf(eq[0], eq[1]), fminf(eq[2], eq[3]));
+          const float mt = (vmask == 0ull) ? -CUDART_INF_F : ext * sl2;
           float a = 1.f;
           if (mt > m_used + kRescaleLog2) {
             if (l > 0.f) a = ex2_approx(m_used - mt);
@@ -679,30 +668,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           if (j == 0) a = 1.f;  // the first P V overwrites O
           const float msub = (m_used == -CUDART_INF_F) ? 0.f : m_used;
-          uint32_t pk[32];
-          float rsq[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            float e0 = ex2_approx(fmaf(__uint_as_float(sraw[2 * c]), sl2, -msub));
-            float e1 = ex2_approx(fmaf(__uint_as_float(sraw[2 * c + 1]), sl2, -msub));
-            if (!full) {
-              e0 = ((vmask >> (2 * c)) & 1ull) ? e0 : 0.f;
-              e1 = ((vmask >> (2 * c + 1)) & 1ull) ? e1 : 0.f;
-            }
-            rsq[c & 3] += e0 + e1;
-            pk[c] = pack_bf16x2(e0, e1);
-          }
-          l += (rsq[0] + rsq[1]) + (rsq[2] + rsq[3]);
 
-          // ---- hand P and the rescale factor to the O-CTA: one bulk copy per tile ----
+          // ---- P into the local buffer (the copy warp hands it to the O-CTA) ----
           // local buffer sb was last read by the copy of tile g-2
           if (!waitb(&bars.pbuf_free[sb], ((g >> 1) & 1) ^ 1, W_S_PFREE, false)) { live = false; break; }
           uint8_t* prow = pbuf + sb * kPBytes + r * 128;
+          float rsq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+          for (int p32 = 0; p32 < kKeys / 32; ++p32) {
+            uint32_t sr[32];
+            tmem_ld32(scol + 32 * p32, sr);
+            tmem_wait_ld();
+            const uint32_t vm = (uint32_t)(vmask >> (32 * p32));
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint4 v4 = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-            *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = v4;
+            for (int c8 = 0; c8 < 4; ++c8) {  // 8 keys -> one 16-byte chunk of P
+              uint32_t w[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int c = 8 * c8 + 2 * u;
+                float e0 = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -msub));
+                float e1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), sl2, -msub));
+                e0 = ((vm >> c) & 1u) ? e0 : 0.f;
+                e1 = ((vm >> (c + 1)) & 1u) ? e1 : 0.f;
+                rsq[u] += e0 + e1;
+                w[u] = pack_bf16x2(e0, e1);
+              }
+              const int kc = 4 * p32 + c8;
+              *reinterpret_cast<uint4*>(prow + ((kc ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
           }
+          tc_fence_before();
+          warp_arrive(&bars.s_go[sb]);  // S buffer sb has been read: it may take tile g+2
+          l += (rsq[0] + rsq[1]) + (rsq[2] + rsq[3]);
           alpha[sb * kRows + r] = a;
           fence_proxy_async_smem();  // the bulk copy reads through the async proxy
           warp_arrive(&bars.pwritten[sb]);
