@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Every wait is made by a whole warp and its outcome is warp-uniform, so no
   // warp reaches a warp-collective tcgen05 instruction with some lanes gone.
   auto waitb = [&](uint64_t* bar, uint32_t parity, uint32_t site) -> bool {
-    bool ok = (*abort_flag == 0) && mbar_wait(bar, parity, err, site, lim);
+    bool ok = (*abort_flag == 0) && mbar_wait_inline(bar, parity, err, site, lim);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) *abort_flag = 1;
     return ok;

@@ -112,8 +112,34 @@ constexpr uint64_t kWaitWallNs = 2000000000ull;
 // Bounded wait.  Returns false (and records `site`) when `spin_limit` tries
 // or kWaitWallNs of wall time have passed, or when another thread already
 // raised an error.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t site,
-                                          uint32_t spin_limit, bool cluster_scope = false) {
+// Not inlined: one copy of the polling loop serves every call site, which keeps the
+// instruction footprint of the warp-specialised kernels small.
+static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t site,
+                                              uint32_t spin_limit, bool cluster_scope = false) {
+  const uint32_t a = smem_u32(bar);
+  uint32_t n = 0;
+  uint64_t t0 = 0;
+  while (true) {
+    bool ok = cluster_scope ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity);
+    if (ok) return true;
+    ++n;
+    bool expired = n >= spin_limit;
+    if ((n & 255u) == 1u) {
+      const uint64_t now = global_ns();
+      if (n == 1u) t0 = now;
+      else if (now - t0 > kWaitWallNs) expired = true;
+      if (n > 1u && error_raised(err)) return false;
+    }
+    if (expired) {
+      record_error(err, DEV_TIMEOUT_BASE | site);
+      return false;
+    }
+  }
+}
+
+// The same wait inlined at its call site (kernels with few wait sites).
+__device__ __forceinline__ bool mbar_wait_inline(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t site,
+                                                 uint32_t spin_limit, bool cluster_scope = false) {
   const uint32_t a = smem_u32(bar);
   uint32_t n = 0;
   uint64_t t0 = 0;
