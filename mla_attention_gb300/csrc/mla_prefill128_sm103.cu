@@ -140,6 +140,9 @@ __device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float a, float b
   asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }
 
+// kUp: the scale is >= 0, so the row extreme of the raw scores is their maximum (else
+// their minimum); one instantiation per sign keeps that choice out of the row loop.
+template <bool kUp>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
     mla_prefill128_kernel(const __grid_constant__ CoreParams p, const __grid_constant__ CoreMaps maps) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -334,7 +337,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
       const uint32_t rem_stats = map_to_rank(smem_u32(smem + kOffStatsO), peer);
       const uint32_t rem_stats_full = map_to_rank(smem_u32(&bars.stats_full), peer);
       const float sl2 = p.scale_log2;
-      const bool up = sl2 >= 0.f;  // the row extreme is the largest raw score, or the smallest
       uint32_t t = 0, i = 0;
       bool live = true;
       while (live && iter.next(it)) {
@@ -400,20 +402,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
           const uint32_t scol = tbase + lane_base + kTmemS + sb * kKeysT;
           float eq[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) eq[k] = up ? -CUDART_INF_F : CUDART_INF_F;
+          for (int k = 0; k < 4; ++k) eq[k] = kUp ? -CUDART_INF_F : CUDART_INF_F;
 #pragma unroll 1
           for (int p32 = 0; p32 < kKeysT / 32; ++p32) {
             uint32_t sr[32];
             tmem_ld32(scol + 32 * p32, sr);
             tmem_wait_ld();
             const int lim = nv - 32 * p32;
+            if (lim >= 32) {  // every key of the piece visible (warp-uniform when H = 128)
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const float v = __uint_as_float(sr[c]);
-              eq[c & 3] = (c >= lim) ? eq[c & 3] : (up ? fmaxf(eq[c & 3], v) : fminf(eq[c & 3], v));
+              for (int c = 0; c < 32; ++c) {
+                const float v = __uint_as_float(sr[c]);
+                eq[c & 3] = kUp ? fmaxf(eq[c & 3], v) : fminf(eq[c & 3], v);
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < 32; ++c) {
+                const float v = __uint_as_float(sr[c]);
+                eq[c & 3] = (c >= lim) ? eq[c & 3] : (kUp ? fmaxf(eq[c & 3], v) : fminf(eq[c & 3], v));
+              }
             }
           }
-          const float e = up ? fmaxf(fmaxf(eq[0], eq[1]), fmaxf(eq[2], eq[3]))
+          const float e = kUp ? fmaxf(fmaxf(eq[0], eq[1]), fmaxf(eq[2], eq[3]))
                              : fminf(fminf(eq[0], eq[1]), fminf(eq[2], eq[3]));
           const float mt = (nv == 0) ? -CUDART_INF_F : e * sl2;
           float a = 1.f;
@@ -434,17 +444,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
             uint32_t sr[32];
             tmem_ld32(scol + 32 * p32, sr);
             tmem_wait_ld();
+            // keys past the row's limit read as -inf (exp2 gives 0) on the masked path
             const int lim = nv - 32 * p32;
+            const float neg = (lim >= 32) ? 0.f : -CUDART_INF_F;
 #pragma unroll
             for (int c8 = 0; c8 < 4; ++c8) {  // 8 keys -> one 16-byte chunk of P
               uint32_t w[4];
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
                 const int c = 8 * c8 + 2 * u;
-                float e0 = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -msub));
-                float e1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), sl2, -msub));
-                e0 = (c < lim) ? e0 : 0.f;
-                e1 = (c + 1 < lim) ? e1 : 0.f;
+                const float t0 = fmaf(__uint_as_float(sr[c]), sl2, -msub);
+                const float t1 = fmaf(__uint_as_float(sr[c + 1]), sl2, -msub);
+                const float e0 = ex2_approx((lim >= 32 || c < lim) ? t0 : neg);
+                const float e1 = ex2_approx((lim >= 32 || c + 1 < lim) ? t1 : neg);
                 rsq[u] += e0 + e1;
                 w[u] = pack_bf16x2(e0, e1);
               }
@@ -705,12 +717,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
 cudaError_t launch_prefill128(const CoreParams& p, const CoreMaps& maps, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(mla_prefill128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemT);
+    cudaError_t e = cudaFuncSetAttribute(mla_prefill128_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemT);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(mla_prefill128_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemT);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   if (p.num_pairs <= 0) return cudaSuccess;
-  mla_prefill128_kernel<<<dim3(2 * p.num_pairs), dim3(kThreadsT), kSmemT, stream>>>(p, maps);
+  if (p.scale_log2 >= 0.f)
+    mla_prefill128_kernel<true><<<dim3(2 * p.num_pairs), dim3(kThreadsT), kSmemT, stream>>>(p, maps);
+  else
+    mla_prefill128_kernel<false><<<dim3(2 * p.num_pairs), dim3(kThreadsT), kSmemT, stream>>>(p, maps);
   return cudaGetLastError();
 }
 

@@ -119,3 +119,17 @@ def test_full_size_chunked_config_sampled():
     ro, rl = mo.mla_prefill(P.q, P.kv, P.scale, causal=True, tokens=toks)
     assert_out_close(out[toks], ro)
     assert_lse_close(lse[:, toks], rl)
+
+
+@pytest.mark.parametrize("scale_mul", [-1.0, 0.0])
+def test_negative_and_zero_scale(scale_mul):
+    """A negative scale makes the row extreme the smallest raw score; a zero scale gives
+    every visible key the same weight (the mean of V)."""
+    P = gen.prefill_inputs(T=100, H=16, Tkv=150, seed=9)
+    scale = P.scale * scale_mul
+    out, lse = mla_prefill(P.q.to(dev()), P.kv.to(dev()), scale, causal=True, q_pos0=40)
+    torch.cuda.synchronize()
+    check_device_status()
+    ro, rl = mo.mla_prefill(P.q, P.kv, scale, causal=True, q_pos0=40)
+    assert_out_close(out, ro)
+    assert_lse_close(lse, rl)
