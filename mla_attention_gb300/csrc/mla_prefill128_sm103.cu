@@ -279,15 +279,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
             if ((t & 1u) != b) continue;
             // S buffer b was read by the rows (this issuer's previous tile)
             if (!wait1(&bars.s_free[b], (nb & 1) ^ 1, X_S_FREE, false)) { live = false; break; }
-            for (int k = 0; k < kGroups; ++k) {
-              if (!wait1(&bars.kfull[k][b], nb & 1, X_K_FULL, false)) { live = false; break; }
+            // Nothing of this issuer is queued now, so testing the later groups costs no drain:
+            // when all three have landed the tile goes out as one block of 36 MMAs; otherwise
+            // group by group, waiting for each.
+            if (!wait1(&bars.kfull[0][b], nb & 1, X_K_FULL, false)) { live = false; break; }
+            const bool all = mbar_try_wait(smem_u32(&bars.kfull[1][b]), nb & 1) &&
+                             mbar_try_wait(smem_u32(&bars.kfull[2][b]), nb & 1);
+            if (all) {
               tc_fence_after();
-              const uint64_t bd = sdesc_sw128(smem_u32(smem + kOffK + k * kGroupBytes), 16, 1024);
-              if (k < 2) mma_s_grp3_n128(d_tmem, tbase + kTmemQ + 96 * k, bd, idesc, (uint32_t)k);
-              else mma_s_grp2r_n128(d_tmem, tbase + kTmemQ + 192, bd, a_rope, idesc);
-              mma_commit(&bars.kempty[k]);
+              mma_s_tile_n128(d_tmem, tbase + kTmemQ, sdesc_sw128(smem_u32(smem + kOffK), 16, 1024), a_rope, idesc,
+                              smem_u32(&bars.kempty[0]), smem_u32(&bars.kempty[1]), smem_u32(&bars.kempty[2]));
+            } else {
+              for (int k = 0; k < kGroups; ++k) {
+                if (k > 0 && !wait1(&bars.kfull[k][b], nb & 1, X_K_FULL, false)) { live = false; break; }
+                tc_fence_after();
+                const uint64_t bd = sdesc_sw128(smem_u32(smem + kOffK + k * kGroupBytes), 16, 1024);
+                if (k < 2) mma_s_grp3_n128(d_tmem, tbase + kTmemQ + 96 * k, bd, idesc, (uint32_t)k);
+                else mma_s_grp2r_n128(d_tmem, tbase + kTmemQ + 192, bd, a_rope, idesc);
+                mma_commit(&bars.kempty[k]);
+              }
+              if (!live) break;
             }
-            if (!live) break;
             mma_commit(&bars.s_full[b]);
             ++nb;
           }
@@ -349,6 +361,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
           const int64_t tt = f / p.H, hh = f - tt * p.H;
           qrow = p.q + tt * p.q_stride_t + hh * p.q_stride_h;
           nkeys = keys_for_token(p, tt);
+        }
+        // warm L2 with the next item's query row while this item runs (its Q load then
+        // does not wait on HBM at the item boundary)
+        {
+          ItemIterT peek = iter;
+          ItemT nx;
+          if (peek.next(nx) && nx.J > 0) {
+            const int64_t fn = (int64_t)nx.id * kRows + r;
+            if (fn < (int64_t)p.T * p.H) {
+              const int64_t tn = fn / p.H, hn = fn - tn * p.H;
+              const char* b = reinterpret_cast<const char*>(p.q + tn * p.q_stride_t + hn * p.q_stride_h);
+              for (int o = 0; o < kDk * 2; o += 128) prefetch_l2(b + o);
+            }
+          }
         }
         // ---- Q: latent part -> TMEM (256 columns), RoPE part -> smem (SW128 K-major) ----
         if (i > 0 && !waitb(&bars.q_taken, (i - 1) & 1, X_Q_TAKEN, false)) break;

@@ -63,6 +63,27 @@ __device__ __forceinline__ void mma_s_grp2r_n128(uint32_t d_tmem, uint32_t a_tme
       : "memory");
 }
 
+// S[128 x 128] = Q * K^T for a whole 128-key tile whose three K groups (boxes 0-2, 3-5,
+// 6-8 of 128 rows, contiguous in smem) have all landed: 32 TS MMAs over the latent boxes
+// and 4 SS MMAs over the RoPE box, with the group release commits in between.
+__device__ __forceinline__ void mma_s_tile_n128(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint64_t a_rope_desc, uint32_t idesc, uint32_t empty0,
+                                                uint32_t empty1, uint32_t empty2) {
+  asm volatile(
+      "{\n\t.reg .pred pf, pt;\n\t.reg .b64 bd, ad;\n\t.reg .b32 at;\n\t"
+      "setp.ne.u32 pf, %3, %3;\n\tsetp.eq.u32 pt, %3, %3;\n\tmov.b64 bd, %2;\n\tmov.b32 at, %1;\n\tmov.b64 ad, %4;\n\t"
+      MLA_TS128_BOX("pf") MLA_TS128_BOX("pt") MLA_TS128_BOX("pt")
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t"
+      MLA_TS128_BOX("pt") MLA_TS128_BOX("pt") MLA_TS128_BOX("pt")
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"
+      MLA_TS128_BOX("pt") MLA_TS128_BOX("pt")
+      MLA_SS128("pt") MLA_SS128("pt") MLA_SS128("pt") MLA_SS128("pt")
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t"
+      "}" ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "l"(a_rope_desc), "r"(empty0), "r"(empty1),
+      "r"(empty2)
+      : "memory");
+}
+
 #define MLA_PV256(ACC) \
   "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd0, %4, " ACC ";\n\t" \
   "tcgen05.mma.cta_group::1.kind::f16 [%1], ad, bd1, %4, " ACC ";\n\t" \
