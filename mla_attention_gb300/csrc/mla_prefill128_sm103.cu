@@ -470,6 +470,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
             uint32_t sr[32];
             tmem_ld32(scol + 32 * p32, sr);
             tmem_wait_ld();
+            if (p32 == kKeysT / 32 - 1) {  // the last piece is in registers: S buffer sb is free
+              tc_fence_before();
+              warp_arrive(&bars.s_free[sb]);
+            }
             // keys past the row's limit read as -inf (exp2 gives 0) on the masked path
             const int lim = nv - 32 * p32;
             const float neg = (lim >= 32) ? 0.f : -CUDART_INF_F;
@@ -492,8 +496,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
                   make_uint4(w[0], w[1], w[2], w[3]);
             }
           }
-          tc_fence_before();
-          warp_arrive(&bars.s_free[sb]);  // S buffer sb has been read
           l += (rsq[0] + rsq[1]) + (rsq[2] + rsq[3]);
           alpha[sb * kRows + r] = a;
           fence_proxy_async_smem();  // the bulk copy reads through the async proxy
