@@ -60,7 +60,7 @@ def recorded_traffic():
         prof = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
         if kernel_source_digest(prof["kernel_sources"]) != prof["kernel_source_sha256"]:
             return None
-        return prof.get("mla_core_kernel_prefill_bytes_per_launch")
+        return prof.get("prefill_kernel_bytes_per_launch")
     except Exception:
         return None
 
@@ -394,7 +394,7 @@ def run_libmla(args, world, rank, local):
                    "inputs": "seeded N(0,1) bf16 drawn on the device"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "mla_core_kernel (prefill mode)", "peak_kind": f"bf16 burst ({peak_kind})"},
+                     "kernel": "mla_prefill128_kernel", "peak_kind": f"bf16 burst ({peak_kind})"},
         "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clk,

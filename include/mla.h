@@ -78,6 +78,14 @@ mla_status mla_check_device_status(void* workspace, void* stream, uint32_t* deta
 void mla_set_spin_limit(uint32_t spin_limit);
 
 /*
+ * Keys per score tile of the dense prefill (mla_prefill): 128 (the default) runs the
+ * 128-key kernel, 64 the 64-key kernel that also serves decode and sparse; 0 restores
+ * the default, any other value is ignored.  Process-wide; both give the same results
+ * within the stated tolerances (tests run both).
+ */
+void mla_set_prefill_tile_keys(int keys);
+
+/*
  * Fault injection for tests (host-side switch, process-wide): when enabled,
  * the MMA warp of every CTA launched afterwards first waits on a barrier that
  * nothing arrives on, so that wait runs out of its bound and the call reports

@@ -112,15 +112,10 @@ uint32_t* ws_err(void* ws) { return reinterpret_cast<uint32_t*>(ws); }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Keys per score tile of the dense prefill: 128 (mla_prefill128_kernel) unless the
-// environment variable MLA_PREFILL_TILE_KEYS is 64 (mla_core_kernel), read once.
-int prefill_tile_keys() {
-  static const int keys = [] {
-    const char* v = getenv("MLA_PREFILL_TILE_KEYS");
-    return (v && atoi(v) == 64) ? 64 : 128;
-  }();
-  return keys;
-}
+// Keys per score tile of the dense prefill: 128 (mla_prefill128_kernel) or 64
+// (mla_core_kernel); set with mla_set_prefill_tile_keys.
+std::atomic<int> g_prefill_tile_keys{128};
+int prefill_tile_keys() { return g_prefill_tile_keys.load(); }
 
 int default_pairs() {
   int p = device_sm_count() / 2;
@@ -152,6 +147,11 @@ const char* mla_status_string(mla_status s) {
 }
 
 void mla_set_spin_limit(uint32_t limit) { g_spin_limit.store(limit ? limit : kDefaultSpinLimit); }
+
+void mla_set_prefill_tile_keys(int keys) {
+  if (keys == 0) keys = 128;
+  if (keys == 64 || keys == 128) g_prefill_tile_keys.store(keys);
+}
 
 void mla_debug_inject_stall(int enable) { g_debug_stall.store(enable ? 1u : 0u); }
 

@@ -5,10 +5,18 @@ import torch
 
 import oracle.mla_oracle as mo
 from mla_attention_gb300 import inputs as gen
-from mla_attention_gb300 import mla_prefill, check_device_status
+from mla_attention_gb300 import check_device_status, mla_prefill, set_prefill_tile_keys
 from tests.helpers import assert_lse_close, assert_out_close, dev, to_np
 
 pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(params=[128, 64], ids=["tile128", "tile64"])
+def tile_keys(request):
+    """Both prefill kernels: 128-key score tiles (the default) and 64-key tiles."""
+    set_prefill_tile_keys(request.param)
+    yield request.param
+    set_prefill_tile_keys(0)
 
 
 def _run(P, **kw):
@@ -20,7 +28,7 @@ def _run(P, **kw):
     return out, lse
 
 
-def test_tiny_config_full_parity():
+def test_tiny_config_full_parity(tile_keys):
     """B=1, H=16, T=Tkv=256 causal, every row (rows pack 8 tokens x 16 heads per tile)."""
     P = gen.prefill_inputs(T=256, H=16, Tkv=256, seed=1)
     out, lse = _run(P)
@@ -36,7 +44,7 @@ def test_tiny_config_full_parity():
     (5, 128, 1, 0, 0, 1, True),           # a single key
     (130, 128, 64, 1000, 0, 64, True),    # every token sees the whole chunk
 ])
-def test_ragged_and_edge_cases(T, H, Tkv, q_pos0, kv_pos0, kv_valid, causal):
+def test_ragged_and_edge_cases(T, H, Tkv, q_pos0, kv_pos0, kv_valid, causal, tile_keys):
     P = gen.prefill_inputs(T=T, H=H, Tkv=Tkv, seed=T + H)
     out, lse = _run(P, causal=causal, q_pos0=q_pos0, kv_pos0=kv_pos0, kv_valid=kv_valid)
     ro, rl = mo.mla_prefill(P.q, P.kv, P.scale, causal=causal, q_pos0=q_pos0, kv_pos0=kv_pos0, kv_valid=kv_valid)
@@ -44,14 +52,14 @@ def test_ragged_and_edge_cases(T, H, Tkv, q_pos0, kv_pos0, kv_valid, causal):
     assert_lse_close(lse, rl)
 
 
-def test_empty_rows_are_zero_and_neg_inf():
+def test_empty_rows_are_zero_and_neg_inf(tile_keys):
     P = gen.prefill_inputs(T=20, H=16, Tkv=64, seed=3)
     out, lse = _run(P, q_pos0=0, kv_pos0=100)   # no token reaches the chunk
     assert torch.all(out == 0)
     assert torch.all(torch.isneginf(lse))
 
 
-def test_prev_merge_and_in_place():
+def test_prev_merge_and_in_place(tile_keys):
     T, H = 96, 128
     P = gen.prefill_inputs(T=T, H=H, Tkv=96, seed=4)
     prev_out, prev_lse = gen.prev_inputs(T, H, 512, seed=44, lse_lo=1.0, lse_hi=6.0)
@@ -66,7 +74,7 @@ def test_prev_merge_and_in_place():
     assert_lse_close(lse, rl)
 
 
-def test_chunked_ring_equals_one_pass():
+def test_chunked_ring_equals_one_pass(tile_keys):
     """4 KV chunks in sequence, each merged in place into (out, lse), equal one causal pass."""
     T, H, C = 512, 128, 128
     P = gen.prefill_inputs(T=T, H=H, Tkv=T, seed=2)
@@ -86,7 +94,7 @@ def test_chunked_ring_equals_one_pass():
     assert_lse_close(lse[:, toks], rl)
 
 
-def test_strided_q():
+def test_strided_q(tile_keys):
     T, H = 40, 16
     P = gen.prefill_inputs(T=T, H=H, Tkv=50, seed=6)
     big = torch.zeros((T, H, 640), dtype=torch.bfloat16)
@@ -122,7 +130,7 @@ def test_full_size_chunked_config_sampled():
 
 
 @pytest.mark.parametrize("scale_mul", [-1.0, 0.0])
-def test_negative_and_zero_scale(scale_mul):
+def test_negative_and_zero_scale(scale_mul, tile_keys):
     """A negative scale makes the row extreme the smallest raw score; a zero scale gives
     every visible key the same weight (the mean of V)."""
     P = gen.prefill_inputs(T=100, H=16, Tkv=150, seed=9)
