@@ -91,6 +91,7 @@ struct Bars {
   uint64_t pb_free[2];
   uint64_t stats_full;      // arrived remotely by the S-CTA rows
   uint64_t o_free;
+  uint64_t ep_half[2];      // O-CTA: both warps of an epilogue half staged their rows (count 2)
   uint64_t stall;           // fault injection: never arrived on
   uint32_t tmem_base;
   uint32_t abort_flag;
@@ -102,6 +103,7 @@ enum : uint32_t {
   W_S_KV_EMPTY = 1, W_S_KV_FULL, W_S_SFREE, W_S_QFULL, W_S_SFULL, W_S_PFREE, W_S_STATSFREE, W_S_PWRITTEN,
   W_S_PBOFREE,
   W_O_KV_EMPTY, W_O_KV_FULL, W_O_PREADY, W_O_PFULL, W_O_PBFREE, W_O_PVDONE, W_O_STATSFULL, W_O_OFREE, W_STALL,
+  W_O_EPHALF,
   R_PAGE = 0x40, R_LEN = 0x41,
 };
 
@@ -324,6 +326,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       mbar_init(&bars.stats_full, kRowWarps);
       mbar_init(&bars.o_free, kRowWarps);
+      mbar_init(&bars.ep_half[0], 2);
+      mbar_init(&bars.ep_half[1], 2);
     }
     mbar_init(&bars.stall, 1);
     bars.abort_flag = 0;
@@ -836,6 +840,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t rem_stats_free = map_to_rank(smem_u32(&bars.stats_free), peer);
       const float* alpha_o = reinterpret_cast<const float*>(smem + kOffAlphaO);
       uint32_t g = 0, gs = 0, i = 0;  // P tiles, stage ring position, items that have KV tiles
+      uint32_t ep_phase = 0;          // staged epilogues done (phase of ep_half)
       bool live = true;
       bool stored = false;            // this thread issued TMA stores that must finish before exit
       while (live && iter.next(it)) {
@@ -986,7 +991,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (row_ok && lse_dst) *lse_dst = lse_out;
           // the 64 rows of this half go out with TMA (rows past the end are clipped)
           fence_proxy_async_smem();
-          named_barrier(1 + half, 64);
+          // both warps of this half staged their rows (a bounded wait: a named barrier would
+          // hang if the other warp left on an abort)
+          warp_arrive(&bars.ep_half[half]);
+          if (!waitb(&bars.ep_half[half], ep_phase & 1, W_O_EPHALF, false)) break;
+          ++ep_phase;
           if (rr == 0) {
             if (half * 64 < rows_per_item) {
               const int32_t row0 = it.id * rows_per_item + half * 64;
