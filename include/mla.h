@@ -78,12 +78,13 @@ mla_status mla_check_device_status(void* workspace, void* stream, uint32_t* deta
 void mla_set_spin_limit(uint32_t spin_limit);
 
 /*
- * Keys per score tile of the dense prefill (mla_prefill): 128 (the default) runs the
- * 128-key kernel, 64 the 64-key kernel that also serves decode and sparse; 0 restores
- * the default, any other value is ignored.  Process-wide; both give the same results
- * within the stated tolerances (tests run both).
+ * Keys per score tile of mla_prefill and of mla_decode: 128 runs the 128-key tile engine,
+ * 64 the 64-key engine (which always serves mla_sparse).  0 restores the default of each
+ * (prefill 128, decode 64: the faster engine for each on GB300); any other value leaves
+ * the setting unchanged.  Process-wide; both engines give the same results within the
+ * stated tolerances (the tests run both).
  */
-void mla_set_prefill_tile_keys(int keys);
+void mla_set_tile_keys(int prefill_keys, int decode_keys);
 
 /*
  * Fault injection for tests (host-side switch, process-wide): when enabled,

@@ -40,7 +40,7 @@ _SIGNATURES = {
     "mla_status_string": ([c_int], ctypes.c_char_p),
     "mla_check_device_status": ([c_void_p, c_void_p, ctypes.POINTER(c_uint32)], c_int),
     "mla_set_spin_limit": ([c_uint32], None),
-    "mla_set_prefill_tile_keys": ([c_int], None),
+    "mla_set_tile_keys": ([c_int, c_int], None),
     "mla_debug_inject_stall": ([c_int], None),
     "mla_prefill_workspace_size": ([c_int, c_int], c_size_t),
     "mla_prefill": ([c_void_p, c_int64, c_int64, c_void_p, c_int64, c_int, c_int, c_int, c_int, c_int, c_float, c_int,
@@ -140,9 +140,10 @@ def set_spin_limit(limit: int):
     lib().mla_set_spin_limit(int(limit))
 
 
-def set_prefill_tile_keys(keys: int):
-    """128 (default) or 64 keys per score tile of mla_prefill; 0 restores the default."""
-    lib().mla_set_prefill_tile_keys(int(keys))
+def set_tile_keys(prefill_keys: int = 0, decode_keys: int = 0):
+    """128 or 64 keys per score tile of mla_prefill and of mla_decode; 0 keeps / restores the
+    default of each (prefill 128, decode 64)."""
+    lib().mla_set_tile_keys(int(prefill_keys), int(decode_keys))
 
 
 def inject_stall(enable: bool):

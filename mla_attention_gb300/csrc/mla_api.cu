@@ -112,10 +112,11 @@ uint32_t* ws_err(void* ws) { return reinterpret_cast<uint32_t*>(ws); }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Keys per score tile of the dense prefill: 128 (mla_prefill128_kernel) or 64
-// (mla_core_kernel); set with mla_set_prefill_tile_keys.
-std::atomic<int> g_prefill_tile_keys{128};
-int prefill_tile_keys() { return g_prefill_tile_keys.load(); }
+// Keys per score tile of prefill and of decode: 128 (mla_prefill128_kernel) or 64
+// (mla_core_kernel); set with mla_set_tile_keys.
+constexpr int kDefaultPrefillKeys = 128, kDefaultDecodeKeys = 64;
+std::atomic<int> g_prefill_keys{kDefaultPrefillKeys};
+std::atomic<int> g_decode_keys{kDefaultDecodeKeys};
 
 int default_pairs() {
   int p = device_sm_count() / 2;
@@ -148,9 +149,11 @@ const char* mla_status_string(mla_status s) {
 
 void mla_set_spin_limit(uint32_t limit) { g_spin_limit.store(limit ? limit : kDefaultSpinLimit); }
 
-void mla_set_prefill_tile_keys(int keys) {
-  if (keys == 0) keys = 128;
-  if (keys == 64 || keys == 128) g_prefill_tile_keys.store(keys);
+void mla_set_tile_keys(int prefill_keys, int decode_keys) {
+  if (prefill_keys == 0) prefill_keys = kDefaultPrefillKeys;
+  if (decode_keys == 0) decode_keys = kDefaultDecodeKeys;
+  if (prefill_keys == 64 || prefill_keys == 128) g_prefill_keys.store(prefill_keys);
+  if (decode_keys == 64 || decode_keys == 128) g_decode_keys.store(decode_keys);
 }
 
 void mla_debug_inject_stall(int enable) { g_debug_stall.store(enable ? 1u : 0u); }
@@ -207,7 +210,7 @@ mla_status mla_prefill(const void* q, int64_t q_stride_t, int64_t q_stride_h, co
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   CoreMaps maps;
   memset(&maps, 0, sizeof(maps));
-  const bool tile128 = prefill_tile_keys() == 128;
+  const bool tile128 = g_prefill_keys.load() == 128;
   if (kv_valid > 0) {
     mla_status s = map2d(&maps.kv, kv, kDk, (uint64_t)kv_valid, (uint64_t)kv_stride, kKeys, "kv");
     if (s == MLA_OK && tile128) s = map2d(&maps.row, kv, kDk, (uint64_t)kv_valid, (uint64_t)kv_stride, 128, "kv");
@@ -306,7 +309,7 @@ mla_status mla_decode(const void* q, const void* kv_cache, int64_t num_pages, in
   p.part_lse = reinterpret_cast<float*>(w);
   w += align_up(sizeof(float) * slots * (size_t)H, 256);
   p.part_o = reinterpret_cast<float*>(w);
-  cudaError_t e = launch_core(p, maps, st);
+  cudaError_t e = (g_decode_keys.load() == 128) ? launch_prefill128(p, maps, st) : launch_core(p, maps, st);
   if (e != cudaSuccess) return cuda_fail(e, "mla_decode launch");
   e = launch_decode_reduce(p, reinterpret_cast<__nv_bfloat16*>(out), lse, st);
   if (e != cudaSuccess) return cuda_fail(e, "mla_decode reduce launch");

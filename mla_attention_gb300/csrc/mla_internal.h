@@ -88,8 +88,9 @@ struct CoreMaps {
 
 // kernels' host launchers (return cudaError_t of the launch)
 cudaError_t launch_core(const CoreParams& p, const CoreMaps& maps, cudaStream_t stream);
-// prefill with 128-key score tiles: maps.row holds the K rows with box {64, 128}, maps.kv
-// the V rows with box {64, 64}
+// prefill and decode with 128-key score tiles.  Prefill: maps.row holds the K rows with box
+// {64, 128}, maps.kv the V rows with box {64, 64}.  Decode: maps.kv the cache rows with box
+// {64, 64} (whole pages), maps.row the cache rows with box {64, 1} (gathers).
 cudaError_t launch_prefill128(const CoreParams& p, const CoreMaps& maps, cudaStream_t stream);
 size_t core_smem_bytes();
 

@@ -1,4 +1,8 @@
-// Absorbed causal MLA prefill with 128-key score tiles (sm_103a: tcgen05, TMEM, TMA).
+// Absorbed MLA prefill and paged decode with 128-key score tiles (sm_103a: tcgen05, TMEM,
+// TMA).  Decode is the pages' seqlen-1 form: the 128 heads of one query token are the 128
+// rows of an item, the request's keys are split into segments of whole tiles over the CTA
+// pairs (split-K), each pair writes an fp32 partial (O / l, LSE) and decode_reduce_kernel
+// merges the partials by LSE.
 //
 // What it computes is the prefill of mla_core_kernel (pages: Tenstorrent ring_mla and
 // Ascend RingMLA "prefill" sections -- scores over all 576 columns of the shared KV row,
@@ -90,13 +94,24 @@ static_assert(sizeof(BarsT) <= 512, "barrier block too large");
 enum : uint32_t {
   X_K_EMPTY = 0x40, X_K_FULL, X_S_FREE, X_S_FULL, X_Q_FULL, X_Q_TAKEN, X_P_WRITTEN, X_PBUF_FREE, X_PB_FREE,
   X_STATS_FREE, X_V_EMPTY, X_V_FULL, X_P_FULL, X_P_READY, X_PV_DONE, X_STATS_FULL, X_O_FREE, X_STALL, X_EP_HALF,
-  X_ALIGN = 0x4F,
+  X_ALIGN = 0x4F, X_PAGE = 0x50, X_LEN = 0x51,
 };
 
 struct ItemT {
-  int id;  // row tile
-  int J;   // 128-key tiles
+  int id;        // prefill: row tile; decode: request
+  int J;         // 128-key tiles
+  int64_t k0;    // decode: first key of this segment (within the request)
+  int64_t k1;    // decode: end key of this segment
+  int slot;      // decode: partial slot (request + pair)
 };
+
+__device__ __forceinline__ int decode_len_t(const CoreParams& p, int b) {
+  int n = p.lens[b];
+  if (n < 0) n = 0;
+  const int64_t cap = (int64_t)p.max_pages * p.page_size;
+  if (n > cap) n = (int)cap;
+  return n;
+}
 
 __device__ __forceinline__ int64_t keys_for_token(const CoreParams& p, int64_t t) {
   int64_t n = p.kv_valid;
@@ -110,15 +125,57 @@ __device__ __forceinline__ int64_t keys_for_token(const CoreParams& p, int64_t t
 // Row tiles in longest-first order, dealt round robin to the CTA pairs.  In place, a row
 // that sees no key keeps its previous (out, lse); J only falls along this order (causal)
 // or is constant, so the first key-less item ends the list.
+// Decode: the key tiles of all requests, in request order, are split into equal shares, one
+// per CTA pair; an item is the part of one request inside this pair's share (an empty
+// share has none).
+template <bool kDec>
 struct ItemIterT {
   const CoreParams* p;
+  int pair;
   int64_t k;
-  __device__ void init(const CoreParams& prm, int pair) {
+  int b;
+  int64_t pre, lo, hi;
+  __device__ void init(const CoreParams& prm, int pair_id) {
     p = &prm;
-    k = pair;
+    pair = pair_id;
+    k = pair_id;
+    b = 0;
+    pre = 0;
+    lo = hi = 0;
+    if constexpr (kDec) {
+      int64_t tot = 0;
+      for (int i = 0; i < prm.B; ++i) tot += (decode_len_t(prm, i) + kKeysT - 1) / kKeysT;
+      lo = tot * pair_id / prm.num_pairs;
+      hi = tot * (pair_id + 1) / prm.num_pairs;
+    }
   }
   __device__ bool next(ItemT& it) {
     const CoreParams& P = *p;
+    if constexpr (kDec) {
+      if (hi <= lo) return false;
+      while (b < P.B) {
+        const int len = decode_len_t(P, b);
+        const int64_t nt = (len + kKeysT - 1) / kKeysT;
+        const int64_t s0 = pre, e0 = pre + nt;
+        const int cur = b;
+        pre = e0;
+        ++b;
+        if (nt == 0 || e0 <= lo) continue;
+        if (s0 >= hi) {
+          b = P.B;
+          return false;
+        }
+        const int64_t t0 = (s0 > lo ? s0 : lo) - s0, t1 = (e0 < hi ? e0 : hi) - s0;
+        if (t1 <= t0) continue;
+        it.id = cur;
+        it.J = (int)(t1 - t0);
+        it.k0 = t0 * kKeysT;
+        it.k1 = t1 * kKeysT < len ? t1 * kKeysT : len;
+        it.slot = cur + pair;
+        return true;
+      }
+      return false;
+    } else {
     const int64_t rows = (int64_t)P.T * P.H;
     const int64_t n_items = (rows + kRows - 1) / kRows;
     if (k >= n_items) return false;
@@ -133,6 +190,7 @@ struct ItemIterT {
         (const void*)P.prev_lse == (const void*)P.lse)
       return false;
     return true;
+    }
   }
 };
 
@@ -140,9 +198,65 @@ __device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float a, float b
   asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }
 
+// ---- decode: where the 64 keys [kh, kh + 64) of a tile half come from ----
+// A whole half inside one valid page is one tiled TMA box per 64 columns; otherwise its
+// rows are gathered four at a time (tile::gather4), keys past the request's length and
+// rows of an out-of-range page as -1 (zero fill; the page is reported).
+struct HalfSrc {
+  bool tiled;
+  int32_t y;                   // tiled: first cache row
+  int32_t a0, a1, a2, a3;      // gathered: rows 4 l .. 4 l + 3 for lane l < 16
+};
+__device__ __forceinline__ HalfSrc decode_half(const CoreParams& p, int req, int len, int64_t kh, uint32_t* err) {
+  const int lane = threadIdx.x & 31;
+  const int32_t* bt = p.block_table + (int64_t)req * p.max_pages;
+  HalfSrc hs;
+  hs.tiled = false;
+  hs.y = 0;
+  if (p.page_size % 64 == 0 && kh + 64 <= len) {
+    const int32_t pg = bt[kh / p.page_size];
+    if (pg >= 0 && pg < p.num_pages) {
+      hs.tiled = true;
+      hs.y = (int32_t)(pg * (int64_t)p.page_size + kh % p.page_size);
+    }
+  }
+  auto row_of = [&](int64_t key) -> int32_t {
+    if (key >= len) return -1;
+    const int32_t pg = bt[key / p.page_size];
+    if (pg < 0 || pg >= p.num_pages) {
+      record_error(err, DEV_RANGE_BASE | X_PAGE);
+      return -1;
+    }
+    return (int32_t)(pg * (int64_t)p.page_size + key % p.page_size);
+  };
+  int32_t re = -1, ro = -1;
+  if (!hs.tiled) {
+    re = row_of(kh + 2 * lane);
+    ro = row_of(kh + 2 * lane + 1);
+  }
+  hs.a0 = __shfl_sync(0xffffffffu, re, (2 * lane) & 31);
+  hs.a1 = __shfl_sync(0xffffffffu, ro, (2 * lane) & 31);
+  hs.a2 = __shfl_sync(0xffffffffu, re, (2 * lane + 1) & 31);
+  hs.a3 = __shfl_sync(0xffffffffu, ro, (2 * lane + 1) & 31);
+  return hs;
+}
+// one 64-column box of a half (64 rows x 128 B at dst): one tiled load or 16 gathers
+__device__ __forceinline__ void load_half_box(uint32_t dst, const CUtensorMap* tiled_map,
+                                              const CUtensorMap* row_map, int32_t x, const HalfSrc& hs,
+                                              uint64_t* bar) {
+  const int lane = threadIdx.x & 31;
+  if (hs.tiled) {
+    if (lane == 0) tma_load_2d(dst, tiled_map, x, hs.y, bar);
+  } else if (lane < 16) {
+    tma_gather4(dst + lane * 512, row_map, x, hs.a0, hs.a1, hs.a2, hs.a3, bar);
+  }
+}
+
 // kUp: the scale is >= 0, so the row extreme of the raw scores is their maximum (else
-// their minimum); one instantiation per sign keeps that choice out of the row loop.
-template <bool kUp>
+// their minimum).  kDecode: paged decode (else prefill).  One instantiation per
+// combination keeps both choices out of the loops: the loop bodies must stay small
+// for the instruction cache.
+template <bool kUp, bool kDecode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
     mla_prefill128_kernel(const __grid_constant__ CoreParams p, const __grid_constant__ CoreMaps maps) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -156,6 +270,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
   const int lane = tid & 31;
   const uint32_t lim = p.spin_limit;
   uint32_t* err = p.err;
+  constexpr bool decode = kDecode;
+  constexpr bool staged = !kDecode;  // prefill stages its epilogue (prev in, out) through the V ring
   // The layout assumes a 1 KB aligned dynamic base (true when the kernel has no static
   // shared memory); anything else is refused before any barrier is touched.
   if (smem_u32(smem) & 1023u) {
@@ -205,8 +321,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
   if (warp == 4 && lane == 0) {
     tma_prefetch_desc(&maps.kv);
     tma_prefetch_desc(&maps.row);
-    tma_prefetch_desc(&maps.out);
-    if (p.prev_out) tma_prefetch_desc(&maps.prev);
+    if (staged) tma_prefetch_desc(&maps.out);
+    if (staged && p.prev_out) tma_prefetch_desc(&maps.prev);
+  }
+  // decode: publish the per-request count of 128-key tiles (prefix sums) for the reduction
+  if (decode && blockIdx.x == 0 && warp == 0) {
+    int64_t run = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+      const int b = b0 + lane;
+      int n = 0;
+      if (b < p.B) {
+        const int raw = p.lens[b];
+        const int64_t cap = (int64_t)p.max_pages * p.page_size;
+        if (raw < 0 || raw > cap) record_error(err, DEV_RANGE_BASE | X_LEN);
+        n = (decode_len_t(p, b) + kKeysT - 1) / kKeysT;
+      }
+      int incl = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (b < p.B) p.tile_prefix[b] = (int32_t)(run + incl - n);
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) p.tile_prefix[p.B] = (int32_t)run;
   }
   tc_fence_before();
   cluster_sync();
@@ -227,7 +366,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
   };
   if (p.debug_stall && warp == 5) waitb(&bars.stall, 0, X_STALL, false);  // runs out: injected fault
 
-  ItemIterT iter;
+  ItemIterT<kDecode> iter;
   iter.init(p, pair);
   ItemT it;
   const CUtensorMap& map_k = maps.row;   // K rows, box {64, 128}
@@ -245,16 +384,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
       uint32_t t = 0;
       bool live = true;
       while (live && iter.next(it)) {
+        const int len = decode ? decode_len_t(p, it.id) : 0;
         for (int j = 0; j < it.J && live; ++j, ++t) {
           const uint32_t par = t & 1;
+          HalfSrc hsrc[2];
+          if constexpr (decode) {
+            const int64_t kb = it.k0 + (int64_t)j * kKeysT;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) hsrc[h] = decode_half(p, it.id, len, kb + 64 * h, err);
+          }
           for (int k = 0; k < kGroups; ++k) {
             if (!waitb(&bars.kempty[k], par ^ 1, X_K_EMPTY, false)) { live = false; break; }
-            if (lane == 0) {
-              uint64_t* fb = &bars.kfull[k][par];
-              mbar_arrive_expect_tx(fb, kGroupBytes);
-              const uint32_t dst = smem_u32(smem + kOffK + k * kGroupBytes);
-              for (int i = 0; i < 3; ++i)
-                tma_load_2d(dst + i * kBoxBytesK, &map_k, (3 * k + i) * kBoxCols, j * kKeysT, fb);
+            uint64_t* fb = &bars.kfull[k][par];
+            if (lane == 0) mbar_arrive_expect_tx(fb, kGroupBytes);
+            __syncwarp();
+            const uint32_t dst = smem_u32(smem + kOffK + k * kGroupBytes);
+            for (int i = 0; i < 3; ++i) {
+              const int32_t x = (3 * k + i) * kBoxCols;
+              if constexpr (!decode) {
+                if (lane == 0) tma_load_2d(dst + i * kBoxBytesK, &map_k, x, j * kKeysT, fb);
+              } else {
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                  load_half_box(dst + i * kBoxBytesK + h * kBoxBytesV, &maps.kv, &maps.row, x, hsrc[h], fb);
+              }
             }
             __syncwarp();
           }
@@ -353,25 +506,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
       bool live = true;
       while (live && iter.next(it)) {
         if (it.J == 0) continue;  // no key: the O-CTA writes these rows on its own
-        const int64_t f = (int64_t)it.id * kRows + r;
-        const bool row_ok = f < (int64_t)p.T * p.H;
+        // this row's query and the keys it sees from the item's first tile on
+        bool row_ok;
         const __nv_bfloat16* qrow = nullptr;
         int64_t nkeys = 0;
-        if (row_ok) {
-          const int64_t tt = f / p.H, hh = f - tt * p.H;
-          qrow = p.q + tt * p.q_stride_t + hh * p.q_stride_h;
-          nkeys = keys_for_token(p, tt);
+        if constexpr (decode) {
+          row_ok = r < p.H;
+          if (row_ok) {
+            qrow = p.q + ((int64_t)it.id * p.H + r) * kDk;
+            nkeys = it.k1 - it.k0;
+          }
+        } else {
+          const int64_t f = (int64_t)it.id * kRows + r;
+          row_ok = f < (int64_t)p.T * p.H;
+          if (row_ok) {
+            const int64_t tt = f / p.H, hh = f - tt * p.H;
+            qrow = p.q + tt * p.q_stride_t + hh * p.q_stride_h;
+            nkeys = keys_for_token(p, tt);
+          }
         }
         // warm L2 with the next item's query row while this item runs (its Q load then
         // does not wait on HBM at the item boundary)
         {
-          ItemIterT peek = iter;
+          ItemIterT<kDecode> peek = iter;
           ItemT nx;
           if (peek.next(nx) && nx.J > 0) {
-            const int64_t fn = (int64_t)nx.id * kRows + r;
-            if (fn < (int64_t)p.T * p.H) {
-              const int64_t tn = fn / p.H, hn = fn - tn * p.H;
-              const char* b = reinterpret_cast<const char*>(p.q + tn * p.q_stride_t + hn * p.q_stride_h);
+            const __nv_bfloat16* nq = nullptr;
+            if constexpr (decode) {
+              if (r < p.H) nq = p.q + ((int64_t)nx.id * p.H + r) * kDk;
+            } else {
+              const int64_t fn = (int64_t)nx.id * kRows + r;
+              if (fn < (int64_t)p.T * p.H) {
+                const int64_t tn = fn / p.H, hn = fn - tn * p.H;
+                nq = p.q + tn * p.q_stride_t + hn * p.q_stride_h;
+              }
+            }
+            if (nq) {
+              const char* b = reinterpret_cast<const char*>(nq);
               for (int o = 0; o < kDk * 2; o += 128) prefetch_l2(b + o);
             }
           }
@@ -518,21 +689,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
       uint32_t u = 0;  // position in the two-slot ring
       bool live = true;
       while (live && iter.next(it)) {
+        const int len = decode ? decode_len_t(p, it.id) : 0;
         for (int j = 0; j < it.J && live; ++j) {
           for (int h = 0; h < 2; ++h, ++u) {
             const int s = u & 1;
+            HalfSrc hs;
+            if constexpr (decode) hs = decode_half(p, it.id, len, it.k0 + (int64_t)j * kKeysT + 64 * h, err);
             if (!waitb(&bars.vempty[s], ((u >> 1) & 1) ^ 1, X_V_EMPTY, false)) { live = false; break; }
-            if (lane == 0) {
-              const uint32_t dst = smem_u32(smem + kOffV + s * kHalfBytesV);
-              mbar_arrive_expect_tx(&bars.vfull[s], kHalfBytesV);
-              for (int bx = 0; bx < kVBoxes; ++bx)
-                tma_load_2d(dst + bx * kBoxBytesV, &map_v, bx * kBoxCols, j * kKeysT + 64 * h, &bars.vfull[s]);
+            const uint32_t dst = smem_u32(smem + kOffV + s * kHalfBytesV);
+            if (lane == 0) mbar_arrive_expect_tx(&bars.vfull[s], kHalfBytesV);
+            __syncwarp();
+            for (int bx = 0; bx < kVBoxes; ++bx) {
+              if constexpr (!decode) {
+                if (lane == 0)
+                  tma_load_2d(dst + bx * kBoxBytesV, &map_v, bx * kBoxCols, j * kKeysT + 64 * h, &bars.vfull[s]);
+              } else {
+                load_half_box(dst + bx * kBoxBytesV, &maps.kv, &maps.row, bx * kBoxCols, hs, &bars.vfull[s]);
+              }
             }
             __syncwarp();
           }
         }
         // the two ring slots then stage the epilogue: rows 0-63 and 64-127 (with prev)
-        if (it.J > 0) {
+        if (staged && it.J > 0) {
           for (int h = 0; h < 2 && live; ++h, ++u) {
             const int s = u & 1;
             if (!waitb(&bars.vempty[s], ((u >> 1) & 1) ^ 1, X_V_EMPTY, false)) { live = false; break; }
@@ -577,7 +756,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
             if (!live) break;
             mma_commit_multicast(&bars.pb_free[pb], 0x3);  // this CTA and the S-CTA
           }
-          u += 2;  // the epilogue's stages
+          if (staged) u += 2;  // the epilogue's stages
           ++i;
         }
       }
@@ -595,24 +774,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
       bool live = true;
       bool stored = false;
       while (live && iter.next(it)) {
-        const int64_t f = (int64_t)it.id * kRows + r;
-        const bool row_ok = f < (int64_t)p.T * p.H;
+        bool row_ok;
         float prev_l = -CUDART_INF_F;
         const __nv_bfloat16* prev_row = nullptr;
         __nv_bfloat16* orow = nullptr;
+        float* orow_f = nullptr;   // decode: fp32 partial row in the workspace
         float* lse_dst = nullptr;
-        if (row_ok) {
-          const int64_t tt = f / p.H, hh = f - tt * p.H;
-          orow = p.out + f * kLatent;
-          lse_dst = p.lse + hh * p.T + tt;
-          if (p.prev_out) {
-            prev_row = p.prev_out + f * kLatent;
-            prev_l = p.prev_lse[hh * p.T + tt];
+        if constexpr (decode) {
+          row_ok = r < p.H;
+          if (row_ok) {
+            orow_f = p.part_o + ((int64_t)it.slot * p.H + r) * kLatent;
+            lse_dst = p.part_lse + (int64_t)it.slot * p.H + r;
+          }
+        } else {
+          const int64_t f = (int64_t)it.id * kRows + r;
+          row_ok = f < (int64_t)p.T * p.H;
+          if (row_ok) {
+            const int64_t tt = f / p.H, hh = f - tt * p.H;
+            orow = p.out + f * kLatent;
+            lse_dst = p.lse + hh * p.T + tt;
+            if (p.prev_out) {
+              prev_row = p.prev_out + f * kLatent;
+              prev_l = p.prev_lse[hh * p.T + tt];
+            }
           }
         }
         if (it.J == 0) {
-          // no key reaches these rows: out = prev (or 0), lse = prev_lse (or -inf)
-          if (row_ok) {
+          // no key reaches these rows: out = prev (or 0), lse = prev_lse (or -inf); only
+          // prefill has such items (decode segments always hold keys)
+          if (row_ok && orow) {
             for (int c = 0; c < kLatent; c += 8) {
               uint4 v = prev_row ? *reinterpret_cast<const uint4*>(prev_row + c) : make_uint4(0, 0, 0, 0);
               *reinterpret_cast<uint4*>(orow + c) = v;
@@ -673,6 +863,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
           }
         }
         const float cn = wn * inv_l;
+        if constexpr (decode) {
+          // fp32 partial rows (O / l) and their LSE for the split-K reduction
+#pragma unroll 1
+          for (int c0 = 0; c0 < kLatent; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tbase + lane_base + c0, v);
+            tmem_wait_ld();
+            if (row_ok) {
+              float4* dst = reinterpret_cast<float4*>(orow_f + c0);
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                dst[q] = make_float4(__uint_as_float(v[4 * q]) * cn, __uint_as_float(v[4 * q + 1]) * cn,
+                                     __uint_as_float(v[4 * q + 2]) * cn, __uint_as_float(v[4 * q + 3]) * cn);
+            }
+          }
+          tc_fence_before();
+          warp_arrive(&bars.o_free);  // O has been read: the next item's P V may start
+          if (row_ok) *lse_dst = lse_out;
+          ++i;
+          continue;
+        }
         // rows of this half live in ring slot (u + half), [8 column boxes][64 rows][128 B] swizzled
         const uint32_t sidx = u + half;
         const int s = sidx & 1;
@@ -745,17 +956,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
 cudaError_t launch_prefill128(const CoreParams& p, const CoreMaps& maps, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(mla_prefill128_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemT);
+    cudaError_t e = cudaFuncSetAttribute(mla_prefill128_kernel<true, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemT);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(mla_prefill128_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemT);
+      e = cudaFuncSetAttribute(mla_prefill128_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemT);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(mla_prefill128_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemT);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(mla_prefill128_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemT);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   if (p.num_pairs <= 0) return cudaSuccess;
-  if (p.scale_log2 >= 0.f)
-    mla_prefill128_kernel<true><<<dim3(2 * p.num_pairs), dim3(kThreadsT), kSmemT, stream>>>(p, maps);
-  else
-    mla_prefill128_kernel<false><<<dim3(2 * p.num_pairs), dim3(kThreadsT), kSmemT, stream>>>(p, maps);
+  const dim3 grid(2 * p.num_pairs), block(kThreadsT);
+  const bool up = p.scale_log2 >= 0.f;
+  if (p.mode == MODE_DECODE) {
+    if (up) mla_prefill128_kernel<true, true><<<grid, block, kSmemT, stream>>>(p, maps);
+    else mla_prefill128_kernel<false, true><<<grid, block, kSmemT, stream>>>(p, maps);
+  } else {
+    if (up) mla_prefill128_kernel<true, false><<<grid, block, kSmemT, stream>>>(p, maps);
+    else mla_prefill128_kernel<false, false><<<grid, block, kSmemT, stream>>>(p, maps);
+  }
   return cudaGetLastError();
 }
 

@@ -334,6 +334,18 @@ __device__ __forceinline__ float ex2_approx(float x) {
 
 __device__ __forceinline__ bool elect_lane0() { return (threadIdx.x & 31u) == 0u; }
 
+// TMA gather of four rows (tile::gather4; the tensor map's box is one row high): rows y0..y3
+// of columns [x, x + 64) land as four consecutive 128-byte rows at dst; a row of -1 (or
+// any row outside the map) is filled with zeros.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y0, int32_t y1,
+                                            int32_t y2, int32_t y3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // bulk copies, TMA stores, cluster commits, warp-level arrivals
 // ---------------------------------------------------------------------------

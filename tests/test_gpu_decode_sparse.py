@@ -8,10 +8,18 @@ import torch
 
 import oracle.mla_oracle as mo
 from mla_attention_gb300 import inputs as gen
-from mla_attention_gb300 import MLAError, check_device_status, mla_decode, mla_sparse
+from mla_attention_gb300 import MLAError, check_device_status, mla_decode, mla_sparse, set_tile_keys
 from tests.helpers import assert_lse_close, assert_out_close, dev, to_np
 
 pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(params=[128, 64], ids=["tile128", "tile64"])
+def tile_keys(request):
+    """Both decode engines: 128-key score tiles (the default) and 64-key tiles."""
+    set_tile_keys(decode_keys=request.param)
+    yield request.param
+    set_tile_keys(0, 0)
 
 
 def _decode(D, num_splits=0):
@@ -29,7 +37,7 @@ def _decode(D, num_splits=0):
     ([513, 96, 33], 64, 32, 7),
     ([4096, 100, 1000], 128, 128, 0),       # 128-token pages
 ])
-def test_decode_parity(lens, H, page, splits):
+def test_decode_parity(lens, H, page, splits, tile_keys):
     D = gen.decode_inputs(lens, H=H, seed=sum(lens) + H, page_size=page, extra_pages=2)
     out, lse = _decode(D, splits)
     ro, rl = mo.mla_decode(D.q, D.cache, D.block_table, D.lens, D.scale)
@@ -37,7 +45,7 @@ def test_decode_parity(lens, H, page, splits):
     assert_lse_close(lse, rl)
 
 
-def test_decode_row_set_is_exact():
+def test_decode_row_set_is_exact(tile_keys):
     """q = 0 makes every score equal; one-hot V rows encode each cache row's id, so
     out * len must be the exact histogram of the rows the page table selects."""
     lens = [64, 128, 7, 256]
@@ -59,7 +67,7 @@ def test_decode_row_set_is_exact():
         assert abs(float(lse[b, 0]) - math.log(n)) < 5e-3
 
 
-def test_decode_bad_page_reported():
+def test_decode_bad_page_reported(tile_keys):
     D = gen.decode_inputs([100, 50], H=16, seed=9, page_size=64)
     D.block_table[0, 1] = 1 << 20          # out of range
     out, lse = mla_decode(D.q.to(dev()), D.cache.to(dev()), D.block_table.to(dev()), D.lens.to(dev()), D.scale)

@@ -5,7 +5,7 @@ import torch
 
 import oracle.mla_oracle as mo
 from mla_attention_gb300 import inputs as gen
-from mla_attention_gb300 import check_device_status, mla_prefill, set_prefill_tile_keys
+from mla_attention_gb300 import check_device_status, mla_prefill, set_tile_keys
 from tests.helpers import assert_lse_close, assert_out_close, dev, to_np
 
 pytestmark = pytest.mark.gpu
@@ -14,9 +14,9 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture(params=[128, 64], ids=["tile128", "tile64"])
 def tile_keys(request):
     """Both prefill kernels: 128-key score tiles (the default) and 64-key tiles."""
-    set_prefill_tile_keys(request.param)
+    set_tile_keys(prefill_keys=request.param)
     yield request.param
-    set_prefill_tile_keys(0)
+    set_tile_keys(0, 0)
 
 
 def _run(P, **kw):
