@@ -647,24 +647,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
             }
             // keys past the row's limit read as -inf (exp2 gives 0) on the masked path
             const int lim = nv - 32 * p32;
-            const float neg = (lim >= 32) ? 0.f : -CUDART_INF_F;
+            uint8_t* pchunk = prow + (p32 >> 1) * kPBoxBytes;  // the 64-key box of this piece
+            if (lim >= 32) {  // every key of the piece visible (warp-uniform when H = 128)
 #pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {  // 8 keys -> one 16-byte chunk of P
-              uint32_t w[4];
+              for (int c8 = 0; c8 < 4; ++c8) {  // 8 keys -> one 16-byte chunk of P
+                uint32_t w[4];
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int c = 8 * c8 + 2 * u;
-                const float t0 = fmaf(__uint_as_float(sr[c]), sl2, -msub);
-                const float t1 = fmaf(__uint_as_float(sr[c + 1]), sl2, -msub);
-                const float e0 = ex2_approx((lim >= 32 || c < lim) ? t0 : neg);
-                const float e1 = ex2_approx((lim >= 32 || c + 1 < lim) ? t1 : neg);
-                rsq[u] += e0 + e1;
-                w[u] = pack_bf16x2(e0, e1);
+                for (int u = 0; u < 4; ++u) {
+                  const int c = 8 * c8 + 2 * u;
+                  const float e0 = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -msub));
+                  const float e1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), sl2, -msub));
+                  rsq[u] += e0 + e1;
+                  w[u] = pack_bf16x2(e0, e1);
+                }
+                const int chunk = (4 * p32 + c8) & 7;
+                *reinterpret_cast<uint4*>(pchunk + ((chunk ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
               }
-              const int kc = 4 * p32 + c8;  // 16-byte chunk of the 128-key row
-              const int box = kc >> 3, chunk = kc & 7;
-              *reinterpret_cast<uint4*>(prow + box * kPBoxBytes + ((chunk ^ (r & 7)) << 4)) =
-                  make_uint4(w[0], w[1], w[2], w[3]);
+            } else {
+#pragma unroll
+              for (int c8 = 0; c8 < 4; ++c8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const int c = 8 * c8 + 2 * u;
+                  const float t0 = fmaf(__uint_as_float(sr[c]), sl2, -msub);
+                  const float t1 = fmaf(__uint_as_float(sr[c + 1]), sl2, -msub);
+                  const float e0 = ex2_approx(c < lim ? t0 : -CUDART_INF_F);
+                  const float e1 = ex2_approx(c + 1 < lim ? t1 : -CUDART_INF_F);
+                  rsq[u] += e0 + e1;
+                  w[u] = pack_bf16x2(e0, e1);
+                }
+                const int chunk = (4 * p32 + c8) & 7;
+                *reinterpret_cast<uint4*>(pchunk + ((chunk ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+              }
             }
           }
           l += (rsq[0] + rsq[1]) + (rsq[2] + rsq[3]);
