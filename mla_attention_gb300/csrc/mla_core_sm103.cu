@@ -43,8 +43,12 @@ namespace mla {
 namespace {
 
 // warps 0-3 rows, warp 4 TMA; S-CTA: warps 5 and 7 issue the S MMAs of even and odd tiles,
-// warp 6 copies P out.  O-CTA: warp 5 issues P V.
-constexpr int kThreads = 256;
+// warp 6 copies P out, and on the sparse path warp 9 copies half of each K tile's gathered
+// rows (warp 8 has no role: warp 9 sits on another scheduler than warp 4).  O-CTA: warp 5
+// issues P V.
+constexpr int kThreadsDense = 256;
+constexpr int kThreadsSparse = 320;
+constexpr int kGatherWarp2 = 9;
 constexpr int kStagesS = 2;  // stage g % 2 pairs with S buffer g % 2
 constexpr int kStagesO = 3;
 constexpr int kBoxBytes = kKeys * 128;                 // 64 rows x 128 B
@@ -271,10 +275,70 @@ __device__ __forceinline__ void issue_gather_tile(uint32_t dst, const CUtensorMa
   }
 }
 
+// Raw top-k entries of tile j that lane l gathers (rows 2l and 2l+1 of the tile); -1 past K.
+// Loaded a tile before their use, so the range check waits for that use (sparse_row).
+__device__ __forceinline__ void sparse_tile_idx(const CoreParams& p, int id, int j, int32_t& re, int32_t& ro) {
+  const int lane = threadIdx.x & 31;
+  const int32_t* tk = p.topk + (int64_t)id * p.K;
+  const int c0 = j * kKeys + 2 * lane;
+  re = (c0 < p.K) ? __ldg(tk + c0) : -1;
+  ro = (c0 + 1 < p.K) ? __ldg(tk + c0 + 1) : -1;
+}
+
+// A top-k entry outside [0, S_kv) is padding: no row (-1 gathers zeros).
+__device__ __forceinline__ int32_t sparse_row(const CoreParams& p, int32_t r) {
+  return (r < 0 || r >= p.S_kv) ? -1 : r;
+}
+
+// One 64-column box of the tile (the RoPE columns of a separate [rows, 64] tensor) by TMA
+// gather: lanes 0..15 each issue rows 4g..4g+3.
+__device__ __forceinline__ void issue_gather_box(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t r_even,
+                                                 int32_t r_odd, uint64_t* bar) {
+  const int lane = threadIdx.x & 31;
+  const int32_t a0 = __shfl_sync(0xffffffffu, r_even, (2 * lane) & 31);
+  const int32_t a1 = __shfl_sync(0xffffffffu, r_odd, (2 * lane) & 31);
+  const int32_t a2 = __shfl_sync(0xffffffffu, r_even, (2 * lane + 1) & 31);
+  const int32_t a3 = __shfl_sync(0xffffffffu, r_odd, (2 * lane + 1) & 31);
+  if (lane < 16) gather4(dst + lane * 512, map, x, a0, a1, a2, a3, bar);
+}
+
+// The 512 latent columns of gathered rows 8*q0 .. 8*q1-1 of a 64-row tile with 16-byte
+// cp.async, in the layout of eight 64-column SW128 boxes.  A TMA gather moves one 128-byte row piece per request and
+// runs at a fraction of the tiled rate on scattered rows; here each warp instruction
+// moves 512 contiguous bytes of one row.  Rows as in issue_gather_tile (lane l: rows 2l,
+// 2l+1; -1 gives a zero row).  Every lane arrives on `bar` (noinc) once its copies have
+// landed; the reader of the stage orders them before its async-proxy reads with a proxy
+// fence.
+__device__ __forceinline__ void lsu_gather_latent(uint32_t dst, const __nv_bfloat16* c_kv, int32_t r_even,
+                                                  int32_t r_odd, uint64_t* bar, int q0, int q1) {
+  const int lane = threadIdx.x & 31;
+  // lane copies chunks `lane` and `lane + 32` of each 1024-byte row: boxes lane/8 and
+  // lane/8 + 4, 16-byte column lane % 8 (XOR the row's swizzle phase)
+  const char* base = reinterpret_cast<const char*>(c_kv) + lane * 16;
+  const uint32_t lp0 = (uint32_t)(lane >> 3) * kBoxBytes + ((uint32_t)(lane & 7) << 4);
+  const uint32_t lp1 = lp0 + 4u * kBoxBytes;
+#pragma unroll 1
+  for (int q = q0; q < q1; ++q) {  // rows 8q..8q+7, held by lanes 4q..4q+3
+    const uint32_t rb = dst + (uint32_t)q * 1024u;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int32_t ri = __shfl_sync(0xffffffffu, (k & 1) ? r_odd : r_even, 4 * q + (k >> 1));
+      const uint32_t n = ri >= 0 ? 16u : 0u;
+      const char* src = base + (int64_t)(ri >= 0 ? ri : 0) * (kLatent * 2);
+      cp_async16_zfill(rb + k * 128 + (lp0 ^ ((uint32_t)k << 4)), src, n);
+      cp_async16_zfill(rb + k * 128 + (lp1 ^ ((uint32_t)k << 4)), src + 512, n);
+    }
+  }
+  cp_async_arrive_noinc(bar);
+}
+
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+// One instantiation for the sparse path and one for prefill and decode: each carries only
+// its own loaders (the shared code is sensitive to instruction-cache footprint).
+template <bool kSparse>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSparse : kThreadsDense, 1)
     mla_core_kernel(const __grid_constant__ CoreParams p, const __grid_constant__ CoreMaps maps) {
   const CUtensorMap& map_kv = maps.kv;
   const CUtensorMap& map_row = maps.row;
@@ -284,7 +348,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // Prefill (128 flat rows per tile) and sparse with H a multiple of 64 stage
   // their output (and the previous output) through two V stages and TMA; decode
   // writes fp32 partials directly, and other head counts write bf16 rows directly.
-  const bool staged = (p.mode == MODE_PREFILL) || (p.mode == MODE_SPARSE && (p.H % 64) == 0);
+  const bool staged = kSparse ? (p.H % 64) == 0 : p.mode == MODE_PREFILL;
   const int rows_per_item = (p.mode == MODE_PREFILL) ? kRows : p.H;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -302,8 +366,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // ---- setup ----
   if (tid == 0) {
     if (is_s) {
+      // sparse: + one noinc arrival per lane of the two gathering warps
       for (int i = 0; i < 2; ++i) {
-        mbar_init(&bars.s_go[i], kRowWarps + 1);
+        mbar_init(&bars.s_go[i], kRowWarps + 1 + (kSparse ? 64 : 0));
         mbar_init(&bars.s_full[i], 1);
         mbar_init(&bars.pb_free[i], 1);
       }
@@ -316,7 +381,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     } else {
       for (int i = 0; i < kStagesO; ++i) {
-        mbar_init(&bars.o_kv_full[i], 1);
+        mbar_init(&bars.o_kv_full[i], 1 + (kSparse ? 32 : 0));
         mbar_init(&bars.o_kv_empty[i], 1);
       }
       for (int i = 0; i < 2; ++i) {
@@ -390,17 +455,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // =====================================================================
     // S-CTA
     // =====================================================================
-    if (warp == 4) {
+    if (warp == 4 || (kSparse && warp == kGatherWarp2)) {
       // ---------------- TMA producer: K tiles (all 576 columns) ----------------
       uint32_t g = 0;
       bool live = true;
       while (live && iter.next(it)) {
+        int32_t nre = -1, nro = -1;  // sparse: top-k entries of the next tile, loaded a tile ahead
+        if (kSparse && it.J > 0) sparse_tile_idx(p, it.id, 0, nre, nro);
         for (int j = 0; j < it.J && live; ++j, ++g) {
           const int s = g & 1;
           // stage s was last read by the S MMA of tile g-2
           if (!waitb(&bars.s_full[s], ((g >> 1) & 1) ^ 1, W_S_KV_EMPTY, false)) { live = false; break; }
           const uint32_t dst = smem_u32(smem + kOffStages + s * kStageBytesS);
-          if (p.mode == MODE_PREFILL) {
+          if (!kSparse && p.mode == MODE_PREFILL) {
             if (lane == 0) {
               mbar_arrive_expect_tx(&bars.s_go[s], kStageBytesS);
               for (int bx = 0; bx < kKBoxes; ++bx)
@@ -410,7 +477,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int32_t re, ro;
             bool tiled = false;
             int32_t ytile = 0;
-            if (p.mode == MODE_DECODE) {
+            if constexpr (!kSparse) {
               const int64_t kb = it.k0 + (int64_t)j * kKeys;  // first key of the tile
               const int len = decode_len(p, it.id);
               const int32_t* bt = p.block_table + (int64_t)it.id * p.max_pages;
@@ -433,27 +500,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               re = row_of(kb + 2 * lane);
               ro = row_of(kb + 2 * lane + 1);
             } else {
-              const int32_t* tk = p.topk + (int64_t)it.id * p.K;
-              const int c0 = j * kKeys + 2 * lane;
-              re = (c0 < p.K) ? tk[c0] : -1;
-              ro = (c0 + 1 < p.K) ? tk[c0 + 1] : -1;
-              if (re < 0 || re >= p.S_kv) re = -1;
-              if (ro < 0 || ro >= p.S_kv) ro = -1;
+              re = sparse_row(p, nre);
+              ro = sparse_row(p, nro);
+              if (j + 1 < it.J) sparse_tile_idx(p, it.id, j + 1, nre, nro);  // lands during this gather
             }
-            if (lane == 0) mbar_arrive_expect_tx(&bars.s_go[s], kStageBytesS);
-            __syncwarp();
-            if (tiled) {
-              if (lane == 0)
-                for (int bx = 0; bx < kKBoxes; ++bx)
-                  tma_load_2d(dst + bx * kBoxBytes, &map_kv, bx * kBoxCols, ytile, &bars.s_go[s]);
+            if constexpr (kSparse) {
+              // RoPE box by TMA gather, latent columns by 16-byte copies: the two run side by
+              // side; warp 4 copies rows 0-31 and warp 9 rows 32-63
+              if (warp == 4) {
+                if (lane == 0) mbar_arrive_expect_tx(&bars.s_go[s], kBoxBytes);
+                __syncwarp();
+                issue_gather_box(dst + kVBoxes * kBoxBytes, &map_pe, 0, re, ro, &bars.s_go[s]);
+              }
+              const int q0 = (warp == 4) ? 0 : kKeys / 16;
+              lsu_gather_latent(dst, p.c_kv, re, ro, &bars.s_go[s], q0, q0 + kKeys / 16);
             } else {
-              issue_gather_tile(dst, &map_row, &map_pe, p.mode == MODE_DECODE ? kLatent : 0, kKBoxes, re, ro,
-                                &bars.s_go[s]);
+              if (lane == 0) mbar_arrive_expect_tx(&bars.s_go[s], kStageBytesS);
+              __syncwarp();
+              if (tiled) {
+                if (lane == 0)
+                  for (int bx = 0; bx < kKBoxes; ++bx)
+                    tma_load_2d(dst + bx * kBoxBytes, &map_kv, bx * kBoxCols, ytile, &bars.s_go[s]);
+              } else {
+                issue_gather_tile(dst, &map_row, &map_pe, kLatent, kKBoxes, re, ro, &bars.s_go[s]);
+              }
             }
           }
           __syncwarp();
         }
       }
+      if (kSparse) cp_async_wait_all();  // no copy into this CTA outlives it
     } else if (warp == 5 || warp == 7) {
       // ---------------- MMA issuers: S = Q K^T ----------------
       // Two warps take turns, warp 5 the even tiles and warp 7 the odd ones; each owns one K
@@ -486,6 +562,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               live = false;
               break;
             }
+            if (kSparse) fence_proxy_async_smem();  // cp.async rows, read by the MMA
             tc_fence_after();
             mma_s_q576_n64(d_tmem, tbase + kTmemQ, bdesc, idesc);
             mma_commit(&bars.s_full[b]);
@@ -568,7 +645,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           int64_t nk;
           if (found && query_row(p, nx, r, nq, npe, nk)) {
             const char* b = reinterpret_cast<const char*>(nq);
-            const int nbytes = (p.mode == MODE_SPARSE) ? kLatent * 2 : kDk * 2;
+            const int nbytes = kSparse ? kLatent * 2 : kDk * 2;
             for (int o = 0; o < nbytes; o += 128) prefetch_l2(b + o);
             if (npe) prefetch_l2(npe);
           }
@@ -585,7 +662,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int c = c0 + cc;
             const uint4* src = nullptr;
             if (row_ok) {
-              if (p.mode == MODE_SPARSE)
+              if (kSparse)
                 src = (c < 8) ? reinterpret_cast<const uint4*>(qrow + c * 64) : reinterpret_cast<const uint4*>(qpe);
               else
                 src = reinterpret_cast<const uint4*>(qrow + c * 64);
@@ -616,11 +693,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int sb = g & 1;
           // ---- per-tile key validity mask ----
           uint64_t vmask;
-          if (p.mode == MODE_PREFILL) {
+          if (!kSparse && p.mode == MODE_PREFILL) {
             int64_t nv = nkeys - (int64_t)j * kKeys;
             nv = nv < 0 ? 0 : (nv > 64 ? 64 : nv);
             vmask = (nv == 64) ? ~0ull : ((1ull << nv) - 1ull);
-          } else if (p.mode == MODE_DECODE) {
+          } else if (!kSparse) {
             int64_t nv = it.k1 - (it.k0 + (int64_t)j * kKeys);
             nv = nv < 0 ? 0 : (nv > 64 ? 64 : nv);
             vmask = (nv == 64) ? ~0ull : ((1ull << nv) - 1ull);
@@ -726,11 +803,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t g = 0;  // position in the stage ring
       bool live = true;
       while (live && iter.next(it)) {
+        int32_t nre = -1, nro = -1;  // sparse: top-k entries of the next tile, loaded a tile ahead
+        if (kSparse && it.J > 0) sparse_tile_idx(p, it.id, 0, nre, nro);
         for (int j = 0; j < it.J && live; ++j, ++g) {
           const int s = g % kStagesO;
           if (!waitb(&bars.o_kv_empty[s], ((g / kStagesO) & 1) ^ 1, W_O_KV_EMPTY, false)) { live = false; break; }
           const uint32_t dst = smem_u32(smem + kOffStages + s * kStageBytesO);
-          if (p.mode == MODE_PREFILL) {
+          if (!kSparse && p.mode == MODE_PREFILL) {
             if (lane == 0) {
               mbar_arrive_expect_tx(&bars.o_kv_full[s], kStageBytesO);
               for (int bx = 0; bx < kVBoxes; ++bx)
@@ -740,7 +819,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int32_t re, ro;
             bool tiled = false;
             int32_t ytile = 0;
-            if (p.mode == MODE_DECODE) {
+            if constexpr (!kSparse) {
               const int64_t kb = it.k0 + (int64_t)j * kKeys;
               const int len = decode_len(p, it.id);
               const int32_t* bt = p.block_table + (int64_t)it.id * p.max_pages;
@@ -760,21 +839,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               re = row_of(kb + 2 * lane);
               ro = row_of(kb + 2 * lane + 1);
             } else {
-              const int32_t* tk = p.topk + (int64_t)it.id * p.K;
-              const int c0 = j * kKeys + 2 * lane;
-              re = (c0 < p.K) ? tk[c0] : -1;
-              ro = (c0 + 1 < p.K) ? tk[c0 + 1] : -1;
-              if (re < 0 || re >= p.S_kv) re = -1;
-              if (ro < 0 || ro >= p.S_kv) ro = -1;
+              re = sparse_row(p, nre);
+              ro = sparse_row(p, nro);
+              if (j + 1 < it.J) sparse_tile_idx(p, it.id, j + 1, nre, nro);  // lands during this gather
             }
-            if (lane == 0) mbar_arrive_expect_tx(&bars.o_kv_full[s], kStageBytesO);
-            __syncwarp();
-            if (tiled) {
-              if (lane == 0)
-                for (int bx = 0; bx < kVBoxes; ++bx)
-                  tma_load_2d(dst + bx * kBoxBytes, &map_kv, bx * kBoxCols, ytile, &bars.o_kv_full[s]);
+            if constexpr (kSparse) {
+              if (lane == 0) mbar_arrive(&bars.o_kv_full[s]);
+              lsu_gather_latent(dst, p.c_kv, re, ro, &bars.o_kv_full[s], 0, kKeys / 8);
             } else {
-              issue_gather_tile(dst, &map_row, &map_pe, 0, kVBoxes, re, ro, &bars.o_kv_full[s]);
+              if (lane == 0) mbar_arrive_expect_tx(&bars.o_kv_full[s], kStageBytesO);
+              __syncwarp();
+              if (tiled) {
+                if (lane == 0)
+                  for (int bx = 0; bx < kVBoxes; ++bx)
+                    tma_load_2d(dst + bx * kBoxBytes, &map_kv, bx * kBoxCols, ytile, &bars.o_kv_full[s]);
+              } else {
+                issue_gather_tile(dst, &map_row, &map_pe, 0, kVBoxes, re, ro, &bars.o_kv_full[s]);
+              }
             }
           }
           __syncwarp();
@@ -796,10 +877,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 mbar_arrive(&bars.o_kv_full[s]);
               }
             }
+            if (kSparse) mbar_arrive(&bars.o_kv_full[s]);  // the lanes' share of the count
             __syncwarp();
           }
         }
       }
+      if (kSparse) cp_async_wait_all();  // no copy into this CTA outlives it
     } else if (warp == 5) {
       // ---------------- MMA issuer: O += P V ----------------
       const uint32_t idesc = idesc_bf16_f32(kRows, 256, false, true);
@@ -818,6 +901,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           if (lane == 0) {
+            if (kSparse) fence_proxy_async_smem();  // cp.async rows, read by the MMA
             const uint32_t vst = smem_u32(smem + kOffStages + s * kStageBytesO);
             const uint32_t pst = smem_u32(smem + kOffPO + pb * kPBytes);
             mma_pv_k64_n512(tbase, tbase + 256, sdesc_sw128(pst, 16, 1024), sdesc_sw128(vst, kBoxBytes, 1024),
@@ -851,7 +935,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __nv_bfloat16* orow = nullptr;
         float* orow_f = nullptr;
         float* lse_dst = nullptr;
-        if (p.mode == MODE_PREFILL) {
+        if (!kSparse && p.mode == MODE_PREFILL) {
           const int64_t f = (int64_t)it.id * kRows + r;
           if (f < (int64_t)p.T * p.H) {
             const int64_t t = f / p.H, h = f - t * p.H;
@@ -863,7 +947,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               prev_l = p.prev_lse[h * p.T + t];
             }
           }
-        } else if (p.mode == MODE_DECODE) {
+        } else if (!kSparse) {
           if (r < p.H) {
             row_ok = true;
             orow_f = p.part_o + ((int64_t)it.slot * p.H + r) * kLatent;
@@ -1063,12 +1147,18 @@ size_t core_smem_bytes() { return kSmemAlloc; }
 cudaError_t launch_core(const CoreParams& p, const CoreMaps& maps, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(mla_core_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    cudaError_t e = cudaFuncSetAttribute(mla_core_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemAlloc);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(mla_core_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   if (p.num_pairs <= 0) return cudaSuccess;
-  mla_core_kernel<<<dim3(2 * p.num_pairs), dim3(kThreads), kSmemAlloc, stream>>>(p, maps);
+  if (p.mode == MODE_SPARSE)
+    mla_core_kernel<true><<<dim3(2 * p.num_pairs), dim3(kThreadsSparse), kSmemAlloc, stream>>>(p, maps);
+  else
+    mla_core_kernel<false><<<dim3(2 * p.num_pairs), dim3(kThreadsDense), kSmemAlloc, stream>>>(p, maps);
   return cudaGetLastError();
 }
 
