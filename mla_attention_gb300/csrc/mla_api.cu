@@ -363,6 +363,7 @@ mla_status mla_sparse(const void* q_lift, const void* q_pe, const void* c_kv, co
   p.lse = lse;
   p.topk = topk;
   p.c_kv = reinterpret_cast<const __nv_bfloat16*>(c_kv);
+  p.k_pe = reinterpret_cast<const __nv_bfloat16*>(k_pe);
   p.K = K;
   p.S_kv = S_kv;
   cudaError_t e = launch_core(p, maps, st);

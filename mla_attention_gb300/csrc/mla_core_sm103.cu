@@ -290,29 +290,18 @@ __device__ __forceinline__ int32_t sparse_row(const CoreParams& p, int32_t r) {
   return (r < 0 || r >= p.S_kv) ? -1 : r;
 }
 
-// One 64-column box of the tile (the RoPE columns of a separate [rows, 64] tensor) by TMA
-// gather: lanes 0..15 each issue rows 4g..4g+3.
-__device__ __forceinline__ void issue_gather_box(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t r_even,
-                                                 int32_t r_odd, uint64_t* bar) {
+// Gathered rows 8*q0 .. 8*q1-1 of a 64-row tile with 16-byte cp.async, in the layout of the
+// SW128 boxes a tiled TMA load gives: the 512 latent columns (eight boxes) and, when k_pe is
+// given, the 64 RoPE columns (the ninth).  A TMA gather moves one 128-byte row piece per
+// request and runs at a fraction of the tiled rate on scattered rows; here each warp
+// instruction moves 512 contiguous bytes of one latent row, or four 128-byte RoPE rows.
+// Rows as in issue_gather_tile (lane l: rows 2l, 2l+1; -1 gives a zero row).  Every lane
+// arrives on `bar` (noinc) once its copies have landed; the reader of the stage orders them
+// before its async-proxy reads with a proxy fence.
+__device__ __forceinline__ void lsu_gather_rows(uint32_t dst, const __nv_bfloat16* c_kv, const __nv_bfloat16* k_pe,
+                                                int32_t r_even, int32_t r_odd, uint64_t* bar, int q0, int q1) {
   const int lane = threadIdx.x & 31;
-  const int32_t a0 = __shfl_sync(0xffffffffu, r_even, (2 * lane) & 31);
-  const int32_t a1 = __shfl_sync(0xffffffffu, r_odd, (2 * lane) & 31);
-  const int32_t a2 = __shfl_sync(0xffffffffu, r_even, (2 * lane + 1) & 31);
-  const int32_t a3 = __shfl_sync(0xffffffffu, r_odd, (2 * lane + 1) & 31);
-  if (lane < 16) gather4(dst + lane * 512, map, x, a0, a1, a2, a3, bar);
-}
-
-// The 512 latent columns of gathered rows 8*q0 .. 8*q1-1 of a 64-row tile with 16-byte
-// cp.async, in the layout of eight 64-column SW128 boxes.  A TMA gather moves one 128-byte row piece per request and
-// runs at a fraction of the tiled rate on scattered rows; here each warp instruction
-// moves 512 contiguous bytes of one row.  Rows as in issue_gather_tile (lane l: rows 2l,
-// 2l+1; -1 gives a zero row).  Every lane arrives on `bar` (noinc) once its copies have
-// landed; the reader of the stage orders them before its async-proxy reads with a proxy
-// fence.
-__device__ __forceinline__ void lsu_gather_latent(uint32_t dst, const __nv_bfloat16* c_kv, int32_t r_even,
-                                                  int32_t r_odd, uint64_t* bar, int q0, int q1) {
-  const int lane = threadIdx.x & 31;
-  // lane copies chunks `lane` and `lane + 32` of each 1024-byte row: boxes lane/8 and
+  // latent: lane copies pieces `lane` and `lane + 32` of each 1024-byte row: boxes lane/8 and
   // lane/8 + 4, 16-byte column lane % 8 (XOR the row's swizzle phase)
   const char* base = reinterpret_cast<const char*>(c_kv) + lane * 16;
   const uint32_t lp0 = (uint32_t)(lane >> 3) * kBoxBytes + ((uint32_t)(lane & 7) << 4);
@@ -327,6 +316,21 @@ __device__ __forceinline__ void lsu_gather_latent(uint32_t dst, const __nv_bfloa
       const char* src = base + (int64_t)(ri >= 0 ? ri : 0) * (kLatent * 2);
       cp_async16_zfill(rb + k * 128 + (lp0 ^ ((uint32_t)k << 4)), src, n);
       cp_async16_zfill(rb + k * 128 + (lp1 ^ ((uint32_t)k << 4)), src + 512, n);
+    }
+  }
+  if (k_pe != nullptr) {
+    // RoPE: lane copies piece lane % 8 of row 4i + lane / 8, for row groups i of these rows
+    const int rr = lane >> 3, c = lane & 7;
+    const char* pbase = reinterpret_cast<const char*>(k_pe) + c * 16;
+    const uint32_t box = dst + (uint32_t)kVBoxes * kBoxBytes;
+#pragma unroll 1
+    for (int i = 2 * q0; i < 2 * q1; ++i) {
+      const int row = 4 * i + rr;
+      const int32_t ae = __shfl_sync(0xffffffffu, r_even, 2 * i + (rr >> 1));
+      const int32_t ao = __shfl_sync(0xffffffffu, r_odd, 2 * i + (rr >> 1));
+      const int32_t ri = (rr & 1) ? ao : ae;
+      cp_async16_zfill(box + (uint32_t)row * 128u + ((uint32_t)(c ^ (row & 7)) << 4),
+                       pbase + (int64_t)(ri >= 0 ? ri : 0) * (kRope * 2), ri >= 0 ? 16u : 0u);
     }
   }
   cp_async_arrive_noinc(bar);
@@ -366,9 +370,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
   // ---- setup ----
   if (tid == 0) {
     if (is_s) {
-      // sparse: + one noinc arrival per lane of the two gathering warps
+      // sparse: one noinc arrival per lane of the two gathering warps instead of the
+      // producer's expect-tx arrival
       for (int i = 0; i < 2; ++i) {
-        mbar_init(&bars.s_go[i], kRowWarps + 1 + (kSparse ? 64 : 0));
+        mbar_init(&bars.s_go[i], kRowWarps + (kSparse ? 64 : 1));
         mbar_init(&bars.s_full[i], 1);
         mbar_init(&bars.pb_free[i], 1);
       }
@@ -462,6 +467,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
       while (live && iter.next(it)) {
         int32_t nre = -1, nro = -1;  // sparse: top-k entries of the next tile, loaded a tile ahead
         if (kSparse && it.J > 0) sparse_tile_idx(p, it.id, 0, nre, nro);
+        // decode with pages of whole tiles: block-table entry of the next tile, loaded a tile ahead
+        const bool whole_pages = !kSparse && p.mode == MODE_DECODE && p.page_size % kKeys == 0;
+        int32_t npg = -1;
+        if (whole_pages && it.J > 0) npg = p.block_table[(int64_t)it.id * p.max_pages + it.k0 / p.page_size];
         for (int j = 0; j < it.J && live; ++j, ++g) {
           const int s = g & 1;
           // stage s was last read by the S MMA of tile g-2
@@ -474,7 +483,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
                 tma_load_2d(dst + bx * kBoxBytes, &map_kv, bx * kBoxCols, j * kKeys, &bars.s_go[s]);
             }
           } else {
-            int32_t re, ro;
+            int32_t re = -1, ro = -1;
             bool tiled = false;
             int32_t ytile = 0;
             if constexpr (!kSparse) {
@@ -490,30 +499,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
                 }
                 return (int32_t)(pg * (int64_t)p.page_size + key % p.page_size);
               };
-              if (p.page_size % kKeys == 0 && kb + kKeys <= len) {
-                const int32_t pg = bt[kb / p.page_size];
-                if (pg >= 0 && pg < p.num_pages) {
-                  tiled = true;
-                  ytile = (int32_t)(pg * (int64_t)p.page_size + kb % p.page_size);
-                }
+              // pages that hold whole tiles: this tile's entry was loaded a tile ago
+              const int32_t pg = npg;
+              if (whole_pages && j + 1 < it.J) npg = bt[(kb + kKeys) / p.page_size];
+              if (whole_pages && kb + kKeys <= len && pg >= 0 && pg < p.num_pages) {
+                tiled = true;
+                ytile = (int32_t)(pg * (int64_t)p.page_size + kb % p.page_size);
+              } else {
+                re = row_of(kb + 2 * lane);
+                ro = row_of(kb + 2 * lane + 1);
               }
-              re = row_of(kb + 2 * lane);
-              ro = row_of(kb + 2 * lane + 1);
             } else {
               re = sparse_row(p, nre);
               ro = sparse_row(p, nro);
               if (j + 1 < it.J) sparse_tile_idx(p, it.id, j + 1, nre, nro);  // lands during this gather
             }
             if constexpr (kSparse) {
-              // RoPE box by TMA gather, latent columns by 16-byte copies: the two run side by
-              // side; warp 4 copies rows 0-31 and warp 9 rows 32-63
-              if (warp == 4) {
-                if (lane == 0) mbar_arrive_expect_tx(&bars.s_go[s], kBoxBytes);
-                __syncwarp();
-                issue_gather_box(dst + kVBoxes * kBoxBytes, &map_pe, 0, re, ro, &bars.s_go[s]);
-              }
+              // all 576 columns by 16-byte copies: warp 4 copies rows 0-31, warp 9 rows 32-63
               const int q0 = (warp == 4) ? 0 : kKeys / 16;
-              lsu_gather_latent(dst, p.c_kv, re, ro, &bars.s_go[s], q0, q0 + kKeys / 16);
+              lsu_gather_rows(dst, p.c_kv, p.k_pe, re, ro, &bars.s_go[s], q0, q0 + kKeys / 16);
             } else {
               if (lane == 0) mbar_arrive_expect_tx(&bars.s_go[s], kStageBytesS);
               __syncwarp();
@@ -805,6 +809,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
       while (live && iter.next(it)) {
         int32_t nre = -1, nro = -1;  // sparse: top-k entries of the next tile, loaded a tile ahead
         if (kSparse && it.J > 0) sparse_tile_idx(p, it.id, 0, nre, nro);
+        // decode with pages of whole tiles: block-table entry of the next tile, loaded a tile ahead
+        const bool whole_pages = !kSparse && p.mode == MODE_DECODE && p.page_size % kKeys == 0;
+        int32_t npg = -1;
+        if (whole_pages && it.J > 0) npg = p.block_table[(int64_t)it.id * p.max_pages + it.k0 / p.page_size];
         for (int j = 0; j < it.J && live; ++j, ++g) {
           const int s = g % kStagesO;
           if (!waitb(&bars.o_kv_empty[s], ((g / kStagesO) & 1) ^ 1, W_O_KV_EMPTY, false)) { live = false; break; }
@@ -816,7 +824,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
                 tma_load_2d(dst + bx * kBoxBytes, &map_kv, bx * kBoxCols, j * kKeys, &bars.o_kv_full[s]);
             }
           } else {
-            int32_t re, ro;
+            int32_t re = -1, ro = -1;
             bool tiled = false;
             int32_t ytile = 0;
             if constexpr (!kSparse) {
@@ -829,15 +837,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
                 if (pg < 0 || pg >= p.num_pages) return -1;
                 return (int32_t)(pg * (int64_t)p.page_size + key % p.page_size);
               };
-              if (p.page_size % kKeys == 0 && kb + kKeys <= len) {
-                const int32_t pg = bt[kb / p.page_size];
-                if (pg >= 0 && pg < p.num_pages) {
-                  tiled = true;
-                  ytile = (int32_t)(pg * (int64_t)p.page_size + kb % p.page_size);
-                }
+              // pages that hold whole tiles: this tile's entry was loaded a tile ago
+              const int32_t pg = npg;
+              if (whole_pages && j + 1 < it.J) npg = bt[(kb + kKeys) / p.page_size];
+              if (whole_pages && kb + kKeys <= len && pg >= 0 && pg < p.num_pages) {
+                tiled = true;
+                ytile = (int32_t)(pg * (int64_t)p.page_size + kb % p.page_size);
+              } else {
+                re = row_of(kb + 2 * lane);
+                ro = row_of(kb + 2 * lane + 1);
               }
-              re = row_of(kb + 2 * lane);
-              ro = row_of(kb + 2 * lane + 1);
             } else {
               re = sparse_row(p, nre);
               ro = sparse_row(p, nro);
@@ -845,7 +854,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
             }
             if constexpr (kSparse) {
               if (lane == 0) mbar_arrive(&bars.o_kv_full[s]);
-              lsu_gather_latent(dst, p.c_kv, re, ro, &bars.o_kv_full[s], 0, kKeys / 8);
+              lsu_gather_rows(dst, p.c_kv, nullptr, re, ro, &bars.o_kv_full[s], 0, kKeys / 8);
             } else {
               if (lane == 0) mbar_arrive_expect_tx(&bars.o_kv_full[s], kStageBytesO);
               __syncwarp();

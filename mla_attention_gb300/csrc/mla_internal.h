@@ -74,6 +74,7 @@ struct CoreParams {
   // ---- sparse ----
   const int32_t* topk;           // [S, K]
   const __nv_bfloat16* c_kv;     // [S_kv, 512] rows, read with 16-byte copies
+  const __nv_bfloat16* k_pe;     // [S_kv, 64] rows, read with 16-byte copies
   int K;
   int S_kv;
 };
