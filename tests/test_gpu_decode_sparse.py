@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 
 @pytest.fixture(params=[128, 64], ids=["tile128", "tile64"])
 def tile_keys(request):
-    """Both decode engines: 128-key score tiles (the default) and 64-key tiles."""
+    """Both decode engines: 64-key score tiles (the default) and 128-key tiles."""
     set_tile_keys(decode_keys=request.param)
     yield request.param
     set_tile_keys(0, 0)
@@ -67,9 +67,12 @@ def test_decode_row_set_is_exact(tile_keys):
         assert abs(float(lse[b, 0]) - math.log(n)) < 5e-3
 
 
-def test_decode_bad_page_reported(tile_keys):
-    D = gen.decode_inputs([100, 50], H=16, seed=9, page_size=64)
-    D.block_table[0, 1] = 1 << 20          # out of range
+@pytest.mark.parametrize("lens,bad", [([100, 50], (0, 1)),     # in a partial tile
+                                      ([300, 50], (0, 2)),     # in a whole tile, mid-request
+                                      ([64, 250], (1, 0))])    # first tile of a request
+def test_decode_bad_page_reported(lens, bad, tile_keys):
+    D = gen.decode_inputs(lens, H=16, seed=9, page_size=64)
+    D.block_table[bad] = 1 << 20           # out of range
     out, lse = mla_decode(D.q.to(dev()), D.cache.to(dev()), D.block_table.to(dev()), D.lens.to(dev()), D.scale)
     torch.cuda.synchronize()
     with pytest.raises(MLAError) as e:
@@ -105,6 +108,8 @@ def test_sparse_parity(S, S_kv, H, K, pos0):
     SI.topk[0, 0, 5] = -1
     SI.topk[0, 1, 7] = S_kv + 5
     SI.topk[0, 2, 9] = SI.topk[0, 2, 8]
+    if K >= 192:
+        SI.topk[0, 3, 64:128] = -1         # a whole 64-row tile of padding mid-list
     out, lse = _sparse(SI)
     ro, rl = mo.mla_sparse(SI.q_lift, SI.q_pe, SI.c_kv, SI.k_pe, SI.topk, SI.scale)
     assert_out_close(out, ro)
