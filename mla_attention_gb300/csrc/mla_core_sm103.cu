@@ -29,8 +29,10 @@
 //   decode  - a paged latent cache; split-K: each CTA pair owns an equal share
 //             of all requests' key tiles and writes per-request partials that
 //             a reduction kernel merges (Mojo "mha_single_batch_pipelined")
-//   sparse  - the top-k rows of each query, gathered with TMA tile::gather4
-//             (AWS NKI "MLA Sparse Attention CTE Kernel API Reference")
+//   sparse  - the top-k rows of each query, gathered with 16-byte cp.async into the
+//             layout the TMA boxes give (AWS NKI "MLA Sparse Attention CTE Kernel
+//             API Reference"); the c_kv and k_pe tensor maps are still encoded
+//             (which validates the tensors) but no load uses them
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
