@@ -46,6 +46,16 @@ def chunk_pairs():
     return [causal_pairs(T_TOTAL, CHUNK, 0, CHUNK * j) for j in range(T_TOTAL // CHUNK)]
 
 
+def prefill_config(world):
+    """The workload both arms report (the reference arm times a bounded sample of it)."""
+    pairs = chunk_pairs()
+    return {"workload": "chunked ring-style causal absorbed MLA prefill: B=1, H=128, dk=576, dv=512, "
+                        "8192 tokens, 4 KV chunks of 2048 in sequence with in-place prev merge",
+            "tflop_per_step": round(sum(pairs) * FLOP_PER_PAIR / 1e12, 4), "unmasked_pairs": sum(pairs),
+            "l2": "inputs larger than L2 (q 1.2 GB, out 1.07 GB per step)", "parallelism": f"replicas x{world}",
+            "inputs": "seeded N(0,1) bf16"}
+
+
 def kernel_source_digest(files):
     h = hashlib.sha256()
     for f in files:
@@ -450,11 +460,7 @@ def run_libmla(args, world, rank, local):
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "chunked ring-style causal absorbed MLA prefill: B=1, H=128, dk=576, dv=512, "
-                               "8192 tokens, 4 KV chunks of 2048 in sequence with in-place prev merge",
-                   "tflop_per_step": round(flops_step / 1e12, 4), "unmasked_pairs": sum(pairs),
-                   "l2": "inputs larger than L2 (q 1.2 GB, out 1.07 GB per step)", "parallelism": f"replicas x{world}",
-                   "inputs": "seeded N(0,1) bf16 drawn on the device"},
+        "config": prefill_config(world),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "mla_prefill128_kernel", "peak_kind": f"bf16 burst ({peak_kind})"},
@@ -490,8 +496,7 @@ def run_reference(args, world, rank):
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": world,
             "steps": steps, "warmup": warmup, "ms_per_step": round(dt / steps * 1e3, 2), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "chunked ring-style causal absorbed MLA prefill: B=1, H=128, dk=576, dv=512, "
-                                   "8192 tokens (oracle on a bounded sample of the rows)"},
+            "config": prefill_config(world),
             "cpu_baseline": cb,
             "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
