@@ -102,3 +102,16 @@ def test_workspace_sizes(L):
     assert L.mla_prefill_workspace_size(8192, 128) >= 256
     # decode partials: (B + pairs) slots x H x (512 + 1) fp32
     assert L.mla_decode_workspace_size(64, 128, 76) >= (64 + 76) * 128 * 513 * 4
+
+
+def test_bench_flop_accounting():
+    """The bench counts unmasked (token, key) pairs per KV chunk; the four chunks of the
+    8192-token causal prefill must add up to T (T + 1) / 2, and chunk j (keys 2048 j ..
+    2048 j + 2047) is a causal triangle plus full rows for the later tokens."""
+    import bench
+    T, C = bench.T_TOTAL, bench.CHUNK
+    pairs = bench.chunk_pairs()
+    assert sum(pairs) == T * (T + 1) // 2
+    for j, n in enumerate(pairs):
+        assert n == C * (C + 1) // 2 + (T - C * (j + 1)) * C
+    assert bench.FLOP_PER_PAIR == 2 * 128 * (576 + 512)
