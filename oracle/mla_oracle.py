@@ -36,7 +36,7 @@ Passages followed (pages by title, with their sections):
   * AWS NKI "MLA Sparse Attention CTE Kernel API Reference": per query,
     absorbed latent + RoPE attention over the top-k selected cache rows.
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
   * lse is the natural log of sum exp(scale * q.k) (Ascend: "exp, sum, and log
     ... in sequence"); prev_lse is fp32 (the page's "float16" for prevLse
     contradicts its float softmaxLse output).
@@ -99,19 +99,6 @@ def attend(q_rows: np.ndarray, keys: np.ndarray, values: np.ndarray, scale: floa
     l = p.sum(axis=1, keepdims=True)               # row sum
     out = (p @ values) / l
     lse = (m + np.log(l))[:, 0]
-    return out, lse
-
-
-def attend_rowwise(q_rows: np.ndarray, keys_per_row: Sequence[np.ndarray],
-                   values_per_row: Sequence[np.ndarray], scale: float):
-    """attend() where each row has its own key set."""
-    R = q_rows.shape[0]
-    dv = values_per_row[0].shape[1] if len(values_per_row) else 0
-    out = np.zeros((R, dv))
-    lse = np.full((R,), NEG_INF)
-    for r in range(R):
-        o, l_ = attend(q_rows[r:r + 1], keys_per_row[r], values_per_row[r], scale)
-        out[r], lse[r] = o[0], l_[0]
     return out, lse
 
 
@@ -342,6 +329,6 @@ def causal_pairs(T: int, Tkv: int, q_pos0: int, kv_pos0: int, kv_valid: Optional
 
 
 __all__ = [
-    "attend", "attend_rowwise", "attend_masked", "merge", "prefill_key_set", "mla_prefill", "mla_prefill_split",
+    "attend", "attend_masked", "merge", "prefill_key_set", "mla_prefill", "mla_prefill_split",
     "gather_pages", "mla_decode", "mla_sparse", "attention_flops", "causal_pairs", "NEG_INF",
 ]

@@ -365,3 +365,24 @@ ALL_CHECKS = [
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda f: f.__name__)
 def test_pin(check):
     check()
+
+
+def test_every_exported_function_is_reached_by_a_pin():
+    """Each function the oracle exports runs inside at least one pin (directly or through a
+    caller), so none of them can drift unchecked."""
+    import sys
+    called = set()
+    src = mo.__file__
+
+    def tracer(frame, event, arg):
+        if event == "call" and frame.f_code.co_filename == src:
+            called.add(frame.f_code.co_name)
+
+    sys.setprofile(tracer)
+    try:
+        for check in ALL_CHECKS:
+            check()
+    finally:
+        sys.setprofile(None)
+    exported = {n for n in mo.__all__ if callable(getattr(mo, n))}
+    assert exported - called == set(), f"oracle functions no pin reaches: {sorted(exported - called)}"
