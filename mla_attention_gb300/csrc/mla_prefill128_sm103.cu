@@ -33,7 +33,7 @@
 namespace mla {
 namespace {
 
-constexpr int kThreadsT = 256;
+constexpr int kThreadsT = 320;  // 10 warps: see the role table above
 constexpr int kKeysT = 128;                           // keys per score tile
 constexpr int kGroups = 3;                            // K groups per tile
 constexpr int kBoxBytesK = kKeysT * 128;              // 128 rows x 128 B
@@ -202,27 +202,38 @@ __device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float a, float b
 // A whole half inside one valid page is one tiled TMA box per 64 columns; otherwise its
 // rows are gathered four at a time (tile::gather4), keys past the request's length and
 // rows of an out-of-range page as -1 (zero fill; the page is reported).
+// The block-table entries are read a tile ahead (load_half_ids) and turned into sources
+// only when the tile is issued (finish_half), so the producer never waits on them.
+struct HalfIds {
+  int32_t pe, po;              // page ids of keys kh + 2 lane, kh + 2 lane + 1 (0 past the length: unused)
+};
 struct HalfSrc {
   bool tiled;
   int32_t y;                   // tiled: first cache row
   int32_t a0, a1, a2, a3;      // gathered: rows 4 l .. 4 l + 3 for lane l < 16
 };
-__device__ __forceinline__ HalfSrc decode_half(const CoreParams& p, int req, int len, int64_t kh, uint32_t* err) {
+__device__ __forceinline__ HalfIds load_half_ids(const CoreParams& p, int req, int len, int64_t kh) {
   const int lane = threadIdx.x & 31;
   const int32_t* bt = p.block_table + (int64_t)req * p.max_pages;
+  const int64_t ke = kh + 2 * lane, ko = ke + 1;
+  HalfIds ids;
+  ids.pe = ke < len ? __ldg(bt + ke / p.page_size) : 0;
+  ids.po = ko < len ? __ldg(bt + ko / p.page_size) : 0;
+  return ids;
+}
+__device__ __forceinline__ HalfSrc finish_half(const CoreParams& p, int len, int64_t kh, const HalfIds& ids,
+                                               uint32_t* err) {
+  const int lane = threadIdx.x & 31;
   HalfSrc hs;
   hs.tiled = false;
   hs.y = 0;
-  if (p.page_size % 64 == 0 && kh + 64 <= len) {
-    const int32_t pg = bt[kh / p.page_size];
-    if (pg >= 0 && pg < p.num_pages) {
-      hs.tiled = true;
-      hs.y = (int32_t)(pg * (int64_t)p.page_size + kh % p.page_size);
-    }
+  const int32_t pg0 = __shfl_sync(0xffffffffu, ids.pe, 0);  // page of key kh
+  if (p.page_size % 64 == 0 && kh + 64 <= len && pg0 >= 0 && pg0 < p.num_pages) {
+    hs.tiled = true;
+    hs.y = (int32_t)(pg0 * (int64_t)p.page_size + kh % p.page_size);
   }
-  auto row_of = [&](int64_t key) -> int32_t {
+  auto row_of = [&](int32_t pg, int64_t key) -> int32_t {
     if (key >= len) return -1;
-    const int32_t pg = bt[key / p.page_size];
     if (pg < 0 || pg >= p.num_pages) {
       record_error(err, DEV_RANGE_BASE | X_PAGE);
       return -1;
@@ -231,8 +242,8 @@ __device__ __forceinline__ HalfSrc decode_half(const CoreParams& p, int req, int
   };
   int32_t re = -1, ro = -1;
   if (!hs.tiled) {
-    re = row_of(kh + 2 * lane);
-    ro = row_of(kh + 2 * lane + 1);
+    re = row_of(ids.pe, kh + 2 * lane);
+    ro = row_of(ids.po, kh + 2 * lane + 1);
   }
   hs.a0 = __shfl_sync(0xffffffffu, re, (2 * lane) & 31);
   hs.a1 = __shfl_sync(0xffffffffu, ro, (2 * lane) & 31);
@@ -376,41 +387,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
     // =====================================================================
     // S-CTA
     // =====================================================================
-    if (warp == 4) {
-      // ---------------- TMA producer: K groups ----------------
+    if (warp == 4 || warp >= 8) {
+      // ---------------- TMA producers: K group k by its own warp (4, 8, 9 for k = 0, 1, 2) ----------------
       // Group k of every tile goes to slot k once the MMAs of group k of the previous tile
       // are done; its landing barrier alternates with the tile's parity, so each issuer
-      // waits only on the barriers of its own tiles.
+      // waits only on the barriers of its own tiles.  One thread issuing every box of a
+      // tile cannot feed the ring fast enough (its issue loop, not the memory, sets the
+      // rate), so the three groups have three issuing warps.
+      const int k = (warp == 4) ? 0 : warp - 7;
+      const uint32_t dst = smem_u32(smem + kOffK + k * kGroupBytes);
       uint32_t t = 0;
       bool live = true;
       while (live && iter.next(it)) {
         const int len = decode ? decode_len_t(p, it.id) : 0;
+        HalfIds ids[2];
+        if constexpr (decode) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) ids[h] = load_half_ids(p, it.id, len, it.k0 + 64 * h);
+        }
         for (int j = 0; j < it.J && live; ++j, ++t) {
           const uint32_t par = t & 1;
           HalfSrc hsrc[2];
           if constexpr (decode) {
             const int64_t kb = it.k0 + (int64_t)j * kKeysT;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) hsrc[h] = decode_half(p, it.id, len, kb + 64 * h, err);
-          }
-          for (int k = 0; k < kGroups; ++k) {
-            if (!waitb(&bars.kempty[k], par ^ 1, X_K_EMPTY, false)) { live = false; break; }
-            uint64_t* fb = &bars.kfull[k][par];
-            if (lane == 0) mbar_arrive_expect_tx(fb, kGroupBytes);
-            __syncwarp();
-            const uint32_t dst = smem_u32(smem + kOffK + k * kGroupBytes);
-            for (int i = 0; i < 3; ++i) {
-              const int32_t x = (3 * k + i) * kBoxCols;
-              if constexpr (!decode) {
-                if (lane == 0) tma_load_2d(dst + i * kBoxBytesK, &map_k, x, j * kKeysT, fb);
-              } else {
+            for (int h = 0; h < 2; ++h) hsrc[h] = finish_half(p, len, kb + 64 * h, ids[h], err);
+            if (j + 1 < it.J) {  // next tile's block-table entries, read while this one is issued
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
-                  load_half_box(dst + i * kBoxBytesK + h * kBoxBytesV, &maps.kv, &maps.row, x, hsrc[h], fb);
-              }
+              for (int h = 0; h < 2; ++h) ids[h] = load_half_ids(p, it.id, len, kb + kKeysT + 64 * h);
             }
-            __syncwarp();
           }
+          if (!waitb(&bars.kempty[k], par ^ 1, X_K_EMPTY, false)) { live = false; break; }
+          uint64_t* fb = &bars.kfull[k][par];
+          if (lane == 0) mbar_arrive_expect_tx(fb, kGroupBytes);
+          __syncwarp();
+          for (int i = 0; i < 3; ++i) {
+            const int32_t x = (3 * k + i) * kBoxCols;
+            if constexpr (!decode) {
+              if (lane == 0) tma_load_2d(dst + i * kBoxBytesK, &map_k, x, j * kKeysT, fb);
+            } else {
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                load_half_box(dst + i * kBoxBytesK + h * kBoxBytesV, &maps.kv, &maps.row, x, hsrc[h], fb);
+            }
+          }
+          __syncwarp();
         }
       }
     } else if (warp == 5 || warp == 6) {
@@ -699,50 +720,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
     // =====================================================================
     // O-CTA
     // =====================================================================
-    if (warp == 4) {
-      // ---------------- TMA producer: V halves (64 keys x 512 columns), epilogue stages ----------------
-      uint32_t u = 0;  // position in the two-slot ring
+    if (warp == 4 || warp == 8) {
+      // ---------------- TMA producers: V halves (64 keys x 512 columns), epilogue stages ----------------
+      // Ring slot h holds key half h of every tile (and then rows 64 h .. 64 h + 63 of the
+      // epilogue); warp 4 fills slot 0 and warp 8 slot 1, each at its own issue rate.
+      const int h = (warp == 4) ? 0 : 1;
+      const uint32_t dst = smem_u32(smem + kOffV + h * kHalfBytesV);
+      uint32_t m = 0;  // uses of this slot
       bool live = true;
       while (live && iter.next(it)) {
         const int len = decode ? decode_len_t(p, it.id) : 0;
-        for (int j = 0; j < it.J && live; ++j) {
-          for (int h = 0; h < 2; ++h, ++u) {
-            const int s = u & 1;
-            HalfSrc hs;
-            if constexpr (decode) hs = decode_half(p, it.id, len, it.k0 + (int64_t)j * kKeysT + 64 * h, err);
-            if (!waitb(&bars.vempty[s], ((u >> 1) & 1) ^ 1, X_V_EMPTY, false)) { live = false; break; }
-            const uint32_t dst = smem_u32(smem + kOffV + s * kHalfBytesV);
-            if (lane == 0) mbar_arrive_expect_tx(&bars.vfull[s], kHalfBytesV);
-            __syncwarp();
-            for (int bx = 0; bx < kVBoxes; ++bx) {
-              if constexpr (!decode) {
-                if (lane == 0)
-                  tma_load_2d(dst + bx * kBoxBytesV, &map_v, bx * kBoxCols, j * kKeysT + 64 * h, &bars.vfull[s]);
-              } else {
-                load_half_box(dst + bx * kBoxBytesV, &maps.kv, &maps.row, bx * kBoxCols, hs, &bars.vfull[s]);
-              }
-            }
-            __syncwarp();
+        HalfIds ids;
+        if constexpr (decode) ids = load_half_ids(p, it.id, len, it.k0 + 64 * h);
+        for (int j = 0; j < it.J && live; ++j, ++m) {
+          HalfSrc hs;
+          if constexpr (decode) {
+            const int64_t kh = it.k0 + (int64_t)j * kKeysT + 64 * h;
+            hs = finish_half(p, len, kh, ids, err);
+            if (j + 1 < it.J) ids = load_half_ids(p, it.id, len, kh + kKeysT);
           }
+          if (!waitb(&bars.vempty[h], (m & 1) ^ 1, X_V_EMPTY, false)) { live = false; break; }
+          if (lane == 0) mbar_arrive_expect_tx(&bars.vfull[h], kHalfBytesV);
+          __syncwarp();
+          for (int bx = 0; bx < kVBoxes; ++bx) {
+            if constexpr (!decode) {
+              if (lane == 0)
+                tma_load_2d(dst + bx * kBoxBytesV, &map_v, bx * kBoxCols, j * kKeysT + 64 * h, &bars.vfull[h]);
+            } else {
+              load_half_box(dst + bx * kBoxBytesV, &maps.kv, &maps.row, bx * kBoxCols, hs, &bars.vfull[h]);
+            }
+          }
+          __syncwarp();
         }
-        // the two ring slots then stage the epilogue: rows 0-63 and 64-127 (with prev)
-        if (staged && it.J > 0) {
-          for (int h = 0; h < 2 && live; ++h, ++u) {
-            const int s = u & 1;
-            if (!waitb(&bars.vempty[s], ((u >> 1) & 1) ^ 1, X_V_EMPTY, false)) { live = false; break; }
-            if (lane == 0) {
-              const int64_t row0 = (int64_t)it.id * kRows + h * 64;
-              if (p.prev_out && row0 < (int64_t)p.T * p.H) {
-                const uint32_t dst = smem_u32(smem + kOffV + s * kHalfBytesV);
-                mbar_arrive_expect_tx(&bars.vfull[s], kHalfBytesV);
-                for (int bx = 0; bx < kVBoxes; ++bx)
-                  tma_load_2d(dst + bx * kBoxBytesV, &maps.prev, bx * kBoxCols, (int32_t)row0, &bars.vfull[s]);
-              } else {
-                mbar_arrive(&bars.vfull[s]);
-              }
+        // the slot then stages the epilogue rows 64 h .. 64 h + 63 (with prev)
+        if (staged && it.J > 0 && live) {
+          if (!waitb(&bars.vempty[h], (m & 1) ^ 1, X_V_EMPTY, false)) { live = false; break; }
+          if (lane == 0) {
+            const int64_t row0 = (int64_t)it.id * kRows + h * 64;
+            if (p.prev_out && row0 < (int64_t)p.T * p.H) {
+              mbar_arrive_expect_tx(&bars.vfull[h], kHalfBytesV);
+              for (int bx = 0; bx < kVBoxes; ++bx)
+                tma_load_2d(dst + bx * kBoxBytesV, &maps.prev, bx * kBoxCols, (int32_t)row0, &bars.vfull[h]);
+            } else {
+              mbar_arrive(&bars.vfull[h]);
             }
-            __syncwarp();
           }
+          __syncwarp();
+          ++m;
         }
       }
     } else if (warp == 5) {

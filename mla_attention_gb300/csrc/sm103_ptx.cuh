@@ -109,13 +109,12 @@ __device__ __forceinline__ uint64_t global_ns() {
 // Longest any single wait may last, whatever the spin bound (2 s).
 constexpr uint64_t kWaitWallNs = 2000000000ull;
 
-// Bounded wait.  Returns false (and records `site`) when `spin_limit` tries
-// or kWaitWallNs of wall time have passed, or when another thread already
-// raised an error.
+// Bounded wait, polling part.  Returns false (and records `site`) when `spin_limit` tries
+// or kWaitWallNs of wall time have passed, or when another thread already raised an error.
 // Not inlined: one copy of the polling loop serves every call site, which keeps the
 // instruction footprint of the warp-specialised kernels small.
-static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t site,
-                                              uint32_t spin_limit, bool cluster_scope = false) {
+static __device__ __noinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t site,
+                                                   uint32_t spin_limit, bool cluster_scope) {
   const uint32_t a = smem_u32(bar);
   uint32_t n = 0;
   uint64_t t0 = 0;
@@ -135,6 +134,17 @@ static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, ui
       return false;
     }
   }
+}
+
+// Bounded wait: one inline test first, the polling call only when the phase is not complete
+// yet.  A call to a non-inlined function goes through the calling convention (registers saved
+// to the local-memory stack and restored), which costs a TMA producer about a third of its
+// issue rate when every wait already succeeds on its first test.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t site,
+                                          uint32_t spin_limit, bool cluster_scope = false) {
+  const uint32_t a = smem_u32(bar);
+  if (cluster_scope ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
+  return mbar_wait_poll(bar, parity, err, site, spin_limit, cluster_scope);
 }
 
 // The same wait inlined at its call site (kernels with few wait sites).
