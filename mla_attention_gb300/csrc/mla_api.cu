@@ -302,6 +302,7 @@ mla_status mla_decode(const void* q, const void* kv_cache, int64_t num_pages, in
   p.max_pages = max_pages;
   p.page_size = page_size;
   p.num_pages = num_pages;
+  p.cache = reinterpret_cast<const __nv_bfloat16*>(kv_cache);
   char* w = reinterpret_cast<char*>(workspace) + kWsHeader;
   const size_t slots = (size_t)B + (size_t)p.num_pairs;
   p.tile_prefix = reinterpret_cast<int32_t*>(w);

@@ -67,6 +67,7 @@ struct CoreParams {
   int max_pages;
   int page_size;
   int64_t num_pages;
+  const __nv_bfloat16* cache;    // [num_pages * page_size, 576] rows (L2 prefetch addresses)
   int32_t* tile_prefix;          // ws: [B+1] tiles before request b (written by CTA 0)
   float* part_o;                 // ws: [slots, H, 512]
   float* part_lse;               // ws: [slots, H]

@@ -64,6 +64,7 @@ static_assert(kOffPS % 1024 == 0 && kOffPO % 1024 == 0 && kOffQpe % 1024 == 0, "
 constexpr uint32_t kTmemQ = 0;      // S: Q latent part [0, 256)
 constexpr uint32_t kTmemS = 256;    // S: S buffers [256, 384), [384, 512)
 constexpr float kRescaleLog2 = 8.0f;
+constexpr int kPrefetchTiles = 4;   // decode: L2 prefetch distance of the O-CTA's V producers
 
 struct BarsT {
   // S-CTA
@@ -96,6 +97,16 @@ enum : uint32_t {
   X_STATS_FREE, X_V_EMPTY, X_V_FULL, X_P_FULL, X_P_READY, X_PV_DONE, X_STATS_FULL, X_O_FREE, X_STALL, X_EP_HALF,
   X_ALIGN = 0x4F, X_PAGE = 0x50, X_LEN = 0x51,
 };
+
+// Optional wait-time trace (built only with -DMLA_TRACE): cycles each warp spends in
+// each wait site, summed over the launch, and each warp's total cycles.
+#ifdef MLA_TRACE
+__device__ unsigned long long g_trace_wait[2][10][32];
+__device__ unsigned long long g_trace_total[2][10];
+#define MLA_TRACE_ONLY(...) __VA_ARGS__
+#else
+#define MLA_TRACE_ONLY(...)
+#endif
 
 struct ItemT {
   int id;        // prefill: row tile; decode: request
@@ -202,15 +213,10 @@ __device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float a, float b
 // A whole half inside one valid page is one tiled TMA box per 64 columns; otherwise its
 // rows are gathered four at a time (tile::gather4), keys past the request's length and
 // rows of an out-of-range page as -1 (zero fill; the page is reported).
-// The block-table entries are read a tile ahead (load_half_ids) and turned into sources
-// only when the tile is issued (finish_half), so the producer never waits on them.
+// The block-table entries are read a tile ahead (load_half_ids) and used only when the
+// tile is issued (issue_half), so the producer never waits on them.
 struct HalfIds {
   int32_t pe, po;              // page ids of keys kh + 2 lane, kh + 2 lane + 1 (0 past the length: unused)
-};
-struct HalfSrc {
-  bool tiled;
-  int32_t y;                   // tiled: first cache row
-  int32_t a0, a1, a2, a3;      // gathered: rows 4 l .. 4 l + 3 for lane l < 16
 };
 __device__ __forceinline__ HalfIds load_half_ids(const CoreParams& p, int req, int len, int64_t kh) {
   const int lane = threadIdx.x & 31;
@@ -221,45 +227,92 @@ __device__ __forceinline__ HalfIds load_half_ids(const CoreParams& p, int req, i
   ids.po = ko < len ? __ldg(bt + ko / p.page_size) : 0;
   return ids;
 }
-__device__ __forceinline__ HalfSrc finish_half(const CoreParams& p, int len, int64_t kh, const HalfIds& ids,
-                                               uint32_t* err) {
+// Rows of a half that is not one tiled box per column block (the last half of a request,
+// pages of 16 or 32 tokens, a bad page): lane l < 16 gathers rows 4 l .. 4 l + 3 of every
+// column block (tile::gather4), keys past the length and rows of an out-of-range page as -1
+// (zero fill; the page is reported).  Rare, so kept out of line: the producers' hot loop
+// stays small for the instruction cache.
+static __device__ __noinline__ void gather_half(uint32_t dst, uint32_t box_stride, int32_t x0, int nbox,
+                                                const CUtensorMap* row_map, int page_size, int64_t num_pages,
+                                                int len, int64_t kh, int32_t pe, int32_t po, uint64_t* bar,
+                                                uint32_t* err) {
   const int lane = threadIdx.x & 31;
-  HalfSrc hs;
-  hs.tiled = false;
-  hs.y = 0;
-  const int32_t pg0 = __shfl_sync(0xffffffffu, ids.pe, 0);  // page of key kh
-  if (p.page_size % 64 == 0 && kh + 64 <= len && pg0 >= 0 && pg0 < p.num_pages) {
-    hs.tiled = true;
-    hs.y = (int32_t)(pg0 * (int64_t)p.page_size + kh % p.page_size);
-  }
   auto row_of = [&](int32_t pg, int64_t key) -> int32_t {
     if (key >= len) return -1;
-    if (pg < 0 || pg >= p.num_pages) {
+    if (pg < 0 || pg >= num_pages) {
       record_error(err, DEV_RANGE_BASE | X_PAGE);
       return -1;
     }
-    return (int32_t)(pg * (int64_t)p.page_size + key % p.page_size);
+    return (int32_t)(pg * (int64_t)page_size + key % page_size);
   };
-  int32_t re = -1, ro = -1;
-  if (!hs.tiled) {
-    re = row_of(ids.pe, kh + 2 * lane);
-    ro = row_of(ids.po, kh + 2 * lane + 1);
-  }
-  hs.a0 = __shfl_sync(0xffffffffu, re, (2 * lane) & 31);
-  hs.a1 = __shfl_sync(0xffffffffu, ro, (2 * lane) & 31);
-  hs.a2 = __shfl_sync(0xffffffffu, re, (2 * lane + 1) & 31);
-  hs.a3 = __shfl_sync(0xffffffffu, ro, (2 * lane + 1) & 31);
-  return hs;
+  const int32_t re = row_of(pe, kh + 2 * lane);
+  const int32_t ro = row_of(po, kh + 2 * lane + 1);
+  const int32_t a0 = __shfl_sync(0xffffffffu, re, (2 * lane) & 31);
+  const int32_t a1 = __shfl_sync(0xffffffffu, ro, (2 * lane) & 31);
+  const int32_t a2 = __shfl_sync(0xffffffffu, re, (2 * lane + 1) & 31);
+  const int32_t a3 = __shfl_sync(0xffffffffu, ro, (2 * lane + 1) & 31);
+  if (lane < 16)
+    for (int i = 0; i < nbox; ++i) tma_gather4(dst + i * box_stride + lane * 512, row_map, x0 + i * kBoxCols, a0, a1, a2, a3, bar);
 }
-// one 64-column box of a half (64 rows x 128 B at dst): one tiled load or 16 gathers
-__device__ __forceinline__ void load_half_box(uint32_t dst, const CUtensorMap* tiled_map,
-                                              const CUtensorMap* row_map, int32_t x, const HalfSrc& hs,
-                                              uint64_t* bar) {
-  const int lane = threadIdx.x & 31;
-  if (hs.tiled) {
-    if (lane == 0) tma_load_2d(dst, tiled_map, x, hs.y, bar);
-  } else if (lane < 16) {
-    tma_gather4(dst + lane * 512, row_map, x, hs.a0, hs.a1, hs.a2, hs.a3, bar);
+
+// Issues the 64-row boxes of one tile half [kh, kh + 64): nbox column blocks starting at
+// column x0, landing box_stride bytes apart from dst.  A half inside one valid page is one
+// tiled box per column block, issued by lane 0.  Warp-uniform.
+__device__ __forceinline__ void issue_half(uint32_t dst, uint32_t box_stride, int32_t x0, int nbox, const CoreParams& p,
+                                           const CoreMaps& maps, int len, int64_t kh, const HalfIds& ids,
+                                           uint64_t* bar, uint32_t* err) {
+  const int32_t pg0 = __shfl_sync(0xffffffffu, ids.pe, 0);  // page of key kh
+  if (p.page_size % 64 == 0 && kh + 64 <= len && pg0 >= 0 && pg0 < p.num_pages) {
+    if ((threadIdx.x & 31) == 0) {
+      const int32_t y = (int32_t)(pg0 * (int64_t)p.page_size + kh % p.page_size);
+#pragma unroll 1
+      for (int i = 0; i < nbox; ++i) tma_load_2d(dst + i * box_stride, &maps.kv, x0 + i * kBoxCols, y, bar);
+    }
+  } else {
+    gather_half(dst, box_stride, x0, nbox, &maps.row, p.page_size, p.num_pages, len, kh, ids.pe, ids.po, bar, err);
+  }
+}
+
+// ---- softmax rows: one 32-column piece of a score row ----
+// Keys of a piece past lim (the visible keys in it) get the score -inf (+inf when the scale
+// is negative), so one mask-free body serves every piece: the extreme ignores them and
+// 2^(s * scale_log2 - m) is 0 for them.  (A zero scale is run as a tiny positive one, so
+// no infinite score is ever multiplied by 0.)
+template <bool kUp>
+__device__ __forceinline__ void mask_piece(uint32_t (&sr)[32], int lim) {
+  if (lim < 32) {
+    const uint32_t hide = __float_as_uint(kUp ? -CUDART_INF_F : CUDART_INF_F);
+#pragma unroll
+    for (int c = 0; c < 32; ++c) sr[c] = (c < lim) ? sr[c] : hide;
+  }
+}
+template <bool kUp>
+__device__ __forceinline__ void row_extreme(const uint32_t (&sr)[32], float (&eq)[4]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float v0 = __uint_as_float(sr[2 * i]), v1 = __uint_as_float(sr[2 * i + 1]);
+    eq[i & 3] = kUp ? max3f(eq[i & 3], v0, v1) : min3f(eq[i & 3], v0, v1);
+  }
+}
+// p = 2^(s * scale_log2 - msub) of a piece as bf16 into four 16-byte chunks (chunk0 .. chunk0 + 3
+// of the row's 128-byte line of the piece's 64-key P box, swizzled), row sums into rsq (two
+// pairs of partial sums).  Scores go through the scale in pairs (packed fp32).
+__device__ __forceinline__ void row_exp(const uint32_t (&sr)[32], uint64_t sl2x2, uint64_t nmsub2, uint8_t* pline,
+                                        int chunk0, int r, uint64_t (&rsq)[2]) {
+#pragma unroll
+  for (int c8 = 0; c8 < 4; ++c8) {  // 8 keys -> one 16-byte chunk of P
+    uint32_t w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = 8 * c8 + 2 * u;
+      float x0, x1;
+      f32x2_split(fma_f32x2(f32x2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2, nmsub2), x0, x1);
+      const float e0 = ex2_approx(x0);
+      const float e1 = ex2_approx(x1);
+      rsq[u & 1] = add_f32x2(rsq[u & 1], f32x2(e0, e1));
+      w[u] = pack_bf16x2(e0, e1);
+    }
+    *reinterpret_cast<uint4*>(pline + (((chunk0 + c8) ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -363,15 +416,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
   tc_fence_after();
   const uint32_t tbase = bars.tmem_base;
   volatile uint32_t* abort_flag = &bars.abort_flag;
+  MLA_TRACE_ONLY(unsigned long long trace_wait[32] = {}; const long long trace_t0 = clock64();)
   auto waitb = [&](uint64_t* bar, uint32_t parity, uint32_t site, bool cl) -> bool {
+    MLA_TRACE_ONLY(const long long tw = clock64();)
     bool ok = (*abort_flag == 0) && mbar_wait(bar, parity, err, site, lim, cl);
+    MLA_TRACE_ONLY(trace_wait[site & 31] += clock64() - tw;)
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) *abort_flag = 1;
     return ok;
   };
   // single-thread wait for the MMA issuers (no warp-collective tcgen05 instruction follows)
   auto wait1 = [&](uint64_t* bar, uint32_t parity, uint32_t site, bool cl) -> bool {
+    MLA_TRACE_ONLY(const long long tw = clock64();)
     const bool ok = (*abort_flag == 0) && mbar_wait(bar, parity, err, site, lim, cl);
+    MLA_TRACE_ONLY(trace_wait[site & 31] += clock64() - tw;)
     if (!ok) *abort_flag = 1;
     return ok;
   };
@@ -407,11 +465,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
         }
         for (int j = 0; j < it.J && live; ++j, ++t) {
           const uint32_t par = t & 1;
-          HalfSrc hsrc[2];
+          const int64_t kb = it.k0 + (int64_t)j * kKeysT;
+          HalfIds cur[2];
           if constexpr (decode) {
-            const int64_t kb = it.k0 + (int64_t)j * kKeysT;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) hsrc[h] = finish_half(p, len, kb + 64 * h, ids[h], err);
+            cur[0] = ids[0];
+            cur[1] = ids[1];
             if (j + 1 < it.J) {  // next tile's block-table entries, read while this one is issued
 #pragma unroll
               for (int h = 0; h < 2; ++h) ids[h] = load_half_ids(p, it.id, len, kb + kKeysT + 64 * h);
@@ -421,15 +479,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
           uint64_t* fb = &bars.kfull[k][par];
           if (lane == 0) mbar_arrive_expect_tx(fb, kGroupBytes);
           __syncwarp();
-          for (int i = 0; i < 3; ++i) {
-            const int32_t x = (3 * k + i) * kBoxCols;
-            if constexpr (!decode) {
-              if (lane == 0) tma_load_2d(dst + i * kBoxBytesK, &map_k, x, j * kKeysT, fb);
-            } else {
-#pragma unroll
-              for (int h = 0; h < 2; ++h)
-                load_half_box(dst + i * kBoxBytesK + h * kBoxBytesV, &maps.kv, &maps.row, x, hsrc[h], fb);
-            }
+          if constexpr (!decode) {
+            if (lane == 0)
+              for (int i = 0; i < 3; ++i) tma_load_2d(dst + i * kBoxBytesK, &map_k, (3 * k + i) * kBoxCols, j * kKeysT, fb);
+          } else {
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h)
+              issue_half(dst + h * kBoxBytesV, kBoxBytesK, 3 * k * kBoxCols, 3, p, maps, len, kb + 64 * h,
+                         h ? cur[1] : cur[0], fb, err);
           }
           __syncwarp();
         }
@@ -522,7 +579,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
       float* alpha = reinterpret_cast<float*>(smem + kOffAlphaS);
       const uint32_t rem_stats = map_to_rank(smem_u32(smem + kOffStatsO), peer);
       const uint32_t rem_stats_full = map_to_rank(smem_u32(&bars.stats_full), peer);
-      const float sl2 = p.scale_log2;
+      const float sl2 = (p.scale_log2 == 0.f) ? 1e-30f : p.scale_log2;  // see mask_piece
       uint32_t t = 0, i = 0;
       bool live = true;
       while (live && iter.next(it)) {
@@ -568,6 +625,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
             }
           }
         }
+        MLA_TRACE_ONLY(long long tq = clock64();)
         // ---- Q: latent part -> TMEM (256 columns), RoPE part -> smem (SW128 K-major) ----
         if (i > 0 && !waitb(&bars.q_taken, (i - 1) & 1, X_Q_TAKEN, false)) break;
 #pragma unroll 1
@@ -606,6 +664,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
         tc_fence_before();
         warp_arrive(&bars.q_full);
 
+        MLA_TRACE_ONLY(trace_wait[24] += clock64() - tq;)
         float m_used = -CUDART_INF_F;  // log2-domain offset of the exponentials
         float l = 0.f;                 // running row sum (relative to m_used)
         for (int j = 0; j < it.J; ++j, ++t) {
@@ -615,32 +674,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
 
           if (!waitb(&bars.s_full[sb], (t >> 1) & 1, X_S_FULL, false)) { live = false; break; }
           tc_fence_after();
-          // Two passes over the tile in 32-column pieces read from TMEM (a rolled loop each,
-          // so the loop body stays small): the row extreme first, then the exponentials.
+          MLA_TRACE_ONLY(long long tp = clock64();)
+          // Two passes over the tile's 128 scores in 32-column pieces: the row extreme (two
+          // pieces loaded from TMEM per wait), then the exponentials, each piece's load in
+          // flight while the previous piece is computed.
           const uint32_t scol = tbase + lane_base + kTmemS + sb * kKeysT;
           float eq[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) eq[k] = kUp ? -CUDART_INF_F : CUDART_INF_F;
 #pragma unroll 1
-          for (int p32 = 0; p32 < kKeysT / 32; ++p32) {
-            uint32_t sr[32];
-            tmem_ld32(scol + 32 * p32, sr);
+          for (int pp = 0; pp < kKeysT / 32; pp += 2) {
+            uint32_t s0[32], s1[32];
+            tmem_ld32(scol + 32 * pp, s0);
+            tmem_ld32(scol + 32 * pp + 32, s1);
             tmem_wait_ld();
-            const int lim = nv - 32 * p32;
-            if (lim >= 32) {  // every key of the piece visible (warp-uniform when H = 128)
-#pragma unroll
-              for (int c = 0; c < 32; ++c) {
-                const float v = __uint_as_float(sr[c]);
-                eq[c & 3] = kUp ? fmaxf(eq[c & 3], v) : fminf(eq[c & 3], v);
-              }
-            } else {
-#pragma unroll
-              for (int c = 0; c < 32; ++c) {
-                const float v = __uint_as_float(sr[c]);
-                eq[c & 3] = (c >= lim) ? eq[c & 3] : (kUp ? fmaxf(eq[c & 3], v) : fminf(eq[c & 3], v));
-              }
-            }
+            mask_piece<kUp>(s0, nv - 32 * pp);
+            mask_piece<kUp>(s1, nv - 32 * pp - 32);
+            row_extreme<kUp>(s0, eq);
+            row_extreme<kUp>(s1, eq);
           }
+          MLA_TRACE_ONLY(trace_wait[25] += clock64() - tp; tp = clock64();)
           const float e = kUp ? fmaxf(fmaxf(eq[0], eq[1]), fmaxf(eq[2], eq[3]))
                              : fminf(fminf(eq[0], eq[1]), fminf(eq[2], eq[3]));
           const float mt = (nv == 0) ? -CUDART_INF_F : e * sl2;
@@ -655,8 +708,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
 
           // ---- P (two K-major boxes of 64 keys) and the rescale factor ----
           if (!waitb(&bars.pbuf_free[sb], ((t >> 1) & 1) ^ 1, X_PBUF_FREE, false)) { live = false; break; }
+          MLA_TRACE_ONLY(tp = clock64();)
           uint8_t* prow = smem + kOffPS + sb * kPBytesT + r * 128;
-          float rsq[4] = {0.f, 0.f, 0.f, 0.f};
+          uint64_t rsq[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
+          const uint64_t sl2x2 = f32x2(sl2, sl2), nmsub2 = f32x2(-msub, -msub);
 #pragma unroll 1
           for (int p32 = 0; p32 < kKeysT / 32; ++p32) {
             uint32_t sr[32];
@@ -666,44 +721,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
               tc_fence_before();
               warp_arrive(&bars.s_free[sb]);
             }
-            // keys past the row's limit read as -inf (exp2 gives 0) on the masked path
-            const int lim = nv - 32 * p32;
-            uint8_t* pchunk = prow + (p32 >> 1) * kPBoxBytes;  // the 64-key box of this piece
-            if (lim >= 32) {  // every key of the piece visible (warp-uniform when H = 128)
-#pragma unroll
-              for (int c8 = 0; c8 < 4; ++c8) {  // 8 keys -> one 16-byte chunk of P
-                uint32_t w[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                  const int c = 8 * c8 + 2 * u;
-                  const float e0 = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -msub));
-                  const float e1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), sl2, -msub));
-                  rsq[u] += e0 + e1;
-                  w[u] = pack_bf16x2(e0, e1);
-                }
-                const int chunk = (4 * p32 + c8) & 7;
-                *reinterpret_cast<uint4*>(pchunk + ((chunk ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-              }
-            } else {
-#pragma unroll
-              for (int c8 = 0; c8 < 4; ++c8) {
-                uint32_t w[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                  const int c = 8 * c8 + 2 * u;
-                  const float t0 = fmaf(__uint_as_float(sr[c]), sl2, -msub);
-                  const float t1 = fmaf(__uint_as_float(sr[c + 1]), sl2, -msub);
-                  const float e0 = ex2_approx(c < lim ? t0 : -CUDART_INF_F);
-                  const float e1 = ex2_approx(c + 1 < lim ? t1 : -CUDART_INF_F);
-                  rsq[u] += e0 + e1;
-                  w[u] = pack_bf16x2(e0, e1);
-                }
-                const int chunk = (4 * p32 + c8) & 7;
-                *reinterpret_cast<uint4*>(pchunk + ((chunk ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-              }
-            }
+            mask_piece<kUp>(sr, nv - 32 * p32);
+            row_exp(sr, sl2x2, nmsub2, prow + (p32 >> 1) * kPBoxBytes, (4 * p32) & 7, r, rsq);
           }
-          l += (rsq[0] + rsq[1]) + (rsq[2] + rsq[3]);
+          MLA_TRACE_ONLY(trace_wait[27] += clock64() - tp;)
+          {
+            float q0, q1, q2, q3;
+            f32x2_split(rsq[0], q0, q1);
+            f32x2_split(rsq[1], q2, q3);
+            l += (q0 + q1) + (q2 + q3);
+          }
           alpha[sb * kRows + r] = a;
           fence_proxy_async_smem();  // the bulk copy reads through the async proxy
           warp_arrive(&bars.pwritten[sb]);
@@ -724,31 +751,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
       // ---------------- TMA producers: V halves (64 keys x 512 columns), epilogue stages ----------------
       // Ring slot h holds key half h of every tile (and then rows 64 h .. 64 h + 63 of the
       // epilogue); warp 4 fills slot 0 and warp 8 slot 1, each at its own issue rate.
+      // Decode: the same warp also brings half h of tile j + kPrefetchTiles into L2 (one bulk
+      // prefetch of its 64 contiguous cache rows when they lie in one page), so the S-CTA's K
+      // loads of that tile hit L2: its one-tile K ring cannot cover the latency of HBM.
       const int h = (warp == 4) ? 0 : 1;
       const uint32_t dst = smem_u32(smem + kOffV + h * kHalfBytesV);
       uint32_t m = 0;  // uses of this slot
       bool live = true;
       while (live && iter.next(it)) {
         const int len = decode ? decode_len_t(p, it.id) : 0;
+        const int32_t* bt = decode ? p.block_table + (int64_t)it.id * p.max_pages : nullptr;
+        const bool pf_ok = decode && p.page_size % 64 == 0;
         HalfIds ids;
-        if constexpr (decode) ids = load_half_ids(p, it.id, len, it.k0 + 64 * h);
+        int32_t pf_pg = -1;  // page under half h of tile j + kPrefetchTiles (read a tile ahead)
+        if constexpr (decode) {
+          ids = load_half_ids(p, it.id, len, it.k0 + 64 * h);
+          const int64_t kp = it.k0 + (int64_t)kPrefetchTiles * kKeysT + 64 * h;
+          if (pf_ok && kp + 64 <= len) pf_pg = __ldg(bt + kp / p.page_size);
+        }
         for (int j = 0; j < it.J && live; ++j, ++m) {
-          HalfSrc hs;
+          const int64_t kh = it.k0 + (int64_t)j * kKeysT + 64 * h;
+          HalfIds cur;
           if constexpr (decode) {
-            const int64_t kh = it.k0 + (int64_t)j * kKeysT + 64 * h;
-            hs = finish_half(p, len, kh, ids, err);
+            cur = ids;
             if (j + 1 < it.J) ids = load_half_ids(p, it.id, len, kh + kKeysT);
+            const int64_t kp = kh + (int64_t)kPrefetchTiles * kKeysT;
+            if (lane == 0 && pf_pg >= 0 && pf_pg < p.num_pages)
+              bulk_prefetch_l2(p.cache + (pf_pg * (int64_t)p.page_size + kp % p.page_size) * kDk, 64 * kDk * 2);
+            pf_pg = (pf_ok && kp + kKeysT + 64 <= len) ? __ldg(bt + (kp + kKeysT) / p.page_size) : -1;
           }
           if (!waitb(&bars.vempty[h], (m & 1) ^ 1, X_V_EMPTY, false)) { live = false; break; }
           if (lane == 0) mbar_arrive_expect_tx(&bars.vfull[h], kHalfBytesV);
           __syncwarp();
-          for (int bx = 0; bx < kVBoxes; ++bx) {
-            if constexpr (!decode) {
-              if (lane == 0)
+          if constexpr (!decode) {
+            if (lane == 0)
+              for (int bx = 0; bx < kVBoxes; ++bx)
                 tma_load_2d(dst + bx * kBoxBytesV, &map_v, bx * kBoxCols, j * kKeysT + 64 * h, &bars.vfull[h]);
-            } else {
-              load_half_box(dst + bx * kBoxBytesV, &maps.kv, &maps.row, bx * kBoxCols, hs, &bars.vfull[h]);
-            }
+          } else {
+            issue_half(dst, kBoxBytesV, 0, kVBoxes, p, maps, len, kh, cur, &bars.vfull[h], err);
           }
           __syncwarp();
         }
@@ -981,6 +1021,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
 
   // ---- teardown: drain on abort, then leave together ----
   __syncwarp();
+  MLA_TRACE_ONLY(if (lane == 0) {
+    for (int q = 0; q < 32; ++q) atomicAdd(&g_trace_wait[is_s ? 0 : 1][warp][q], trace_wait[q]);
+    atomicAdd(&g_trace_total[is_s ? 0 : 1][warp], (unsigned long long)(clock64() - trace_t0));
+  })
   if (*abort_flag) {
     for (int k = 0; k < 200; ++k) __nanosleep(1000);
   }
@@ -991,6 +1035,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
 }
 
 }  // namespace
+
+#ifdef MLA_TRACE
+// copies the trace (2 x 10 x 32 wait sums, then 2 x 10 totals) to host and clears it
+extern "C" int mla_trace_read(unsigned long long* host) {
+  static unsigned long long zero[2 * 10 * 32] = {};
+  if (cudaMemcpyFromSymbol(host, g_trace_wait, sizeof(g_trace_wait)) != cudaSuccess) return 1;
+  if (cudaMemcpyFromSymbol(host + 640, g_trace_total, sizeof(g_trace_total)) != cudaSuccess) return 1;
+  if (cudaMemcpyToSymbol(g_trace_wait, zero, sizeof(g_trace_wait)) != cudaSuccess) return 1;
+  if (cudaMemcpyToSymbol(g_trace_total, zero, sizeof(g_trace_total)) != cudaSuccess) return 1;
+  return 0;
+}
+#endif
 
 cudaError_t launch_prefill128(const CoreParams& p, const CoreMaps& maps, cudaStream_t stream) {
   static bool attr_set = false;
