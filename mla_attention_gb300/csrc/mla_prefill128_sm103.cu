@@ -33,7 +33,7 @@
 namespace mla {
 namespace {
 
-constexpr int kThreadsT = 320;  // 10 warps: see the role table above
+constexpr int kThreadsT = 416;  // 13 warps: see the role table above
 constexpr int kKeysT = 128;                           // keys per score tile
 constexpr int kGroups = 3;                            // K groups per tile
 constexpr int kBoxBytesK = kKeysT * 128;              // 128 rows x 128 B
@@ -347,8 +347,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
   if (tid == 0) {
     if (is_s) {
       for (int k = 0; k < kGroups; ++k) {
-        mbar_init(&bars.kfull[k][0], 1);
-        mbar_init(&bars.kfull[k][1], 1);
+        mbar_init(&bars.kfull[k][0], 2);  // the two producers of group k (one per 64-row half)
+        mbar_init(&bars.kfull[k][1], 2);
         mbar_init(&bars.kempty[k], 1);
       }
       for (int b = 0; b < 2; ++b) {
@@ -438,7 +438,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
   ItemIterT<kDecode> iter;
   iter.init(p, pair);
   ItemT it;
-  const CUtensorMap& map_k = maps.row;   // K rows, box {64, 128}
   const CUtensorMap& map_v = maps.kv;    // V rows, box {64, 64}
 
   if (is_s) {
@@ -446,47 +445,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
     // S-CTA
     // =====================================================================
     if (warp == 4 || warp >= 8) {
-      // ---------------- TMA producers: K group k by its own warp (4, 8, 9 for k = 0, 1, 2) ----------------
-      // Group k of every tile goes to slot k once the MMAs of group k of the previous tile
-      // are done; its landing barrier alternates with the tile's parity, so each issuer
-      // waits only on the barriers of its own tiles.  One thread issuing every box of a
-      // tile cannot feed the ring fast enough (its issue loop, not the memory, sets the
-      // rate), so the three groups have three issuing warps.
-      const int k = (warp == 4) ? 0 : warp - 7;
-      const uint32_t dst = smem_u32(smem + kOffK + k * kGroupBytes);
+      // ---------------- TMA producers: rows 64 h .. 64 h + 63 of K group k ----------------
+      // Six warps (4, 8, 9, 10, 11, 12), one per (group k, half h).  Group k of every tile
+      // goes to slot k once the MMAs of group k of the previous tile are done; its landing
+      // barrier alternates with the tile's parity, so each issuer waits only on the barriers
+      // of its own tiles.  A thread issues a TMA box every few hundred cycles whatever the
+      // memory does, so the ring is fed by many threads, each with few boxes per tile.
+      const int q = (warp == 4) ? 0 : warp - 7;
+      const int k = q % kGroups, h = q / kGroups;
+      const uint32_t dst = smem_u32(smem + kOffK + k * kGroupBytes + h * kBoxBytesV);
       uint32_t t = 0;
       bool live = true;
       while (live && iter.next(it)) {
         const int len = decode ? decode_len_t(p, it.id) : 0;
-        HalfIds ids[2];
-        if constexpr (decode) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) ids[h] = load_half_ids(p, it.id, len, it.k0 + 64 * h);
-        }
+        HalfIds ids;
+        if constexpr (decode) ids = load_half_ids(p, it.id, len, it.k0 + 64 * h);
         for (int j = 0; j < it.J && live; ++j, ++t) {
           const uint32_t par = t & 1;
-          const int64_t kb = it.k0 + (int64_t)j * kKeysT;
-          HalfIds cur[2];
+          const int64_t kh = it.k0 + (int64_t)j * kKeysT + 64 * h;
+          HalfIds cur;
           if constexpr (decode) {
-            cur[0] = ids[0];
-            cur[1] = ids[1];
-            if (j + 1 < it.J) {  // next tile's block-table entries, read while this one is issued
-#pragma unroll
-              for (int h = 0; h < 2; ++h) ids[h] = load_half_ids(p, it.id, len, kb + kKeysT + 64 * h);
-            }
+            cur = ids;
+            if (j + 1 < it.J) ids = load_half_ids(p, it.id, len, kh + kKeysT);  // read while this tile is issued
           }
           if (!waitb(&bars.kempty[k], par ^ 1, X_K_EMPTY, false)) { live = false; break; }
           uint64_t* fb = &bars.kfull[k][par];
-          if (lane == 0) mbar_arrive_expect_tx(fb, kGroupBytes);
+          if (lane == 0) mbar_arrive_expect_tx(fb, kGroupBytes / 2);
           __syncwarp();
           if constexpr (!decode) {
             if (lane == 0)
-              for (int i = 0; i < 3; ++i) tma_load_2d(dst + i * kBoxBytesK, &map_k, (3 * k + i) * kBoxCols, j * kKeysT, fb);
+              for (int i = 0; i < 3; ++i)
+                tma_load_2d(dst + i * kBoxBytesK, &map_v, (3 * k + i) * kBoxCols, j * kKeysT + 64 * h, fb);
           } else {
-#pragma unroll 1
-            for (int h = 0; h < 2; ++h)
-              issue_half(dst + h * kBoxBytesV, kBoxBytesK, 3 * k * kBoxCols, 3, p, maps, len, kb + 64 * h,
-                         h ? cur[1] : cur[0], fb, err);
+            issue_half(dst, kBoxBytesK, 3 * k * kBoxCols, 3, p, maps, len, kh, cur, fb, err);
           }
           __syncwarp();
         }
