@@ -142,7 +142,7 @@ def set_spin_limit(limit: int):
 
 def set_tile_keys(prefill_keys: int = 0, decode_keys: int = 0):
     """128 or 64 keys per score tile of mla_prefill and of mla_decode; 0 keeps / restores the
-    default of each (prefill 128, decode 64)."""
+    default of each (128 for both)."""
     lib().mla_set_tile_keys(int(prefill_keys), int(decode_keys))
 
 

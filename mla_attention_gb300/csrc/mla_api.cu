@@ -114,7 +114,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Keys per score tile of prefill and of decode: 128 (mla_prefill128_kernel) or 64
 // (mla_core_kernel); set with mla_set_tile_keys.
-constexpr int kDefaultPrefillKeys = 128, kDefaultDecodeKeys = 64;
+constexpr int kDefaultPrefillKeys = 128, kDefaultDecodeKeys = 128;
 std::atomic<int> g_prefill_keys{kDefaultPrefillKeys};
 std::atomic<int> g_decode_keys{kDefaultDecodeKeys};
 

@@ -101,8 +101,8 @@ enum : uint32_t {
 // Optional wait-time trace (built only with -DMLA_TRACE): cycles each warp spends in
 // each wait site, summed over the launch, and each warp's total cycles.
 #ifdef MLA_TRACE
-__device__ unsigned long long g_trace_wait[2][10][32];
-__device__ unsigned long long g_trace_total[2][10];
+__device__ unsigned long long g_trace_wait[2][16][32];
+__device__ unsigned long long g_trace_total[2][16];
 #define MLA_TRACE_ONLY(...) __VA_ARGS__
 #else
 #define MLA_TRACE_ONLY(...)
@@ -296,17 +296,21 @@ __device__ __forceinline__ void row_extreme(const uint32_t (&sr)[32], float (&eq
 }
 // p = 2^(s * scale_log2 - msub) of a piece as bf16 into four 16-byte chunks (chunk0 .. chunk0 + 3
 // of the row's 128-byte line of the piece's 64-key P box, swizzled), row sums into rsq (two
-// pairs of partial sums).  Scores go through the scale in pairs (packed fp32).
+// pairs of partial sums), and the extreme of the raw scores into eq.  Scores go through the
+// scale in pairs (packed fp32).
+template <bool kUp>
 __device__ __forceinline__ void row_exp(const uint32_t (&sr)[32], uint64_t sl2x2, uint64_t nmsub2, uint8_t* pline,
-                                        int chunk0, int r, uint64_t (&rsq)[2]) {
+                                        int chunk0, int r, uint64_t (&rsq)[2], float (&eq)[4]) {
 #pragma unroll
   for (int c8 = 0; c8 < 4; ++c8) {  // 8 keys -> one 16-byte chunk of P
     uint32_t w[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int c = 8 * c8 + 2 * u;
+      const float v0 = __uint_as_float(sr[c]), v1 = __uint_as_float(sr[c + 1]);
+      eq[u] = kUp ? max3f(eq[u], v0, v1) : min3f(eq[u], v0, v1);
       float x0, x1;
-      f32x2_split(fma_f32x2(f32x2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2, nmsub2), x0, x1);
+      f32x2_split(fma_f32x2(f32x2(v0, v1), sl2x2, nmsub2), x0, x1);
       const float e0 = ex2_approx(x0);
       const float e1 = ex2_approx(x1);
       rsq[u & 1] = add_f32x2(rsq[u & 1], f32x2(e0, e1));
@@ -530,7 +534,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
       }
       __syncwarp();
     } else if (warp == 7) {
-      // ---------------- P copies into the O-CTA, two in flight ----------------
+      // ---------------- P copies into the O-CTA ----------------
       const uint8_t* pbuf = smem + kOffPS;
       const float* alpha = reinterpret_cast<const float*>(smem + kOffAlphaS);
       const uint32_t rem_p_full0 = map_to_rank(smem_u32(&bars.p_full[0]), peer);
@@ -553,16 +557,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
             bulk_copy_to_peer(rem_p_o + sb * kPBytesT, smem_u32(pbuf + sb * kPBytesT), kPBytesT, bar);
             bulk_copy_to_peer(rem_alpha_o + sb * kRows * 4, smem_u32(alpha + sb * kRows), kRows * 4, bar);
             bulk_commit();
-            bulk_wait_read_le1();  // every copy but this one has been read
-            if (t > 0) mbar_arrive(&bars.pbuf_free[sb ^ 1]);
+            bulk_wait_read_all();  // this copy has read local buffer sb: the rows may refill it
+            mbar_arrive(&bars.pbuf_free[sb]);
           }
           __syncwarp();
         }
       }
-      if (lane == 0) {
-        bulk_wait_all();
-        if (t > 0) mbar_arrive(&bars.pbuf_free[(t - 1) & 1]);
-      }
+      if (lane == 0) bulk_wait_all();
     } else if (warp < kRowWarpsS) {
       // ---------------- rows: Q load, online softmax, one row per thread ----------------
       const int r = tid;  // row within the item = TMEM lane
@@ -666,55 +667,72 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
           if (!waitb(&bars.s_full[sb], (t >> 1) & 1, X_S_FULL, false)) { live = false; break; }
           tc_fence_after();
           MLA_TRACE_ONLY(long long tp = clock64();)
-          // Two passes over the tile's 128 scores in 32-column pieces: the row extreme (two
-          // pieces loaded from TMEM per wait), then the exponentials, each piece's load in
-          // flight while the previous piece is computed.
+          // The exponentials are taken against the running offset m_used in one pass over the
+          // tile's 128 scores (32-column pieces read from TMEM), which also finds the tile's
+          // extreme.  Only when that extreme passes m_used by more than 2^8 (rare after a row's
+          // first tile) does the row move m_used and take the pass again.  A row that has seen
+          // no key yet finds the extreme first.
           const uint32_t scol = tbase + lane_base + kTmemS + sb * kKeysT;
-          float eq[4];
+          auto tile_offset = [&](const float (&eq)[4]) -> float {
+            const float e = kUp ? fmaxf(fmaxf(eq[0], eq[1]), fmaxf(eq[2], eq[3]))
+                               : fminf(fminf(eq[0], eq[1]), fminf(eq[2], eq[3]));
+            return (nv == 0) ? -CUDART_INF_F : e * sl2;
+          };
+          float a = 1.f;  // factor on the O accumulated so far
+          // (tcgen05.ld is warp-collective: every branch around one is taken by the whole warp;
+          // rows that need nothing from it recompute what they already have)
+          if (__any_sync(0xffffffffu, m_used == -CUDART_INF_F)) {
+            float eq[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) eq[k] = kUp ? -CUDART_INF_F : CUDART_INF_F;
+            for (int k = 0; k < 4; ++k) eq[k] = kUp ? -CUDART_INF_F : CUDART_INF_F;
 #pragma unroll 1
-          for (int pp = 0; pp < kKeysT / 32; pp += 2) {
-            uint32_t s0[32], s1[32];
-            tmem_ld32(scol + 32 * pp, s0);
-            tmem_ld32(scol + 32 * pp + 32, s1);
-            tmem_wait_ld();
-            mask_piece<kUp>(s0, nv - 32 * pp);
-            mask_piece<kUp>(s1, nv - 32 * pp - 32);
-            row_extreme<kUp>(s0, eq);
-            row_extreme<kUp>(s1, eq);
+            for (int pp = 0; pp < kKeysT / 32; pp += 2) {
+              uint32_t s0[32], s1[32];
+              tmem_ld32(scol + 32 * pp, s0);
+              tmem_ld32(scol + 32 * pp + 32, s1);
+              tmem_wait_ld();
+              mask_piece<kUp>(s0, nv - 32 * pp);
+              mask_piece<kUp>(s1, nv - 32 * pp - 32);
+              row_extreme<kUp>(s0, eq);
+              row_extreme<kUp>(s1, eq);
+            }
+            if (m_used == -CUDART_INF_F) m_used = tile_offset(eq);  // still -inf when the tile shows no key
           }
-          MLA_TRACE_ONLY(trace_wait[25] += clock64() - tp; tp = clock64();)
-          const float e = kUp ? fmaxf(fmaxf(eq[0], eq[1]), fmaxf(eq[2], eq[3]))
-                             : fminf(fminf(eq[0], eq[1]), fminf(eq[2], eq[3]));
-          const float mt = (nv == 0) ? -CUDART_INF_F : e * sl2;
-          float a = 1.f;
-          if (mt > m_used + kRescaleLog2) {
-            a = ex2_approx(m_used - mt);  // 0 while nothing was accumulated (m_used = -inf)
-            l *= a;
-            m_used = mt;
-          }
-          if (j == 0) a = 1.f;  // the first P V overwrites O
-          const float msub = (m_used == -CUDART_INF_F) ? 0.f : m_used;
+          MLA_TRACE_ONLY(trace_wait[25] += clock64() - tp;)
 
           // ---- P (two K-major boxes of 64 keys) and the rescale factor ----
           if (!waitb(&bars.pbuf_free[sb], ((t >> 1) & 1) ^ 1, X_PBUF_FREE, false)) { live = false; break; }
           MLA_TRACE_ONLY(tp = clock64();)
           uint8_t* prow = smem + kOffPS + sb * kPBytesT + r * 128;
-          uint64_t rsq[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
-          const uint64_t sl2x2 = f32x2(sl2, sl2), nmsub2 = f32x2(-msub, -msub);
+          uint64_t rsq[2];
+          const uint64_t sl2x2 = f32x2(sl2, sl2);
+          for (int pass = 0;; ++pass) {  // at most two passes: the second finds no larger extreme
+            const float msub = (m_used == -CUDART_INF_F) ? 0.f : m_used;
+            const uint64_t nmsub2 = f32x2(-msub, -msub);
+            rsq[0] = rsq[1] = f32x2(0.f, 0.f);
+            float eq[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) eq[k] = kUp ? -CUDART_INF_F : CUDART_INF_F;
 #pragma unroll 1
-          for (int p32 = 0; p32 < kKeysT / 32; ++p32) {
-            uint32_t sr[32];
-            tmem_ld32(scol + 32 * p32, sr);
-            tmem_wait_ld();
-            if (p32 == kKeysT / 32 - 1) {  // the last piece is in registers: S buffer sb is free
-              tc_fence_before();
-              warp_arrive(&bars.s_free[sb]);
+            for (int p32 = 0; p32 < kKeysT / 32; ++p32) {
+              uint32_t sr[32];
+              tmem_ld32(scol + 32 * p32, sr);
+              tmem_wait_ld();
+              mask_piece<kUp>(sr, nv - 32 * p32);
+              row_exp<kUp>(sr, sl2x2, nmsub2, prow + (p32 >> 1) * kPBoxBytes, (4 * p32) & 7, r, rsq, eq);
             }
-            mask_piece<kUp>(sr, nv - 32 * p32);
-            row_exp(sr, sl2x2, nmsub2, prow + (p32 >> 1) * kPBoxBytes, (4 * p32) & 7, r, rsq);
+            const float mt = tile_offset(eq);
+            const bool move = mt > m_used + kRescaleLog2;
+            if (move) {  // the pass again, against the tile's own extreme
+              const float an = ex2_approx(m_used - mt);
+              a *= an;
+              l *= an;
+              m_used = mt;
+            }
+            if (!__any_sync(0xffffffffu, move) || pass == 1) break;
           }
+          tc_fence_before();
+          warp_arrive(&bars.s_free[sb]);  // every score of the tile is read: S buffer sb is free
           MLA_TRACE_ONLY(trace_wait[27] += clock64() - tp;)
           {
             float q0, q1, q2, q3;
@@ -722,6 +740,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
             f32x2_split(rsq[1], q2, q3);
             l += (q0 + q1) + (q2 + q3);
           }
+          if (j == 0) a = 1.f;  // the first P V overwrites O
           alpha[sb * kRows + r] = a;
           fence_proxy_async_smem();  // the bulk copy reads through the async proxy
           warp_arrive(&bars.pwritten[sb]);
@@ -1028,11 +1047,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
 }  // namespace
 
 #ifdef MLA_TRACE
-// copies the trace (2 x 10 x 32 wait sums, then 2 x 10 totals) to host and clears it
+// copies the trace (2 x 16 x 32 wait sums, then 2 x 16 totals) to host and clears it
 extern "C" int mla_trace_read(unsigned long long* host) {
-  static unsigned long long zero[2 * 10 * 32] = {};
+  static unsigned long long zero[2 * 16 * 32] = {};
   if (cudaMemcpyFromSymbol(host, g_trace_wait, sizeof(g_trace_wait)) != cudaSuccess) return 1;
-  if (cudaMemcpyFromSymbol(host + 640, g_trace_total, sizeof(g_trace_total)) != cudaSuccess) return 1;
+  if (cudaMemcpyFromSymbol(host + 1024, g_trace_total, sizeof(g_trace_total)) != cudaSuccess) return 1;
   if (cudaMemcpyToSymbol(g_trace_wait, zero, sizeof(g_trace_wait)) != cudaSuccess) return 1;
   if (cudaMemcpyToSymbol(g_trace_total, zero, sizeof(g_trace_total)) != cudaSuccess) return 1;
   return 0;
