@@ -101,13 +101,21 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
-def _need(t: torch.Tensor, name: str, dtype, device=None):
+def _need(t: torch.Tensor, name: str, dtype, device=None, contiguous: bool = True, shape=None):
+    """Refuse (MLAError, status 1) a tensor the C ABI would misread: wrong dtype or device, a
+    strided view where the call takes dense rows, or an unexpected shape."""
+    if not isinstance(t, torch.Tensor):
+        raise MLAError(1, f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
         raise MLAError(1, f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_cuda:
         raise MLAError(1, f"{name} must be a CUDA tensor")
     if device is not None and t.device != device:
         raise MLAError(1, f"{name} is on {t.device}, expected {device}")
+    if contiguous and not t.is_contiguous():
+        raise MLAError(1, f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise MLAError(1, f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
 # ---------------------------------------------------------------------------
@@ -159,8 +167,8 @@ def mla_prefill(q: torch.Tensor, kv: torch.Tensor, scale: float, causal: bool = 
                 prev_lse: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
                 lse: Optional[torch.Tensor] = None, dv: int = 512, ws: Optional[torch.Tensor] = None, stream=None):
     """Absorbed causal MLA prefill: q [T,H,576], kv [Tkv,576] -> out [T,H,dv], lse [H,T]."""
-    _need(q, "q", torch.bfloat16)
-    _need(kv, "kv", torch.bfloat16, q.device)
+    _need(q, "q", torch.bfloat16, contiguous=False)    # rows may be strided (the ABI takes strides)
+    _need(kv, "kv", torch.bfloat16, q.device, contiguous=False)
     T, H, dk = q.shape
     Tkv = kv.shape[0]
     if q.stride(2) != 1 or kv.stride(1) != 1:
@@ -169,6 +177,12 @@ def mla_prefill(q: torch.Tensor, kv: torch.Tensor, scale: float, causal: bool = 
         out = torch.empty((T, H, dv), dtype=torch.bfloat16, device=q.device)
     if lse is None:
         lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.bfloat16, q.device, shape=(T, H, dv))
+    _need(lse, "lse", torch.float32, q.device, shape=(H, T))
+    if prev_out is not None:
+        _need(prev_out, "prev_out", torch.bfloat16, q.device, shape=(T, H, dv))
+    if prev_lse is not None:
+        _need(prev_lse, "prev_lse", torch.float32, q.device, shape=(H, T))
     nbytes = lib().mla_prefill_workspace_size(T, H)
     ws = workspace(nbytes, q.device) if ws is None else ws
     s = lib().mla_prefill(_ptr(q), q.stride(0), q.stride(1), _ptr(kv), kv.stride(0), T, H, Tkv, dk, dv, float(scale),
@@ -211,12 +225,17 @@ def mla_decode(q, kv_cache, block_table, lens, scale: float, num_splits: int = 0
     _need(kv_cache, "kv_cache", torch.bfloat16, q.device)
     _need(block_table, "block_table", torch.int32, q.device)
     _need(lens, "lens", torch.int32, q.device)
+    if q.dim() != 3 or kv_cache.dim() != 3 or block_table.dim() != 2:
+        raise MLAError(1, "q [B,H,576], kv_cache [pages,page,576], block_table [B,max_pages] expected")
     B, H, _ = q.shape
     num_pages, page_size, _ = kv_cache.shape
+    _need(lens, "lens", torch.int32, q.device, shape=(B,))
     if out is None:
         out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=q.device)
     if lse is None:
         lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.bfloat16, q.device, shape=(B, H, 512))
+    _need(lse, "lse", torch.float32, q.device, shape=(B, H))
     nbytes = lib().mla_decode_workspace_size(B, H, int(num_splits))
     ws = workspace(nbytes, q.device) if ws is None else ws
     s = lib().mla_decode(_ptr(q), _ptr(kv_cache), num_pages, page_size, _ptr(block_table), block_table.shape[1],
@@ -233,12 +252,17 @@ def mla_decode_noalloc(q, kv_cache, block_table, lens, scale: float, num_splits:
     _need(kv_cache, "kv_cache", torch.bfloat16, q.device)
     _need(block_table, "block_table", torch.int32, q.device)
     _need(lens, "lens", torch.int32, q.device)
+    if q.dim() != 3 or kv_cache.dim() != 3 or block_table.dim() != 2:
+        raise MLAError(1, "q [B,H,576], kv_cache [pages,page,576], block_table [B,max_pages] expected")
     B, H, _ = q.shape
     num_pages, page_size, _ = kv_cache.shape
+    _need(lens, "lens", torch.int32, q.device, shape=(B,))
     if out is None:
         out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=q.device)
     if lse is None:
         lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.bfloat16, q.device, shape=(B, H, 512))
+    _need(lse, "lse", torch.float32, q.device, shape=(B, H))
     s = lib().mla_decode_noalloc(_ptr(q), _ptr(kv_cache), num_pages, page_size, _ptr(block_table),
                                  block_table.shape[1], _ptr(lens), B, H, float(scale), int(num_splits), _ptr(out),
                                  _ptr(lse), _stream(stream))
@@ -251,13 +275,20 @@ def mla_sparse(q_lift, q_pe, c_kv, k_pe, topk, softmax_scale: float, out=None, l
     for name, t in (("q_lift", q_lift), ("q_pe", q_pe), ("c_kv", c_kv), ("k_pe", k_pe)):
         _need(t, name, torch.bfloat16, q_lift.device)
     _need(topk, "topk", torch.int32, q_lift.device)
+    if q_lift.dim() != 4 or c_kv.dim() != 3 or topk.dim() != 3:
+        raise MLAError(1, "q_lift [B,S,H,512], c_kv [B,S_kv,512], topk [B,S,K] expected")
     B, S, H, L = q_lift.shape
     S_kv = c_kv.shape[1]
     K = topk.shape[-1]
+    _need(q_pe, "q_pe", torch.bfloat16, q_lift.device, shape=(B, S, H, 64))
+    _need(k_pe, "k_pe", torch.bfloat16, q_lift.device, shape=(B, S_kv, 64))
+    _need(topk, "topk", torch.int32, q_lift.device, shape=(B, S, K))
     if out is None:
         out = torch.empty((B, S, H * L), dtype=torch.bfloat16, device=q_lift.device)
     if lse is None:
         lse = torch.empty((B, S, H), dtype=torch.float32, device=q_lift.device)
+    _need(out, "out", torch.bfloat16, q_lift.device, shape=(B, S, H * L))
+    _need(lse, "lse", torch.float32, q_lift.device, shape=(B, S, H))
     nbytes = lib().mla_sparse_workspace_size(S, H)
     ws = workspace(nbytes, q_lift.device) if ws is None else ws
     s = lib().mla_sparse(_ptr(q_lift), _ptr(q_pe), _ptr(c_kv), _ptr(k_pe), _ptr(topk), B, S, S_kv, H, K,
@@ -268,11 +299,20 @@ def mla_sparse(q_lift, q_pe, c_kv, k_pe, topk, softmax_scale: float, out=None, l
 
 def mla_merge_lse(out_a, lse_a, out_b, lse_b, out=None, lse=None, stream=None):
     """Merge two partial results by LSE: out_* [rows,H,dv] bf16, lse_* [H,rows] fp32."""
+    _need(out_a, "out_a", torch.bfloat16)
+    if out_a.dim() != 3:
+        raise MLAError(1, "out_a must be [rows, H, dv]")
     rows, H, dv = out_a.shape
+    dev = out_a.device
+    _need(out_b, "out_b", torch.bfloat16, dev, shape=(rows, H, dv))
+    _need(lse_a, "lse_a", torch.float32, dev, shape=(H, rows))
+    _need(lse_b, "lse_b", torch.float32, dev, shape=(H, rows))
     if out is None:
         out = torch.empty_like(out_a)
     if lse is None:
         lse = torch.empty_like(lse_a)
+    _need(out, "out", torch.bfloat16, dev, shape=(rows, H, dv))
+    _need(lse, "lse", torch.float32, dev, shape=(H, rows))
     s = lib().mla_merge_lse(_ptr(out_a), _ptr(lse_a), _ptr(out_b), _ptr(lse_b), _ptr(out), _ptr(lse), rows, H, dv,
                             _stream(stream))
     _check(s)

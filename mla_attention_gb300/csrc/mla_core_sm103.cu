@@ -99,6 +99,7 @@ struct Bars {
   uint64_t o_free;
   uint64_t ep_half[2];      // O-CTA: both warps of an epilogue half staged their rows (count 2)
   uint64_t stall;           // fault injection: never arrived on
+  uint64_t drain[2];        // abort: one commit of each MMA issuer lands here
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
@@ -402,6 +403,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
       mbar_init(&bars.ep_half[1], 2);
     }
     mbar_init(&bars.stall, 1);
+    mbar_init(&bars.drain[0], 1);
+    mbar_init(&bars.drain[1], 1);
     bars.abort_flag = 0;
     fence_mbar_init();
   }
@@ -456,6 +459,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
   ItemIter iter;
   iter.init(p, pair);
   Item it;
+  // abort drain: the last barrier phase this thread's TMA loads were counted on
+  uint64_t* drain_bar = nullptr;
+  uint32_t drain_par = 0;
   if (p.debug_stall && warp == 5) waitb(&bars.stall, 0, W_STALL, false);  // runs out: injected fault
 
   if (is_s) {
@@ -484,6 +490,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
               for (int bx = 0; bx < kKBoxes; ++bx)
                 tma_load_2d(dst + bx * kBoxBytes, &map_kv, bx * kBoxCols, j * kKeys, &bars.s_go[s]);
             }
+            drain_bar = &bars.s_go[s];
+            drain_par = (g >> 1) & 1;
           } else {
             int32_t re = -1, ro = -1;
             bool tiled = false;
@@ -523,6 +531,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
             } else {
               if (lane == 0) mbar_arrive_expect_tx(&bars.s_go[s], kStageBytesS);
               __syncwarp();
+              drain_bar = &bars.s_go[s];
+              drain_par = (g >> 1) & 1;
               if (tiled) {
                 if (lane == 0)
                   for (int bx = 0; bx < kKBoxes; ++bx)
@@ -825,6 +835,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
               for (int bx = 0; bx < kVBoxes; ++bx)
                 tma_load_2d(dst + bx * kBoxBytes, &map_kv, bx * kBoxCols, j * kKeys, &bars.o_kv_full[s]);
             }
+            drain_bar = &bars.o_kv_full[s];
+            drain_par = (g / kStagesO) & 1;
           } else {
             int32_t re = -1, ro = -1;
             bool tiled = false;
@@ -860,6 +872,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
             } else {
               if (lane == 0) mbar_arrive_expect_tx(&bars.o_kv_full[s], kStageBytesO);
               __syncwarp();
+              drain_bar = &bars.o_kv_full[s];
+              drain_par = (g / kStagesO) & 1;
               if (tiled) {
                 if (lane == 0)
                   for (int bx = 0; bx < kVBoxes; ++bx)
@@ -884,6 +898,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
                 mbar_arrive_expect_tx(&bars.o_kv_full[s], kStageBytesO);
                 for (int bx = 0; bx < kVBoxes; ++bx)
                   tma_load_2d(dst + bx * kBoxBytes, &map_prev, bx * kBoxCols, (int32_t)row0, &bars.o_kv_full[s]);
+                drain_bar = &bars.o_kv_full[s];
+                drain_par = (g / kStagesO) & 1;
               } else {
                 mbar_arrive(&bars.o_kv_full[s]);
               }
@@ -1142,8 +1158,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
   // ---- teardown: drain on abort, then leave together ----
   __syncwarp();
   if (*abort_flag) {
-    // let copies and MMAs already in flight land before the CTA exits
-    for (int k = 0; k < 200; ++k) __nanosleep(1000);
+    // let what this thread issued land before the CTA leaves: its MMAs (one more commit, which
+    // arrives once they are all done) and its TMA loads (their last full barrier phase)
+    const bool mma_thread = lane == 0 && (is_s ? (warp == 5 || warp == 7) : warp == 5);
+    if (mma_thread) {
+      uint64_t* db = &bars.drain[(is_s && warp == 7) ? 1 : 0];
+      mma_commit(db);
+      mbar_drain(db, 0);
+    }
+    mbar_drain(drain_bar, drain_par);
   }
   tc_fence_before();
   __syncthreads();
@@ -1156,15 +1179,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
 size_t core_smem_bytes() { return kSmemAlloc; }
 
 cudaError_t launch_core(const CoreParams& p, const CoreMaps& maps, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(mla_core_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  static PerDeviceOnce attrs;
+  cudaError_t e = attrs.run([] {
+    cudaError_t r = cudaFuncSetAttribute(mla_core_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemAlloc);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(mla_core_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(mla_core_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    return r;
+  });
+  if (e != cudaSuccess) return e;
   if (p.num_pairs <= 0) return cudaSuccess;
   if (p.mode == MODE_SPARSE)
     mla_core_kernel<true><<<dim3(2 * p.num_pairs), dim3(kThreadsSparse), kSmemAlloc, stream>>>(p, maps);

@@ -3,8 +3,10 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 #include "../../include/mla.h"
 #include "mla_device_status.h"
@@ -87,6 +89,31 @@ struct CoreMaps {
   CUtensorMap pe;    // sparse: k_pe [S_kv, 64], box {64, 1}
   CUtensorMap out;   // prefill / sparse output rows [rows, 512], box {64, 64}
   CUtensorMap prev;  // prefill previous output rows [rows, 512], box {64, 64}
+};
+
+// Runs a set-up step (the kernels' shared-memory attributes) once on each device that launches
+// the kernel, from any number of host threads: the attribute belongs to the device that is
+// current when it is set, so a process that drives several GPUs sets it on each.
+class PerDeviceOnce {
+ public:
+  template <class F>
+  cudaError_t run(F&& setup) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (done_[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (done_[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+    e = setup();
+    if (e == cudaSuccess) done_[dev].store(true, std::memory_order_release);
+    return e;
+  }
+
+ private:
+  static constexpr int kMaxDevices = 64;
+  std::mutex mu_;
+  std::atomic<bool> done_[kMaxDevices] = {};
 };
 
 // kernels' host launchers (return cudaError_t of the launch)

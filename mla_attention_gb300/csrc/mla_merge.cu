@@ -35,12 +35,12 @@ __device__ __forceinline__ uint4 f32_to_bf16x8(const float (&f)[8]) {
   return v;
 }
 
-// one warp per (row, head); lanes stride over dv in 8-element (16-byte) chunks
-__global__ void __launch_bounds__(256) merge_kernel(const __nv_bfloat16* __restrict__ out_a,
-                                                    const float* __restrict__ lse_a,
-                                                    const __nv_bfloat16* __restrict__ out_b,
-                                                    const float* __restrict__ lse_b, __nv_bfloat16* out,
-                                                    float* lse, int64_t rows, int H, int dv) {
+// one warp per (row, head); lanes stride over dv in 8-element (16-byte) chunks.  out / lse may
+// be the same buffers as out_a / lse_a or out_b / lse_b (an in-place merge), so no pointer is
+// declared __restrict__: every element is read before the same lane writes it.
+__global__ void __launch_bounds__(256) merge_kernel(const __nv_bfloat16* out_a, const float* lse_a,
+                                                    const __nv_bfloat16* out_b, const float* lse_b,
+                                                    __nv_bfloat16* out, float* lse, int64_t rows, int H, int dv) {
   const int lane = threadIdx.x & 31;
   const int64_t nitems = rows * (int64_t)H;
   const int64_t warp0 = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
@@ -71,6 +71,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const __nv_bfloat16* __restr
       for (int i = 0; i < 8; ++i) fo[i] = (wsum > 0.f) ? (ca * fa[i] + cb * fb[i]) : 0.f;
       po[c] = f32_to_bf16x8(fo);
     }
+    __syncwarp();  // every lane has read lse_a / lse_b of this item before lse (maybe the same word) is written
     if (lane == 0) lse[(int64_t)h * rows + r] = (wsum > 0.f) ? m + logf(wsum) : -CUDART_INF_F;
   }
 }

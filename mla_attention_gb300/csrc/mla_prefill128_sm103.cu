@@ -87,6 +87,7 @@ struct BarsT {
   // both
   uint64_t pb_free[2];         // P V of O-CTA buffer b done (multicast commit)
   uint64_t stall;              // fault injection: never arrived on
+  uint64_t drain[2];           // abort: one commit of each MMA issuer lands here
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
@@ -379,6 +380,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
       mbar_init(&bars.ep_half[1], 2);
     }
     mbar_init(&bars.stall, 1);
+    mbar_init(&bars.drain[0], 1);
+    mbar_init(&bars.drain[1], 1);
     bars.abort_flag = 0;
     fence_mbar_init();
   }
@@ -442,6 +445,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
   ItemIterT<kDecode> iter;
   iter.init(p, pair);
   ItemT it;
+  // abort drain: the last barrier phase this thread's TMA loads were counted on
+  uint64_t* drain_bar = nullptr;
+  uint32_t drain_par = 0;
   const CUtensorMap& map_v = maps.kv;    // V rows, box {64, 64}
 
   if (is_s) {
@@ -475,6 +481,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
           if (!waitb(&bars.kempty[k], par ^ 1, X_K_EMPTY, false)) { live = false; break; }
           uint64_t* fb = &bars.kfull[k][par];
           if (lane == 0) mbar_arrive_expect_tx(fb, kGroupBytes / 2);
+          drain_bar = fb;
+          drain_par = (t >> 1) & 1;
           __syncwarp();
           if constexpr (!decode) {
             if (lane == 0)
@@ -792,6 +800,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
           }
           if (!waitb(&bars.vempty[h], (m & 1) ^ 1, X_V_EMPTY, false)) { live = false; break; }
           if (lane == 0) mbar_arrive_expect_tx(&bars.vfull[h], kHalfBytesV);
+          drain_bar = &bars.vfull[h];
+          drain_par = m & 1;
           __syncwarp();
           if constexpr (!decode) {
             if (lane == 0)
@@ -809,6 +819,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
             const int64_t row0 = (int64_t)it.id * kRows + h * 64;
             if (p.prev_out && row0 < (int64_t)p.T * p.H) {
               mbar_arrive_expect_tx(&bars.vfull[h], kHalfBytesV);
+              drain_bar = &bars.vfull[h];
+              drain_par = m & 1;
               for (int bx = 0; bx < kVBoxes; ++bx)
                 tma_load_2d(dst + bx * kBoxBytesV, &maps.prev, bx * kBoxCols, (int32_t)row0, &bars.vfull[h]);
             } else {
@@ -1036,7 +1048,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
     atomicAdd(&g_trace_total[is_s ? 0 : 1][warp], (unsigned long long)(clock64() - trace_t0));
   })
   if (*abort_flag) {
-    for (int k = 0; k < 200; ++k) __nanosleep(1000);
+    // let what this thread issued land before the CTA leaves: its MMAs (one more commit, which
+    // arrives once they are all done) and its TMA loads (their last full barrier phase)
+    const bool mma_thread = lane == 0 && (is_s ? (warp == 5 || warp == 6) : warp == 5);
+    if (mma_thread) {
+      uint64_t* db = &bars.drain[is_s ? warp - 5 : 0];
+      mma_commit(db);
+      mbar_drain(db, 0);
+    }
+    mbar_drain(drain_bar, drain_par);
   }
   tc_fence_before();
   __syncthreads();
@@ -1059,21 +1079,21 @@ extern "C" int mla_trace_read(unsigned long long* host) {
 #endif
 
 cudaError_t launch_prefill128(const CoreParams& p, const CoreMaps& maps, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(mla_prefill128_kernel<true, false>,
+  static PerDeviceOnce attrs;
+  cudaError_t e = attrs.run([] {
+    cudaError_t r = cudaFuncSetAttribute(mla_prefill128_kernel<true, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemT);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(mla_prefill128_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(mla_prefill128_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kSmemT);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(mla_prefill128_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemT);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(mla_prefill128_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(mla_prefill128_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemT);
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(mla_prefill128_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kSmemT);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+    return r;
+  });
+  if (e != cudaSuccess) return e;
   if (p.num_pairs <= 0) return cudaSuccess;
   const dim3 grid(2 * p.num_pairs), block(kThreadsT);
   const bool up = p.scale_log2 >= 0.f;

@@ -51,9 +51,12 @@ struct Bars {
   uint64_t p_full[2];
   uint64_t pv_done[2];  // pv_done[b]: the P V that read P from S buffer b is complete
   uint64_t stall;  // fault injection: never arrived on
+  uint64_t drain;  // abort: one commit of the MMA issuer lands here
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
+
+static_assert(sizeof(Bars) <= 256, "barrier block larger than its shared-memory slot");
 
 enum : uint32_t { W_QFULL = 0x20, W_KVEMPTY, W_KVFULL, W_SFULL, W_PFULL, W_ODONE, W_STALL };
 
@@ -117,6 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars.pv_done[0], 1);
     mbar_init(&bars.pv_done[1], 1);
     mbar_init(&bars.stall, 1);
+    mbar_init(&bars.drain, 1);
     bars.abort_flag = 0;
     fence_mbar_init();
   }
@@ -140,8 +144,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int qz = ti.q0 + ti.tile * kTile;  // first query token of the tile
   if (p.debug_stall && warp == 5) waitb(&bars.stall, 0, W_STALL);  // runs out: injected fault
 
+  // abort drain: the last barrier phase this thread's TMA loads were counted on
+  uint64_t* drain_bar = nullptr;
+  uint32_t drain_par = 0;
   if (warp == 4) {
     // ---------------- TMA producer ----------------
+    if (ti.J > 0) {
+      drain_bar = &bars.q_full;
+      drain_par = 0;
+    }
     if (lane == 0 && ti.J > 0) {
       const uint32_t sq = smem_u32(smem + kOffQ);
       mbar_arrive_expect_tx(&bars.q_full, kQBytes);
@@ -162,6 +173,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(st + kKBytes, &mv, 0, ti.hk, kz, &bars.kv_full[s]);
         tma_load_3d(st + kKBytes + kBox, &mv, 64, ti.hk, kz, &bars.kv_full[s]);
       }
+      drain_bar = &bars.kv_full[s];
+      drain_par = (j / kStages) & 1;
       __syncwarp();
     }
   } else if (warp == 5) {
@@ -338,7 +351,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   __syncwarp();
   if (*abort_flag) {
-    for (int k = 0; k < 200; ++k) __nanosleep(1000);
+    // let what this thread issued land before the CTA leaves: its MMAs (one more commit, which
+    // arrives once they are all done) and its TMA loads (their last full barrier phase)
+    if (warp == 5 && lane == 0) {
+      mma_commit(&bars.drain);
+      mbar_drain(&bars.drain, 0);
+    }
+    mbar_drain(drain_bar, drain_par);
   }
   tc_fence_before();
   __syncthreads();
@@ -350,12 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_split(const SplitParams& p, const CUtensorMap& mq_nope, const CUtensorMap& mq_pe,
                          const CUtensorMap& mk_nope, const CUtensorMap& mk_pe, const CUtensorMap& mv,
                          cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(mla_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static PerDeviceOnce attrs;
+  cudaError_t e = attrs.run(
+      [] { return cudaFuncSetAttribute(mla_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc); });
+  if (e != cudaSuccess) return e;
   const int64_t blocks = (int64_t)p.total_q_tiles * p.H;
   if (blocks == 0) return cudaSuccess;
   mla_split_kernel<<<dim3((unsigned)blocks), dim3(kThreads), kSmemAlloc, stream>>>(p, mq_nope, mq_pe, mk_nope, mk_pe,

@@ -147,6 +147,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   return mbar_wait_poll(bar, parity, err, site, spin_limit, cluster_scope);
 }
 
+// After an abort: waits for one barrier phase that this thread's own asynchronous work
+// completes (the last full barrier its TMA loads were counted on, or a commit of its MMAs), so
+// that nothing it issued is still writing shared or tensor memory when the CTA leaves.  Bounded
+// by kDrainNs of wall time, far beyond any copy or MMA latency: a phase that also needs an
+// arrival which an aborted partner never made runs out of the bound instead of hanging.
+constexpr uint64_t kDrainNs = 200000ull;
+__device__ __noinline__ static void mbar_drain(uint64_t* bar, uint32_t parity) {
+  if (!bar) return;
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (global_ns() - t0 > kDrainNs) return;
+  }
+}
+
 // The same wait inlined at its call site (kernels with few wait sites).
 __device__ __forceinline__ bool mbar_wait_inline(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t site,
                                                  uint32_t spin_limit, bool cluster_scope = false) {

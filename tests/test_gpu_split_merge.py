@@ -65,9 +65,12 @@ def test_split_full_size_sampled():
     assert_lse_close(lse[:, toks], rl)
 
 
-def test_merge_parity_and_in_place():
-    g = torch.Generator().manual_seed(8)
-    rows, H, dv = 300, 16, 512
+@pytest.mark.parametrize("dv,alias", [(512, "a"), (128, "a"), (128, "b"), (8, "none")])
+def test_merge_parity_and_in_place(dv, alias):
+    """dv = 512 (the absorbed path), 128 (the split layout's width), 8 (the smallest allowed);
+    the result written over side a, over side b, or to fresh buffers."""
+    g = torch.Generator().manual_seed(8 + dv)
+    rows, H = 300, 16
     oa = gen.randn_bf16((rows, H, dv), g)
     ob = gen.randn_bf16((rows, H, dv), g)
     la = torch.randn((H, rows), generator=g) * 3
@@ -77,8 +80,13 @@ def test_merge_parity_and_in_place():
     ro, rl = mo.merge(oa.double().numpy().transpose(1, 0, 2), la.double().numpy(),
                       ob.double().numpy().transpose(1, 0, 2), lb.double().numpy())
     d = dev()
-    a_o, a_l = oa.to(d), la.to(d)
-    out, lse = mla_merge_lse(a_o, a_l, ob.to(d), lb.to(d), out=a_o, lse=a_l)
+    a_o, a_l, b_o, b_l = oa.to(d), la.to(d), ob.to(d), lb.to(d)
+    dst = {"a": (a_o, a_l), "b": (b_o, b_l), "none": (None, None)}[alias]
+    out, lse = mla_merge_lse(a_o, a_l, b_o, b_l, out=dst[0], lse=dst[1])
     torch.cuda.synchronize()
+    if alias != "none":
+        assert out.data_ptr() == dst[0].data_ptr() and lse.data_ptr() == dst[1].data_ptr()
     assert_out_close(out, ro.transpose(1, 0, 2))
     assert_lse_close(lse, rl)
+    assert not torch.isnan(out).any() and not torch.isnan(lse).any()
+    assert (out[5:10, 0] == 0).all() and torch.isneginf(lse[0, 5:10]).all()  # both sides empty

@@ -6,7 +6,7 @@ import torch
 
 from mla_attention_gb300 import inputs as gen
 from mla_attention_gb300 import (MLAError, check_device_status, inject_stall, mla_decode, mla_prefill,
-                                 mla_prefill_split, set_spin_limit)
+                                 mla_prefill_split, mla_sparse, set_spin_limit, set_tile_keys)
 from tests.helpers import dev
 
 pytestmark = pytest.mark.gpu
@@ -28,7 +28,15 @@ def _expect_timeout(run):
     check_device_status()   # the word was cleared
 
 
-def test_core_kernel_timeout_and_context_survives():
+@pytest.fixture(params=[128, 64], ids=["keys128", "keys64"])
+def engine(request):
+    """Both tile engines: the abort path of each instantiation is driven."""
+    set_tile_keys(request.param, request.param)
+    yield request.param
+    set_tile_keys(0, 0)
+
+
+def test_prefill_timeout_and_context_survives(engine):
     P = gen.prefill_inputs(T=64, H=128, Tkv=256, seed=1)
     q, kv = P.q.to(dev()), P.kv.to(dev())
     _expect_timeout(lambda: mla_prefill(q, kv, P.scale, q_pos0=192))
@@ -48,7 +56,22 @@ def test_split_kernel_timeout():
     check_device_status()
 
 
-def test_decode_timeout():
+def test_decode_timeout(engine):
     D = gen.decode_inputs([200, 70], H=16, seed=3)
     a = [D.q.to(dev()), D.cache.to(dev()), D.block_table.to(dev()), D.lens.to(dev()), D.scale]
     _expect_timeout(lambda: mla_decode(*a))
+    out, lse = mla_decode(*a)
+    torch.cuda.synchronize()
+    check_device_status()
+    assert torch.isfinite(out.float()).all()
+
+
+def test_sparse_timeout():
+    S = gen.sparse_inputs(S=8, S_kv=300, H=16, K=128, pos0=200, seed=4)
+    d = dev()
+    a = [S.q_lift.to(d), S.q_pe.to(d), S.c_kv.to(d), S.k_pe.to(d), S.topk.to(d), S.scale]
+    _expect_timeout(lambda: mla_sparse(*a))
+    out, lse = mla_sparse(*a)
+    torch.cuda.synchronize()
+    check_device_status()
+    assert torch.isfinite(out.float()).all()
