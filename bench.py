@@ -481,6 +481,11 @@ def run_reference(args, world, rank):
     """The oracle on the host cores: each step is a bounded sample of the same workload."""
     if rank != 0:
         return
+    try:  # a launcher may have limited the BLAS threads to one per process; rank 0 runs alone
+        from threadpoolctl import threadpool_limits
+        threadpool_limits(os.cpu_count())
+    except Exception:
+        pass
     steps, warmup = args.steps, args.warmup
     budget = max(1.0, min(8.0, 150.0 / max(1, steps + warmup)))
     for _ in range(warmup):
@@ -560,6 +565,15 @@ def main():
         return
     if args.warmup < 3:
         args.warmup = 3
+    env_world = os.environ.get("WORLD_SIZE")
+    if env_world is None and args.gpus > 1:
+        # N replicas requested without a launcher: start them (one process per GPU)
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+               "--master-addr=127.0.0.1", "--master-port=29517", os.path.abspath(__file__)] + sys.argv[1:]
+        sys.exit(subprocess.call(cmd))
+    if env_world is not None and int(env_world) != args.gpus:
+        sys.stderr.write(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={env_world}; launch one process per GPU\n")
+        sys.exit(2)
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
