@@ -312,6 +312,77 @@ def mla_sparse(q_lift, q_pe, c_kv, k_pe, topk, scale: float,
     return out, lse
 
 
+# ---------------------------------------------------------------------------
+# decode step before attention: RoPE and the paged latent-cache append
+# ---------------------------------------------------------------------------
+def rope(x, cos, sin, is_neox: bool) -> np.ndarray:
+    """Rotary position embedding of the last axis (2n values = n rotation pairs).
+
+    Pair i is rotated by the angle whose cosine and sine are cos[..., i], sin[..., i]:
+    (a, b) -> (a cos - b sin, a sin + b cos).  The pairs are (x[2i], x[2i+1]) (interleaved)
+    or, with is_neox, (x[i], x[i+n]) (halves) -- the two layouts TensorRT-LLM "mla.py"
+    selects with RotaryEmbedding(..., is_neox=...) for the qk_rope_head_dim part.
+    """
+    x = _f64(x)
+    c = _f64(cos)
+    s = _f64(sin)
+    n = x.shape[-1] // 2
+    out = np.empty_like(x)
+    if is_neox:
+        a, b = x[..., :n], x[..., n:]
+        out[..., :n] = a * c - b * s
+        out[..., n:] = a * s + b * c
+    else:
+        a, b = x[..., 0::2], x[..., 1::2]
+        out[..., 0::2] = a * c - b * s
+        out[..., 1::2] = a * s + b * c
+    return out
+
+
+def mla_rope_append(q_pe, c_kv, k_pe, positions, cos_sin, is_neox: bool, cache, block_table, page_size: int):
+    """One decode step's RoPE and latent-cache append (TensorRT-LLM "mla.py",
+    forward_absorption_generation: q_pe and k_pe rotated at the new token's position
+    (apply_rope), the rotated q_pe forms the RoPE part of the fused query, and the latent
+    cache row of the new token receives [compressed_kv | rotated k_pe]
+    (mla_rope_generation / mla_rope_append_paged_kv_assign_q append it to the paged cache)).
+
+    q_pe [B, H, R], c_kv [B, L], k_pe [B, R], positions [B] (the token's index in its
+    request's cache), cos_sin [max_pos, R] (cos of the R/2 angles, then their sin),
+    cache [pages, page_size, L + R], block_table [B, max_pages].
+    Returns (q_rope [B, H, R], cache after the append (a new array)).
+    """
+    qp, ck, kp = _f64(q_pe), _f64(c_kv), _f64(k_pe)
+    cs = _f64(cos_sin)
+    pos = _i64(positions)
+    bt = _i64(block_table)
+    new_cache = _f64(cache).copy()
+    R = qp.shape[-1]
+    n = R // 2
+    q_rope = np.empty_like(qp)
+    for b in range(qp.shape[0]):
+        c, s = cs[pos[b], :n], cs[pos[b], n:]
+        q_rope[b] = rope(qp[b], c[None, :], s[None, :], is_neox)
+        page = bt[b, pos[b] // page_size]
+        new_cache[page, pos[b] % page_size] = np.concatenate([ck[b], rope(kp[b], c, s, is_neox)])
+    return q_rope, new_cache
+
+
+# ---------------------------------------------------------------------------
+# the absorption BMMs around the latent attention
+# ---------------------------------------------------------------------------
+def absorb_q(q_nope, k_b_proj_trans) -> np.ndarray:
+    """q_lift[t, h, l] = sum_d q_nope[t, h, d] W[h, l, d] with W = k_b_proj_trans [H, L, D_nope]
+    (TensorRT-LLM "mla.py", forward_absorption_generation: q_nope (per head) times
+    k_b_proj_trans transposed, written into the latent part of the fused query)."""
+    return np.einsum("thd,hld->thl", _f64(q_nope), _f64(k_b_proj_trans))
+
+
+def project_out(o_latent, v_b_proj) -> np.ndarray:
+    """out[t, h, v] = sum_l O[t, h, l] W[h, v, l] with W = v_b_proj [H, D_v, L] (TensorRT-LLM
+    "mla.py": the latent attention output times v_b_proj transposed, per head)."""
+    return np.einsum("thl,hvl->thv", _f64(o_latent), _f64(v_b_proj))
+
+
 def attention_flops(pairs: int, H: int, dk: int, dv: int) -> float:
     """Algorithmic FLOPs of attention over `pairs` unmasked (query token, key) pairs."""
     return 2.0 * float(pairs) * H * (dk + dv)
@@ -330,5 +401,6 @@ def causal_pairs(T: int, Tkv: int, q_pos0: int, kv_pos0: int, kv_valid: Optional
 
 __all__ = [
     "attend", "attend_masked", "merge", "prefill_key_set", "mla_prefill", "mla_prefill_split",
-    "gather_pages", "mla_decode", "mla_sparse", "attention_flops", "causal_pairs", "NEG_INF",
+    "gather_pages", "mla_decode", "mla_sparse", "rope", "mla_rope_append", "absorb_q", "project_out",
+    "attention_flops", "causal_pairs", "NEG_INF",
 ]

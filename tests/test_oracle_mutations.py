@@ -52,6 +52,19 @@ MUTANTS = {
                                      "qrows = np.concatenate([qp[toks[sel], h], qn[toks[sel], h]], axis=1)"),
     "masked softmax keeps hidden keys": [("s = np.where(visible, s, NEG_INF)", "pass"),
                                          ("p = np.where(visible, np.exp(s - m), 0.0)", "p = np.exp(s - m)")],
+    "rope sine sign (interleaved)": ("out[..., 0::2] = a * c - b * s", "out[..., 0::2] = a * c + b * s"),
+    "rope halves paired as neighbours": ("a, b = x[..., :n], x[..., n:]", "a, b = x[..., 0::2], x[..., 1::2]"),
+    "rope second output uses cos twice": ("out[..., n:] = a * s + b * c", "out[..., n:] = a * c + b * c"),
+    "appended row in the next slot": ("new_cache[page, pos[b] % page_size] =",
+                                      "new_cache[page, (pos[b] + 1) % page_size] ="),
+    "appended row keeps k_pe unrotated": ("np.concatenate([ck[b], rope(kp[b], c, s, is_neox)])",
+                                          "np.concatenate([ck[b], kp[b]])"),
+    "absorb sums over the latent axis": ('return np.einsum("thd,hld->thl", _f64(q_nope), _f64(k_b_proj_trans))',
+                                         'return np.einsum("thd,hld->thl", _f64(q_nope), '
+                                         '_f64(k_b_proj_trans)[:, ::-1, :])'),
+    "project_out with the head's weight of the next head": (
+        'return np.einsum("thl,hvl->thv", _f64(o_latent), _f64(v_b_proj))',
+        'return np.einsum("thl,hvl->thv", _f64(o_latent), np.roll(_f64(v_b_proj), 1, axis=0))'),
 }
 
 

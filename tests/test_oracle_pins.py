@@ -317,24 +317,25 @@ def check_split_lse_brute():
 
 
 def check_absorbed_equals_non_absorbed():
-    """q_lift = q_nope W_UK^T and O W_UV^T reproduce MHA over the up-projected KV."""
+    """absorb_q (q_nope times k_b_proj_trans^T) and project_out (O times v_b_proj^T) around the
+    latent attention reproduce MHA over the explicitly up-projected keys and values."""
     rng = np.random.default_rng(8)
     T, H, L, R, dn, dvh = 5, 2, 16, 4, 6, 5
     c = rng.standard_normal((T, L))           # latent cache rows
     k_pe = rng.standard_normal((T, R))
     q_nope = rng.standard_normal((T, H, dn))
     q_pe = rng.standard_normal((T, H, R))
-    W_UK = rng.standard_normal((H, dn, L)) / 4    # k_nope[h] = c @ W_UK[h].T
-    W_UV = rng.standard_normal((H, dvh, L)) / 4   # v[h] = c @ W_UV[h].T
+    W_k = rng.standard_normal((H, L, dn)) / 4    # k_b_proj_trans: k_nope[h] = c @ W_k[h]
+    W_v = rng.standard_normal((H, dvh, L)) / 4   # v_b_proj: v[h] = c @ W_v[h].T
     scale = 0.3
-    q_lift = np.einsum("thd,hdl->thl", q_nope, W_UK)
+    q_lift = mo.absorb_q(q_nope, W_k)
     q_abs = np.concatenate([q_lift, q_pe], -1)
     kv = np.concatenate([c, k_pe], -1)
     o_lat, lse_a = mo.mla_prefill(q_abs, kv, scale, dv=L, causal=True)
-    o_abs = np.einsum("thl,hvl->thv", o_lat, W_UV)
+    o_abs = mo.project_out(o_lat, W_v)
     for h in range(H):
-        k_nope = c @ W_UK[h].T
-        v = c @ W_UV[h].T
+        k_nope = c @ W_k[h]
+        v = c @ W_v[h].T
         q = np.concatenate([q_nope[:, h], q_pe[:, h]], -1)
         k = np.concatenate([k_nope, k_pe], -1)
         qs = torch.from_numpy(q)[None, None]
@@ -342,6 +343,78 @@ def check_absorbed_equals_non_absorbed():
         vs = torch.from_numpy(v)[None, None]
         ref = torch.nn.functional.scaled_dot_product_attention(qs, ks, vs, is_causal=True, scale=scale)[0, 0]
         np.testing.assert_allclose(o_abs[:, h], ref.numpy(), atol=1e-12)
+    # one entry by hand: q_lift[t, h, l] = sum_d q_nope[t, h, d] W_k[h, l, d]
+    assert abs(q_lift[3, 1, 7] - sum(q_nope[3, 1, d] * W_k[1, 7, d] for d in range(dn))) < 1e-12
+    assert abs(o_abs[2, 0, 4] - sum(o_lat[2, 0, l] * W_v[0, 4, l] for l in range(L))) < 1e-12
+
+
+def check_rope_golden():
+    """Hand-rotated pairs.  x = (1, 2, 3, 4): pair 0 turns by 90 degrees (cos 0, sin 1), pair 1 by 0.
+    Interleaved pairs (1, 2), (3, 4): (1, 2) -> (1*0 - 2*1, 1*1 + 2*0) = (-2, 1); (3, 4) stays.
+    Halves pairs (1, 3), (2, 4): (1, 3) -> (-3, 1) at positions 0 and 2; (2, 4) stays."""
+    x = np.array([1.0, 2.0, 3.0, 4.0])
+    c, s = np.array([0.0, 1.0]), np.array([1.0, 0.0])
+    np.testing.assert_array_equal(mo.rope(x, c, s, False), [-2.0, 1.0, 3.0, 4.0])
+    np.testing.assert_array_equal(mo.rope(x, c, s, True), [-3.0, 2.0, 1.0, 4.0])
+    # the identity angle leaves any vector unchanged
+    y = np.random.default_rng(3).standard_normal(64)
+    np.testing.assert_array_equal(mo.rope(y, np.ones(32), np.zeros(32), False), y)
+
+
+def _rope_table(max_pos, R=64, base=10000.0):
+    inv = base ** (-np.arange(0, R, 2) / R)          # R/2 frequencies
+    ang = np.arange(max_pos)[:, None] * inv[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], 1)
+
+
+def check_rope_properties():
+    """Rotation keeps each pair's length; scores depend on the position difference only; the halves
+    layout is the interleaved one under the pair permutation."""
+    rng = np.random.default_rng(12)
+    cs = _rope_table(64)
+    q, k = rng.standard_normal(64), rng.standard_normal(64)
+    for neox in (False, True):
+        for m in (0, 5, 40):
+            r = mo.rope(q, cs[m, :32], cs[m, 32:], neox)
+            pairs = (lambda v: np.stack([v[:32], v[32:]])) if neox else (lambda v: np.stack([v[0::2], v[1::2]]))
+            np.testing.assert_allclose(np.linalg.norm(pairs(r), axis=0), np.linalg.norm(pairs(q), axis=0), atol=1e-12)
+        for m, n in ((7, 3), (50, 50), (63, 0)):
+            lhs = mo.rope(q, cs[m, :32], cs[m, 32:], neox) @ mo.rope(k, cs[n, :32], cs[n, 32:], neox)
+            rhs = mo.rope(q, cs[m - n, :32], cs[m - n, 32:], neox) @ k
+            assert abs(lhs - rhs) < 1e-10
+    perm = np.empty(64, dtype=int)          # interleaved index 2i <- halves i, 2i+1 <- halves i + 32
+    perm[0::2], perm[1::2] = np.arange(32), np.arange(32) + 32
+    x = rng.standard_normal(64)
+    inter = mo.rope(x[perm], cs[9, :32], cs[9, 32:], False)
+    back = np.empty(64)
+    back[perm] = inter
+    np.testing.assert_allclose(mo.rope(x, cs[9, :32], cs[9, 32:], True), back, atol=1e-12)
+
+
+def check_rope_append():
+    """The appended row lands at (block_table[b][pos // P], pos % P) and nowhere else, holds
+    [c_kv | rotated k_pe], and a decode over pos + 1 keys then attends to it like any other key."""
+    rng = np.random.default_rng(21)
+    B, H, P, L, R = 2, 3, 4, 8, 4
+    pages = 5
+    cache = rng.standard_normal((pages, P, L + R))
+    bt = np.array([[3, 0, -1], [1, 4, 2]])
+    pos = np.array([5, 9])
+    q_pe, c_kv, k_pe = rng.standard_normal((B, H, R)), rng.standard_normal((B, L)), rng.standard_normal((B, R))
+    cs = _rope_table(16, R)
+    q_rope, new = mo.mla_rope_append(q_pe, c_kv, k_pe, pos, cs, False, cache, bt, P)
+    changed = np.argwhere(np.any(new != cache, axis=-1))
+    assert sorted(map(tuple, changed)) == [(0, 1), (2, 1)]        # (page 0, slot 1) and (page 2, slot 1)
+    np.testing.assert_array_equal(new[0, 1, :L], c_kv[0])
+    np.testing.assert_allclose(new[2, 1, L:], mo.rope(k_pe[1], cs[9, :2], cs[9, 2:], False), atol=1e-15)
+    np.testing.assert_allclose(q_rope[1, 2], mo.rope(q_pe[1, 2], cs[9, :2], cs[9, 2:], False), atol=1e-15)
+    q_lat = rng.standard_normal((B, H, L))
+    q = np.concatenate([q_lat, q_rope], -1)
+    out, lse = mo.mla_decode(q, new, bt, pos + 1, 0.5, dv=L)
+    keys = np.stack([new[bt[1, j // P], j % P] for j in range(10)])
+    o_ref, l_ref = mo.attend(q[1], keys, keys[:, :L], 0.5)
+    np.testing.assert_allclose(out[1], o_ref, atol=1e-12)
+    np.testing.assert_allclose(lse[1], l_ref, atol=1e-12)
 
 
 def check_flop_count():
@@ -358,7 +431,7 @@ ALL_CHECKS = [
     check_closed_forms_prefill, check_rope_columns_count, check_chunk_merge_equals_one_pass,
     check_invariances, check_sparse_full_prefix_equals_dense, check_decode_equals_prefill_last_row,
     check_split_equals_library_sdpa, check_split_lse_brute, check_absorbed_equals_non_absorbed,
-    check_flop_count,
+    check_flop_count, check_rope_golden, check_rope_properties, check_rope_append,
 ]
 
 
