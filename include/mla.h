@@ -202,6 +202,67 @@ mla_status mla_decode_noalloc(const void* q, const void* kv_cache, int64_t num_p
                               float scale, int num_splits, void* out, float* lse, void* stream);
 
 /* ------------------------------------------------------------------------- */
+/* The absorption BMMs around the latent attention                            */
+/* ------------------------------------------------------------------------- */
+/*
+ * Defined by: TensorRT-LLM "mla.py", forward_absorption_generation (per head, q_nope times
+ * k_b_proj_trans transposed gives the latent part of the fused query; the latent attention
+ * output times v_b_proj transposed gives the head's output; create_weights: k_b_proj_trans
+ * [num_heads, kv_lora_rank, qk_nope_head_dim], v_b_proj [num_heads, v_head_dim, kv_lora_rank]).
+ * bf16 in and out, fp32 accumulation, on the tensor cores.
+ *
+ * mla_absorb_q: q_out[t, h, 0:512] = sum_d q_nope[t, h, d] k_b_proj_trans[h, :, d].
+ *   q_nope  bf16, element (t, h, d) at q_nope + t * q_nope_stride_t + h * q_nope_stride_h + d,
+ *           d < 128 contiguous (a view into the projection output is fine); strides are
+ *           multiples of 8 elements, q_nope_stride_h >= 128, q_nope_stride_t >= H * q_nope_stride_h.
+ *   k_b_proj_trans bf16 [H, 512, 128] contiguous.
+ *   q_out   bf16 with the same kind of strides (e.g. the fused query [T, H, 576]: strides
+ *           (H * 576, 576)); only columns 0..511 of each row are written.
+ * mla_project_out: out[t, h, 0:128] = sum_l o_latent[t, h, l] v_b_proj[h, :, l].
+ *   o_latent bf16 [T, H, 512] contiguous (the out of mla_prefill / mla_decode).
+ *   v_b_proj bf16 [H, 128, 512] contiguous.  out bf16 rows of 128 with strides as above.
+ * workspace: >= 256 bytes (the status word).  T = 0 launches nothing.
+ */
+mla_status mla_absorb_q(const void* q_nope, int64_t q_nope_stride_t, int64_t q_nope_stride_h,
+                        const void* k_b_proj_trans, int T, int H, void* q_out, int64_t q_out_stride_t,
+                        int64_t q_out_stride_h, void* workspace, size_t workspace_bytes, void* stream);
+mla_status mla_project_out(const void* o_latent, const void* v_b_proj, int T, int H, void* out,
+                           int64_t out_stride_t, int64_t out_stride_h, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/* ------------------------------------------------------------------------- */
+/* Decode step: RoPE and the paged latent-cache append                        */
+/* ------------------------------------------------------------------------- */
+/*
+ * Defined by: TensorRT-LLM "mla.py", forward_absorption_generation (q_pe and k_pe rotated at
+ * the new token's position by RotaryEmbedding(head_dim = qk_rope_head_dim, is_neox); the
+ * rotated q_pe is the RoPE part of the fused query; the token's latent-cache row
+ * [compressed_kv | rotated k_pe] is appended to the paged cache, as mla_rope_generation /
+ * mla_rope_append_paged_kv_assign_q do inside the attention op).
+ *
+ * q_pe       bf16 [B, H, 64], un-rotated; c_kv bf16 [B, 512]; k_pe bf16 [B, 64], un-rotated
+ *            (all contiguous, 16-byte aligned).
+ * positions  DEVICE int32 [B]: the new token's index in its request = the cache row it is
+ *            written to (a decode afterwards passes lens[b] = positions[b] + 1).
+ * cos_sin    DEVICE fp32 [max_pos, 64]: for position p the 32 cosines, then the 32 sines, of the
+ *            rotation angles (any frequency scheme of the caller's model).
+ * is_neox    0: pair i is (x[2i], x[2i+1]); 1: pair i is (x[i], x[i+32]).  Pair i turns by its
+ *            angle: (a, b) -> (a cos - b sin, a sin + b cos), computed in fp32, stored as bf16.
+ * kv_cache / num_pages / page_size / block_table / max_pages: the paged cache of mla_decode;
+ *            the row of position p is row p % page_size of page block_table[b][p / page_size].
+ * q_out      bf16 [B, H, 576]: columns 512..575 receive the rotated q_pe; columns 0..511 (the
+ *            absorbed latent query, see mla_absorb_q) are left as they are.
+ * A position outside [0, max_pos) or beyond max_pages * page_size, or a page id outside
+ * [0, num_pages), skips that request and records MLA_ERR_DEVICE_RANGE in the workspace's status
+ * word (mla_check_device_status).
+ */
+size_t mla_rope_append_workspace_size(int B);
+mla_status mla_rope_append(const void* q_pe, const void* c_kv, const void* k_pe, const int32_t* positions,
+                           const float* cos_sin, int max_pos, int is_neox, void* kv_cache, int64_t num_pages,
+                           int page_size, const int32_t* block_table, int max_pages, int B, int H, void* q_out,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------- */
 /* Top-k sparse latent + RoPE attention                                       */
 /* ------------------------------------------------------------------------- */
 /*

@@ -58,6 +58,13 @@ _SIGNATURES = {
     "mla_sparse_workspace_size": ([c_int, c_int], c_size_t),
     "mla_sparse": ([c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_float,
                     c_void_p, c_void_p, c_void_p, c_size_t, c_void_p], c_int),
+    "mla_absorb_q": ([c_void_p, c_int64, c_int64, c_void_p, c_int, c_int, c_void_p, c_int64, c_int64, c_void_p,
+                      c_size_t, c_void_p], c_int),
+    "mla_project_out": ([c_void_p, c_void_p, c_int, c_int, c_void_p, c_int64, c_int64, c_void_p, c_size_t,
+                         c_void_p], c_int),
+    "mla_rope_append_workspace_size": ([c_int], c_size_t),
+    "mla_rope_append": ([c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_void_p, c_int64, c_int,
+                         c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_size_t, c_void_p], c_int),
     "mla_merge_lse": ([c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int, c_int, c_void_p],
                       c_int),
 }
@@ -295,6 +302,79 @@ def mla_sparse(q_lift, q_pe, c_kv, k_pe, topk, softmax_scale: float, out=None, l
                          float(softmax_scale), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
     _check(s)
     return out, lse
+
+
+def mla_absorb_q(q_nope, k_b_proj_trans, q_out=None, ws=None, stream=None):
+    """q_out[t, h, :512] = q_nope[t, h] @ k_b_proj_trans[h].T.  q_nope [T,H,128] may be a strided view
+    (last dimension contiguous); q_out defaults to a new fused query [T,H,576] (columns 512.. unset)."""
+    _need(q_nope, "q_nope", torch.bfloat16, contiguous=False)
+    if q_nope.dim() != 3 or q_nope.shape[2] != 128 or q_nope.stride(2) != 1:
+        raise MLAError(1, "q_nope must be [T, H, 128] with a contiguous last dimension")
+    T, H, _ = q_nope.shape
+    dev = q_nope.device
+    _need(k_b_proj_trans, "k_b_proj_trans", torch.bfloat16, dev, shape=(H, 512, 128))
+    if q_out is None:
+        q_out = torch.empty((T, H, 576), dtype=torch.bfloat16, device=dev)
+    _need(q_out, "q_out", torch.bfloat16, dev, contiguous=False)
+    if q_out.dim() != 3 or q_out.shape[:2] != (T, H) or q_out.shape[2] < 512 or q_out.stride(2) != 1:
+        raise MLAError(1, "q_out must be [T, H, >= 512] with a contiguous last dimension")
+    ws = workspace(256, dev) if ws is None else ws
+    s = lib().mla_absorb_q(_ptr(q_nope), q_nope.stride(0), q_nope.stride(1), _ptr(k_b_proj_trans), T, H,
+                           _ptr(q_out), q_out.stride(0), q_out.stride(1), _ptr(ws), ws.numel(), _stream(stream))
+    _check(s)
+    return q_out
+
+
+def mla_project_out(o_latent, v_b_proj, out=None, ws=None, stream=None):
+    """out[t, h] = o_latent[t, h] @ v_b_proj[h].T: o_latent [T,H,512], v_b_proj [H,128,512] -> [T,H,128]."""
+    _need(o_latent, "o_latent", torch.bfloat16)
+    if o_latent.dim() != 3 or o_latent.shape[2] != 512:
+        raise MLAError(1, "o_latent must be [T, H, 512]")
+    T, H, _ = o_latent.shape
+    dev = o_latent.device
+    _need(v_b_proj, "v_b_proj", torch.bfloat16, dev, shape=(H, 128, 512))
+    if out is None:
+        out = torch.empty((T, H, 128), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, dev, contiguous=False)
+    if out.dim() != 3 or out.shape != (T, H, 128) or out.stride(2) != 1:
+        raise MLAError(1, "out must be [T, H, 128] with a contiguous last dimension")
+    ws = workspace(256, dev) if ws is None else ws
+    s = lib().mla_project_out(_ptr(o_latent), _ptr(v_b_proj), T, H, _ptr(out), out.stride(0), out.stride(1), _ptr(ws),
+                              ws.numel(), _stream(stream))
+    _check(s)
+    return out
+
+
+def mla_rope_append(q_pe, c_kv, k_pe, positions, cos_sin, kv_cache, block_table, q_out, is_neox: bool = False,
+                    ws=None, stream=None):
+    """Decode step: rotate q_pe [B,H,64] into q_out[:, :, 512:] and append [c_kv | rotated k_pe] at
+    row positions[b] of request b's pages in kv_cache (in place).  Returns q_out."""
+    _need(q_pe, "q_pe", torch.bfloat16)
+    if q_pe.dim() != 3 or q_pe.shape[2] != 64:
+        raise MLAError(1, "q_pe must be [B, H, 64]")
+    B, H, _ = q_pe.shape
+    dev = q_pe.device
+    _need(c_kv, "c_kv", torch.bfloat16, dev, shape=(B, 512))
+    _need(k_pe, "k_pe", torch.bfloat16, dev, shape=(B, 64))
+    _need(positions, "positions", torch.int32, dev, shape=(B,))
+    _need(cos_sin, "cos_sin", torch.float32, dev)
+    if cos_sin.dim() != 2 or cos_sin.shape[1] != 64:
+        raise MLAError(1, "cos_sin must be [max_pos, 64]")
+    _need(kv_cache, "kv_cache", torch.bfloat16, dev)
+    if kv_cache.dim() != 3 or kv_cache.shape[2] != 576:
+        raise MLAError(1, "kv_cache must be [pages, page_size, 576]")
+    _need(block_table, "block_table", torch.int32, dev)
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise MLAError(1, "block_table must be [B, max_pages]")
+    _need(q_out, "q_out", torch.bfloat16, dev, shape=(B, H, 576))
+    nbytes = lib().mla_rope_append_workspace_size(B)
+    ws = workspace(nbytes, dev) if ws is None else ws
+    s = lib().mla_rope_append(_ptr(q_pe), _ptr(c_kv), _ptr(k_pe), _ptr(positions), _ptr(cos_sin), cos_sin.shape[0],
+                              int(bool(is_neox)), _ptr(kv_cache), kv_cache.shape[0], kv_cache.shape[1],
+                              _ptr(block_table), block_table.shape[1], B, H, _ptr(q_out), _ptr(ws), ws.numel(),
+                              _stream(stream))
+    _check(s)
+    return q_out
 
 
 def mla_merge_lse(out_a, lse_a, out_b, lse_b, out=None, lse=None, stream=None):

@@ -128,6 +128,56 @@ int default_pairs() {
 
 using namespace mla;
 
+// ---------------------------------------------------------------------------
+namespace {
+// 3-D bf16 map over rows of one head: {K columns, H heads, T tokens}, box {64, 1, 128}, SW128
+mla_status map_head_rows(CUtensorMap* m, const void* base, uint64_t K, uint64_t H, uint64_t T, int64_t stride_h,
+                         int64_t stride_t, const char* what) {
+  uint64_t dims[3] = {K, H, T};
+  uint64_t strides[2] = {(uint64_t)stride_h * 2, (uint64_t)stride_t * 2};
+  uint32_t box[3] = {64, 1, 128};
+  CUresult r = encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box,
+                            CU_TENSOR_MAP_SWIZZLE_128B);
+  if (r != CUDA_SUCCESS) return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", what, (int)r);
+  return MLA_OK;
+}
+
+mla_status run_bmm(bool lift, const void* a, int64_t a_st, int64_t a_sh, const void* w, int T, int H, void* out,
+                   int64_t o_st, int64_t o_sh, void* workspace, size_t workspace_bytes, void* stream,
+                   const char* name) {
+  const int K = lift ? 128 : kLatent, N = lift ? kLatent : 128;
+  MLA_REQUIRE(T >= 0 && H >= 1, "%s: need T >= 0, H >= 1", name);
+  if (!workspace || workspace_bytes < kWsHeader)
+    return fail(MLA_ERR_WORKSPACE, "%s: workspace must hold %zu bytes", name, (size_t)kWsHeader);
+  if (T == 0) return ok();
+  MLA_REQUIRE(a && w && out, "%s: every tensor is required", name);
+  MLA_REQUIRE(aligned16(a) && aligned16(w) && aligned16(out), "%s: tensors must be 16-byte aligned", name);
+  MLA_REQUIRE(a_sh >= K && a_st >= (int64_t)H * a_sh && (a_sh * 2) % 16 == 0 && (a_st * 2) % 16 == 0,
+              "%s: input rows need head stride >= %d and token stride >= H x head stride, multiples of 8 elements",
+              name, K);
+  MLA_REQUIRE(o_sh >= N && o_st >= (int64_t)H * o_sh && o_sh % 8 == 0 && o_st % 8 == 0,
+              "%s: output rows need head stride >= %d, token stride >= H x head stride, multiples of 8", name, N);
+  CUtensorMap ma, mb;
+  mla_status s = map_head_rows(&ma, a, K, H, T, a_sh, a_st, "bmm rows");
+  if (s != MLA_OK) return s;
+  s = map2d(&mb, w, K, (uint64_t)H * N, K, lift ? 256 : 128, "bmm weights");
+  if (s != MLA_OK) return s;
+  BmmParams p;
+  p.out = reinterpret_cast<__nv_bfloat16*>(out);
+  p.out_stride_t = o_st;
+  p.out_stride_h = o_sh;
+  p.T = T;
+  p.H = H;
+  p.N = N;
+  p.err = ws_err(workspace);
+  p.spin_limit = spin_limit();
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = lift ? launch_absorb_q(p, ma, mb, st) : launch_project_out(p, ma, mb, st);
+  if (e != cudaSuccess) return cuda_fail(e, name);
+  return ok();
+}
+}  // namespace
+
 extern "C" {
 
 int mla_version(void) { return 100; }
@@ -459,6 +509,63 @@ mla_status mla_prefill_split(const void* q_nope, const void* q_pe, const void* k
   p.lse = lse;
   cudaError_t e = launch_split(p, m[0], m[1], m[2], m[3], m[4], st);
   if (e != cudaSuccess) return cuda_fail(e, "mla_prefill_split launch");
+  return ok();
+}
+
+
+mla_status mla_absorb_q(const void* q_nope, int64_t q_nope_stride_t, int64_t q_nope_stride_h,
+                        const void* k_b_proj_trans, int T, int H, void* q_out, int64_t q_out_stride_t,
+                        int64_t q_out_stride_h, void* workspace, size_t workspace_bytes, void* stream) {
+  return run_bmm(true, q_nope, q_nope_stride_t, q_nope_stride_h, k_b_proj_trans, T, H, q_out, q_out_stride_t,
+                 q_out_stride_h, workspace, workspace_bytes, stream, "mla_absorb_q");
+}
+
+mla_status mla_project_out(const void* o_latent, const void* v_b_proj, int T, int H, void* out,
+                           int64_t out_stride_t, int64_t out_stride_h, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  return run_bmm(false, o_latent, (int64_t)H * kLatent, kLatent, v_b_proj, T, H, out, out_stride_t, out_stride_h,
+                 workspace, workspace_bytes, stream, "mla_project_out");
+}
+
+// ---------------------------------------------------------------------------
+size_t mla_rope_append_workspace_size(int B) {
+  (void)B;
+  return kWsHeader;
+}
+
+mla_status mla_rope_append(const void* q_pe, const void* c_kv, const void* k_pe, const int32_t* positions,
+                           const float* cos_sin, int max_pos, int is_neox, void* kv_cache, int64_t num_pages,
+                           int page_size, const int32_t* block_table, int max_pages, int B, int H, void* q_out,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  MLA_REQUIRE(B >= 0 && H >= 1 && max_pos >= 1 && num_pages >= 0 && page_size >= 1 && max_pages >= 0,
+              "mla_rope_append: need B >= 0, H >= 1, max_pos >= 1, num_pages >= 0, page_size >= 1, max_pages >= 0");
+  MLA_REQUIRE(is_neox == 0 || is_neox == 1, "mla_rope_append: is_neox must be 0 or 1");
+  if (!workspace || workspace_bytes < mla_rope_append_workspace_size(B))
+    return fail(MLA_ERR_WORKSPACE, "mla_rope_append: workspace must hold %zu bytes", mla_rope_append_workspace_size(B));
+  if (B == 0) return ok();
+  MLA_REQUIRE(q_pe && c_kv && k_pe && positions && cos_sin && kv_cache && block_table && q_out,
+              "mla_rope_append: every tensor is required");
+  MLA_REQUIRE(aligned16(q_pe) && aligned16(c_kv) && aligned16(k_pe) && aligned16(kv_cache) && aligned16(q_out),
+              "mla_rope_append: bf16 tensors must be 16-byte aligned");
+  RopeAppendParams p;
+  p.q_pe = reinterpret_cast<const __nv_bfloat16*>(q_pe);
+  p.c_kv = reinterpret_cast<const __nv_bfloat16*>(c_kv);
+  p.k_pe = reinterpret_cast<const __nv_bfloat16*>(k_pe);
+  p.positions = positions;
+  p.cos_sin = cos_sin;
+  p.block_table = block_table;
+  p.cache = reinterpret_cast<__nv_bfloat16*>(kv_cache);
+  p.q_out = reinterpret_cast<__nv_bfloat16*>(q_out);
+  p.err = ws_err(workspace);
+  p.num_pages = num_pages;
+  p.max_pos = max_pos;
+  p.is_neox = is_neox;
+  p.page_size = page_size;
+  p.max_pages = max_pages;
+  p.B = B;
+  p.H = H;
+  cudaError_t e = launch_rope_append(p, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mla_rope_append launch");
   return ok();
 }
 

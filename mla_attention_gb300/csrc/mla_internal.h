@@ -116,6 +116,35 @@ class PerDeviceOnce {
   std::atomic<bool> done_[kMaxDevices] = {};
 };
 
+// decode step: RoPE on q_pe / k_pe and the paged latent-cache append
+struct RopeAppendParams {
+  const __nv_bfloat16* q_pe;     // [B, H, 64]
+  const __nv_bfloat16* c_kv;     // [B, 512]
+  const __nv_bfloat16* k_pe;     // [B, 64]
+  const int32_t* positions;      // [B]
+  const float* cos_sin;          // [max_pos, 64]
+  const int32_t* block_table;    // [B, max_pages]
+  __nv_bfloat16* cache;          // [num_pages * page_size, 576] rows
+  __nv_bfloat16* q_out;          // [B, H, 576] (columns 512..575 written)
+  uint32_t* err;
+  int64_t num_pages;
+  int max_pos, is_neox, page_size, max_pages, B, H;
+};
+cudaError_t launch_rope_append(const RopeAppendParams& p, cudaStream_t stream);
+
+// absorption BMMs: D[t, n] = sum_k A[t, k] B[h][n, k] per head, bf16 out with token/head strides
+struct BmmParams {
+  __nv_bfloat16* out;
+  int64_t out_stride_t, out_stride_h;  // elements
+  int T, H, N;                         // tokens, heads, columns of D (512 for q_lift, 128 for the output)
+  uint32_t* err;
+  uint32_t spin_limit;
+};
+// A map: 3-D {K, H, T} box {64, 1, 128}; B map: 2-D {K, H * N} box {64, 256 (q_lift) / 128 (output)}
+cudaError_t launch_absorb_q(const BmmParams& p, const CUtensorMap& ma, const CUtensorMap& mb, cudaStream_t stream);
+cudaError_t launch_project_out(const BmmParams& p, const CUtensorMap& ma, const CUtensorMap& mb,
+                               cudaStream_t stream);
+
 // kernels' host launchers (return cudaError_t of the launch)
 cudaError_t launch_core(const CoreParams& p, const CoreMaps& maps, cudaStream_t stream);
 // prefill and decode with 128-key score tiles.  Prefill: maps.row holds the K rows with box

@@ -226,3 +226,23 @@ def randn_bf16_device(shape, seed: int, device) -> torch.Tensor:
     g = torch.Generator(device=device)
     g.manual_seed(int(seed))
     return torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
+# ---------------------------------------------------------------------------
+# decode step inputs: RoPE angle table and the absorption weights
+# ---------------------------------------------------------------------------
+def rope_cos_sin(max_pos: int, base: float = 10000.0, rope: int = ROPE) -> torch.Tensor:
+    """fp32 [max_pos, rope]: for position p the rope/2 cosines, then the sines, of the angles
+    p * base^(-2i / rope) (the usual geometric frequency ladder; any table is valid input)."""
+    inv = base ** (-torch.arange(0, rope, 2, dtype=torch.float64) / rope)
+    ang = torch.arange(max_pos, dtype=torch.float64)[:, None] * inv[None, :]
+    return torch.cat([torch.cos(ang), torch.sin(ang)], 1).to(torch.float32)
+
+
+def absorb_weights(H: int, seed: int, nope: int = 128, v_head: int = 128):
+    """Synthetic k_b_proj_trans [H, 512, nope] and v_b_proj [H, v_head, 512] (bf16), scaled so the
+    lifted query and the projected output stay of order one for N(0,1) activations."""
+    g = _gen(seed)
+    wk = (torch.randn((H, LATENT, nope), generator=g) / nope ** 0.5).to(torch.bfloat16)
+    wv = (torch.randn((H, v_head, LATENT), generator=g) / LATENT ** 0.5).to(torch.bfloat16)
+    return wk, wv
