@@ -281,6 +281,36 @@ def mla_decode(q, cache, block_table, lens, scale: float, dv: int = 512,
     return out, lse
 
 
+def mla_decode_ex(q, cache, block_table, lens, scale: float, sinks=None, dv: int = 512):
+    """Decode with q_per_req query tokens per request and optional attention sinks.
+
+    q [B, s, H, dk].  Token i of request b sits at position lens[b] - s + i and sees keys
+    0 .. lens[b] - s + i (TensorRT-LLM "mla.py", predicted_tokens_per_seq: several generated
+    tokens per request in one step, causal among them).  With sinks [H], head h's sink logit
+    joins the softmax denominator as one more term with no value (Modular Mojo
+    "mha_single_batch_pipelined", sink_weights): the result is the attention output merged by
+    LSE with an empty-valued partial (O = 0, lse = sinks[h]).
+    Returns out [B, s, H, dv], lse [B, s, H].
+    """
+    qq = _f64(q)
+    cc = _f64(cache)
+    bt = _i64(block_table)
+    ln = _i64(lens)
+    B, S, H, dk = qq.shape
+    P = cc.shape[1]
+    out = np.zeros((B, S, H, dv))
+    lse = np.full((B, S, H), NEG_INF)
+    for b in range(B):
+        for i in range(S):
+            n = max(0, int(ln[b]) - S + 1 + i)
+            rows = gather_pages(cc, bt[b], n, P)
+            out[b, i], lse[b, i] = attend(qq[b, i], rows, rows[:, :dv], scale)
+    if sinks is not None:
+        sk = _f64(sinks)
+        out, lse = merge(out, lse, np.zeros_like(out), np.broadcast_to(sk, lse.shape))
+    return out, lse
+
+
 # ---------------------------------------------------------------------------
 # top-k sparse latent + RoPE attention
 # ---------------------------------------------------------------------------
@@ -401,6 +431,6 @@ def causal_pairs(T: int, Tkv: int, q_pos0: int, kv_pos0: int, kv_valid: Optional
 
 __all__ = [
     "attend", "attend_masked", "merge", "prefill_key_set", "mla_prefill", "mla_prefill_split",
-    "gather_pages", "mla_decode", "mla_sparse", "rope", "mla_rope_append", "absorb_q", "project_out",
+    "gather_pages", "mla_decode", "mla_decode_ex", "mla_sparse", "rope", "mla_rope_append", "absorb_q", "project_out",
     "attention_flops", "causal_pairs", "NEG_INF",
 ]

@@ -62,6 +62,11 @@ MUTANTS = {
     "absorb sums over the latent axis": ('return np.einsum("thd,hld->thl", _f64(q_nope), _f64(k_b_proj_trans))',
                                          'return np.einsum("thd,hld->thl", _f64(q_nope), '
                                          '_f64(k_b_proj_trans)[:, ::-1, :])'),
+    "multi-token decode: every token sees all keys": ("n = max(0, int(ln[b]) - S + 1 + i)", "n = int(ln[b])"),
+    "multi-token decode: token order reversed": ("n = max(0, int(ln[b]) - S + 1 + i)",
+                                                  "n = max(0, int(ln[b]) - i)"),
+    "sink weight ignored": ("out, lse = merge(out, lse, np.zeros_like(out), np.broadcast_to(sk, lse.shape))",
+                            "pass"),
     "project_out with the head's weight of the next head": (
         'return np.einsum("thl,hvl->thv", _f64(o_latent), _f64(v_b_proj))',
         'return np.einsum("thl,hvl->thv", _f64(o_latent), np.roll(_f64(v_b_proj), 1, axis=0))'),

@@ -417,6 +417,49 @@ def check_rope_append():
     np.testing.assert_allclose(lse[1], l_ref, atol=1e-12)
 
 
+def _small_decode():
+    D = gen.decode_inputs([5, 64, 130, 2], H=3, seed=6, page_size=16, extra_pages=2)
+    return {"q": D.q.double().numpy(), "cache": D.cache.double().numpy(), "bt": D.block_table.numpy(),
+            "lens": D.lens.numpy(), "dv": 512}
+
+
+def check_decode_ex():
+    """Several query tokens per request: token i equals the causal prefill row at position
+    len - s + i over the request's gathered rows; one token and no sinks is mla_decode; a sink
+    adds e^{sink} to the denominator (closed form with one key) and -inf sinks change nothing."""
+    D = _small_decode()
+    rng = np.random.default_rng(30)
+    B, H = D["q"].shape[0], D["q"].shape[1]
+    S = 3
+    q = rng.standard_normal((B, S, H, D["q"].shape[2]))
+    out, lse = mo.mla_decode_ex(q, D["cache"], D["bt"], D["lens"], 0.4, dv=D["dv"])
+    for b in range(B):
+        n = int(D["lens"][b])
+        rows = mo.gather_pages(D["cache"], D["bt"][b], n, D["cache"].shape[1])
+        for i in range(S):
+            po, pl = mo.mla_prefill(q[b, i][None], rows, 0.4, dv=D["dv"], causal=True, q_pos0=n - S + i)
+            np.testing.assert_allclose(out[b, i], po[0], atol=1e-12)
+            np.testing.assert_allclose(lse[b, i], pl[:, 0], atol=1e-12)
+    o1, l1 = mo.mla_decode_ex(D["q"][:, None], D["cache"], D["bt"], D["lens"], 0.4, dv=D["dv"])
+    o0, l0 = mo.mla_decode(D["q"], D["cache"], D["bt"], D["lens"], 0.4, dv=D["dv"])
+    np.testing.assert_allclose(o1[:, 0], o0, atol=1e-12)
+    np.testing.assert_allclose(l1[:, 0], l0, atol=1e-12)
+    on, ln_ = mo.mla_decode_ex(q, D["cache"], D["bt"], D["lens"], 0.4, sinks=np.full(H, -np.inf), dv=D["dv"])
+    np.testing.assert_allclose(on, out, atol=1e-12)
+    # one key of score s and value v with a sink z: out = v e^s / (e^s + e^z), lse = ln(e^s + e^z)
+    cache = np.zeros((1, 4, 3))
+    cache[0, 0] = [2.0, 1.5, -1.0]                     # key (dk = 3), value = first 2 columns
+    qq = np.array([[[[0.5, 1.0, 2.0]]]])               # s = 0.5 * (1 + 1.5 - 2) = 0.25
+    o, l_ = mo.mla_decode_ex(qq, cache, np.array([[0]]), np.array([1]), 0.5, sinks=np.array([1.0]), dv=2)
+    w = np.exp(0.25) / (np.exp(0.25) + np.exp(1.0))
+    np.testing.assert_allclose(o[0, 0, 0], w * np.array([2.0, 1.5]), atol=1e-15)
+    assert abs(l_[0, 0, 0] - np.log(np.exp(0.25) + np.exp(1.0))) < 1e-14
+    # a token that sees no key: out = 0, lse = the sink (or -inf without one)
+    o, l_ = mo.mla_decode_ex(np.zeros((1, 2, 1, 3)), cache, np.array([[0]]), np.array([1]), 0.5,
+                             sinks=np.array([0.7]), dv=2)
+    assert (o[0, 0] == 0).all() and l_[0, 0, 0] == 0.7
+
+
 def check_flop_count():
     # causal T = Tkv = n: n(n+1)/2 pairs
     assert mo.causal_pairs(256, 256, 0, 0) == 256 * 257 // 2
@@ -431,7 +474,7 @@ ALL_CHECKS = [
     check_closed_forms_prefill, check_rope_columns_count, check_chunk_merge_equals_one_pass,
     check_invariances, check_sparse_full_prefix_equals_dense, check_decode_equals_prefill_last_row,
     check_split_equals_library_sdpa, check_split_lse_brute, check_absorbed_equals_non_absorbed,
-    check_flop_count, check_rope_golden, check_rope_properties, check_rope_append,
+    check_flop_count, check_rope_golden, check_rope_properties, check_rope_append, check_decode_ex,
 ]
 
 
