@@ -182,6 +182,30 @@ mla_status mla_decode(const void* q, const void* kv_cache, int64_t num_pages, in
                       int num_splits, void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Decode with several query tokens per request and optional attention sinks.
+ *
+ * Several tokens: TensorRT-LLM "mla.py" (predicted_tokens_per_seq: each request generates
+ * q_per_req tokens in one step -- draft tokens of speculative / multi-token prediction).  Token i
+ * of request b sits at position lens[b] - q_per_req + i and sees keys 0 .. lens[b] - q_per_req + i
+ * (the cache holds all of them; causal among the request's own tokens).  A token that sees no
+ * key gets out = 0, lse = -inf (or the sink's logit).
+ * Sinks: Modular Mojo "mha_single_batch_pipelined" (sink, sink_weights): head h's sink logit
+ * sinks[h] joins the softmax denominator as one more term with no value:
+ *   out = sum_j e^{s_j} v_j / (e^{sinks[h]} + sum_j e^{s_j}),  lse = ln(e^{sinks[h]} + sum_j e^{s_j}),
+ * with s_j = scale * q.k_j (the sink is in the units of the scaled scores).
+ *
+ * q      bf16 [B, q_per_req, H, 576] contiguous; out bf16 [B, q_per_req, H, 512];
+ *        lse (nullable) fp32 [B, q_per_req, H]; sinks (nullable) DEVICE fp32 [H].
+ * Other arguments as mla_decode (which is this call with q_per_req = 1 and no sinks).
+ * workspace_bytes >= mla_decode_ex_workspace_size(B, q_per_req, H, num_splits).
+ */
+size_t mla_decode_ex_workspace_size(int B, int q_per_req, int H, int num_splits);
+mla_status mla_decode_ex(const void* q, int q_per_req, const void* kv_cache, int64_t num_pages, int page_size,
+                         const int32_t* block_table, int max_pages, const int32_t* lens, int B, int H, float scale,
+                         const float* sinks, int num_splits, void* out, float* lse, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/*
  * mla_decode without a workspace, for callers that cannot allocate device
  * memory (the pages have no counterpart of this call): plug-ins handed only
  * their input and output buffers by a framework that owns every device

@@ -53,6 +53,9 @@ _SIGNATURES = {
     "mla_decode_workspace_size": ([c_int, c_int, c_int], c_size_t),
     "mla_decode": ([c_void_p, c_void_p, c_int64, c_int, c_void_p, c_int, c_void_p, c_int, c_int, c_float, c_int,
                     c_void_p, c_void_p, c_void_p, c_size_t, c_void_p], c_int),
+    "mla_decode_ex_workspace_size": ([c_int, c_int, c_int, c_int], c_size_t),
+    "mla_decode_ex": ([c_void_p, c_int, c_void_p, c_int64, c_int, c_void_p, c_int, c_void_p, c_int, c_int, c_float,
+                       c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p], c_int),
     "mla_decode_noalloc": ([c_void_p, c_void_p, c_int64, c_int, c_void_p, c_int, c_void_p, c_int, c_int, c_float,
                             c_int, c_void_p, c_void_p, c_void_p], c_int),
     "mla_sparse_workspace_size": ([c_int, c_int], c_size_t),
@@ -248,6 +251,39 @@ def mla_decode(q, kv_cache, block_table, lens, scale: float, num_splits: int = 0
     s = lib().mla_decode(_ptr(q), _ptr(kv_cache), num_pages, page_size, _ptr(block_table), block_table.shape[1],
                          _ptr(lens), B, H, float(scale), int(num_splits), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
                          _stream(stream))
+    _check(s)
+    return out, lse
+
+
+def mla_decode_ex(q, kv_cache, block_table, lens, scale: float, sinks=None, num_splits: int = 0, out=None,
+                  lse=None, ws=None, stream=None):
+    """Decode with q_per_req tokens per request (q [B,s,H,576]; token i sits at position lens[b]-s+i,
+    causal among the request's tokens) and optional per-head sink logits sinks [H] (fp32).
+    Returns out [B,s,H,512], lse [B,s,H]."""
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 4 or q.shape[3] != 576:
+        raise MLAError(1, "q must be [B, q_per_req, H, 576]")
+    B, S, H, _ = q.shape
+    dev = q.device
+    _need(kv_cache, "kv_cache", torch.bfloat16, dev)
+    if kv_cache.dim() != 3 or block_table.dim() != 2:
+        raise MLAError(1, "kv_cache [pages,page,576], block_table [B,max_pages] expected")
+    _need(block_table, "block_table", torch.int32, dev)
+    _need(lens, "lens", torch.int32, dev, shape=(B,))
+    if sinks is not None:
+        _need(sinks, "sinks", torch.float32, dev, shape=(H,))
+    num_pages, page_size, _ = kv_cache.shape
+    if out is None:
+        out = torch.empty((B, S, H, 512), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, S, H), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, dev, shape=(B, S, H, 512))
+    _need(lse, "lse", torch.float32, dev, shape=(B, S, H))
+    nbytes = lib().mla_decode_ex_workspace_size(B, S, H, int(num_splits))
+    ws = workspace(nbytes, dev) if ws is None else ws
+    s = lib().mla_decode_ex(_ptr(q), S, _ptr(kv_cache), num_pages, page_size, _ptr(block_table),
+                            block_table.shape[1], _ptr(lens), B, H, float(scale), _ptr(sinks), int(num_splits),
+                            _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
     _check(s)
     return out, lse
 

@@ -311,16 +311,31 @@ size_t mla_decode_workspace_size(int B, int H, int num_splits) {
   return sz;
 }
 
+size_t mla_decode_ex_workspace_size(int B, int q_per_req, int H, int num_splits) {
+  return mla_decode_workspace_size(B * (q_per_req > 0 ? q_per_req : 1), H, num_splits);
+}
+
 mla_status mla_decode(const void* q, const void* kv_cache, int64_t num_pages, int page_size,
                       const int32_t* block_table, int max_pages, const int32_t* lens, int B, int H, float scale,
                       int num_splits, void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  return mla_decode_ex(q, 1, kv_cache, num_pages, page_size, block_table, max_pages, lens, B, H, scale, nullptr,
+                       num_splits, out, lse, workspace, workspace_bytes, stream);
+}
+
+mla_status mla_decode_ex(const void* q, int q_per_req, const void* kv_cache, int64_t num_pages, int page_size,
+                         const int32_t* block_table, int max_pages, const int32_t* lens, int B, int H, float scale,
+                         const float* sinks, int num_splits, void* out, float* lse, void* workspace,
+                         size_t workspace_bytes, void* stream) {
   MLA_REQUIRE(B >= 0 && H >= 1 && num_pages >= 0 && max_pages >= 0 && num_splits >= 0,
               "mla_decode: need B >= 0, H >= 1, num_pages >= 0, max_pages >= 0, num_splits >= 0");
+  MLA_REQUIRE(q_per_req >= 1 && (int64_t)B * q_per_req <= (int64_t)1 << 24,
+              "mla_decode: q_per_req >= 1 and B * q_per_req <= 2^24 (got %d, %d)", q_per_req, B);
+  const int G = B * q_per_req;  // query groups: one query token of one request each
   if (H > kRows) return fail(MLA_ERR_UNSUPPORTED, "mla_decode: H <= 128 (got %d)", H);
   MLA_REQUIRE(page_size == 16 || page_size == 32 || (page_size > 0 && page_size % 64 == 0),
               "mla_decode: page_size must be 16, 32 or a multiple of 64 (got %d)", page_size);
   MLA_REQUIRE(std::isfinite(scale), "mla_decode: scale must be finite");
-  const size_t need = mla_decode_workspace_size(B, H, num_splits);
+  const size_t need = mla_decode_workspace_size(G, H, num_splits);
   if (!workspace || workspace_bytes < need)
     return fail(MLA_ERR_WORKSPACE, "mla_decode: workspace must hold %zu bytes", need);
   if (B == 0) return ok();
@@ -348,15 +363,17 @@ mla_status mla_decode(const void* q, const void* kv_cache, int64_t num_pages, in
   p.H = H;
   p.block_table = block_table;
   p.lens = lens;
-  p.B = B;
+  p.B = G;
+  p.q_per_req = q_per_req;
+  p.sinks = sinks;
   p.max_pages = max_pages;
   p.page_size = page_size;
   p.num_pages = num_pages;
   p.cache = reinterpret_cast<const __nv_bfloat16*>(kv_cache);
   char* w = reinterpret_cast<char*>(workspace) + kWsHeader;
-  const size_t slots = (size_t)B + (size_t)p.num_pairs;
+  const size_t slots = (size_t)G + (size_t)p.num_pairs;
   p.tile_prefix = reinterpret_cast<int32_t*>(w);
-  w += align_up(sizeof(int32_t) * ((size_t)B + 1), 256);
+  w += align_up(sizeof(int32_t) * ((size_t)G + 1), 256);
   p.part_lse = reinterpret_cast<float*>(w);
   w += align_up(sizeof(float) * slots * (size_t)H, 256);
   p.part_o = reinterpret_cast<float*>(w);

@@ -134,13 +134,8 @@ __device__ __forceinline__ int64_t prefill_keys_for_token(const CoreParams& p, i
   return n < 0 ? 0 : n;
 }
 
-__device__ __forceinline__ int decode_len(const CoreParams& p, int b) {
-  int n = p.lens[b];
-  if (n < 0) n = 0;
-  const int64_t cap = (int64_t)p.max_pages * p.page_size;
-  if (n > cap) n = (int)cap;
-  return n;
-}
+// keys seen by decode query group b (one query token of a request; see decode_group_len)
+__device__ __forceinline__ int decode_len(const CoreParams& p, int b) { return decode_group_len(p, b); }
 
 struct ItemIter {
   const CoreParams* p;
@@ -426,7 +421,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
       const int b = b0 + lane;
       int n = 0;
       if (b < p.B) {
-        const int raw = p.lens[b];
+        const int raw = p.lens[decode_request(p, b)];
         const int64_t cap = (int64_t)p.max_pages * p.page_size;
         if (raw < 0 || raw > cap) record_error(err, DEV_RANGE_BASE | R_LEN);
         n = (decode_len(p, b) + kKeys - 1) / kKeys;
@@ -478,7 +473,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
         // decode with pages of whole tiles: block-table entry of the next tile, loaded a tile ahead
         const bool whole_pages = !kSparse && p.mode == MODE_DECODE && p.page_size % kKeys == 0;
         int32_t npg = -1;
-        if (whole_pages && it.J > 0) npg = p.block_table[(int64_t)it.id * p.max_pages + it.k0 / p.page_size];
+        if (whole_pages && it.J > 0) npg = p.block_table[(int64_t)decode_request(p, it.id) * p.max_pages + it.k0 / p.page_size];
         for (int j = 0; j < it.J && live; ++j, ++g) {
           const int s = g & 1;
           // stage s was last read by the S MMA of tile g-2
@@ -499,7 +494,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
             if constexpr (!kSparse) {
               const int64_t kb = it.k0 + (int64_t)j * kKeys;  // first key of the tile
               const int len = decode_len(p, it.id);
-              const int32_t* bt = p.block_table + (int64_t)it.id * p.max_pages;
+              const int32_t* bt = p.block_table + (int64_t)decode_request(p, it.id) * p.max_pages;
               auto row_of = [&](int64_t key) -> int32_t {
                 if (key >= len) return -1;
                 const int32_t pg = bt[key / p.page_size];
@@ -824,7 +819,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
         // decode with pages of whole tiles: block-table entry of the next tile, loaded a tile ahead
         const bool whole_pages = !kSparse && p.mode == MODE_DECODE && p.page_size % kKeys == 0;
         int32_t npg = -1;
-        if (whole_pages && it.J > 0) npg = p.block_table[(int64_t)it.id * p.max_pages + it.k0 / p.page_size];
+        if (whole_pages && it.J > 0) npg = p.block_table[(int64_t)decode_request(p, it.id) * p.max_pages + it.k0 / p.page_size];
         for (int j = 0; j < it.J && live; ++j, ++g) {
           const int s = g % kStagesO;
           if (!waitb(&bars.o_kv_empty[s], ((g / kStagesO) & 1) ^ 1, W_O_KV_EMPTY, false)) { live = false; break; }
@@ -844,7 +839,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
             if constexpr (!kSparse) {
               const int64_t kb = it.k0 + (int64_t)j * kKeys;
               const int len = decode_len(p, it.id);
-              const int32_t* bt = p.block_table + (int64_t)it.id * p.max_pages;
+              const int32_t* bt = p.block_table + (int64_t)decode_request(p, it.id) * p.max_pages;
               auto row_of = [&](int64_t key) -> int32_t {
                 if (key >= len) return -1;
                 const int32_t pg = bt[key / p.page_size];

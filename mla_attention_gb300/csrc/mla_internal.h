@@ -70,6 +70,8 @@ struct CoreParams {
   int page_size;
   int64_t num_pages;
   const __nv_bfloat16* cache;    // [num_pages * page_size, 576] rows (L2 prefetch addresses)
+  int q_per_req;                 // query tokens per request (B above counts B_req * q_per_req groups)
+  const float* sinks;            // [H] per-head sink logit, or null (used by the reduction)
   int32_t* tile_prefix;          // ws: [B+1] tiles before request b (written by CTA 0)
   float* part_o;                 // ws: [slots, H, 512]
   float* part_lse;               // ws: [slots, H]
@@ -81,6 +83,28 @@ struct CoreParams {
   int K;
   int S_kv;
 };
+
+// Decode query groups: group g is query token g % q_per_req of request g / q_per_req.  Token i of a
+// request of len keys sits at position len - q_per_req + i and sees keys 0 .. len - q_per_req + i
+// (causal among the request's query tokens; with one token it sees all len keys).
+__device__ __forceinline__ int decode_request(const CoreParams& p, int g) {
+  return p.q_per_req > 1 ? g / p.q_per_req : g;
+}
+__device__ __forceinline__ int decode_group_len(const CoreParams& p, int g) {
+  const int64_t cap = (int64_t)p.max_pages * p.page_size;
+  int64_t n;
+  if (p.q_per_req <= 1) {  // one token per request: it sees all len keys
+    n = p.lens[g];
+    if (n > cap) n = cap;
+  } else {
+    const int s = p.q_per_req;
+    const int b = g / s;
+    int64_t len = p.lens[b];
+    if (len > cap) len = cap;
+    n = len - s + 1 + (g - (int64_t)b * s);
+  }
+  return (int)(n < 0 ? 0 : n);
+}
 
 // TMA descriptors of one launch of the absorbed engine
 struct CoreMaps {

@@ -76,12 +76,16 @@ __global__ void __launch_bounds__(256) merge_kernel(const __nv_bfloat16* out_a, 
   }
 }
 
-// Decode split-K reduction: request b, head h merges the partials of the CTA
-// pairs whose key ranges overlapped request b (slot = b + pair).
+// Decode split-K reduction: query group b, head h merges the partials of the CTA
+// pairs whose key ranges overlapped group b (slot = b + pair).  With sinks, head h's sink
+// logit joins the softmax denominator as one more term that carries no value (Modular Mojo
+// "mha_single_batch_pipelined", sink / sink_weights): out = sum_j e^{s_j} v_j / (e^{sink_h} +
+// sum_j e^{s_j}), lse = ln(e^{sink_h} + sum_j e^{s_j}).
 __global__ void __launch_bounds__(256) decode_reduce_kernel(const float* __restrict__ part_o,
                                                             const float* __restrict__ part_lse,
                                                             const int32_t* __restrict__ tile_prefix, int B, int H,
-                                                            int num_pairs, __nv_bfloat16* out, float* lse) {
+                                                            int num_pairs, const float* __restrict__ sinks,
+                                                            __nv_bfloat16* out, float* lse) {
   const int lane = threadIdx.x & 31;
   const int64_t nitems = (int64_t)B * H;
   const int64_t warp0 = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
@@ -92,9 +96,10 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const float* __restr
     const int h = (int)(it - (int64_t)b * H);
     const int64_t t0 = tile_prefix[b], t1 = tile_prefix[b + 1];
     __nv_bfloat16* orow = out + it * kLatent;
-    if (t1 <= t0) {  // no key: out = 0, lse = -inf
+    const float sink = sinks ? sinks[h] : -CUDART_INF_F;
+    if (t1 <= t0) {  // no key: out = 0, lse = -inf (or the sink's logit)
       for (int c = lane; c < kLatent / 8; c += 32) reinterpret_cast<uint4*>(orow)[c] = make_uint4(0, 0, 0, 0);
-      if (lane == 0 && lse) lse[it] = -CUDART_INF_F;
+      if (lane == 0 && lse) lse[it] = sink;
       continue;
     }
     // pair owning tile t: the largest p with floor(p * total / P) <= t
@@ -102,13 +107,13 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const float* __restr
     const int p_last = (int)(((t1) * (int64_t)num_pairs - 1) / total);
     // a pair whose share of the tiles is empty wrote no partial: skip it
     auto owns = [&](int p) { return (int64_t)p * total / num_pairs < (int64_t)(p + 1) * total / num_pairs; };
-    float m = -CUDART_INF_F;
+    float m = sink;
     for (int p = p_first; p <= p_last; ++p)
       if (owns(p)) m = fmaxf(m, part_lse[(int64_t)(b + p) * H + h]);
     float acc[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-    float wsum = 0.f;
+    float wsum = (sink == -CUDART_INF_F) ? 0.f : expf(sink - m);
     if (m != -CUDART_INF_F) {
       for (int p = p_first; p <= p_last; ++p) {
         if (!owns(p)) continue;
@@ -166,7 +171,7 @@ cudaError_t launch_decode_reduce(const CoreParams& p, __nv_bfloat16* out, float*
   const int64_t items = (int64_t)p.B * p.H;
   if (items == 0) return cudaSuccess;
   decode_reduce_kernel<<<grid_for(items), 256, 0, stream>>>(p.part_o, p.part_lse, p.tile_prefix, p.B, p.H,
-                                                           p.num_pairs, out, lse);
+                                                           p.num_pairs, p.sinks, out, lse);
   return cudaGetLastError();
 }
 

@@ -117,13 +117,8 @@ struct ItemT {
   int slot;      // decode: partial slot (request + pair)
 };
 
-__device__ __forceinline__ int decode_len_t(const CoreParams& p, int b) {
-  int n = p.lens[b];
-  if (n < 0) n = 0;
-  const int64_t cap = (int64_t)p.max_pages * p.page_size;
-  if (n > cap) n = (int)cap;
-  return n;
-}
+// keys seen by decode query group b (one query token of a request; see decode_group_len)
+__device__ __forceinline__ int decode_len_t(const CoreParams& p, int b) { return decode_group_len(p, b); }
 
 __device__ __forceinline__ int64_t keys_for_token(const CoreParams& p, int64_t t) {
   int64_t n = p.kv_valid;
@@ -221,7 +216,7 @@ struct HalfIds {
 };
 __device__ __forceinline__ HalfIds load_half_ids(const CoreParams& p, int req, int len, int64_t kh) {
   const int lane = threadIdx.x & 31;
-  const int32_t* bt = p.block_table + (int64_t)req * p.max_pages;
+  const int32_t* bt = p.block_table + (int64_t)decode_request(p, req) * p.max_pages;
   const int64_t ke = kh + 2 * lane, ko = ke + 1;
   HalfIds ids;
   ids.pe = ke < len ? __ldg(bt + ke / p.page_size) : 0;
@@ -402,7 +397,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
       const int b = b0 + lane;
       int n = 0;
       if (b < p.B) {
-        const int raw = p.lens[b];
+        const int raw = p.lens[decode_request(p, b)];
         const int64_t cap = (int64_t)p.max_pages * p.page_size;
         if (raw < 0 || raw > cap) record_error(err, DEV_RANGE_BASE | X_LEN);
         n = (decode_len_t(p, b) + kKeysT - 1) / kKeysT;
@@ -778,7 +773,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
       bool live = true;
       while (live && iter.next(it)) {
         const int len = decode ? decode_len_t(p, it.id) : 0;
-        const int32_t* bt = decode ? p.block_table + (int64_t)it.id * p.max_pages : nullptr;
+        const int32_t* bt = decode ? p.block_table + (int64_t)decode_request(p, it.id) * p.max_pages : nullptr;
         const bool pf_ok = decode && p.page_size % 64 == 0;
         HalfIds ids;
         int32_t pf_pg = -1;  // page under half h of tile j + kPrefetchTiles (read a tile ahead)

@@ -185,3 +185,33 @@ def test_absorbed_chain_equals_non_absorbed_attention():
     ro, rl = mo.mla_prefill_split(q_nope, q_pe, k_nope, k_pe_h, v, [T], H, H, scale, 1)
     assert_out_close(out, ro)
     assert_lse_close(lse, rl, tol=1e-2)
+
+
+# ---------------------------------------------------------------------------
+# several query tokens per request, attention sinks
+# ---------------------------------------------------------------------------
+@pytest.fixture(params=[128, 64], ids=["keys128", "keys64"])
+def decode_engine(request):
+    from mla_attention_gb300 import set_tile_keys
+    set_tile_keys(decode_keys=request.param)
+    yield request.param
+    set_tile_keys(0, 0)
+
+
+@pytest.mark.parametrize("S,H,sinks,splits", [(2, 128, False, 0), (4, 16, True, 0), (3, 128, True, 7),
+                                              (1, 64, True, 0)])
+def test_multi_token_decode_with_sinks(decode_engine, S, H, sinks, splits):
+    from mla_attention_gb300 import mla_decode_ex
+    lens = [1, 3, 64, 129, 700, 2]                     # tokens of the short requests see few or no keys
+    D = gen.decode_inputs(lens, H=H, seed=70 + S, page_size=64)
+    g = torch.Generator().manual_seed(71 + S)
+    q = gen.randn_bf16((len(lens), S, H, 576), g)
+    sk = (torch.randn((H,), generator=g) * 2.0).float() if sinks else None
+    d = dev()
+    out, lse = mla_decode_ex(q.to(d), D.cache.to(d), D.block_table.to(d), D.lens.to(d), D.scale,
+                             sinks=None if sk is None else sk.to(d), num_splits=splits)
+    torch.cuda.synchronize()
+    check_device_status()
+    ro, rl = mo.mla_decode_ex(q, D.cache, D.block_table, D.lens, D.scale, sinks=sk)
+    assert_out_close(out, ro)
+    assert_lse_close(lse, rl)
