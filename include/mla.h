@@ -127,6 +127,26 @@ mla_status mla_prefill(const void* q, int64_t q_stride_t, int64_t q_stride_h, co
                        int64_t kv_pos0, int kv_valid, const void* prev_out, const float* prev_lse, void* out,
                        float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * A batch of sequences packed back to back (Tenstorrent "ttnn.transformer.ring_mla": batched
+ * inputs with per-sequence valid lengths; TensorRT-LLM "mla.py": context attention over a batch
+ * of requests).  Sequence b owns query tokens [cu_seqlens_q[b], cu_seqlens_q[b+1]) of q and key
+ * rows [cu_seqlens_kv[b], cu_seqlens_kv[b+1]) of kv; with causal, its cached prefix comes first:
+ * its query i sees its keys j <= kv_len - q_len + i (all of them without causal).
+ * q [total_q, H, 576] with strides as in mla_prefill; kv [total_kv, 576] (row stride kv_stride);
+ * out [total_q, H, 512] contiguous; lse fp32 [H, total_q]; prev_out / prev_lse (both or neither)
+ * as out / lse, merged per row, and out / lse may be the same buffers.
+ * cu_seqlens_q / cu_seqlens_kv: HOST int32 [batch + 1], starting at 0, non-decreasing.  A
+ * sequence with no query is skipped; one with no key leaves its rows at prev (or 0 / -inf).
+ * Each sequence is one launch of the prefill engine on `stream`.
+ */
+size_t mla_prefill_varlen_workspace_size(int total_q, int H);
+mla_status mla_prefill_varlen(const void* q, int64_t q_stride_t, int64_t q_stride_h, const void* kv,
+                              int64_t kv_stride, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, int batch,
+                              int H, int dk, int dv, float scale, int causal, const void* prev_out,
+                              const float* prev_lse, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
 /* ------------------------------------------------------------------------- */
 /* Non-absorbed split-layout prefill (Ascend RingMLAOperation)               */
 /* ------------------------------------------------------------------------- */

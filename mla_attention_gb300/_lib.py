@@ -61,6 +61,10 @@ _SIGNATURES = {
     "mla_sparse_workspace_size": ([c_int, c_int], c_size_t),
     "mla_sparse": ([c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_float,
                     c_void_p, c_void_p, c_void_p, c_size_t, c_void_p], c_int),
+    "mla_prefill_varlen_workspace_size": ([c_int, c_int], c_size_t),
+    "mla_prefill_varlen": ([c_void_p, c_int64, c_int64, c_void_p, c_int64, c_void_p, c_void_p, c_int, c_int, c_int,
+                            c_int, c_float, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                            c_void_p], c_int),
     "mla_absorb_q": ([c_void_p, c_int64, c_int64, c_void_p, c_int, c_int, c_void_p, c_int64, c_int64, c_void_p,
                       c_size_t, c_void_p], c_int),
     "mla_project_out": ([c_void_p, c_void_p, c_int, c_int, c_void_p, c_int64, c_int64, c_void_p, c_size_t,
@@ -198,6 +202,42 @@ def mla_prefill(q: torch.Tensor, kv: torch.Tensor, scale: float, causal: bool = 
     s = lib().mla_prefill(_ptr(q), q.stride(0), q.stride(1), _ptr(kv), kv.stride(0), T, H, Tkv, dk, dv, float(scale),
                           int(bool(causal)), int(q_pos0), int(kv_pos0), int(kv_valid), _ptr(prev_out),
                           _ptr(prev_lse), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+    _check(s)
+    return out, lse
+
+
+def mla_prefill_varlen(q, kv, cu_seqlens_q, cu_seqlens_kv, scale: float, causal: bool = True, prev_out=None,
+                       prev_lse=None, out=None, lse=None, dv: int = 512, ws=None, stream=None):
+    """Packed batch of sequences: q [total_q,H,576], kv [total_kv,576], cu_seqlens_* HOST int32 [batch+1].
+    Query i of sequence b sees its keys j <= kv_len - q_len + i (causal).  Returns out, lse [H,total_q]."""
+    _need(q, "q", torch.bfloat16, contiguous=False)
+    _need(kv, "kv", torch.bfloat16, q.device, contiguous=False)
+    if q.dim() != 3 or kv.dim() != 2 or q.stride(2) != 1 or kv.stride(1) != 1:
+        raise MLAError(1, "q [total_q, H, 576] and kv [total_kv, 576] with contiguous last dimensions")
+    cq = torch.as_tensor(cu_seqlens_q, dtype=torch.int32).cpu().contiguous()
+    ck = torch.as_tensor(cu_seqlens_kv, dtype=torch.int32).cpu().contiguous()
+    if cq.dim() != 1 or cq.shape != ck.shape or cq.numel() < 1:
+        raise MLAError(1, "cu_seqlens_q and cu_seqlens_kv: host int32 [batch + 1]")
+    batch = cq.numel() - 1
+    Tq, H, dk = q.shape
+    if int(cq[-1]) != Tq or int(ck[-1]) > kv.shape[0]:
+        raise MLAError(1, "cu_seqlens must end at the packed lengths of q and kv")
+    if out is None:
+        out = torch.empty((Tq, H, dv), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((H, Tq), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.bfloat16, q.device, shape=(Tq, H, dv))
+    _need(lse, "lse", torch.float32, q.device, shape=(H, Tq))
+    if prev_out is not None:
+        _need(prev_out, "prev_out", torch.bfloat16, q.device, shape=(Tq, H, dv))
+    if prev_lse is not None:
+        _need(prev_lse, "prev_lse", torch.float32, q.device, shape=(H, Tq))
+    nbytes = lib().mla_prefill_varlen_workspace_size(Tq, H)
+    ws = workspace(nbytes, q.device) if ws is None else ws
+    s = lib().mla_prefill_varlen(_ptr(q), q.stride(0), q.stride(1), _ptr(kv), kv.stride(0),
+                                 ctypes.c_void_p(cq.data_ptr()), ctypes.c_void_p(ck.data_ptr()), batch, H, dk, dv,
+                                 float(scale), int(bool(causal)), _ptr(prev_out), _ptr(prev_lse), _ptr(out),
+                                 _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
     _check(s)
     return out, lse
 

@@ -178,63 +178,11 @@ mla_status run_bmm(bool lift, const void* a, int64_t a_st, int64_t a_sh, const v
 }
 }  // namespace
 
-extern "C" {
-
-int mla_version(void) { return 100; }
-
-const char* mla_last_error_string(void) { return g_err; }
-
-const char* mla_status_string(mla_status s) {
-  switch (s) {
-    case MLA_OK: return "MLA_OK";
-    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
-    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
-    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
-    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
-    case MLA_ERR_DEVICE_RANGE: return "MLA_ERR_DEVICE_RANGE";
-    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE";
-  }
-  return "MLA_UNKNOWN";
-}
-
-void mla_set_spin_limit(uint32_t limit) { g_spin_limit.store(limit ? limit : kDefaultSpinLimit); }
-
-void mla_set_tile_keys(int prefill_keys, int decode_keys) {
-  if (prefill_keys == 0) prefill_keys = kDefaultPrefillKeys;
-  if (decode_keys == 0) decode_keys = kDefaultDecodeKeys;
-  if (prefill_keys == 64 || prefill_keys == 128) g_prefill_keys.store(prefill_keys);
-  if (decode_keys == 64 || decode_keys == 128) g_decode_keys.store(decode_keys);
-}
-
-void mla_debug_inject_stall(int enable) { g_debug_stall.store(enable ? 1u : 0u); }
-
-mla_status mla_check_device_status(void* workspace, void* stream, uint32_t* detail) {
-  if (!workspace) return fail(MLA_ERR_INVALID_ARG, "mla_check_device_status: workspace is NULL");
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  uint32_t word = 0;
-  cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, st);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof(word), st);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-  if (e != cudaSuccess) return cuda_fail(e, "mla_check_device_status");
-  if (detail) *detail = word;
-  if (word == 0) return ok();
-  if ((word & 0xF000u) == DEV_TIMEOUT_BASE)
-    return fail(MLA_ERR_TIMEOUT, "a device wait ran out of its spin bound (site 0x%x)", word & 0xFFFu);
-  return fail(MLA_ERR_DEVICE_RANGE, "a kernel met an out-of-range index (site 0x%x)", word & 0xFFFu);
-}
-
-// ---------------------------------------------------------------------------
-size_t mla_prefill_workspace_size(int T, int H) {
-  (void)T;
-  (void)H;
-  return kWsHeader;
-}
-
-mla_status mla_prefill(const void* q, int64_t q_stride_t, int64_t q_stride_h, const void* kv, int64_t kv_stride,
+namespace {
+mla_status prefill_one(const void* q, int64_t q_stride_t, int64_t q_stride_h, const void* kv, int64_t kv_stride,
                        int T, int H, int Tkv, int dk, int dv, float scale, int causal, int64_t q_pos0,
                        int64_t kv_pos0, int kv_valid, const void* prev_out, const float* prev_lse, void* out,
-                       float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+                       float* lse, int64_t lse_stride, void* workspace, size_t workspace_bytes, void* stream) {
   MLA_REQUIRE(T >= 0 && H >= 1 && Tkv >= 0, "mla_prefill: need T >= 0, H >= 1, Tkv >= 0 (T=%d H=%d Tkv=%d)", T, H,
               Tkv);
   MLA_REQUIRE(dk > dv && dv > 0, "mla_prefill: V must be narrower than K (dk=%d dv=%d)", dk, dv);
@@ -293,10 +241,109 @@ mla_status mla_prefill(const void* q, int64_t q_stride_t, int64_t q_stride_h, co
   p.prev_lse = prev_lse;
   p.out = reinterpret_cast<__nv_bfloat16*>(out);
   p.lse = lse;
+  p.lse_stride = lse_stride;
   const int64_t items = ((int64_t)T * H + kRows - 1) / kRows;
   if (items < p.num_pairs) p.num_pairs = (int)items;
   cudaError_t e = tile128 ? launch_prefill128(p, maps, st) : launch_core(p, maps, st);
   if (e != cudaSuccess) return cuda_fail(e, "mla_prefill launch");
+  return ok();
+}
+}  // namespace
+
+extern "C" {
+
+int mla_version(void) { return 100; }
+
+const char* mla_last_error_string(void) { return g_err; }
+
+const char* mla_status_string(mla_status s) {
+  switch (s) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
+    case MLA_ERR_DEVICE_RANGE: return "MLA_ERR_DEVICE_RANGE";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE";
+  }
+  return "MLA_UNKNOWN";
+}
+
+void mla_set_spin_limit(uint32_t limit) { g_spin_limit.store(limit ? limit : kDefaultSpinLimit); }
+
+void mla_set_tile_keys(int prefill_keys, int decode_keys) {
+  if (prefill_keys == 0) prefill_keys = kDefaultPrefillKeys;
+  if (decode_keys == 0) decode_keys = kDefaultDecodeKeys;
+  if (prefill_keys == 64 || prefill_keys == 128) g_prefill_keys.store(prefill_keys);
+  if (decode_keys == 64 || decode_keys == 128) g_decode_keys.store(decode_keys);
+}
+
+void mla_debug_inject_stall(int enable) { g_debug_stall.store(enable ? 1u : 0u); }
+
+mla_status mla_check_device_status(void* workspace, void* stream, uint32_t* detail) {
+  if (!workspace) return fail(MLA_ERR_INVALID_ARG, "mla_check_device_status: workspace is NULL");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof(word), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "mla_check_device_status");
+  if (detail) *detail = word;
+  if (word == 0) return ok();
+  if ((word & 0xF000u) == DEV_TIMEOUT_BASE)
+    return fail(MLA_ERR_TIMEOUT, "a device wait ran out of its spin bound (site 0x%x)", word & 0xFFFu);
+  return fail(MLA_ERR_DEVICE_RANGE, "a kernel met an out-of-range index (site 0x%x)", word & 0xFFFu);
+}
+
+// ---------------------------------------------------------------------------
+size_t mla_prefill_workspace_size(int T, int H) {
+  (void)T;
+  (void)H;
+  return kWsHeader;
+}
+
+mla_status mla_prefill(const void* q, int64_t q_stride_t, int64_t q_stride_h, const void* kv, int64_t kv_stride,
+                       int T, int H, int Tkv, int dk, int dv, float scale, int causal, int64_t q_pos0,
+                       int64_t kv_pos0, int kv_valid, const void* prev_out, const float* prev_lse, void* out,
+                       float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  return prefill_one(q, q_stride_t, q_stride_h, kv, kv_stride, T, H, Tkv, dk, dv, scale, causal, q_pos0, kv_pos0,
+                     kv_valid, prev_out, prev_lse, out, lse, 0, workspace, workspace_bytes, stream);
+}
+
+size_t mla_prefill_varlen_workspace_size(int total_q, int H) { return mla_prefill_workspace_size(total_q, H); }
+
+mla_status mla_prefill_varlen(const void* q, int64_t q_stride_t, int64_t q_stride_h, const void* kv,
+                              int64_t kv_stride, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, int batch,
+                              int H, int dk, int dv, float scale, int causal, const void* prev_out,
+                              const float* prev_lse, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  MLA_REQUIRE(batch >= 0 && cu_seqlens_q && cu_seqlens_kv, "mla_prefill_varlen: batch >= 0 and host cu_seqlens");
+  MLA_REQUIRE(cu_seqlens_q[0] == 0 && cu_seqlens_kv[0] == 0, "mla_prefill_varlen: cu_seqlens start at 0");
+  for (int b = 0; b < batch; ++b)
+    MLA_REQUIRE(cu_seqlens_q[b + 1] >= cu_seqlens_q[b] && cu_seqlens_kv[b + 1] >= cu_seqlens_kv[b],
+                "mla_prefill_varlen: cu_seqlens must not decrease (sequence %d)", b);
+  const int64_t total_q = cu_seqlens_q[batch];
+  MLA_REQUIRE((prev_out == nullptr) == (prev_lse == nullptr), "mla_prefill_varlen: prev_out and prev_lse go together");
+  if (!workspace || workspace_bytes < mla_prefill_varlen_workspace_size((int)total_q, H))
+    return fail(MLA_ERR_WORKSPACE, "mla_prefill_varlen: workspace must hold %zu bytes",
+                mla_prefill_varlen_workspace_size((int)total_q, H));
+  const char* bq = reinterpret_cast<const char*>(q);
+  const char* bkv = reinterpret_cast<const char*>(kv);
+  for (int b = 0; b < batch; ++b) {
+    const int q0 = cu_seqlens_q[b], ql = cu_seqlens_q[b + 1] - q0;
+    const int k0 = cu_seqlens_kv[b], kl = cu_seqlens_kv[b + 1] - k0;
+    if (ql == 0) continue;
+    // one sequence: the cached prefix precedes its queries (query i sees keys j <= kl - ql + i)
+    const int64_t row0 = (int64_t)q0 * H;  // first (token, head) row of the sequence
+    mla_status s = prefill_one(
+        bq + 2 * (int64_t)q0 * q_stride_t, q_stride_t, q_stride_h, kl ? bkv + 2 * (int64_t)k0 * kv_stride : nullptr,
+        kv_stride, ql, H, kl, dk, dv, scale, causal, (int64_t)kl - ql, 0, kl,
+        prev_out ? reinterpret_cast<const char*>(prev_out) + 2 * row0 * dv : nullptr,
+        prev_lse ? prev_lse + q0 : nullptr, reinterpret_cast<char*>(out) + 2 * row0 * dv, lse + q0, total_q,
+        workspace, workspace_bytes, stream);
+    if (s != MLA_OK) return s;
+  }
   return ok();
 }
 

@@ -963,10 +963,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
             const int64_t t = f / p.H, h = f - t * p.H;
             row_ok = true;
             orow = p.out + f * kLatent;
-            lse_dst = p.lse + h * p.T + t;
+            lse_dst = p.lse + h * (p.lse_stride ? p.lse_stride : (int64_t)p.T) + t;
             if (p.prev_out) {
               prev_row = p.prev_out + f * kLatent;
-              prev_l = p.prev_lse[h * p.T + t];
+              prev_l = p.prev_lse[h * (p.lse_stride ? p.lse_stride : (int64_t)p.T) + t];
             }
           }
         } else if (!kSparse) {

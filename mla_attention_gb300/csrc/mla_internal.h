@@ -61,6 +61,7 @@ struct CoreParams {
   const float* prev_lse;         // [H,T] or null
   __nv_bfloat16* out;            // prefill: [T,H,512]; sparse: [S,H*512]
   float* lse;                    // prefill: [H,T]; sparse: [S,H] (nullable)
+  int64_t lse_stride;            // prefill: head stride of lse / prev_lse (0 = T)
 
   // ---- decode ----
   const int32_t* block_table;    // [B, max_pages]

@@ -888,10 +888,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
           if (row_ok) {
             const int64_t tt = f / p.H, hh = f - tt * p.H;
             orow = p.out + f * kLatent;
-            lse_dst = p.lse + hh * p.T + tt;
+            lse_dst = p.lse + hh * (p.lse_stride ? p.lse_stride : (int64_t)p.T) + tt;
             if (p.prev_out) {
               prev_row = p.prev_out + f * kLatent;
-              prev_l = p.prev_lse[hh * p.T + tt];
+              prev_l = p.prev_lse[hh * (p.lse_stride ? p.lse_stride : (int64_t)p.T) + tt];
             }
           }
         }

@@ -141,3 +141,35 @@ def test_negative_and_zero_scale(scale_mul, tile_keys):
     ro, rl = mo.mla_prefill(P.q, P.kv, scale, causal=True, q_pos0=40)
     assert_out_close(out, ro)
     assert_lse_close(lse, rl)
+
+
+@pytest.mark.parametrize("H", [128, 16])
+def test_varlen_batch_with_prev_and_empty_sequences(tile_keys, H):
+    """Four packed sequences of unequal lengths (one with no query, one with a cached prefix longer
+    than its queries, one with no key), causal, merged in place with a previous pair; each
+    sequence against the oracle's single-sequence prefill with its bottom-right alignment."""
+    from mla_attention_gb300 import mla_prefill_varlen
+    q_lens = [70, 0, 33, 200, 5]
+    kv_lens = [70, 10, 150, 200, 0]
+    g = torch.Generator().manual_seed(90 + H)
+    Tq, Tk = sum(q_lens), sum(kv_lens)
+    q = gen.randn_bf16((Tq, H, 576), g)
+    kv = gen.randn_bf16((Tk, 576), g)
+    prev_out, prev_lse = gen.prev_inputs(Tq, H, 512, seed=91, lse_lo=1.0, lse_hi=6.0)
+    prev_lse[:, :3] = -float("inf")
+    cq = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    ck = np.concatenate([[0], np.cumsum(kv_lens)]).astype(np.int32)
+    d = dev()
+    po, pl = prev_out.to(d), prev_lse.to(d)
+    out, lse = mla_prefill_varlen(q.to(d), kv.to(d), cq, ck, gen.SCALE_192, causal=True, prev_out=po, prev_lse=pl,
+                                  out=po, lse=pl)
+    torch.cuda.synchronize()
+    check_device_status()
+    for b in range(len(q_lens)):
+        if q_lens[b] == 0:
+            continue
+        qs, ks = slice(cq[b], cq[b + 1]), slice(ck[b], ck[b + 1])
+        ro, rl = mo.mla_prefill(q[qs], kv[ks], gen.SCALE_192, causal=True, q_pos0=kv_lens[b] - q_lens[b], kv_pos0=0,
+                                prev_out=prev_out[qs], prev_lse=prev_lse[:, qs])
+        assert_out_close(out[qs], ro, what=f"out of sequence {b}")
+        assert_lse_close(lse[:, qs], rl, what=f"lse of sequence {b}")
