@@ -332,6 +332,87 @@ def measure_split(lib, dev, peaks, steps=5, warmup=3):
             "TFLOP_per_s": round(tf, 1), "tensor_frac": round(tf / peaks["bf16_tflops"], 4)}
 
 
+def measure_absorb(lib, dev, peaks, steps=10, warmup=3):
+    """The absorption BMMs at the prefill workload's size: T = 8192 tokens, H = 128."""
+    from mla_attention_gb300 import inputs as gen
+    T = T_TOTAL
+    q_nope = gen.randn_bf16_device((T, H, 192), 91, dev)[:, :, :128]   # a view into the projection output
+    wk = (gen.randn_bf16_device((H, 512, 128), 92, dev).float() / 128 ** 0.5).to(torch.bfloat16)
+    wv = (gen.randn_bf16_device((H, 128, 512), 93, dev).float() / 512 ** 0.5).to(torch.bfloat16)
+    fused = torch.empty((T, H, 576), dtype=torch.bfloat16, device=dev)
+    o_lat = gen.randn_bf16_device((T, H, 512), 94, dev)
+    out = torch.empty((T, H, 128), dtype=torch.bfloat16, device=dev)
+    res = {}
+    for name, fn, nbytes in (
+            ("absorb_q", lambda: lib.mla_absorb_q(q_nope, wk, q_out=fused),
+             T * H * 128 * 2 + T * H * 512 * 2 + wk.numel() * 2),
+            ("project_out", lambda: lib.mla_project_out(o_lat, wv, out=out),
+             T * H * 512 * 2 + T * H * 128 * 2 + wv.numel() * 2)):
+        for _ in range(warmup):
+            fn()
+        ms = time_region(fn, steps)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[name] = {"ms": round(ms, 4), "GB_per_s": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+                     "TFLOP_per_s": round(2.0 * T * H * 128 * 512 / (ms * 1e-3) / 1e12, 1)}
+    res["workload"] = "T=8192 tokens, H=128: q_nope [T,H,128] (view) x k_b_proj_trans^T -> fused q; O [T,H,512] x v_b_proj^T"
+    return res
+
+
+def _decode_config4(dev):
+    from mla_attention_gb300 import inputs as gen
+    lens = gen.decode_lens(64, 4096, 32768, seed=4)
+    page = 64
+    pages_per = [(n + 1 + page - 1) // page for n in lens]       # room for one appended row
+    num_pages = sum(pages_per)
+    g = torch.Generator().manual_seed(4)
+    perm = torch.randperm(num_pages, generator=g).to(torch.int32)
+    bt = torch.full((64, max(pages_per)), -1, dtype=torch.int32)
+    o = 0
+    for b, n in enumerate(pages_per):
+        bt[b, :n] = perm[o:o + n]
+        o += n
+    cache = gen.randn_bf16_device((num_pages, page, DK), 42, dev)
+    return lens, cache, bt.to(dev)
+
+
+def measure_decode_step(lib, dev, peaks, steps=10, warmup=3):
+    """The decode workload's step around attention (RoPE + cache append) and two query tokens per
+    request with per-head sinks (multi-token decode)."""
+    from mla_attention_gb300 import inputs as gen
+    lens, cache, bt = _decode_config4(dev)
+    B = len(lens)
+    q_pe = gen.randn_bf16_device((B, H, 64), 95, dev)
+    c_kv = gen.randn_bf16_device((B, 512), 96, dev)
+    k_pe = gen.randn_bf16_device((B, 64), 97, dev)
+    pos = torch.tensor(lens, dtype=torch.int32, device=dev)
+    cs = gen.rope_cos_sin(40000).to(dev)
+    q = gen.randn_bf16_device((B, H, DK), 41, dev)
+    fn = lambda: lib.mla_rope_append(q_pe, c_kv, k_pe, pos, cs, cache, bt, q)  # noqa: E731
+    for _ in range(warmup):
+        fn()
+    ms_r = time_region(fn, steps)
+    rope_bytes = B * H * 64 * 2 * 2 + B * (512 + 64) * 2 * 2 + B * 64 * 4 * 2
+    S = 2
+    q2 = gen.randn_bf16_device((B, S, H, DK), 98, dev)
+    sinks = torch.linspace(-1.0, 3.0, H, device=dev)
+    lens_d = torch.tensor(lens, dtype=torch.int32, device=dev)
+    out = torch.empty((B, S, H, DV), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, S, H), dtype=torch.float32, device=dev)
+    fn2 = lambda: lib.mla_decode_ex(q2, cache, bt, lens_d, SCALE, sinks=sinks, out=out, lse=lse)  # noqa: E731
+    for _ in range(warmup):
+        fn2()
+    ms_m = time_region(fn2, steps)
+    kv_bytes = sum(lens) * DK * 2
+    gbs = (kv_bytes + q2.numel() * 2 + out.numel() * 2) / (ms_m * 1e-3) / 1e9
+    flops = 2.0 * sum(S * n - S * (S - 1) // 2 for n in lens) * H * (DK + DV)
+    return {"rope_append": {"workload": "B=64, H=128: rotate q_pe/k_pe, append [c_kv | k_pe] to the paged cache",
+                            "ms": round(ms_r, 4), "GB_per_s": round(rope_bytes / (ms_r * 1e-3) / 1e9, 1)},
+            "multi_token_decode": {"workload": "decode B=64 H=128 lens U[4096,32768], 2 query tokens per request, "
+                                               "per-head sinks", "ms": round(ms_m, 4), "GB_per_s": round(gbs, 1),
+                                   "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+                                   "TFLOP_per_s": round(flops / (ms_m * 1e-3) / 1e12, 1)}}
+
+
 def cpu_baseline_sample(budget_s=20.0):
     """The oracle, as it stands, on a bounded sample of the prefill workload (host cores)."""
     import numpy as np
@@ -446,7 +527,8 @@ def run_libmla(args, world, rank, local):
 
     extra = {}
     if not args.no_extra:
-        for name, fn in (("decode", measure_decode), ("sparse", measure_sparse), ("split", measure_split)):
+        for name, fn in (("decode", measure_decode), ("sparse", measure_sparse), ("split", measure_split),
+                         ("absorb", measure_absorb), ("decode_step", measure_decode_step)):
             try:
                 extra[name] = fn(lib, dev, peaks)
                 torch.cuda.empty_cache()
@@ -470,6 +552,7 @@ def run_libmla(args, world, rank, local):
         "gpu_launches": launches,
         "clocks": clk,
         "decode": extra.get("decode"), "sparse": extra.get("sparse"), "split": extra.get("split"),
+        "absorb": extra.get("absorb"), "decode_step": extra.get("decode_step"),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_sample(args.cpu_budget)

@@ -157,8 +157,9 @@ mla_status run_bmm(bool lift, const void* a, int64_t a_st, int64_t a_sh, const v
               name, K);
   MLA_REQUIRE(o_sh >= N && o_st >= (int64_t)H * o_sh && o_sh % 8 == 0 && o_st % 8 == 0,
               "%s: output rows need head stride >= %d, token stride >= H x head stride, multiples of 8", name, N);
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, mo;
   mla_status s = map_head_rows(&ma, a, K, H, T, a_sh, a_st, "bmm rows");
+  if (s == MLA_OK) s = map_head_rows(&mo, out, N, H, T, o_sh, o_st, "bmm output rows");
   if (s != MLA_OK) return s;
   s = map2d(&mb, w, K, (uint64_t)H * N, K, lift ? 256 : 128, "bmm weights");
   if (s != MLA_OK) return s;
@@ -172,7 +173,7 @@ mla_status run_bmm(bool lift, const void* a, int64_t a_st, int64_t a_sh, const v
   p.err = ws_err(workspace);
   p.spin_limit = spin_limit();
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = lift ? launch_absorb_q(p, ma, mb, st) : launch_project_out(p, ma, mb, st);
+  cudaError_t e = lift ? launch_absorb_q(p, ma, mb, mo, st) : launch_project_out(p, ma, mb, mo, st);
   if (e != cudaSuccess) return cuda_fail(e, name);
   return ok();
 }

@@ -10,8 +10,9 @@
 // TMA stages (A: a 3-D box {64 columns, 1 head, 128 tokens} -> 128 rows x 128 B, SW128; B: a
 // 2-D box of kN weight rows), one thread issues M128 x kN x K16 MMAs (both operands from
 // shared memory) into a TMEM accumulator of kN columns, and the four warps read it back (one
-// token row per thread) and store bf16 rows.  kN <= 256 columns of TMEM and a ring of at most
-// ~100 KB keep two CTAs on an SM, so one CTA's epilogue overlaps the other's loads.
+// token row per thread) into bf16 rows staged in shared memory, which TMA stores write out.
+// kN <= 256 columns of TMEM and a ring of at most ~100 KB keep two CTAs on an SM, so one CTA's
+// epilogue overlaps the other's loads.
 #include "mla_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -33,7 +34,7 @@ struct BmmBars {
 template <int kN, int kK, int kStages>
 __global__ void __launch_bounds__(128, 2)
     absorb_bmm_kernel(const __grid_constant__ BmmParams p, const __grid_constant__ CUtensorMap ma,
-                      const __grid_constant__ CUtensorMap mb) {
+                      const __grid_constant__ CUtensorMap mb, const __grid_constant__ CUtensorMap mo) {
   constexpr int kBBytes = kN * 128;
   constexpr int kStageBytes = kABytes + kBBytes;
   constexpr int kChunks = kK / kChunk;
@@ -112,27 +113,37 @@ __global__ void __launch_bounds__(128, 2)
   }
   __syncwarp();
 
-  // ---- epilogue: token row (warp * 32 + lane) of the tile, kN columns -> bf16 ----
+  // ---- epilogue: token row (warp * 32 + lane) of the tile, kN columns -> bf16 rows staged in the
+  // (now idle) ring as 64-column SW128 boxes, then TMA stores (rows past T are clipped) ----
+  bool stored = false;
   if (wait1(&bars.done, 0, B_DONE)) {
     tc_fence_after();
-    const int t = t0 + warp * 32 + lane;
+    const int r = warp * 32 + lane;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    __nv_bfloat16* orow = p.out + (int64_t)t * p.out_stride_t + (int64_t)h * p.out_stride_h + n0;
 #pragma unroll 1
     for (int c0 = 0; c0 < kN; c0 += 32) {
       uint32_t v[32];
       tmem_ld32(tbase + lane_base + c0, v);
       tmem_wait_ld();
-      if (t < p.T) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+      uint8_t* line = smem + (c0 >> 6) * kABytes + r * 128;
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          dst[q] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
-                              pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
-                              pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
-                              pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+      for (int q = 0; q < 4; ++q) {
+        const int chunk = ((c0 & 63) >> 3) + q;
+        *reinterpret_cast<uint4*>(line + ((chunk ^ (r & 7)) << 4)) =
+            make_uint4(pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                       pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                       pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                       pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
       }
     }
+    fence_proxy_async_smem();  // the TMA stores read the staged rows through the async proxy
+    stored = true;
+  }
+  __syncthreads();
+  if (stored && threadIdx.x == 0) {
+    for (int c = 0; c < kN / 64; ++c) tma_store_3d(&mo, n0 + 64 * c, h, t0, smem_u32(smem + c * kABytes));
+    bulk_commit();
+    bulk_wait_all();
   }
 
   // ---- teardown: on abort, let this thread's MMAs and TMA loads land first ----
@@ -155,7 +166,9 @@ constexpr int bmm_smem() {
 }
 
 template <int kN, int kK, int kStages>
-cudaError_t launch_bmm(const BmmParams& p, const CUtensorMap& ma, const CUtensorMap& mb, cudaStream_t stream) {
+cudaError_t launch_bmm(const BmmParams& p, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
+                       cudaStream_t stream) {
+  static_assert(kStages * (kABytes + kN * 128) >= (kN / 64) * kABytes, "the ring holds the staged output tile");
   constexpr int smem = bmm_smem<kN, kK, kStages>();
   static_assert(2 * smem <= 232448, "two CTAs per SM");
   static PerDeviceOnce attrs;
@@ -165,7 +178,7 @@ cudaError_t launch_bmm(const BmmParams& p, const CUtensorMap& ma, const CUtensor
   });
   if (e != cudaSuccess) return e;
   const dim3 grid((p.T + kRowsM - 1) / kRowsM, p.H, p.N / kN);
-  absorb_bmm_kernel<kN, kK, kStages><<<grid, 128, smem, stream>>>(p, ma, mb);
+  absorb_bmm_kernel<kN, kK, kStages><<<grid, 128, smem, stream>>>(p, ma, mb, mo);
   return cudaGetLastError();
 }
 
@@ -173,14 +186,15 @@ cudaError_t launch_bmm(const BmmParams& p, const CUtensorMap& ma, const CUtensor
 
 // q_lift: K = 128 (q_nope), N = 512 in two CTAs of 256 columns; project_out: K = 512 (latent),
 // N = 128.
-cudaError_t launch_absorb_q(const BmmParams& p, const CUtensorMap& ma, const CUtensorMap& mb, cudaStream_t stream) {
+cudaError_t launch_absorb_q(const BmmParams& p, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
+                            cudaStream_t stream) {
   if (p.T <= 0) return cudaSuccess;
-  return launch_bmm<256, 128, 2>(p, ma, mb, stream);
+  return launch_bmm<256, 128, 2>(p, ma, mb, mo, stream);
 }
-cudaError_t launch_project_out(const BmmParams& p, const CUtensorMap& ma, const CUtensorMap& mb,
+cudaError_t launch_project_out(const BmmParams& p, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
                                cudaStream_t stream) {
   if (p.T <= 0) return cudaSuccess;
-  return launch_bmm<128, 512, 3>(p, ma, mb, stream);
+  return launch_bmm<128, 512, 3>(p, ma, mb, mo, stream);
 }
 
 }  // namespace mla

@@ -166,8 +166,10 @@ struct BmmParams {
   uint32_t spin_limit;
 };
 // A map: 3-D {K, H, T} box {64, 1, 128}; B map: 2-D {K, H * N} box {64, 256 (q_lift) / 128 (output)}
-cudaError_t launch_absorb_q(const BmmParams& p, const CUtensorMap& ma, const CUtensorMap& mb, cudaStream_t stream);
-cudaError_t launch_project_out(const BmmParams& p, const CUtensorMap& ma, const CUtensorMap& mb,
+// (output map: 3-D {N, H, T} with the output strides, box {64, 1, 128})
+cudaError_t launch_absorb_q(const BmmParams& p, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
+                            cudaStream_t stream);
+cudaError_t launch_project_out(const BmmParams& p, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
                                cudaStream_t stream);
 
 // kernels' host launchers (return cudaError_t of the launch)
