@@ -251,18 +251,18 @@ static __device__ __noinline__ void gather_half(uint32_t dst, uint32_t box_strid
     for (int i = 0; i < nbox; ++i) tma_gather4(dst + i * box_stride + lane * 512, row_map, x0 + i * kBoxCols, a0, a1, a2, a3, bar);
 }
 
-// Issues the 64-row boxes of one tile half [kh, kh + 64): nbox column blocks starting at
-// column x0, landing box_stride bytes apart from dst.  A half inside one valid page is one
-// tiled box per column block, issued by lane 0.  Warp-uniform.
+// Issues the 64-row boxes of one tile half [kh, kh + 64): nbox (<= 32) column blocks starting
+// at column x0, landing box_stride bytes apart from dst.  A half inside one valid page is one
+// tiled box per column block, lane i issuing block i.  Warp-uniform.
 __device__ __forceinline__ void issue_half(uint32_t dst, uint32_t box_stride, int32_t x0, int nbox, const CoreParams& p,
                                            const CoreMaps& maps, int len, int64_t kh, const HalfIds& ids,
                                            uint64_t* bar, uint32_t* err) {
   const int32_t pg0 = __shfl_sync(0xffffffffu, ids.pe, 0);  // page of key kh
   if (p.page_size % 64 == 0 && kh + 64 <= len && pg0 >= 0 && pg0 < p.num_pages) {
-    if ((threadIdx.x & 31) == 0) {
+    const int lane = threadIdx.x & 31;  // one box per lane: lanes overlap their TMA issues
+    if (lane < nbox) {
       const int32_t y = (int32_t)(pg0 * (int64_t)p.page_size + kh % p.page_size);
-#pragma unroll 1
-      for (int i = 0; i < nbox; ++i) tma_load_2d(dst + i * box_stride, &maps.kv, x0 + i * kBoxCols, y, bar);
+      tma_load_2d(dst + lane * box_stride, &maps.kv, x0 + lane * kBoxCols, y, bar);
     }
   } else {
     gather_half(dst, box_stride, x0, nbox, &maps.row, p.page_size, p.num_pages, len, kh, ids.pe, ids.po, bar, err);
@@ -479,10 +479,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
           drain_bar = fb;
           drain_par = (t >> 1) & 1;
           __syncwarp();
-          if constexpr (!decode) {
-            if (lane == 0)
-              for (int i = 0; i < 3; ++i)
-                tma_load_2d(dst + i * kBoxBytesK, &map_v, (3 * k + i) * kBoxCols, j * kKeysT + 64 * h, fb);
+          if constexpr (!decode) {  // one box per lane: lanes overlap their TMA issues
+            if (lane < 3) tma_load_2d(dst + lane * kBoxBytesK, &map_v, (3 * k + lane) * kBoxCols, j * kKeysT + 64 * h, fb);
           } else {
             issue_half(dst, kBoxBytesK, 3 * k * kBoxCols, 3, p, maps, len, kh, cur, fb, err);
           }
@@ -798,10 +796,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
           drain_bar = &bars.vfull[h];
           drain_par = m & 1;
           __syncwarp();
-          if constexpr (!decode) {
-            if (lane == 0)
-              for (int bx = 0; bx < kVBoxes; ++bx)
-                tma_load_2d(dst + bx * kBoxBytesV, &map_v, bx * kBoxCols, j * kKeysT + 64 * h, &bars.vfull[h]);
+          if constexpr (!decode) {  // one box per lane
+            if (lane < kVBoxes)
+              tma_load_2d(dst + lane * kBoxBytesV, &map_v, lane * kBoxCols, j * kKeysT + 64 * h, &bars.vfull[h]);
           } else {
             issue_half(dst, kBoxBytesV, 0, kVBoxes, p, maps, len, kh, cur, &bars.vfull[h], err);
           }
@@ -810,17 +807,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
         // the slot then stages the epilogue rows 64 h .. 64 h + 63 (with prev)
         if (staged && it.J > 0 && live) {
           if (!waitb(&bars.vempty[h], (m & 1) ^ 1, X_V_EMPTY, false)) { live = false; break; }
-          if (lane == 0) {
-            const int64_t row0 = (int64_t)it.id * kRows + h * 64;
-            if (p.prev_out && row0 < (int64_t)p.T * p.H) {
-              mbar_arrive_expect_tx(&bars.vfull[h], kHalfBytesV);
-              drain_bar = &bars.vfull[h];
-              drain_par = m & 1;
-              for (int bx = 0; bx < kVBoxes; ++bx)
-                tma_load_2d(dst + bx * kBoxBytesV, &maps.prev, bx * kBoxCols, (int32_t)row0, &bars.vfull[h]);
-            } else {
-              mbar_arrive(&bars.vfull[h]);
-            }
+          const int64_t row0 = (int64_t)it.id * kRows + h * 64;
+          if (p.prev_out && row0 < (int64_t)p.T * p.H) {
+            if (lane == 0) mbar_arrive_expect_tx(&bars.vfull[h], kHalfBytesV);
+            __syncwarp();
+            if (lane < kVBoxes)
+              tma_load_2d(dst + lane * kBoxBytesV, &maps.prev, lane * kBoxCols, (int32_t)row0, &bars.vfull[h]);
+            drain_bar = &bars.vfull[h];
+            drain_par = m & 1;
+          } else if (lane == 0) {
+            mbar_arrive(&bars.vfull[h]);
           }
           __syncwarp();
           ++m;

@@ -75,10 +75,13 @@ __device__ __forceinline__ int keys_for_query(const SplitParams& p, int ql, int 
 
 __device__ __forceinline__ TileInfo tile_info(const SplitParams& p, int block) {
   TileInfo t;
-  // longest tiles first: walk the global tile list backwards
+  // Head-major: the CTAs running at one time work on one or a few heads, so those heads' K/V
+  // stay in L2 while every query tile of the head reads them (head-minor order had ~150 heads'
+  // K/V in flight at once and re-read them from HBM for every query tile).  Within a head the
+  // tiles go longest first.
   const int per_head = p.total_q_tiles;
-  const int gt = per_head - 1 - block / p.H;
-  t.h = block % p.H;
+  const int gt = per_head - 1 - block % per_head;
+  t.h = block / per_head;
   t.hk = t.h / (p.H / p.Hkv);
   int s = 0;
   while (s + 1 < p.batch && p.tile_off[s + 1] <= gt) ++s;
@@ -153,25 +156,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_bar = &bars.q_full;
       drain_par = 0;
     }
-    if (lane == 0 && ti.J > 0) {
+    if (ti.J > 0) {
       const uint32_t sq = smem_u32(smem + kOffQ);
-      mbar_arrive_expect_tx(&bars.q_full, kQBytes);
-      tma_load_3d(sq, &mq_nope, 0, ti.h, qz, &bars.q_full);
-      tma_load_3d(sq + kBox, &mq_nope, 64, ti.h, qz, &bars.q_full);
-      tma_load_3d(sq + 2 * kBox, &mq_pe, 0, ti.h, qz, &bars.q_full);
+      if (lane == 0) mbar_arrive_expect_tx(&bars.q_full, kQBytes);
+      __syncwarp();
+      if (lane < 3) tma_load_3d(sq + lane * kBox, lane < 2 ? &mq_nope : &mq_pe, lane == 1 ? 64 : 0, ti.h, qz, &bars.q_full);
     }
     for (int j = 0; j < ti.J; ++j) {
       const int s = j % kStages;
       if (!waitb(&bars.kv_empty[s], ((j / kStages) & 1) ^ 1, W_KVEMPTY)) break;
-      if (lane == 0) {
-        const uint32_t st = smem_u32(smem + kOffStage + s * kStageBytes);
-        const int kz = ti.kv0 + j * kTile;
-        mbar_arrive_expect_tx(&bars.kv_full[s], kStageBytes);
-        tma_load_3d(st, &mk_nope, 0, ti.hk, kz, &bars.kv_full[s]);
-        tma_load_3d(st + kBox, &mk_nope, 64, ti.hk, kz, &bars.kv_full[s]);
-        tma_load_3d(st + 2 * kBox, &mk_pe, 0, ti.hk, kz, &bars.kv_full[s]);
-        tma_load_3d(st + kKBytes, &mv, 0, ti.hk, kz, &bars.kv_full[s]);
-        tma_load_3d(st + kKBytes + kBox, &mv, 64, ti.hk, kz, &bars.kv_full[s]);
+      // the stage's five boxes go out from five lanes at once: one thread issues a TMA box only
+      // every few hundred cycles, lanes of a warp overlap theirs
+      const uint32_t st = smem_u32(smem + kOffStage + s * kStageBytes);
+      const int kz = ti.kv0 + j * kTile;
+      if (lane == 0) mbar_arrive_expect_tx(&bars.kv_full[s], kStageBytes);
+      __syncwarp();
+      if (lane < 5) {
+        const CUtensorMap* m = lane < 2 ? &mk_nope : (lane == 2 ? &mk_pe : &mv);
+        const int x = (lane == 1 || lane == 4) ? 64 : 0;
+        const uint32_t dst = st + (lane < 3 ? lane * kBox : kKBytes + (lane - 3) * kBox);
+        tma_load_3d(dst, m, x, ti.hk, kz, &bars.kv_full[s]);
       }
       drain_bar = &bars.kv_full[s];
       drain_par = (j / kStages) & 1;
