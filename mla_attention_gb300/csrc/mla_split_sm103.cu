@@ -46,7 +46,8 @@ constexpr float kRescaleLog2 = 8.0f;
 
 struct Bars {
   uint64_t q_full;
-  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t k_full[kStages], k_empty[kStages];  // K part of stage s (freed by the S MMA)
+  uint64_t v_full[kStages], v_empty[kStages];  // V part of stage s (freed by the P V MMA)
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t pv_done[2];  // pv_done[b]: the P V that read P from S buffer b is complete
@@ -113,8 +114,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     mbar_init(&bars.q_full, 1);
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&bars.kv_full[i], 1);
-      mbar_init(&bars.kv_empty[i], 1);
+      mbar_init(&bars.k_full[i], 1);
+      mbar_init(&bars.k_empty[i], 1);
+      mbar_init(&bars.v_full[i], 1);
+      mbar_init(&bars.v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.s_full[i], 1);
@@ -162,24 +165,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane < 3) tma_load_3d(sq + lane * kBox, lane < 2 ? &mq_nope : &mq_pe, lane == 1 ? 64 : 0, ti.h, qz, &bars.q_full);
     }
-    for (int j = 0; j < ti.J; ++j) {
+    // K of a stage goes back to the producer once its S MMA is done, V once its P V MMA is done,
+    // so K runs one tile ahead of V.  The boxes of a part go out from separate lanes at once: one
+    // thread issues a TMA box only every few hundred cycles, lanes of a warp overlap theirs.
+    auto load_k = [&](int j) -> bool {
       const int s = j % kStages;
-      if (!waitb(&bars.kv_empty[s], ((j / kStages) & 1) ^ 1, W_KVEMPTY)) break;
-      // the stage's five boxes go out from five lanes at once: one thread issues a TMA box only
-      // every few hundred cycles, lanes of a warp overlap theirs
+      if (!waitb(&bars.k_empty[s], ((j / kStages) & 1) ^ 1, W_KVEMPTY)) return false;
       const uint32_t st = smem_u32(smem + kOffStage + s * kStageBytes);
-      const int kz = ti.kv0 + j * kTile;
-      if (lane == 0) mbar_arrive_expect_tx(&bars.kv_full[s], kStageBytes);
+      if (lane == 0) mbar_arrive_expect_tx(&bars.k_full[s], kKBytes);
       __syncwarp();
-      if (lane < 5) {
-        const CUtensorMap* m = lane < 2 ? &mk_nope : (lane == 2 ? &mk_pe : &mv);
-        const int x = (lane == 1 || lane == 4) ? 64 : 0;
-        const uint32_t dst = st + (lane < 3 ? lane * kBox : kKBytes + (lane - 3) * kBox);
-        tma_load_3d(dst, m, x, ti.hk, kz, &bars.kv_full[s]);
-      }
-      drain_bar = &bars.kv_full[s];
+      if (lane < 3) tma_load_3d(st + lane * kBox, lane < 2 ? &mk_nope : &mk_pe, lane == 1 ? 64 : 0, ti.hk,
+                                ti.kv0 + j * kTile, &bars.k_full[s]);
+      drain_bar = &bars.k_full[s];
       drain_par = (j / kStages) & 1;
       __syncwarp();
+      return true;
+    };
+    auto load_v = [&](int j) -> bool {
+      const int s = j % kStages;
+      if (!waitb(&bars.v_empty[s], ((j / kStages) & 1) ^ 1, W_KVEMPTY)) return false;
+      const uint32_t st = smem_u32(smem + kOffStage + s * kStageBytes + kKBytes);
+      if (lane == 0) mbar_arrive_expect_tx(&bars.v_full[s], kVBytes);
+      __syncwarp();
+      if (lane < 2) tma_load_3d(st + lane * kBox, &mv, 64 * lane, ti.hk, ti.kv0 + j * kTile, &bars.v_full[s]);
+      drain_bar = &bars.v_full[s];
+      drain_par = (j / kStages) & 1;
+      __syncwarp();
+      return true;
+    };
+    bool ok = ti.J == 0 || load_k(0);
+    for (int j = 0; ok && j < ti.J; ++j) {
+      if (j + 1 < ti.J && !load_k(j + 1)) break;
+      ok = load_v(j);
     }
   } else if (warp == 5) {
     // ---------------- MMA issuer ----------------
@@ -188,12 +205,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sq = smem_u32(smem + kOffQ);
     auto issue_s = [&](int j) -> bool {
       const int s = j % kStages;
-      if (!waitb(&bars.kv_full[s], (j / kStages) & 1, W_KVFULL)) return false;
+      if (!waitb(&bars.k_full[s], (j / kStages) & 1, W_KVFULL)) return false;
       tc_fence_after();
       if (lane == 0) {
         const uint32_t st = smem_u32(smem + kOffStage + s * kStageBytes);
         mma_s_k192_n128(tbase + kTmemS + (j & 1) * kTile, sdesc_sw128(sq, 16, 1024), sdesc_sw128(st, 16, 1024),
                         idesc_s);
+        mma_commit(&bars.k_empty[s]);
         mma_commit(&bars.s_full[j & 1]);
       }
       __syncwarp();
@@ -204,13 +222,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; live && j < ti.J; ++j) {
       if (j + 1 < ti.J && !issue_s(j + 1)) break;
       if (!waitb(&bars.p_full[j & 1], (j >> 1) & 1, W_PFULL)) break;
+      if (!waitb(&bars.v_full[j % kStages], (j / kStages) & 1, W_KVFULL)) break;
       tc_fence_after();
       if (lane == 0) {
         const int s = j % kStages;
         const uint32_t vst = smem_u32(smem + kOffStage + s * kStageBytes + kKBytes);
         mma_pv_tmem_k128_n128(tbase + kTmemO, tbase + kTmemS + (j & 1) * kTile, sdesc_sw128(vst, kBox, 1024), idesc_o,
                               j > 0 ? 1u : 0u);
-        mma_commit(&bars.kv_empty[s]);
+        mma_commit(&bars.v_empty[s]);
         mma_commit(&bars.pv_done[j & 1]);
       }
       __syncwarp();
