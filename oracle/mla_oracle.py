@@ -311,6 +311,14 @@ def mla_decode_ex(q, cache, block_table, lens, scale: float, sinks=None, dv: int
     return out, lse
 
 
+def mla_decode_fp8(q, cache_e4m3, kv_scale: float, block_table, lens, scale: float, sinks=None, dv: int = 512):
+    """Decode over an FP8 (e4m3) latent cache with one per-tensor scale (TensorRT-LLM "mla.py":
+    FP8 KV cache, use_fp8_mla, with the cache's scale applied to both BMMs, mla_bmm1_scale and
+    mla_bmm2_scale): every cache value stands for e4m3_value * kv_scale.  cache_e4m3 holds the
+    e4m3 values (decoded exactly); q as in mla_decode_ex ([B, s, H, dk])."""
+    return mla_decode_ex(q, _f64(cache_e4m3) * float(kv_scale), block_table, lens, scale, sinks=sinks, dv=dv)
+
+
 # ---------------------------------------------------------------------------
 # top-k sparse latent + RoPE attention
 # ---------------------------------------------------------------------------
@@ -431,6 +439,6 @@ def causal_pairs(T: int, Tkv: int, q_pos0: int, kv_pos0: int, kv_valid: Optional
 
 __all__ = [
     "attend", "attend_masked", "merge", "prefill_key_set", "mla_prefill", "mla_prefill_split",
-    "gather_pages", "mla_decode", "mla_decode_ex", "mla_sparse", "rope", "mla_rope_append", "absorb_q", "project_out",
+    "gather_pages", "mla_decode", "mla_decode_ex", "mla_decode_fp8", "mla_sparse", "rope", "mla_rope_append", "absorb_q", "project_out",
     "attention_flops", "causal_pairs", "NEG_INF",
 ]

@@ -65,6 +65,8 @@ MUTANTS = {
     "multi-token decode: every token sees all keys": ("n = max(0, int(ln[b]) - S + 1 + i)", "n = int(ln[b])"),
     "multi-token decode: token order reversed": ("n = max(0, int(ln[b]) - S + 1 + i)",
                                                   "n = max(0, int(ln[b]) - i)"),
+    "fp8 cache scale dropped": ("return mla_decode_ex(q, _f64(cache_e4m3) * float(kv_scale), block_table,",
+                                "return mla_decode_ex(q, _f64(cache_e4m3), block_table,"),
     "sink weight ignored": ("out, lse = merge(out, lse, np.zeros_like(out), np.broadcast_to(sk, lse.shape))",
                             "pass"),
     "project_out with the head's weight of the next head": (

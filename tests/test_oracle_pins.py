@@ -460,6 +460,23 @@ def check_decode_ex():
     assert (o[0, 0] == 0).all() and l_[0, 0, 0] == 0.7
 
 
+def check_decode_fp8():
+    """An e4m3 cache stands for its values times kv_scale: the same keys/values given in fp64 (scaled)
+    give the same result; doubling kv_scale doubles every score and every output value."""
+    D = _small_decode()
+    rng = np.random.default_rng(33)
+    c8 = torch.from_numpy(D["cache"] / 3.0).to(torch.float8_e4m3fn)
+    vals = c8.double().numpy()
+    q = rng.standard_normal((D["q"].shape[0], 2, D["q"].shape[1], D["q"].shape[2]))
+    out, lse = mo.mla_decode_fp8(q, c8, 3.0, D["bt"], D["lens"], 0.2)
+    ro, rl = mo.mla_decode_ex(q, vals * 3.0, D["bt"], D["lens"], 0.2)
+    np.testing.assert_allclose(out, ro, atol=1e-12)
+    np.testing.assert_allclose(lse, rl, atol=1e-12)
+    o2, l2 = mo.mla_decode_fp8(q, c8, 6.0, D["bt"], D["lens"], 0.1)   # scores unchanged, values doubled
+    np.testing.assert_allclose(o2, 2.0 * out, atol=1e-12)
+    np.testing.assert_allclose(l2, lse, atol=1e-12)
+
+
 def check_flop_count():
     # causal T = Tkv = n: n(n+1)/2 pairs
     assert mo.causal_pairs(256, 256, 0, 0) == 256 * 257 // 2
@@ -474,7 +491,7 @@ ALL_CHECKS = [
     check_closed_forms_prefill, check_rope_columns_count, check_chunk_merge_equals_one_pass,
     check_invariances, check_sparse_full_prefix_equals_dense, check_decode_equals_prefill_last_row,
     check_split_equals_library_sdpa, check_split_lse_brute, check_absorbed_equals_non_absorbed,
-    check_flop_count, check_rope_golden, check_rope_properties, check_rope_append, check_decode_ex,
+    check_flop_count, check_rope_golden, check_rope_properties, check_rope_append, check_decode_ex, check_decode_fp8,
 ]
 
 
