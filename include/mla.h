@@ -226,6 +226,23 @@ mla_status mla_decode_ex(const void* q, int q_per_req, const void* kv_cache, int
                          size_t workspace_bytes, void* stream);
 
 /*
+ * Decode over an FP8 latent cache.  Defined by: TensorRT-LLM "mla.py" (FP8 KV cache: use_fp8_mla
+ * with mla_bmm1_scale / mla_bmm2_scale, the cache's scale applied to the QK and PV products).
+ * kv_cache_e4m3 holds e4m3 values (one byte each, [num_pages, page_size, 576] contiguous); every
+ * value stands for e4m3_value * kv_scale (one per-tensor scale, > 0).  Arguments otherwise as
+ * mla_decode_ex (q bf16 [B, q_per_req, H, 576], sinks, out, lse).  The kernel converts the cache
+ * rows to f16 (exactly) on the way into shared memory, runs both products on the tensor cores with
+ * f16 operands (q is rounded to f16: |q| must stay below 65504) and fp32 accumulation; the cache
+ * traffic is half that of the bf16 cache.  Always runs the 128-key tile engine.
+ * workspace_bytes >= mla_decode_fp8_workspace_size(B, q_per_req, H, num_splits).
+ */
+size_t mla_decode_fp8_workspace_size(int B, int q_per_req, int H, int num_splits);
+mla_status mla_decode_fp8(const void* q, int q_per_req, const void* kv_cache_e4m3, float kv_scale, int64_t num_pages,
+                          int page_size, const int32_t* block_table, int max_pages, const int32_t* lens, int B, int H,
+                          float scale, const float* sinks, int num_splits, void* out, float* lse, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/*
  * mla_decode without a workspace, for callers that cannot allocate device
  * memory (the pages have no counterpart of this call): plug-ins handed only
  * their input and output buffers by a framework that owns every device

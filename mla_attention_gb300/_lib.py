@@ -56,6 +56,9 @@ _SIGNATURES = {
     "mla_decode_ex_workspace_size": ([c_int, c_int, c_int, c_int], c_size_t),
     "mla_decode_ex": ([c_void_p, c_int, c_void_p, c_int64, c_int, c_void_p, c_int, c_void_p, c_int, c_int, c_float,
                        c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p], c_int),
+    "mla_decode_fp8_workspace_size": ([c_int, c_int, c_int, c_int], c_size_t),
+    "mla_decode_fp8": ([c_void_p, c_int, c_void_p, c_float, c_int64, c_int, c_void_p, c_int, c_void_p, c_int, c_int,
+                        c_float, c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p], c_int),
     "mla_decode_noalloc": ([c_void_p, c_void_p, c_int64, c_int, c_void_p, c_int, c_void_p, c_int, c_int, c_float,
                             c_int, c_void_p, c_void_p, c_void_p], c_int),
     "mla_sparse_workspace_size": ([c_int, c_int], c_size_t),
@@ -326,6 +329,44 @@ def mla_decode_ex(q, kv_cache, block_table, lens, scale: float, sinks=None, num_
                             _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
     _check(s)
     return out, lse
+
+
+def mla_decode_fp8(q, kv_cache_e4m3, kv_scale: float, block_table, lens, scale: float, sinks=None,
+                   num_splits: int = 0, out=None, lse=None, ws=None, stream=None):
+    """Decode over an e4m3 latent cache (torch.float8_e4m3fn [pages,page,576]; value = e4m3 x kv_scale).
+    q bf16 [B,H,576] or [B,s,H,576].  Returns out, lse shaped like mla_decode / mla_decode_ex."""
+    single = q.dim() == 3
+    q4 = q.unsqueeze(1) if single else q
+    _need(q4, "q", torch.bfloat16)
+    if q4.dim() != 4 or q4.shape[3] != 576:
+        raise MLAError(1, "q must be [B, H, 576] or [B, q_per_req, H, 576]")
+    B, S, H, _ = q4.shape
+    dev = q4.device
+    if kv_cache_e4m3.dtype not in (torch.float8_e4m3fn, torch.uint8):
+        raise MLAError(1, "kv_cache_e4m3 must be torch.float8_e4m3fn (or its bytes as uint8)")
+    _need(kv_cache_e4m3, "kv_cache_e4m3", kv_cache_e4m3.dtype, dev)
+    if kv_cache_e4m3.dim() != 3 or kv_cache_e4m3.shape[2] != 576 or block_table.dim() != 2:
+        raise MLAError(1, "kv_cache_e4m3 [pages,page,576], block_table [B,max_pages] expected")
+    _need(block_table, "block_table", torch.int32, dev)
+    _need(lens, "lens", torch.int32, dev, shape=(B,))
+    if sinks is not None:
+        _need(sinks, "sinks", torch.float32, dev, shape=(H,))
+    num_pages, page_size, _ = kv_cache_e4m3.shape
+    if out is None:
+        out = torch.empty((B, S, H, 512), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, S, H), dtype=torch.float32, device=dev)
+    o4 = out.unsqueeze(1) if (single and out.dim() == 3) else out
+    l3 = lse.unsqueeze(1) if (single and lse.dim() == 2) else lse
+    _need(o4, "out", torch.bfloat16, dev, shape=(B, S, H, 512))
+    _need(l3, "lse", torch.float32, dev, shape=(B, S, H))
+    nbytes = lib().mla_decode_fp8_workspace_size(B, S, H, int(num_splits))
+    ws = workspace(nbytes, dev) if ws is None else ws
+    s = lib().mla_decode_fp8(_ptr(q4), S, _ptr(kv_cache_e4m3), float(kv_scale), num_pages, page_size,
+                             _ptr(block_table), block_table.shape[1], _ptr(lens), B, H, float(scale), _ptr(sinks),
+                             int(num_splits), _ptr(o4), _ptr(l3), _ptr(ws), ws.numel(), _stream(stream))
+    _check(s)
+    return (o4[:, 0], l3[:, 0]) if single else (o4, l3)
 
 
 def mla_decode_noalloc(q, kv_cache, block_table, lens, scale: float, num_splits: int = 0, out=None, lse=None,

@@ -251,6 +251,75 @@ mla_status prefill_one(const void* q, int64_t q_stride_t, int64_t q_stride_h, co
 }
 }  // namespace
 
+namespace {
+mla_status decode_impl(const void* q, int q_per_req, const void* kv_cache, bool fp8, float kv_scale, int64_t num_pages,
+                       int page_size, const int32_t* block_table, int max_pages, const int32_t* lens, int B, int H,
+                       float scale, const float* sinks, int num_splits, void* out, float* lse, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  MLA_REQUIRE(B >= 0 && H >= 1 && num_pages >= 0 && max_pages >= 0 && num_splits >= 0,
+              "mla_decode: need B >= 0, H >= 1, num_pages >= 0, max_pages >= 0, num_splits >= 0");
+  MLA_REQUIRE(q_per_req >= 1 && (int64_t)B * q_per_req <= (int64_t)1 << 24,
+              "mla_decode: q_per_req >= 1 and B * q_per_req <= 2^24 (got %d, %d)", q_per_req, B);
+  const int G = B * q_per_req;  // query groups: one query token of one request each
+  if (H > kRows) return fail(MLA_ERR_UNSUPPORTED, "mla_decode: H <= 128 (got %d)", H);
+  MLA_REQUIRE(page_size == 16 || page_size == 32 || (page_size > 0 && page_size % 64 == 0),
+              "mla_decode: page_size must be 16, 32 or a multiple of 64 (got %d)", page_size);
+  MLA_REQUIRE(std::isfinite(scale), "mla_decode: scale must be finite");
+  const size_t need = mla_decode_workspace_size(G, H, num_splits);
+  if (!workspace || workspace_bytes < need)
+    return fail(MLA_ERR_WORKSPACE, "mla_decode: workspace must hold %zu bytes", need);
+  if (B == 0) return ok();
+  MLA_REQUIRE(q && kv_cache && block_table && lens && out, "mla_decode: q, kv_cache, block_table, lens, out required");
+  MLA_REQUIRE(aligned16(q) && aligned16(kv_cache) && aligned16(out), "mla_decode: q, kv_cache, out 16-byte aligned");
+  MLA_REQUIRE(num_pages >= 1 && max_pages >= 1, "mla_decode: need at least one page");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  CoreMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  const uint64_t rows = (uint64_t)num_pages * (uint64_t)page_size;
+  if (!fp8) {  // FP8 decode reads the cache with ordinary loads
+    mla_status s = map2d(&maps.kv, kv_cache, kDk, rows, kDk, page_size >= kKeys ? kKeys : (uint32_t)page_size, "cache");
+    if (s != MLA_OK) return s;
+    s = map2d(&maps.row, kv_cache, kDk, rows, kDk, 1, "cache rows");
+    if (s != MLA_OK) return s;
+    maps.pe = maps.row;
+  }
+  CoreParams p;
+  memset(&p, 0, sizeof(p));
+  p.mode = MODE_DECODE;
+  p.num_pairs = num_splits > 0 ? num_splits : default_pairs();
+  p.scale_log2 = scale * (fp8 ? kv_scale : 1.f) * 1.4426950408889634f;  // FP8: scores of e4m3 units
+  p.spin_limit = spin_limit();
+  p.debug_stall = debug_stall();
+  p.err = ws_err(workspace);
+  p.q = reinterpret_cast<const __nv_bfloat16*>(q);
+  p.H = H;
+  p.block_table = block_table;
+  p.lens = lens;
+  p.B = G;
+  p.q_per_req = q_per_req;
+  p.sinks = sinks;
+  p.max_pages = max_pages;
+  p.page_size = page_size;
+  p.num_pages = num_pages;
+  p.cache = fp8 ? nullptr : reinterpret_cast<const __nv_bfloat16*>(kv_cache);
+  p.cache8 = fp8 ? reinterpret_cast<const uint8_t*>(kv_cache) : nullptr;
+  p.kv_scale = kv_scale;
+  char* w = reinterpret_cast<char*>(workspace) + kWsHeader;
+  const size_t slots = (size_t)G + (size_t)p.num_pairs;
+  p.tile_prefix = reinterpret_cast<int32_t*>(w);
+  w += align_up(sizeof(int32_t) * ((size_t)G + 1), 256);
+  p.part_lse = reinterpret_cast<float*>(w);
+  w += align_up(sizeof(float) * slots * (size_t)H, 256);
+  p.part_o = reinterpret_cast<float*>(w);
+  // FP8 runs on the 128-key engine only
+  cudaError_t e = (fp8 || g_decode_keys.load() == 128) ? launch_prefill128(p, maps, st) : launch_core(p, maps, st);
+  if (e != cudaSuccess) return cuda_fail(e, "mla_decode launch");
+  e = launch_decode_reduce(p, reinterpret_cast<__nv_bfloat16*>(out), lse, st);
+  if (e != cudaSuccess) return cuda_fail(e, "mla_decode reduce launch");
+  return ok();
+}
+}  // namespace
+
 extern "C" {
 
 int mla_version(void) { return 100; }
@@ -374,63 +443,23 @@ mla_status mla_decode_ex(const void* q, int q_per_req, const void* kv_cache, int
                          const int32_t* block_table, int max_pages, const int32_t* lens, int B, int H, float scale,
                          const float* sinks, int num_splits, void* out, float* lse, void* workspace,
                          size_t workspace_bytes, void* stream) {
-  MLA_REQUIRE(B >= 0 && H >= 1 && num_pages >= 0 && max_pages >= 0 && num_splits >= 0,
-              "mla_decode: need B >= 0, H >= 1, num_pages >= 0, max_pages >= 0, num_splits >= 0");
-  MLA_REQUIRE(q_per_req >= 1 && (int64_t)B * q_per_req <= (int64_t)1 << 24,
-              "mla_decode: q_per_req >= 1 and B * q_per_req <= 2^24 (got %d, %d)", q_per_req, B);
-  const int G = B * q_per_req;  // query groups: one query token of one request each
-  if (H > kRows) return fail(MLA_ERR_UNSUPPORTED, "mla_decode: H <= 128 (got %d)", H);
-  MLA_REQUIRE(page_size == 16 || page_size == 32 || (page_size > 0 && page_size % 64 == 0),
-              "mla_decode: page_size must be 16, 32 or a multiple of 64 (got %d)", page_size);
-  MLA_REQUIRE(std::isfinite(scale), "mla_decode: scale must be finite");
-  const size_t need = mla_decode_workspace_size(G, H, num_splits);
-  if (!workspace || workspace_bytes < need)
-    return fail(MLA_ERR_WORKSPACE, "mla_decode: workspace must hold %zu bytes", need);
-  if (B == 0) return ok();
-  MLA_REQUIRE(q && kv_cache && block_table && lens && out, "mla_decode: q, kv_cache, block_table, lens, out required");
-  MLA_REQUIRE(aligned16(q) && aligned16(kv_cache) && aligned16(out), "mla_decode: q, kv_cache, out 16-byte aligned");
-  MLA_REQUIRE(num_pages >= 1 && max_pages >= 1, "mla_decode: need at least one page");
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  CoreMaps maps;
-  memset(&maps, 0, sizeof(maps));
-  const uint64_t rows = (uint64_t)num_pages * (uint64_t)page_size;
-  mla_status s = map2d(&maps.kv, kv_cache, kDk, rows, kDk, page_size >= kKeys ? kKeys : (uint32_t)page_size, "cache");
-  if (s != MLA_OK) return s;
-  s = map2d(&maps.row, kv_cache, kDk, rows, kDk, 1, "cache rows");
-  if (s != MLA_OK) return s;
-  maps.pe = maps.row;
-  CoreParams p;
-  memset(&p, 0, sizeof(p));
-  p.mode = MODE_DECODE;
-  p.num_pairs = num_splits > 0 ? num_splits : default_pairs();
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.spin_limit = spin_limit();
-  p.debug_stall = debug_stall();
-  p.err = ws_err(workspace);
-  p.q = reinterpret_cast<const __nv_bfloat16*>(q);
-  p.H = H;
-  p.block_table = block_table;
-  p.lens = lens;
-  p.B = G;
-  p.q_per_req = q_per_req;
-  p.sinks = sinks;
-  p.max_pages = max_pages;
-  p.page_size = page_size;
-  p.num_pages = num_pages;
-  p.cache = reinterpret_cast<const __nv_bfloat16*>(kv_cache);
-  char* w = reinterpret_cast<char*>(workspace) + kWsHeader;
-  const size_t slots = (size_t)G + (size_t)p.num_pairs;
-  p.tile_prefix = reinterpret_cast<int32_t*>(w);
-  w += align_up(sizeof(int32_t) * ((size_t)G + 1), 256);
-  p.part_lse = reinterpret_cast<float*>(w);
-  w += align_up(sizeof(float) * slots * (size_t)H, 256);
-  p.part_o = reinterpret_cast<float*>(w);
-  cudaError_t e = (g_decode_keys.load() == 128) ? launch_prefill128(p, maps, st) : launch_core(p, maps, st);
-  if (e != cudaSuccess) return cuda_fail(e, "mla_decode launch");
-  e = launch_decode_reduce(p, reinterpret_cast<__nv_bfloat16*>(out), lse, st);
-  if (e != cudaSuccess) return cuda_fail(e, "mla_decode reduce launch");
-  return ok();
+  return decode_impl(q, q_per_req, kv_cache, false, 1.f, num_pages, page_size, block_table, max_pages, lens, B, H,
+                     scale, sinks, num_splits, out, lse, workspace, workspace_bytes, stream);
 }
+
+size_t mla_decode_fp8_workspace_size(int B, int q_per_req, int H, int num_splits) {
+  return mla_decode_ex_workspace_size(B, q_per_req, H, num_splits);
+}
+
+mla_status mla_decode_fp8(const void* q, int q_per_req, const void* kv_cache_e4m3, float kv_scale, int64_t num_pages,
+                          int page_size, const int32_t* block_table, int max_pages, const int32_t* lens, int B, int H,
+                          float scale, const float* sinks, int num_splits, void* out, float* lse, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  MLA_REQUIRE(std::isfinite(kv_scale) && kv_scale > 0.f, "mla_decode_fp8: kv_scale must be finite and > 0");
+  return decode_impl(q, q_per_req, kv_cache_e4m3, true, kv_scale, num_pages, page_size, block_table, max_pages, lens,
+                     B, H, scale, sinks, num_splits, out, lse, workspace, workspace_bytes, stream);
+}
+
 
 // ---------------------------------------------------------------------------
 size_t mla_sparse_workspace_size(int S, int H) {

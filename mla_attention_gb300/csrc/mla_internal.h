@@ -71,6 +71,8 @@ struct CoreParams {
   int page_size;
   int64_t num_pages;
   const __nv_bfloat16* cache;    // [num_pages * page_size, 576] rows (L2 prefetch addresses)
+  const uint8_t* cache8;         // FP8 decode: e4m3 rows [num_pages * page_size, 576] (else null)
+  float kv_scale;                // FP8 decode: value of one e4m3 unit (the epilogue scales O by it)
   int q_per_req;                 // query tokens per request (B above counts B_req * q_per_req groups)
   const float* sinks;            // [H] per-head sink logit, or null (used by the reduction)
   int32_t* tile_prefix;          // ws: [B+1] tiles before request b (written by CTA 0)

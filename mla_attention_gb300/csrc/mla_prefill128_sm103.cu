@@ -269,6 +269,55 @@ __device__ __forceinline__ void issue_half(uint32_t dst, uint32_t box_stride, in
   }
 }
 
+// FP8 decode: rows [kh, kh + 64) of column blocks cb0 .. cb0 + kBlk - 1 (64 values each) of the
+// e4m3 cache, converted to f16 (exactly) into 64-row SW128 boxes box_stride bytes apart from dst.
+// Lane l converts whole 64-value row pieces (units l, l + 32, ...: four 16-byte loads, eight
+// 16-byte chunks), the loads of kBlk units in flight together.  Keys past len and rows of an
+// out-of-range page give zero rows (the page is reported).  The caller fences the async proxy
+// and arrives once every lane has stored.  The cache rows are normally in L2 already: the
+// O-CTA's producers prefetch each page a few tiles ahead.
+template <int kBlk>
+__device__ __forceinline__ void fill_half_fp8(uint8_t* dst, uint32_t box_stride, int cb0, const CoreParams& p,
+                                              int len, int64_t kh, const HalfIds& ids, uint32_t* err) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll 1
+  for (int batch = 0; batch < 2; ++batch) {
+    uint4 v[kBlk][4];
+    int rows[kBlk];
+#pragma unroll
+    for (int i = 0; i < kBlk; ++i) {
+      const int u = lane + 32 * (batch * kBlk + i);  // 64 * kBlk units, 2 * kBlk per lane
+      const int r = u / kBlk, b = u - r * kBlk;
+      rows[i] = r;
+      const int32_t pe = __shfl_sync(0xffffffffu, ids.pe, r >> 1);
+      const int32_t po = __shfl_sync(0xffffffffu, ids.po, r >> 1);
+      const int32_t pg = (r & 1) ? po : pe;
+      const int64_t key = kh + r;
+      const bool in_len = key < len;
+      const bool ok = in_len && pg >= 0 && pg < p.num_pages;
+      if (in_len && !ok) record_error(err, DEV_RANGE_BASE | X_PAGE);
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.cache8 + ((int64_t)pg * p.page_size + key % p.page_size) * kDk + (cb0 + b) * 64);
+#pragma unroll
+      for (int w = 0; w < 4; ++w) v[i][w] = ok ? __ldg(src + w) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < kBlk; ++i) {
+      const int u = lane + 32 * (batch * kBlk + i);
+      const int r = rows[i], b = u - r * kBlk;
+      uint8_t* line = dst + b * box_stride + r * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {  // chunk c: values 8c .. 8c + 7 = bytes 8c .. 8c + 7 of the piece
+        const uint4& q = v[i][c >> 1];
+        const uint32_t w0 = (c & 1) ? q.z : q.x, w1 = (c & 1) ? q.w : q.y;
+        *reinterpret_cast<uint4*>(line + ((c ^ (r & 7)) << 4)) =
+            make_uint4(e4m3x2_to_f16x2((uint16_t)(w0 & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(w0 >> 16)),
+                       e4m3x2_to_f16x2((uint16_t)(w1 & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(w1 >> 16)));
+      }
+    }
+  }
+}
+
 // ---- softmax rows: one 32-column piece of a score row ----
 // Keys of a piece past lim (the visible keys in it) get the score -inf (+inf when the scale
 // is negative), so one mask-free body serves every piece: the extreme ignores them and
@@ -294,7 +343,7 @@ __device__ __forceinline__ void row_extreme(const uint32_t (&sr)[32], float (&eq
 // of the row's 128-byte line of the piece's 64-key P box, swizzled), row sums into rsq (two
 // pairs of partial sums), and the extreme of the raw scores into eq.  Scores go through the
 // scale in pairs (packed fp32).
-template <bool kUp>
+template <bool kUp, bool kF16>
 __device__ __forceinline__ void row_exp(const uint32_t (&sr)[32], uint64_t sl2x2, uint64_t nmsub2, uint8_t* pline,
                                         int chunk0, int r, uint64_t (&rsq)[2], float (&eq)[4]) {
 #pragma unroll
@@ -310,17 +359,19 @@ __device__ __forceinline__ void row_exp(const uint32_t (&sr)[32], uint64_t sl2x2
       const float e0 = ex2_approx(x0);
       const float e1 = ex2_approx(x1);
       rsq[u & 1] = add_f32x2(rsq[u & 1], f32x2(e0, e1));
-      w[u] = pack_bf16x2(e0, e1);
+      w[u] = kF16 ? pack_f16x2(e0, e1) : pack_bf16x2(e0, e1);
     }
     *reinterpret_cast<uint4*>(pline + (((chunk0 + c8) ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
 // kUp: the scale is >= 0, so the row extreme of the raw scores is their maximum (else
-// their minimum).  kDecode: paged decode (else prefill).  One instantiation per
-// combination keeps both choices out of the loops: the loop bodies must stay small
-// for the instruction cache.
-template <bool kUp, bool kDecode>
+// their minimum).  kDecode: paged decode (else prefill).  kFp8 (decode only): the cache is
+// e4m3 with a per-tensor scale; producers convert its rows to f16 (exact) into the K and V
+// rings with ordinary loads, Q and P are f16, and both MMAs take f16 operands.  One
+// instantiation per combination keeps the choices out of the loops: the loop bodies must stay
+// small for the instruction cache.
+template <bool kUp, bool kDecode, bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
     mla_prefill128_kernel(const __grid_constant__ CoreParams p, const __grid_constant__ CoreMaps maps) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -363,7 +414,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
       mbar_init(&bars.stats_free, kRowWarpsO);
     } else {
       for (int b = 0; b < 2; ++b) {
-        mbar_init(&bars.vfull[b], 1);
+        mbar_init(&bars.vfull[b], kFp8 ? 4 : 1);  // FP8: the four warps that fill half b
         mbar_init(&bars.vempty[b], 1);
         mbar_init(&bars.p_full[b], 1);
         mbar_init(&bars.p_ready[b], kRowWarpsO);
@@ -384,7 +435,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
     tmem_alloc(&bars.tmem_base, 512);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
+  if (!kFp8 && warp == 4 && lane == 0) {  // (FP8 decode reads the cache without TMA)
     tma_prefetch_desc(&maps.kv);
     tma_prefetch_desc(&maps.row);
     if (staged) tma_prefetch_desc(&maps.out);
@@ -475,6 +526,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
           }
           if (!waitb(&bars.kempty[k], par ^ 1, X_K_EMPTY, false)) { live = false; break; }
           uint64_t* fb = &bars.kfull[k][par];
+          if constexpr (kFp8) {  // ordinary loads, converted into the slot, then one arrival
+            fill_half_fp8<3>(smem + kOffK + k * kGroupBytes + h * kBoxBytesV, kBoxBytesK, 3 * k, p, len, kh, cur, err);
+            fence_proxy_async_smem();  // the MMA reads the slot through the async proxy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(fb);
+            continue;
+          }
           if (lane == 0) mbar_arrive_expect_tx(fb, kGroupBytes / 2);
           drain_bar = fb;
           drain_par = (t >> 1) & 1;
@@ -493,7 +551,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
       // the other issuer's queued tile keeps the tensor pipe busy meanwhile.
       if (lane == 0) {
         const uint32_t b = (uint32_t)(warp - 5);
-        const uint32_t idesc = idesc_bf16_f32(kRows, kKeysT, false, false);
+        const uint32_t idesc = kFp8 ? idesc_f16_f32(kRows, kKeysT, false, false) : idesc_bf16_f32(kRows, kKeysT, false, false);
         const uint64_t a_rope = sdesc_sw128(smem_u32(smem + kOffQpe), 16, 1024);
         const uint32_t d_tmem = tbase + kTmemS + b * kKeysT;
         uint32_t t = 0, i = 0, nb = 0;  // all tiles, items with keys, this issuer's tiles
@@ -640,6 +698,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
               v[4 * u + 2] = x[cc][u].z;
               v[4 * u + 3] = x[cc][u].w;
             }
+            if constexpr (kFp8) {  // the MMAs take f16 operands
+#pragma unroll
+              for (int u = 0; u < 32; ++u) v[u] = bf16x2_to_f16x2(v[u]);
+            }
             tmem_st32(tbase + lane_base + kTmemQ + 32 * (c0 + cc), v);
           }
         }
@@ -648,7 +710,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
           const uint4* src = row_ok ? reinterpret_cast<const uint4*>(qrow + kLatent) : nullptr;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            const uint4 v = src ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+            uint4 v = src ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+            if constexpr (kFp8)
+              v = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
             *reinterpret_cast<uint4*>(qpe_row + ((c ^ (r & 7)) << 4)) = v;
           }
           fence_proxy_async_smem();  // read by the MMA through the async proxy
@@ -720,7 +784,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
               tmem_ld32(scol + 32 * p32, sr);
               tmem_wait_ld();
               mask_piece<kUp>(sr, nv - 32 * p32);
-              row_exp<kUp>(sr, sl2x2, nmsub2, prow + (p32 >> 1) * kPBoxBytes, (4 * p32) & 7, r, rsq, eq);
+              row_exp<kUp, kFp8>(sr, sl2x2, nmsub2, prow + (p32 >> 1) * kPBoxBytes, (4 * p32) & 7, r, rsq, eq);
             }
             const float mt = tile_offset(eq);
             const bool move = mt > m_used + kRescaleLog2;
@@ -758,14 +822,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
     // =====================================================================
     // O-CTA
     // =====================================================================
-    if (warp == 4 || warp == 8) {
+    if (kFp8 ? (warp == 4 || warp >= 6) : (warp == 4 || warp == 8)) {
       // ---------------- TMA producers: V halves (64 keys x 512 columns), epilogue stages ----------------
       // Ring slot h holds key half h of every tile (and then rows 64 h .. 64 h + 63 of the
       // epilogue); warp 4 fills slot 0 and warp 8 slot 1, each at its own issue rate.
       // Decode: the same warp also brings half h of tile j + kPrefetchTiles into L2 (one bulk
       // prefetch of its 64 contiguous cache rows when they lie in one page), so the S-CTA's K
       // loads of that tile hit L2: its one-tile K ring cannot cover the latency of HBM.
-      const int h = (warp == 4) ? 0 : 1;
+      // FP8: eight warps convert the slots, four per half, two column boxes each (warp 4 and
+      // warps 6-12 in order: half = index / 4, boxes 2 (index % 4) and the next).
+      const int vq = (warp == 4) ? 0 : warp - 5;
+      const int h = kFp8 ? (vq >> 2) : ((warp == 4) ? 0 : 1);
+      const int qq = kFp8 ? (vq & 3) : 0;
       const uint32_t dst = smem_u32(smem + kOffV + h * kHalfBytesV);
       uint32_t m = 0;  // uses of this slot
       bool live = true;
@@ -787,11 +855,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
             cur = ids;
             if (j + 1 < it.J) ids = load_half_ids(p, it.id, len, kh + kKeysT);
             const int64_t kp = kh + (int64_t)kPrefetchTiles * kKeysT;
-            if (lane == 0 && pf_pg >= 0 && pf_pg < p.num_pages)
-              bulk_prefetch_l2(p.cache + (pf_pg * (int64_t)p.page_size + kp % p.page_size) * kDk, 64 * kDk * 2);
+            if (lane == 0 && qq == 0 && pf_pg >= 0 && pf_pg < p.num_pages) {
+              const int64_t row = pf_pg * (int64_t)p.page_size + kp % p.page_size;
+              if constexpr (kFp8) bulk_prefetch_l2(p.cache8 + row * kDk, 64 * kDk);
+              else bulk_prefetch_l2(p.cache + row * kDk, 64 * kDk * 2);
+            }
             pf_pg = (pf_ok && kp + kKeysT + 64 <= len) ? __ldg(bt + (kp + kKeysT) / p.page_size) : -1;
           }
           if (!waitb(&bars.vempty[h], (m & 1) ^ 1, X_V_EMPTY, false)) { live = false; break; }
+          if constexpr (kFp8) {
+            fill_half_fp8<2>(smem + kOffV + h * kHalfBytesV + 2 * qq * kBoxBytesV, kBoxBytesV, 2 * qq, p, len, kh, cur,
+                             err);
+            fence_proxy_async_smem();  // the MMA reads the slot through the async proxy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.vfull[h]);
+            continue;
+          }
           if (lane == 0) mbar_arrive_expect_tx(&bars.vfull[h], kHalfBytesV);
           drain_bar = &bars.vfull[h];
           drain_par = m & 1;
@@ -825,7 +904,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
     } else if (warp == 5) {
       // ---------------- P V issuer ----------------
       if (lane == 0) {
-        const uint32_t idesc = idesc_bf16_f32(kRows, 256, false, true);
+        const uint32_t idesc = kFp8 ? idesc_f16_f32(kRows, 256, false, true) : idesc_bf16_f32(kRows, 256, false, true);
         uint32_t t = 0, u = 0, i = 0;
         bool live = true;
         while (live && iter.next(it)) {
@@ -954,7 +1033,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
             wn /= ws;
           }
         }
-        const float cn = wn * inv_l;
+        const float cn = wn * inv_l * (kFp8 ? p.kv_scale : 1.f);  // FP8: one e4m3 unit of V is kv_scale
         if constexpr (decode) {
           // fp32 partial rows (O / l) and their LSE for the split-K reduction
 #pragma unroll 1
@@ -1072,28 +1151,31 @@ extern "C" int mla_trace_read(unsigned long long* host) {
 cudaError_t launch_prefill128(const CoreParams& p, const CoreMaps& maps, cudaStream_t stream) {
   static PerDeviceOnce attrs;
   cudaError_t e = attrs.run([] {
-    cudaError_t r = cudaFuncSetAttribute(mla_prefill128_kernel<true, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemT);
-    if (r == cudaSuccess)
-      r = cudaFuncSetAttribute(mla_prefill128_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSmemT);
-    if (r == cudaSuccess)
-      r = cudaFuncSetAttribute(mla_prefill128_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemT);
-    if (r == cudaSuccess)
-      r = cudaFuncSetAttribute(mla_prefill128_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSmemT);
+    cudaError_t r = cudaSuccess;
+    auto set = [&](const void* fn) {
+      if (r == cudaSuccess) r = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemT);
+    };
+    set((const void*)mla_prefill128_kernel<true, false, false>);
+    set((const void*)mla_prefill128_kernel<false, false, false>);
+    set((const void*)mla_prefill128_kernel<true, true, false>);
+    set((const void*)mla_prefill128_kernel<false, true, false>);
+    set((const void*)mla_prefill128_kernel<true, true, true>);
+    set((const void*)mla_prefill128_kernel<false, true, true>);
     return r;
   });
   if (e != cudaSuccess) return e;
   if (p.num_pairs <= 0) return cudaSuccess;
   const dim3 grid(2 * p.num_pairs), block(kThreadsT);
   const bool up = p.scale_log2 >= 0.f;
-  if (p.mode == MODE_DECODE) {
-    if (up) mla_prefill128_kernel<true, true><<<grid, block, kSmemT, stream>>>(p, maps);
-    else mla_prefill128_kernel<false, true><<<grid, block, kSmemT, stream>>>(p, maps);
+  if (p.mode == MODE_DECODE && p.cache8) {
+    if (up) mla_prefill128_kernel<true, true, true><<<grid, block, kSmemT, stream>>>(p, maps);
+    else mla_prefill128_kernel<false, true, true><<<grid, block, kSmemT, stream>>>(p, maps);
+  } else if (p.mode == MODE_DECODE) {
+    if (up) mla_prefill128_kernel<true, true, false><<<grid, block, kSmemT, stream>>>(p, maps);
+    else mla_prefill128_kernel<false, true, false><<<grid, block, kSmemT, stream>>>(p, maps);
   } else {
-    if (up) mla_prefill128_kernel<true, false><<<grid, block, kSmemT, stream>>>(p, maps);
-    else mla_prefill128_kernel<false, false><<<grid, block, kSmemT, stream>>>(p, maps);
+    if (up) mla_prefill128_kernel<true, false, false><<<grid, block, kSmemT, stream>>>(p, maps);
+    else mla_prefill128_kernel<false, false, false><<<grid, block, kSmemT, stream>>>(p, maps);
   }
   return cudaGetLastError();
 }

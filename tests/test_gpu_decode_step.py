@@ -215,3 +215,53 @@ def test_multi_token_decode_with_sinks(decode_engine, S, H, sinks, splits):
     ro, rl = mo.mla_decode_ex(q, D.cache, D.block_table, D.lens, D.scale, sinks=sk)
     assert_out_close(out, ro)
     assert_lse_close(lse, rl)
+
+
+# ---------------------------------------------------------------------------
+# FP8 (e4m3) latent cache
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("lens,S,H,page_size,splits,sinks", [
+    ([1, 63, 64, 65, 200, 4100], 1, 128, 64, 0, False),
+    ([3000, 17, 0, 129, 64], 2, 16, 64, 7, True),
+    ([70, 5, 130, 300], 1, 128, 16, 0, False),
+])
+def test_fp8_cache_decode(lens, S, H, page_size, splits, sinks):
+    from mla_attention_gb300 import mla_decode_fp8
+    D = gen.decode_inputs(lens, H=H, seed=80 + S, page_size=page_size)
+    kv_scale = 0.37
+    c8 = (D.cache.float() / kv_scale).to(torch.float8_e4m3fn)      # the caller's quantised cache
+    g = torch.Generator().manual_seed(81)
+    q = gen.randn_bf16((len(lens), S, H, 576), g)
+    sk = (torch.randn((H,), generator=g) * 2.0).float() if sinks else None
+    d = dev()
+    out, lse = mla_decode_fp8(q.to(d), c8.to(d), kv_scale, D.block_table.to(d), D.lens.to(d), D.scale,
+                              sinks=None if sk is None else sk.to(d), num_splits=splits)
+    torch.cuda.synchronize()
+    check_device_status()
+    ro, rl = mo.mla_decode_fp8(q, c8, kv_scale, D.block_table, D.lens, D.scale, sinks=sk)
+    assert_out_close(out, ro)
+    assert_lse_close(lse, rl)
+
+
+def test_fp8_cache_row_set_is_exact():
+    """q = 0 makes every score equal; one-hot e4m3 value rows then give out = (keys' one-hots) / n,
+    so a wrong or missed row shows up exactly."""
+    from mla_attention_gb300 import mla_decode_fp8
+    lens = [5, 64, 129, 300]
+    D = gen.decode_inputs(lens, H=16, seed=85, page_size=64)
+    pages = D.cache.shape[0]
+    cache = torch.zeros((pages, 64, 576))
+    ids = torch.arange(pages * 64)
+    cache.view(-1, 576)[ids, ids % 512] = 1.0                      # row i holds a one at column i % 512
+    c8 = cache.to(torch.float8_e4m3fn)
+    q = torch.zeros((len(lens), 16, 576), dtype=torch.bfloat16)
+    d = dev()
+    out, _ = mla_decode_fp8(q.to(d), c8.to(d), 1.0, D.block_table.to(d), D.lens.to(d), D.scale)
+    torch.cuda.synchronize()
+    check_device_status()
+    for b, n in enumerate(lens):
+        want = torch.zeros(512, dtype=torch.float64)
+        for j in range(n):
+            row = int(D.block_table[b, j // 64]) * 64 + j % 64
+            want[row % 512] += 1.0 / n
+        np.testing.assert_allclose(to_np(out[b, 0]), want.numpy(), atol=2.0 ** -8)
