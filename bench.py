@@ -405,7 +405,21 @@ def measure_decode_step(lib, dev, peaks, steps=10, warmup=3):
     kv_bytes = sum(lens) * DK * 2
     gbs = (kv_bytes + q2.numel() * 2 + out.numel() * 2) / (ms_m * 1e-3) / 1e9
     flops = 2.0 * sum(S * n - S * (S - 1) // 2 for n in lens) * H * (DK + DV)
-    return {"rope_append": {"workload": "B=64, H=128: rotate q_pe/k_pe, append [c_kv | k_pe] to the paged cache",
+    # the same decode over an e4m3 copy of the cache (half the bytes)
+    c8 = (cache.float() / 0.05).to(torch.float8_e4m3fn)
+    q1 = gen.randn_bf16_device((B, H, DK), 41, dev)
+    fn3 = lambda: lib.mla_decode_fp8(q1, c8, 0.05, bt, lens_d, SCALE)  # noqa: E731
+    for _ in range(warmup):
+        fn3()
+    ms_f = time_region(fn3, steps)
+    del c8
+    kv8 = sum(lens) * DK
+    gbs8 = (kv8 + q1.numel() * 2 + B * H * DV * 2) / (ms_f * 1e-3) / 1e9
+    return {"fp8_decode": {"workload": "decode B=64 H=128 lens U[4096,32768] over an e4m3 cache (per-tensor scale)",
+                           "ms": round(ms_f, 4), "GB_per_s": round(gbs8, 1), "hbm_frac": round(gbs8 / peaks["hbm_gbs"], 4),
+                           "kv_bytes": kv8,
+                           "TFLOP_per_s": round(2.0 * sum(lens) * H * (DK + DV) / (ms_f * 1e-3) / 1e12, 1)},
+            "rope_append": {"workload": "B=64, H=128: rotate q_pe/k_pe, append [c_kv | k_pe] to the paged cache",
                             "ms": round(ms_r, 4), "GB_per_s": round(rope_bytes / (ms_r * 1e-3) / 1e9, 1)},
             "multi_token_decode": {"workload": "decode B=64 H=128 lens U[4096,32768], 2 query tokens per request, "
                                                "per-head sinks", "ms": round(ms_m, 4), "GB_per_s": round(gbs, 1),
