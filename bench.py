@@ -28,6 +28,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
+from torch.cuda import nvtx  # noqa: E402  (named ranges for profilers; no-ops otherwise)
 
 H, DK, DV, T_TOTAL, CHUNK = 128, 576, 512, 8192, 2048
 SCALE = 192.0 ** -0.5
@@ -492,8 +493,9 @@ def run_libmla(args, world, rank, local):
     stop = torch.cuda.Event(enable_timing=True)
     start.record()
     launches = 0
-    for _ in range(args.steps):
-        launches += prefill_step(lib, q, kv, out, lse, events)
+    with nvtx.range("prefill: timed steps"):
+        for _ in range(args.steps):
+            launches += prefill_step(lib, q, kv, out, lse, events)
     stop.record()
     torch.cuda.synchronize()
     barrier(world)
@@ -528,11 +530,13 @@ def run_libmla(args, world, rank, local):
     for _ in range(2):
         e2e_step()
     e2e_steps = max(2, args.steps // 2)
-    e2e_serial_ms = max_over_ranks(time_region(e2e_step, e2e_steps), world)
+    with nvtx.range("prefill: end to end, copies in series"):
+        e2e_serial_ms = max_over_ranks(time_region(e2e_step, e2e_steps), world)
 
     # the same steps with two device buffer sets: step s uploads into set s%2 on one side stream
     # and downloads from it on another while step s-1 computes, so the link copies overlap compute
-    e2e_ms = max_over_ranks(pipelined_e2e(lib, hq, hkv, hout, hlse, out, lse, e2e_steps), world)
+    with nvtx.range("prefill: end to end, double-buffered"):
+        e2e_ms = max_over_ranks(pipelined_e2e(lib, hq, hkv, hout, hlse, out, lse, e2e_steps), world)
     e2e_val = world * flops_step / (e2e_ms * 1e-3) / 1e12
     e2e_serial_val = world * flops_step / (e2e_serial_ms * 1e-3) / 1e12
     h2d = hq.numel() * 2 + hkv.numel() * 2
@@ -544,7 +548,8 @@ def run_libmla(args, world, rank, local):
         for name, fn in (("decode", measure_decode), ("sparse", measure_sparse), ("split", measure_split),
                          ("absorb", measure_absorb), ("decode_step", measure_decode_step)):
             try:
-                extra[name] = fn(lib, dev, peaks)
+                with nvtx.range(name):
+                    extra[name] = fn(lib, dev, peaks)
                 torch.cuda.empty_cache()
             except Exception as e:  # reported, never silently dropped
                 extra[name] = {"error": repr(e)[:300]}

@@ -78,8 +78,8 @@ mla_status mla_check_device_status(void* workspace, void* stream, uint32_t* deta
 void mla_set_spin_limit(uint32_t spin_limit);
 
 /*
- * Keys per score tile of mla_prefill and of mla_decode: 128 runs the 128-key tile engine,
- * 64 the 64-key engine (which always serves mla_sparse).  0 restores the default of each
+ * Keys per score tile of mla_prefill (and of mla_sparse, which follows the prefill setting) and
+ * of mla_decode: 128 runs the 128-key tile engine, 64 the 64-key engine.  0 restores the default of each
  * (128 for both: the faster engine for each on GB300); any other value leaves
  * the setting unchanged.  Process-wide; both engines give the same results within the
  * stated tolerances (the tests run both).

@@ -395,7 +395,8 @@ def mla_decode_noalloc(q, kv_cache, block_table, lens, scale: float, num_splits:
 
 
 def mla_sparse(q_lift, q_pe, c_kv, k_pe, topk, softmax_scale: float, out=None, lse=None, ws=None, stream=None):
-    """Top-k sparse MLA: returns out [B,S,H*512] (natural order), lse [B,S,H]."""
+    """Top-k sparse MLA: returns out [B,S,H*512] (natural order), lse [B,S,H] (lse=False: no LSE is
+    written and None is returned for it)."""
     for name, t in (("q_lift", q_lift), ("q_pe", q_pe), ("c_kv", c_kv), ("k_pe", k_pe)):
         _need(t, name, torch.bfloat16, q_lift.device)
     _need(topk, "topk", torch.int32, q_lift.device)
@@ -409,16 +410,19 @@ def mla_sparse(q_lift, q_pe, c_kv, k_pe, topk, softmax_scale: float, out=None, l
     _need(topk, "topk", torch.int32, q_lift.device, shape=(B, S, K))
     if out is None:
         out = torch.empty((B, S, H * L), dtype=torch.bfloat16, device=q_lift.device)
+    no_lse = lse is False
     if lse is None:
         lse = torch.empty((B, S, H), dtype=torch.float32, device=q_lift.device)
     _need(out, "out", torch.bfloat16, q_lift.device, shape=(B, S, H * L))
-    _need(lse, "lse", torch.float32, q_lift.device, shape=(B, S, H))
+    if not no_lse:
+        _need(lse, "lse", torch.float32, q_lift.device, shape=(B, S, H))
     nbytes = lib().mla_sparse_workspace_size(S, H)
     ws = workspace(nbytes, q_lift.device) if ws is None else ws
     s = lib().mla_sparse(_ptr(q_lift), _ptr(q_pe), _ptr(c_kv), _ptr(k_pe), _ptr(topk), B, S, S_kv, H, K,
-                         float(softmax_scale), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+                         float(softmax_scale), _ptr(out), None if no_lse else _ptr(lse), _ptr(ws), ws.numel(),
+                         _stream(stream))
     _check(s)
-    return out, lse
+    return out, (None if no_lse else lse)
 
 
 def mla_absorb_q(q_nope, k_b_proj_trans, q_out=None, ws=None, stream=None):

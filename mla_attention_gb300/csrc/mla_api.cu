@@ -112,7 +112,7 @@ uint32_t* ws_err(void* ws) { return reinterpret_cast<uint32_t*>(ws); }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Keys per score tile of prefill and of decode: 128 (mla_prefill128_kernel) or 64
+// Keys per score tile of prefill (and sparse) and of decode: 128 (mla_prefill128_kernel) or 64
 // (mla_core_kernel); set with mla_set_tile_keys.
 constexpr int kDefaultPrefillKeys = 128, kDefaultDecodeKeys = 128;
 std::atomic<int> g_prefill_keys{kDefaultPrefillKeys};
@@ -511,7 +511,8 @@ mla_status mla_sparse(const void* q_lift, const void* q_pe, const void* c_kv, co
   p.k_pe = reinterpret_cast<const __nv_bfloat16*>(k_pe);
   p.K = K;
   p.S_kv = S_kv;
-  cudaError_t e = launch_core(p, maps, st);
+  // the prefill engine choice applies to sparse as well (both are context-phase attention)
+  cudaError_t e = g_prefill_keys.load() == 128 ? launch_prefill128(p, maps, st) : launch_core(p, maps, st);
   if (e != cudaSuccess) return cuda_fail(e, "mla_sparse launch");
   return ok();
 }

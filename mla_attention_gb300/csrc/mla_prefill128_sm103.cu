@@ -12,16 +12,17 @@
 // where the 64-key tile of mla_core_kernel runs at about 55%.
 //
 // Cluster of two CTAs per 128-row item, as in mla_core_kernel (an fp32 O tile of
-// 128 x 512 fills one SM's TMEM):
+// 128 x 512 fills one SM's TMEM); 13 warps per CTA:
 //   S-CTA  TMEM: Q latent part (512 bf16 = 256 columns) + two S buffers of 128 columns.
 //          smem: K ring of three 48 KB groups (64-column boxes 0-2, 3-5, 6-8 of 128 rows),
 //          Q RoPE part (128 x 64, SW128), two local P buffers (128 x 128 bf16) and factors.
-//          warps 0-3: softmax, one row per thread (the 128 scores of a tile in registers,
-//          read with one TMEM wait); warp 4: TMA; warps 5, 6: S MMAs of even / odd tiles;
-//          warp 7: P copies.
+//          warps 0-3: softmax, one row per thread (the scores of a tile read from TMEM in
+//          32-column pieces); warps 4, 8-12: K producers, one per (group, 64-key half);
+//          warps 5, 6: S MMAs of even / odd tiles; warp 7: P copies.
 //   O-CTA  TMEM: O (512 columns).  smem: V ring of two 64-key halves (64 KB each), two P
 //          buffers and factors, the row statistics.
-//          warps 0-3: rescale and epilogue rows; warp 4: TMA; warp 5: P V MMAs.
+//          warps 0-3: rescale and epilogue rows; warps 4, 8: V producers, one per half
+//          (FP8 cache: warps 4, 6-12, four per half); warp 5: P V MMAs.
 // Every wait is bounded (see mbar_wait); a timeout sets the abort flag, the CTA lets its
 // copies and MMAs land and leaves through the cluster barrier.
 #include <math_constants.h>
@@ -65,6 +66,14 @@ constexpr uint32_t kTmemQ = 0;      // S: Q latent part [0, 256)
 constexpr uint32_t kTmemS = 256;    // S: S buffers [256, 384), [384, 512)
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kPrefetchTiles = 4;   // decode: L2 prefetch distance of the O-CTA's V producers
+// decode: L2 eviction priorities of the cache stream (see l2_policy).  Every cache row is read
+// twice, by the K load (576 columns) and a tile or two later by the V load (512 columns): the K
+// load marks its lines evict-last so that they survive until the V load, which marks them
+// evict-first (their last use).  Measured on the 64 x U[4096, 32768] decode: DRAM reads 1.62 ->
+// 1.46 GB for 1.37 GB of cache, 3813 -> 3888 GB/s.
+constexpr int kHintPf = kL2Plain;
+constexpr int kHintK = kL2Keep;
+constexpr int kHintV = kL2Done;
 
 struct BarsT {
   // S-CTA
@@ -135,7 +144,7 @@ __device__ __forceinline__ int64_t keys_for_token(const CoreParams& p, int64_t t
 // Decode: the key tiles of all requests, in request order, are split into equal shares, one
 // per CTA pair; an item is the part of one request inside this pair's share (an empty
 // share has none).
-template <bool kDec>
+template <bool kDec, bool kSp = false>
 struct ItemIterT {
   const CoreParams* p;
   int pair;
@@ -182,6 +191,14 @@ struct ItemIterT {
         return true;
       }
       return false;
+    } else if constexpr (kSp) {  // one query token (all its heads) per item, every top-k tile
+      if (k >= P.T) return false;
+      it.id = (int)k;
+      it.J = (P.K + kKeysT - 1) / kKeysT;
+      it.k0 = 0;
+      it.k1 = P.K;
+      k += P.num_pairs;
+      return true;
     } else {
     const int64_t rows = (int64_t)P.T * P.H;
     const int64_t n_items = (rows + kRows - 1) / kRows;
@@ -254,6 +271,7 @@ static __device__ __noinline__ void gather_half(uint32_t dst, uint32_t box_strid
 // Issues the 64-row boxes of one tile half [kh, kh + 64): nbox (<= 32) column blocks starting
 // at column x0, landing box_stride bytes apart from dst.  A half inside one valid page is one
 // tiled box per column block, lane i issuing block i.  Warp-uniform.
+template <int kHint>
 __device__ __forceinline__ void issue_half(uint32_t dst, uint32_t box_stride, int32_t x0, int nbox, const CoreParams& p,
                                            const CoreMaps& maps, int len, int64_t kh, const HalfIds& ids,
                                            uint64_t* bar, uint32_t* err) {
@@ -262,11 +280,55 @@ __device__ __forceinline__ void issue_half(uint32_t dst, uint32_t box_stride, in
     const int lane = threadIdx.x & 31;  // one box per lane: lanes overlap their TMA issues
     if (lane < nbox) {
       const int32_t y = (int32_t)(pg0 * (int64_t)p.page_size + kh % p.page_size);
-      tma_load_2d(dst + lane * box_stride, &maps.kv, x0 + lane * kBoxCols, y, bar);
+      tma_load_2d_hint<kHint>(dst + lane * box_stride, &maps.kv, x0 + lane * kBoxCols, y, bar);
     }
   } else {
     gather_half(dst, box_stride, x0, nbox, &maps.row, p.page_size, p.num_pages, len, kh, ids.pe, ids.po, bar, err);
   }
+}
+
+// ---- sparse: the top-k rows of a tile half ----
+// Raw top-k entries of keys kh + 2 lane and kh + 2 lane + 1 of token `id` (-1 past K), read a
+// tile ahead and range-checked where they are used: an entry outside [0, S_kv) is padding.
+__device__ __forceinline__ HalfIds sparse_half_ids(const CoreParams& p, int id, int64_t kh) {
+  const int lane = threadIdx.x & 31;
+  const int32_t* tk = p.topk + (int64_t)id * p.K;
+  const int64_t c0 = kh + 2 * lane;
+  HalfIds ids;
+  ids.pe = c0 < p.K ? __ldg(tk + c0) : -1;
+  ids.po = c0 + 1 < p.K ? __ldg(tk + c0 + 1) : -1;
+  return ids;
+}
+// Gathers the 64 rows of a tile half listed in ids, column boxes cb0 .. cb0 + kBox - 1 (boxes 0-7
+// from c_kv, box 8 = the RoPE columns from k_pe), into 64-row SW128 boxes box_stride bytes
+// apart from dst, with 16-byte cp.async.  Each warp instruction moves one 128-byte box row of
+// four rows (lane / 8: which of the four, lane % 8: the 16-byte chunk), so the warp reads four
+// whole 128-byte lines.  Padding rows are zero-filled (source size 0).  Every lane then arrives
+// (noinc) on bar once its copies have landed; the reader of the stage orders them before its
+// async-proxy reads with a proxy fence.
+template <int kBox>
+__device__ __forceinline__ void gather_half_sparse(uint32_t dst, uint32_t box_stride, int cb0, const CoreParams& p,
+                                                   const HalfIds& ids, uint64_t* bar) {
+  const int lane = threadIdx.x & 31;
+  const int rq = lane >> 3, c = lane & 7;
+#pragma unroll 2
+  for (int i = 0; i < 16; ++i) {
+    const int rr = 4 * i + rq;  // row of the half
+    const int32_t ae = __shfl_sync(0xffffffffu, ids.pe, rr >> 1);
+    const int32_t ao = __shfl_sync(0xffffffffu, ids.po, rr >> 1);
+    const int32_t raw = (rr & 1) ? ao : ae;
+    const bool ok = raw >= 0 && raw < p.S_kv;
+    const int64_t row = ok ? raw : 0;
+    const uint32_t line = dst + (uint32_t)rr * 128u + ((uint32_t)(c ^ (rr & 7)) << 4);
+#pragma unroll
+    for (int b = 0; b < kBox; ++b) {
+      const int gb = cb0 + b;
+      const __nv_bfloat16* src = (gb < kVBoxes) ? p.c_kv + row * kLatent + gb * kBoxCols + c * 8
+                                                : p.k_pe + row * kRope + c * 8;
+      cp_async16_zfill(line + b * box_stride, src, ok ? 16u : 0u);
+    }
+  }
+  cp_async_arrive_noinc(bar);
 }
 
 // FP8 decode: rows [kh, kh + 64) of column blocks cb0 .. cb0 + kBlk - 1 (64 values each) of the
@@ -331,6 +393,25 @@ __device__ __forceinline__ void mask_piece(uint32_t (&sr)[32], int lim) {
     for (int c = 0; c < 32; ++c) sr[c] = (c < lim) ? sr[c] : hide;
   }
 }
+// Sparse: the same with the piece's visible keys given as bits (bit c: key c is listed).
+template <bool kUp>
+__device__ __forceinline__ void mask_bits(uint32_t (&sr)[32], uint32_t bits) {
+  if (bits != 0xffffffffu) {
+    const uint32_t hide = __float_as_uint(kUp ? -CUDART_INF_F : CUDART_INF_F);
+#pragma unroll
+    for (int c = 0; c < 32; ++c) sr[c] = ((bits >> c) & 1u) ? sr[c] : hide;
+  }
+}
+// Sparse: raw top-k entries of tile j of token id, key 32 q + lane in e[q] (-1 past K).
+__device__ __forceinline__ void sparse_tile_entries(const CoreParams& p, int id, int j, int32_t (&e)[4]) {
+  const int lane = threadIdx.x & 31;
+  const int32_t* tk = p.topk + (int64_t)id * p.K;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int c = j * kKeysT + 32 * q + lane;
+    e[q] = c < p.K ? __ldg(tk + c) : -1;
+  }
+}
 template <bool kUp>
 __device__ __forceinline__ void row_extreme(const uint32_t (&sr)[32], float (&eq)[4]) {
 #pragma unroll
@@ -371,9 +452,8 @@ __device__ __forceinline__ void row_exp(const uint32_t (&sr)[32], uint64_t sl2x2
 // rings with ordinary loads, Q and P are f16, and both MMAs take f16 operands.  One
 // instantiation per combination keeps the choices out of the loops: the loop bodies must stay
 // small for the instruction cache.
-template <bool kUp, bool kDecode, bool kFp8>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
-    mla_prefill128_kernel(const __grid_constant__ CoreParams p, const __grid_constant__ CoreMaps maps) {
+template <bool kUp, bool kDecode, bool kFp8, bool kSparse>
+__device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreMaps& maps) {
   extern __shared__ __align__(1024) uint8_t smem[];
   BarsT& bars = *reinterpret_cast<BarsT*>(smem + kOffBarsT);
   const uint32_t rank = cluster_ctarank();
@@ -386,7 +466,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
   const uint32_t lim = p.spin_limit;
   uint32_t* err = p.err;
   constexpr bool decode = kDecode;
-  constexpr bool staged = !kDecode;  // prefill stages its epilogue (prev in, out) through the V ring
+  // prefill stages its epilogue (prev in, out) through the V ring; sparse when an item's 128 rows
+  // are 128 consecutive output rows (H = 128), else its rows store themselves
+  const bool staged = kSparse ? (p.H == kRows) : !kDecode;
   // The layout assumes a 1 KB aligned dynamic base (true when the kernel has no static
   // shared memory); anything else is refused before any barrier is touched.
   if (smem_u32(smem) & 1023u) {
@@ -398,8 +480,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
   if (tid == 0) {
     if (is_s) {
       for (int k = 0; k < kGroups; ++k) {
-        mbar_init(&bars.kfull[k][0], 2);  // the two producers of group k (one per 64-row half)
-        mbar_init(&bars.kfull[k][1], 2);
+        // the two producers of group k (one per 64-row half); sparse: every lane of both (noinc
+        // arrivals of its row copies)
+        mbar_init(&bars.kfull[k][0], kSparse ? 64 : 2);
+        mbar_init(&bars.kfull[k][1], kSparse ? 64 : 2);
         mbar_init(&bars.kempty[k], 1);
       }
       for (int b = 0; b < 2; ++b) {
@@ -414,7 +498,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
       mbar_init(&bars.stats_free, kRowWarpsO);
     } else {
       for (int b = 0; b < 2; ++b) {
-        mbar_init(&bars.vfull[b], kFp8 ? 4 : 1);  // FP8: the four warps that fill half b
+        // FP8: the four warps that fill half b; sparse: every lane of those four
+        mbar_init(&bars.vfull[b], kSparse ? 128 : (kFp8 ? 4 : 1));
         mbar_init(&bars.vempty[b], 1);
         mbar_init(&bars.p_full[b], 1);
         mbar_init(&bars.p_ready[b], kRowWarpsO);
@@ -435,9 +520,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
     tmem_alloc(&bars.tmem_base, 512);
     tmem_relinquish();
   }
-  if (!kFp8 && warp == 4 && lane == 0) {  // (FP8 decode reads the cache without TMA)
-    tma_prefetch_desc(&maps.kv);
-    tma_prefetch_desc(&maps.row);
+  if (!kFp8 && warp == 4 && lane == 0) {  // (FP8 decode and sparse read the cache without TMA)
+    if (!kSparse) {
+      tma_prefetch_desc(&maps.kv);
+      tma_prefetch_desc(&maps.row);
+    }
     if (staged) tma_prefetch_desc(&maps.out);
     if (staged && p.prev_out) tma_prefetch_desc(&maps.prev);
   }
@@ -488,7 +575,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
   };
   if (p.debug_stall && warp == 5) waitb(&bars.stall, 0, X_STALL, false);  // runs out: injected fault
 
-  ItemIterT<kDecode> iter;
+  ItemIterT<kDecode, kSparse> iter;
   iter.init(p, pair);
   ItemT it;
   // abort drain: the last barrier phase this thread's TMA loads were counted on
@@ -516,6 +603,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
         const int len = decode ? decode_len_t(p, it.id) : 0;
         HalfIds ids;
         if constexpr (decode) ids = load_half_ids(p, it.id, len, it.k0 + 64 * h);
+        if constexpr (kSparse) ids = sparse_half_ids(p, it.id, 64 * h);
         for (int j = 0; j < it.J && live; ++j, ++t) {
           const uint32_t par = t & 1;
           const int64_t kh = it.k0 + (int64_t)j * kKeysT + 64 * h;
@@ -524,8 +612,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
             cur = ids;
             if (j + 1 < it.J) ids = load_half_ids(p, it.id, len, kh + kKeysT);  // read while this tile is issued
           }
+          if constexpr (kSparse) {
+            cur = ids;
+            if (j + 1 < it.J) ids = sparse_half_ids(p, it.id, kh + kKeysT);  // lands during this gather
+          }
           if (!waitb(&bars.kempty[k], par ^ 1, X_K_EMPTY, false)) { live = false; break; }
           uint64_t* fb = &bars.kfull[k][par];
+          if constexpr (kSparse) {  // the listed rows by cp.async; each lane arrives (noinc) once they land
+            gather_half_sparse<3>(dst, kBoxBytesK, 3 * k, p, cur, fb);
+            continue;
+          }
           if constexpr (kFp8) {  // ordinary loads, converted into the slot, then one arrival
             fill_half_fp8<3>(smem + kOffK + k * kGroupBytes + h * kBoxBytesV, kBoxBytesK, 3 * k, p, len, kh, cur, err);
             fence_proxy_async_smem();  // the MMA reads the slot through the async proxy
@@ -540,11 +636,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
           if constexpr (!decode) {  // one box per lane: lanes overlap their TMA issues
             if (lane < 3) tma_load_2d(dst + lane * kBoxBytesK, &map_v, (3 * k + lane) * kBoxCols, j * kKeysT + 64 * h, fb);
           } else {
-            issue_half(dst, kBoxBytesK, 3 * k * kBoxCols, 3, p, maps, len, kh, cur, fb, err);
+            issue_half<kHintK>(dst, kBoxBytesK, 3 * k * kBoxCols, 3, p, maps, len, kh, cur, fb, err);
           }
           __syncwarp();
         }
       }
+      if constexpr (kSparse) cp_async_wait_all();  // no copy into this CTA outlives it
     } else if (warp == 5 || warp == 6) {
       // ---------------- S MMA issuers: even tiles (warp 5), odd tiles (warp 6) ----------------
       // A barrier wait by the thread that issued MMAs stalls until its queued MMAs drain;
@@ -572,12 +669,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
                              mbar_try_wait(smem_u32(&bars.kfull[2][b]), nb & 1);
             if (all) {
               tc_fence_after();
+              if constexpr (kSparse) fence_proxy_async_smem();  // cp.async rows, read by the MMA
               mma_s_tile_n128(d_tmem, tbase + kTmemQ, sdesc_sw128(smem_u32(smem + kOffK), 16, 1024), a_rope, idesc,
                               smem_u32(&bars.kempty[0]), smem_u32(&bars.kempty[1]), smem_u32(&bars.kempty[2]));
             } else {
               for (int k = 0; k < kGroups; ++k) {
                 if (k > 0 && !wait1(&bars.kfull[k][b], nb & 1, X_K_FULL, false)) { live = false; break; }
                 tc_fence_after();
+                if constexpr (kSparse) fence_proxy_async_smem();
                 const uint64_t bd = sdesc_sw128(smem_u32(smem + kOffK + k * kGroupBytes), 16, 1024);
                 if (k < 2) mma_s_grp3_n128(d_tmem, tbase + kTmemQ + 96 * k, bd, idesc, (uint32_t)k);
                 else mma_s_grp2r_n128(d_tmem, tbase + kTmemQ + 192, bd, a_rope, idesc);
@@ -637,13 +736,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
         if (it.J == 0) continue;  // no key: the O-CTA writes these rows on its own
         // this row's query and the keys it sees from the item's first tile on
         bool row_ok;
-        const __nv_bfloat16* qrow = nullptr;
+        const __nv_bfloat16* qrow = nullptr;  // the latent part (512 columns)
+        const __nv_bfloat16* qpe = nullptr;   // the RoPE part (64 columns)
         int64_t nkeys = 0;
         if constexpr (decode) {
           row_ok = r < p.H;
           if (row_ok) {
             qrow = p.q + ((int64_t)it.id * p.H + r) * kDk;
             nkeys = it.k1 - it.k0;
+          }
+        } else if constexpr (kSparse) {  // q_lift and q_pe rows of head r of token it.id
+          row_ok = r < p.H;
+          if (row_ok) {
+            qrow = p.q + ((int64_t)it.id * p.H + r) * kLatent;
+            qpe = p.q_pe + ((int64_t)it.id * p.H + r) * kRope;
           }
         } else {
           const int64_t f = (int64_t)it.id * kRows + r;
@@ -654,15 +760,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
             nkeys = keys_for_token(p, tt);
           }
         }
+        if (!kSparse && row_ok) qpe = qrow + kLatent;
         // warm L2 with the next item's query row while this item runs (its Q load then
         // does not wait on HBM at the item boundary)
         {
-          ItemIterT<kDecode> peek = iter;
+          ItemIterT<kDecode, kSparse> peek = iter;
           ItemT nx;
           if (peek.next(nx) && nx.J > 0) {
             const __nv_bfloat16* nq = nullptr;
             if constexpr (decode) {
               if (r < p.H) nq = p.q + ((int64_t)nx.id * p.H + r) * kDk;
+            } else if constexpr (kSparse) {
+              if (r < p.H) {
+                const char* b = reinterpret_cast<const char*>(p.q + ((int64_t)nx.id * p.H + r) * kLatent);
+                for (int o = 0; o < kLatent * 2; o += 128) prefetch_l2(b + o);
+                prefetch_l2(p.q_pe + ((int64_t)nx.id * p.H + r) * kRope);
+              }
             } else {
               const int64_t fn = (int64_t)nx.id * kRows + r;
               if (fn < (int64_t)p.T * p.H) {
@@ -707,7 +820,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
         }
         {
           uint8_t* qpe_row = smem + kOffQpe + r * 128;
-          const uint4* src = row_ok ? reinterpret_cast<const uint4*>(qrow + kLatent) : nullptr;
+          const uint4* src = row_ok ? reinterpret_cast<const uint4*>(qpe) : nullptr;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             uint4 v = src ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
@@ -724,10 +837,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
         MLA_TRACE_ONLY(trace_wait[24] += clock64() - tq;)
         float m_used = -CUDART_INF_F;  // log2-domain offset of the exponentials
         float l = 0.f;                 // running row sum (relative to m_used)
+        int32_t nidx[4];               // sparse: raw top-k entries of the next tile (key 32 q + lane)
+        if constexpr (kSparse) sparse_tile_entries(p, it.id, 0, nidx);
         for (int j = 0; j < it.J; ++j, ++t) {
           const int sb = t & 1;
-          int64_t nv64 = nkeys - (int64_t)j * kKeysT;  // keys of this tile visible to the row
-          const int nv = (int)(nv64 < 0 ? 0 : (nv64 > kKeysT ? kKeysT : nv64));
+          int nv;                              // keys of this tile visible to the row (sparse: 0 or 128)
+          uint64_t vlo = ~0ull, vhi = ~0ull;   // sparse: which of keys 0-63 / 64-127 are listed
+          if constexpr (kSparse) {
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) w[q] = __ballot_sync(0xffffffffu, nidx[q] >= 0 && nidx[q] < p.S_kv);
+            vlo = row_ok ? (w[0] | ((uint64_t)w[1] << 32)) : 0ull;
+            vhi = row_ok ? (w[2] | ((uint64_t)w[3] << 32)) : 0ull;
+            nv = (vlo | vhi) ? kKeysT : 0;
+            if (j + 1 < it.J) sparse_tile_entries(p, it.id, j + 1, nidx);  // lands during this tile
+          } else {
+            const int64_t nv64 = nkeys - (int64_t)j * kKeysT;
+            nv = (int)(nv64 < 0 ? 0 : (nv64 > kKeysT ? kKeysT : nv64));
+          }
 
           if (!waitb(&bars.s_full[sb], (t >> 1) & 1, X_S_FULL, false)) { live = false; break; }
           tc_fence_after();
@@ -756,8 +883,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
               tmem_ld32(scol + 32 * pp, s0);
               tmem_ld32(scol + 32 * pp + 32, s1);
               tmem_wait_ld();
-              mask_piece<kUp>(s0, nv - 32 * pp);
-              mask_piece<kUp>(s1, nv - 32 * pp - 32);
+              if constexpr (kSparse) {
+                const uint64_t w = pp == 0 ? vlo : vhi;
+                mask_bits<kUp>(s0, (uint32_t)w);
+                mask_bits<kUp>(s1, (uint32_t)(w >> 32));
+              } else {
+                mask_piece<kUp>(s0, nv - 32 * pp);
+                mask_piece<kUp>(s1, nv - 32 * pp - 32);
+              }
               row_extreme<kUp>(s0, eq);
               row_extreme<kUp>(s1, eq);
             }
@@ -783,7 +916,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
               uint32_t sr[32];
               tmem_ld32(scol + 32 * p32, sr);
               tmem_wait_ld();
-              mask_piece<kUp>(sr, nv - 32 * p32);
+              if constexpr (kSparse) mask_bits<kUp>(sr, (uint32_t)((p32 < 2 ? vlo : vhi) >> (32 * (p32 & 1))));
+              else mask_piece<kUp>(sr, nv - 32 * p32);
               row_exp<kUp, kFp8>(sr, sl2x2, nmsub2, prow + (p32 >> 1) * kPBoxBytes, (4 * p32) & 7, r, rsq, eq);
             }
             const float mt = tile_offset(eq);
@@ -822,18 +956,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
     // =====================================================================
     // O-CTA
     // =====================================================================
-    if (kFp8 ? (warp == 4 || warp >= 6) : (warp == 4 || warp == 8)) {
+    if ((kFp8 || kSparse) ? (warp == 4 || warp >= 6) : (warp == 4 || warp == 8)) {
       // ---------------- TMA producers: V halves (64 keys x 512 columns), epilogue stages ----------------
       // Ring slot h holds key half h of every tile (and then rows 64 h .. 64 h + 63 of the
       // epilogue); warp 4 fills slot 0 and warp 8 slot 1, each at its own issue rate.
       // Decode: the same warp also brings half h of tile j + kPrefetchTiles into L2 (one bulk
       // prefetch of its 64 contiguous cache rows when they lie in one page), so the S-CTA's K
       // loads of that tile hit L2: its one-tile K ring cannot cover the latency of HBM.
-      // FP8: eight warps convert the slots, four per half, two column boxes each (warp 4 and
-      // warps 6-12 in order: half = index / 4, boxes 2 (index % 4) and the next).
+      // FP8 and sparse: eight warps fill the slots, four per half, two column boxes each (warp
+      // 4 and warps 6-12 in order: half = index / 4, boxes 2 (index % 4) and the next).
+      constexpr bool kEight = kFp8 || kSparse;
       const int vq = (warp == 4) ? 0 : warp - 5;
-      const int h = kFp8 ? (vq >> 2) : ((warp == 4) ? 0 : 1);
-      const int qq = kFp8 ? (vq & 3) : 0;
+      const int h = kEight ? (vq >> 2) : ((warp == 4) ? 0 : 1);
+      const int qq = kEight ? (vq & 3) : 0;
       const uint32_t dst = smem_u32(smem + kOffV + h * kHalfBytesV);
       uint32_t m = 0;  // uses of this slot
       bool live = true;
@@ -848,21 +983,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
           const int64_t kp = it.k0 + (int64_t)kPrefetchTiles * kKeysT + 64 * h;
           if (pf_ok && kp + 64 <= len) pf_pg = __ldg(bt + kp / p.page_size);
         }
+        if constexpr (kSparse) ids = sparse_half_ids(p, it.id, 64 * h);
         for (int j = 0; j < it.J && live; ++j, ++m) {
           const int64_t kh = it.k0 + (int64_t)j * kKeysT + 64 * h;
           HalfIds cur;
+          if constexpr (kSparse) {
+            cur = ids;
+            if (j + 1 < it.J) ids = sparse_half_ids(p, it.id, kh + kKeysT);
+          }
           if constexpr (decode) {
             cur = ids;
             if (j + 1 < it.J) ids = load_half_ids(p, it.id, len, kh + kKeysT);
             const int64_t kp = kh + (int64_t)kPrefetchTiles * kKeysT;
             if (lane == 0 && qq == 0 && pf_pg >= 0 && pf_pg < p.num_pages) {
               const int64_t row = pf_pg * (int64_t)p.page_size + kp % p.page_size;
-              if constexpr (kFp8) bulk_prefetch_l2(p.cache8 + row * kDk, 64 * kDk);
-              else bulk_prefetch_l2(p.cache + row * kDk, 64 * kDk * 2);
+              if constexpr (kFp8) bulk_prefetch_l2_hint<kHintPf>(p.cache8 + row * kDk, 64 * kDk);
+              else bulk_prefetch_l2_hint<kHintPf>(p.cache + row * kDk, 64 * kDk * 2);
             }
             pf_pg = (pf_ok && kp + kKeysT + 64 <= len) ? __ldg(bt + (kp + kKeysT) / p.page_size) : -1;
           }
           if (!waitb(&bars.vempty[h], (m & 1) ^ 1, X_V_EMPTY, false)) { live = false; break; }
+          if constexpr (kSparse) {  // each lane arrives (noinc) once its row copies land
+            gather_half_sparse<2>(dst + 2 * qq * kBoxBytesV, kBoxBytesV, 2 * qq, p, cur, &bars.vfull[h]);
+            continue;
+          }
           if constexpr (kFp8) {
             fill_half_fp8<2>(smem + kOffV + h * kHalfBytesV + 2 * qq * kBoxBytesV, kBoxBytesV, 2 * qq, p, len, kh, cur,
                              err);
@@ -879,7 +1023,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
             if (lane < kVBoxes)
               tma_load_2d(dst + lane * kBoxBytesV, &map_v, lane * kBoxCols, j * kKeysT + 64 * h, &bars.vfull[h]);
           } else {
-            issue_half(dst, kBoxBytesV, 0, kVBoxes, p, maps, len, kh, cur, &bars.vfull[h], err);
+            issue_half<kHintV>(dst, kBoxBytesV, 0, kVBoxes, p, maps, len, kh, cur, &bars.vfull[h], err);
           }
           __syncwarp();
         }
@@ -887,7 +1031,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
         if (staged && it.J > 0 && live) {
           if (!waitb(&bars.vempty[h], (m & 1) ^ 1, X_V_EMPTY, false)) { live = false; break; }
           const int64_t row0 = (int64_t)it.id * kRows + h * 64;
-          if (p.prev_out && row0 < (int64_t)p.T * p.H) {
+          if (kSparse) {  // no prev: every lane of the half's four warps arrives
+            mbar_arrive(&bars.vfull[h]);
+          } else if (p.prev_out && row0 < (int64_t)p.T * p.H) {
             if (lane == 0) mbar_arrive_expect_tx(&bars.vfull[h], kHalfBytesV);
             __syncwarp();
             if (lane < kVBoxes)
@@ -901,6 +1047,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
           ++m;
         }
       }
+      if constexpr (kSparse) cp_async_wait_all();  // no copy into this CTA outlives it
     } else if (warp == 5) {
       // ---------------- P V issuer ----------------
       if (lane == 0) {
@@ -917,6 +1064,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
               const int s = u & 1;
               if (!wait1(&bars.vfull[s], (u >> 1) & 1, X_V_FULL, false)) { live = false; break; }
               tc_fence_after();
+              if constexpr (kSparse) fence_proxy_async_smem();  // cp.async rows, read by the MMA
               const uint32_t vst = smem_u32(smem + kOffV + s * kHalfBytesV);
               const uint32_t pst = smem_u32(smem + kOffPO + pb * kPBytesT + h * kPBoxBytes);
               mma_pv_k64_n512(tbase, tbase + 256, sdesc_sw128(pst, 16, 1024), sdesc_sw128(vst, kBoxBytesV, 1024),
@@ -956,6 +1104,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
           if (row_ok) {
             orow_f = p.part_o + ((int64_t)it.slot * p.H + r) * kLatent;
             lse_dst = p.part_lse + (int64_t)it.slot * p.H + r;
+          }
+        } else if constexpr (kSparse) {  // out [S, H * 512] = rows (t, h); lse [S, H] (nullable)
+          row_ok = r < p.H;
+          if (row_ok) {
+            const int64_t f = (int64_t)it.id * p.H + r;
+            orow = p.out + f * kLatent;
+            if (p.lse) lse_dst = p.lse + f;
           }
         } else {
           const int64_t f = (int64_t)it.id * kRows + r;
@@ -1055,6 +1210,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
           ++i;
           continue;
         }
+        if (!staged) {
+          // sparse with H < 128: each row stores its own bf16 row
+#pragma unroll 1
+          for (int c0 = 0; c0 < kLatent; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tbase + lane_base + c0, v);
+            tmem_wait_ld();
+            if (row_ok) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                dst[q] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * q]) * cn, __uint_as_float(v[8 * q + 1]) * cn),
+                                    pack_bf16x2(__uint_as_float(v[8 * q + 2]) * cn, __uint_as_float(v[8 * q + 3]) * cn),
+                                    pack_bf16x2(__uint_as_float(v[8 * q + 4]) * cn, __uint_as_float(v[8 * q + 5]) * cn),
+                                    pack_bf16x2(__uint_as_float(v[8 * q + 6]) * cn, __uint_as_float(v[8 * q + 7]) * cn));
+            }
+          }
+          tc_fence_before();
+          warp_arrive(&bars.o_free);
+          if (row_ok && lse_dst) *lse_dst = lse_out;
+          ++i;
+          continue;
+        }
         // rows of this half live in ring slot (u + half), [8 column boxes][64 rows][128 B] swizzled
         const uint32_t sidx = u + half;
         const int s = sidx & 1;
@@ -1090,7 +1268,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
         }
         tc_fence_before();
         warp_arrive(&bars.o_free);  // O has been read: the next item's P V may start
-        if (row_ok) *lse_dst = lse_out;
+        if (row_ok && lse_dst) *lse_dst = lse_out;
         fence_proxy_async_smem();
         // both warps of this half staged their rows (a bounded wait, unlike a named barrier)
         warp_arrive(&bars.ep_half[half]);
@@ -1134,6 +1312,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
   if (warp == 5) tmem_dealloc(tbase, 512);
 }
 
+template <bool kUp, bool kDecode>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
+    mla_prefill128_kernel(const __grid_constant__ CoreParams p, const __grid_constant__ CoreMaps maps) {
+  prefill128_body<kUp, kDecode, false, false>(p, maps);
+}
+
+// Decode over the e4m3 cache.
+template <bool kUp>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
+    mla_prefill128_fp8_kernel(const __grid_constant__ CoreParams p, const __grid_constant__ CoreMaps maps) {
+  prefill128_body<kUp, true, true, false>(p, maps);
+}
+
+// Top-k sparse attention (the scale is positive).
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsT, 1)
+    mla_prefill128_sparse_kernel(const __grid_constant__ CoreParams p, const __grid_constant__ CoreMaps maps) {
+  prefill128_body<true, false, false, true>(p, maps);
+}
+
 }  // namespace
 
 #ifdef MLA_TRACE
@@ -1155,27 +1352,30 @@ cudaError_t launch_prefill128(const CoreParams& p, const CoreMaps& maps, cudaStr
     auto set = [&](const void* fn) {
       if (r == cudaSuccess) r = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemT);
     };
-    set((const void*)mla_prefill128_kernel<true, false, false>);
-    set((const void*)mla_prefill128_kernel<false, false, false>);
-    set((const void*)mla_prefill128_kernel<true, true, false>);
-    set((const void*)mla_prefill128_kernel<false, true, false>);
-    set((const void*)mla_prefill128_kernel<true, true, true>);
-    set((const void*)mla_prefill128_kernel<false, true, true>);
+    set((const void*)mla_prefill128_kernel<true, false>);
+    set((const void*)mla_prefill128_kernel<false, false>);
+    set((const void*)mla_prefill128_kernel<true, true>);
+    set((const void*)mla_prefill128_kernel<false, true>);
+    set((const void*)mla_prefill128_fp8_kernel<true>);
+    set((const void*)mla_prefill128_fp8_kernel<false>);
+    set((const void*)mla_prefill128_sparse_kernel);
     return r;
   });
   if (e != cudaSuccess) return e;
   if (p.num_pairs <= 0) return cudaSuccess;
   const dim3 grid(2 * p.num_pairs), block(kThreadsT);
   const bool up = p.scale_log2 >= 0.f;
-  if (p.mode == MODE_DECODE && p.cache8) {
-    if (up) mla_prefill128_kernel<true, true, true><<<grid, block, kSmemT, stream>>>(p, maps);
-    else mla_prefill128_kernel<false, true, true><<<grid, block, kSmemT, stream>>>(p, maps);
+  if (p.mode == MODE_SPARSE) {
+    mla_prefill128_sparse_kernel<<<grid, block, kSmemT, stream>>>(p, maps);
+  } else if (p.mode == MODE_DECODE && p.cache8) {
+    if (up) mla_prefill128_fp8_kernel<true><<<grid, block, kSmemT, stream>>>(p, maps);
+    else mla_prefill128_fp8_kernel<false><<<grid, block, kSmemT, stream>>>(p, maps);
   } else if (p.mode == MODE_DECODE) {
-    if (up) mla_prefill128_kernel<true, true, false><<<grid, block, kSmemT, stream>>>(p, maps);
-    else mla_prefill128_kernel<false, true, false><<<grid, block, kSmemT, stream>>>(p, maps);
+    if (up) mla_prefill128_kernel<true, true><<<grid, block, kSmemT, stream>>>(p, maps);
+    else mla_prefill128_kernel<false, true><<<grid, block, kSmemT, stream>>>(p, maps);
   } else {
-    if (up) mla_prefill128_kernel<true, false, false><<<grid, block, kSmemT, stream>>>(p, maps);
-    else mla_prefill128_kernel<false, false, false><<<grid, block, kSmemT, stream>>>(p, maps);
+    if (up) mla_prefill128_kernel<true, false><<<grid, block, kSmemT, stream>>>(p, maps);
+    else mla_prefill128_kernel<false, false><<<grid, block, kSmemT, stream>>>(p, maps);
   }
   return cudaGetLastError();
 }

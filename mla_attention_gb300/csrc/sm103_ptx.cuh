@@ -214,6 +214,17 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
 // ---------------------------------------------------------------------------
 // TMA
 // ---------------------------------------------------------------------------
+// L2 eviction priorities for streamed data (createpolicy: the whole access range gets the
+// priority).  kL2Keep marks lines that are read again soon (evict last), kL2Done lines whose
+// last read this is (evict first); kL2Plain gives no hint.
+enum L2Hint : int { kL2Plain = 0, kL2Keep = 1, kL2Done = 2 };
+template <int kHint>
+__device__ __forceinline__ uint64_t l2_policy() {
+  uint64_t pol = 0;
+  if constexpr (kHint == kL2Keep) asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  if constexpr (kHint == kL2Done) asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst_smem, const void* tmap, int32_t x, int32_t y,
                                             uint64_t* bar) {
   asm volatile(
@@ -221,6 +232,20 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst_smem, const void* tmap,
           "r"(dst_smem),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
+}
+// The same with an L2 eviction priority (see l2_policy).
+template <int kHint>
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst_smem, const void* tmap, int32_t x, int32_t y,
+                                                 uint64_t* bar) {
+  if constexpr (kHint == 0) {
+    tma_load_2d(dst_smem, tmap, x, y, bar);
+  } else {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+        "%3}], [%4], %5;" ::"r"(dst_smem),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(l2_policy<kHint>())
+        : "memory");
+  }
 }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst_smem, const void* tmap, int32_t x, int32_t y, int32_t z,
@@ -506,6 +531,17 @@ __device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t mas
 // instruction for a whole contiguous range, no shared memory and no completion to wait for.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* ptr, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+
+template <int kHint>
+__device__ __forceinline__ void bulk_prefetch_l2_hint(const void* ptr, uint32_t bytes) {
+  if constexpr (kHint == kL2Plain) {
+    bulk_prefetch_l2(ptr, bytes);
+  } else {
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(ptr), "r"(bytes),
+                 "l"(l2_policy<kHint>())
+                 : "memory");
+  }
 }
 
 __device__ __forceinline__ void prefetch_l2(const void* ptr) {

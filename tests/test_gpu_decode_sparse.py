@@ -92,31 +92,59 @@ def test_decode_full_size_all_rows():
 
 
 # ---------------------------------------------------------------------------
-def _sparse(SI):
+@pytest.fixture(params=[128, 64], ids=["sparse128", "sparse64"])
+def sparse_engine(request):
+    """Both tile engines for mla_sparse (it follows the prefill setting): 128-key tiles (the
+    default) and 64-key tiles."""
+    set_tile_keys(prefill_keys=request.param)
+    yield request.param
+    set_tile_keys(0, 0)
+
+
+def _sparse(SI, lse=None):
     out, lse = mla_sparse(SI.q_lift.to(dev()), SI.q_pe.to(dev()), SI.c_kv.to(dev()), SI.k_pe.to(dev()),
-                          SI.topk.to(dev()), SI.scale)
+                          SI.topk.to(dev()), SI.scale, lse=lse)
     torch.cuda.synchronize()
     check_device_status()
     return out, lse
 
 
-@pytest.mark.parametrize("S,S_kv,H,K,pos0", [(64, 300, 16, 128, 200), (40, 2048, 128, 256, 1900),
-                                             (33, 100, 128, 130, 0)])
-def test_sparse_parity(S, S_kv, H, K, pos0):
+@pytest.mark.parametrize("S,S_kv,H,K,pos0", [
+    (64, 300, 16, 128, 200),
+    (40, 2048, 128, 256, 1900),
+    (33, 100, 128, 130, 0),        # a second tile with two listed keys
+    (9, 5000, 128, 512, 4990),     # H = 128: rows staged and stored by TMA
+    (21, 3000, 64, 384, 2900),     # H = 64: rows stored by the row threads
+    (1, 700, 100, 200, 650),       # one token, H not a multiple of 32
+])
+def test_sparse_parity(S, S_kv, H, K, pos0, sparse_engine):
     SI = gen.sparse_inputs(S, S_kv, H, K, pos0, seed=S + K)
     # plant padding and a duplicate
     SI.topk[0, 0, 5] = -1
-    SI.topk[0, 1, 7] = S_kv + 5
-    SI.topk[0, 2, 9] = SI.topk[0, 2, 8]
-    if K >= 192:
-        SI.topk[0, 3, 64:128] = -1         # a whole 64-row tile of padding mid-list
+    if S > 1:
+        SI.topk[0, 1, 7] = S_kv + 5
+        SI.topk[0, 2, 9] = SI.topk[0, 2, 8]
+    if K >= 192 and S > 3:
+        SI.topk[0, 3, 64:128] = -1         # a whole 64-key tile of padding mid-list
+    if K >= 384 and S > 4:
+        SI.topk[0, 4, 128:256] = -1        # a whole 128-key tile of padding mid-list
     out, lse = _sparse(SI)
     ro, rl = mo.mla_sparse(SI.q_lift, SI.q_pe, SI.c_kv, SI.k_pe, SI.topk, SI.scale)
     assert_out_close(out, ro)
     assert_lse_close(lse, rl)
 
 
-def test_sparse_row_set_is_exact():
+@pytest.mark.parametrize("H", [128, 48])
+def test_sparse_without_lse(H, sparse_engine):
+    """lse is optional: the output is the same without it."""
+    SI = gen.sparse_inputs(12, 800, H, 256, 700, seed=77)
+    out, none = _sparse(SI, lse=False)
+    assert none is None
+    ro, _ = mo.mla_sparse(SI.q_lift, SI.q_pe, SI.c_kv, SI.k_pe, SI.topk, SI.scale)
+    assert_out_close(out, ro)
+
+
+def test_sparse_row_set_is_exact(sparse_engine):
     S, S_kv, H, K = 16, 512, 4, 128
     SI = gen.sparse_inputs(S, S_kv, H, K, pos0=S_kv - S, seed=11)
     SI.topk[0, 3, 10:20] = -1
@@ -138,7 +166,7 @@ def test_sparse_row_set_is_exact():
         assert abs(float(lse[0, s, 1]) - math.log(n)) < 5e-3
 
 
-def test_sparse_all_padding_row():
+def test_sparse_all_padding_row(sparse_engine):
     SI = gen.sparse_inputs(4, 64, 16, 64, pos0=60, seed=12)
     SI.topk[0, 2, :] = -1
     out, lse = _sparse(SI)

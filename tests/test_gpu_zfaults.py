@@ -30,7 +30,7 @@ def _expect_timeout(run):
 
 @pytest.fixture(params=[128, 64], ids=["keys128", "keys64"])
 def engine(request):
-    """Both tile engines: the abort path of each instantiation is driven."""
+    """Both tile engines (prefill, decode and sparse): the abort path of each instantiation is driven."""
     set_tile_keys(request.param, request.param)
     yield request.param
     set_tile_keys(0, 0)
@@ -66,7 +66,7 @@ def test_decode_timeout(engine):
     assert torch.isfinite(out.float()).all()
 
 
-def test_sparse_timeout():
+def test_sparse_timeout(engine):
     S = gen.sparse_inputs(S=8, S_kv=300, H=16, K=128, pos0=200, seed=4)
     d = dev()
     a = [S.q_lift.to(d), S.q_pe.to(d), S.c_kv.to(d), S.k_pe.to(d), S.topk.to(d), S.scale]
