@@ -83,6 +83,7 @@ struct BarsT {
   uint64_t s_free[2];          // every row warp read S buffer b
   uint64_t q_full;             // Q of the item in TMEM / smem
   uint64_t q_taken;            // both issuers passed q_full (count 2)
+  uint64_t q_free;             // every S MMA of the item is done: Q may be replaced (one commit per issuer)
   uint64_t pwritten[2];        // rows wrote local P buffer b
   uint64_t pbuf_free[2];       // the copy out of local P buffer b has been read
   uint64_t stats_free;         // the O-CTA read the row statistics (remote)
@@ -105,6 +106,7 @@ static_assert(sizeof(BarsT) <= 512, "barrier block too large");
 enum : uint32_t {
   X_K_EMPTY = 0x40, X_K_FULL, X_S_FREE, X_S_FULL, X_Q_FULL, X_Q_TAKEN, X_P_WRITTEN, X_PBUF_FREE, X_PB_FREE,
   X_STATS_FREE, X_V_EMPTY, X_V_FULL, X_P_FULL, X_P_READY, X_PV_DONE, X_STATS_FULL, X_O_FREE, X_STALL, X_EP_HALF,
+  X_Q_FREE,
   X_ALIGN = 0x4F, X_PAGE = 0x50, X_LEN = 0x51,
 };
 
@@ -380,6 +382,57 @@ __device__ __forceinline__ void fill_half_fp8(uint8_t* dst, uint32_t box_stride,
   }
 }
 
+// ---- Q of an item: latent part -> TMEM (256 columns), RoPE part -> smem (SW128 K-major) ----
+// Pieces [c_begin, c_end) of 64 latent columns of this thread's query row go to TMEM columns
+// 32 c .. 32 c + 31 of its lane (tq: the lane's TMEM address of the Q region); two pieces'
+// loads are in flight together.  Warp-uniform (tcgen05.st is warp-collective).  The row warps
+// and four producer warps (one per TMEM lane quadrant) split the pieces, so the next item's
+// Q is in place sooner.  FP8 decode: the MMAs take f16 operands.
+template <bool kF16>
+__device__ __forceinline__ void load_q_pieces(uint32_t tq, const __nv_bfloat16* qrow, int c_begin, int c_end) {
+#pragma unroll 1
+  for (int c0 = c_begin; c0 < c_end; c0 += 2) {
+    const bool two = c0 + 1 < c_end;
+    uint4 x[2][8];
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      const uint4* src = (qrow && (cc == 0 || two)) ? reinterpret_cast<const uint4*>(qrow + 64 * (c0 + cc)) : nullptr;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) x[cc][u] = src ? __ldg(src + u) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      if (cc == 1 && !two) break;
+      uint32_t v[32];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        v[4 * u + 0] = x[cc][u].x;
+        v[4 * u + 1] = x[cc][u].y;
+        v[4 * u + 2] = x[cc][u].z;
+        v[4 * u + 3] = x[cc][u].w;
+      }
+      if constexpr (kF16) {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) v[u] = bf16x2_to_f16x2(v[u]);
+      }
+      tmem_st32(tq + 32 * (c0 + cc), v);
+    }
+  }
+}
+template <bool kF16>
+__device__ __forceinline__ void load_q_rope(uint8_t* qpe_row, const __nv_bfloat16* qpe, int r) {
+  const uint4* src = reinterpret_cast<const uint4*>(qpe);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint4 v = src ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+    if constexpr (kF16)
+      v = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+    *reinterpret_cast<uint4*>(qpe_row + ((c ^ (r & 7)) << 4)) = v;
+  }
+  fence_proxy_async_smem();  // read by the MMA through the async proxy
+}
+constexpr int kQRowPieces = 3;  // latent pieces the row warps load; the producers load the rest and the RoPE part
+
 // ---- softmax rows: one 32-column piece of a score row ----
 // Keys of a piece past lim (the visible keys in it) get the score -inf (+inf when the scale
 // is negative), so one mask-free body serves every piece: the extreme ignores them and
@@ -493,8 +546,9 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
         mbar_init(&bars.pbuf_free[b], 1);
         mbar_init(&bars.pb_free[b], 1);
       }
-      mbar_init(&bars.q_full, kRowWarpsS);
+      mbar_init(&bars.q_full, kRowWarpsS + (kDecode ? 0 : 4));  // the row warps (and producer warps 8-11)
       mbar_init(&bars.q_taken, 2);
+      mbar_init(&bars.q_free, 2);
       mbar_init(&bars.stats_free, kRowWarpsO);
     } else {
       for (int b = 0; b < 2; ++b) {
@@ -576,6 +630,30 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
   if (p.debug_stall && warp == 5) waitb(&bars.stall, 0, X_STALL, false);  // runs out: injected fault
 
   ItemIterT<kDecode, kSparse> iter;
+  // The query row of row r of an item: its latent part (512 columns) and RoPE part (64), or
+  // null for a row past the item's end.
+  auto q_row_ptrs = [&](const ItemT& itm, int r, const __nv_bfloat16*& qr, const __nv_bfloat16*& qp) {
+    qr = nullptr;
+    qp = nullptr;
+    if constexpr (decode) {
+      if (r < p.H) {
+        qr = p.q + ((int64_t)itm.id * p.H + r) * kDk;
+        qp = qr + kLatent;
+      }
+    } else if constexpr (kSparse) {  // q_lift and q_pe rows of head r of token itm.id
+      if (r < p.H) {
+        qr = p.q + ((int64_t)itm.id * p.H + r) * kLatent;
+        qp = p.q_pe + ((int64_t)itm.id * p.H + r) * kRope;
+      }
+    } else {
+      const int64_t f = (int64_t)itm.id * kRows + r;
+      if (f < (int64_t)p.T * p.H) {
+        const int64_t tt = f / p.H, hh = f - tt * p.H;
+        qr = p.q + tt * p.q_stride_t + hh * p.q_stride_h;
+        qp = qr + kLatent;
+      }
+    }
+  };
   iter.init(p, pair);
   ItemT it;
   // abort drain: the last barrier phase this thread's TMA loads were counted on
@@ -597,7 +675,10 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
       const int q = (warp == 4) ? 0 : warp - 7;
       const int k = q % kGroups, h = q / kGroups;
       const uint32_t dst = smem_u32(smem + kOffK + k * kGroupBytes + h * kBoxBytesV);
-      uint32_t t = 0;
+      // prefill and sparse: one per TMEM lane quadrant, they load most of each item's Q (decode has
+      // few, long items: its rows load Q alone)
+      const bool q_helper = !kDecode && warp >= 8 && warp <= 11;
+      uint32_t t = 0, items = 0;
       bool live = true;
       while (live && iter.next(it)) {
         const int len = decode ? decode_len_t(p, it.id) : 0;
@@ -620,26 +701,39 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
           uint64_t* fb = &bars.kfull[k][par];
           if constexpr (kSparse) {  // the listed rows by cp.async; each lane arrives (noinc) once they land
             gather_half_sparse<3>(dst, kBoxBytesK, 3 * k, p, cur, fb);
-            continue;
-          }
-          if constexpr (kFp8) {  // ordinary loads, converted into the slot, then one arrival
+          } else if constexpr (kFp8) {  // ordinary loads, converted into the slot, then one arrival
             fill_half_fp8<3>(smem + kOffK + k * kGroupBytes + h * kBoxBytesV, kBoxBytesK, 3 * k, p, len, kh, cur, err);
             fence_proxy_async_smem();  // the MMA reads the slot through the async proxy
             __syncwarp();
             if (lane == 0) mbar_arrive(fb);
-            continue;
-          }
-          if (lane == 0) mbar_arrive_expect_tx(fb, kGroupBytes / 2);
-          drain_bar = fb;
-          drain_par = (t >> 1) & 1;
-          __syncwarp();
-          if constexpr (!decode) {  // one box per lane: lanes overlap their TMA issues
-            if (lane < 3) tma_load_2d(dst + lane * kBoxBytesK, &map_v, (3 * k + lane) * kBoxCols, j * kKeysT + 64 * h, fb);
           } else {
-            issue_half<kHintK>(dst, kBoxBytesK, 3 * k * kBoxCols, 3, p, maps, len, kh, cur, fb, err);
+            if (lane == 0) mbar_arrive_expect_tx(fb, kGroupBytes / 2);
+            drain_bar = fb;
+            drain_par = (t >> 1) & 1;
+            __syncwarp();
+            if constexpr (!decode) {  // one box per lane: lanes overlap their TMA issues
+              if (lane < 3) tma_load_2d(dst + lane * kBoxBytesK, &map_v, (3 * k + lane) * kBoxCols, j * kKeysT + 64 * h, fb);
+            } else {
+              issue_half<kHintK>(dst, kBoxBytesK, 3 * k * kBoxCols, 3, p, maps, len, kh, cur, fb, err);
+            }
+            __syncwarp();
           }
-          __syncwarp();
+          if (q_helper && j == 0) {
+            // This item's Q: latent pieces kQRowPieces.. and the RoPE part of the rows of this warp's
+            // TMEM lane quadrant, once every S MMA of the previous item is done (both issuers commit
+            // to q_free after their last tile of an item), so the Q region and the RoPE box are free.
+            if (items > 0 && !waitb(&bars.q_free, (items - 1) & 1, X_Q_FREE, false)) { live = false; break; }
+            const int rq = (warp & 3) * 32 + lane;
+            const __nv_bfloat16 *qr, *qp;
+            q_row_ptrs(it, rq, qr, qp);
+            load_q_pieces<kFp8>(tbase + ((uint32_t)((warp & 3) * 32) << 16) + kTmemQ, qr, kQRowPieces, 8);
+            load_q_rope<kFp8>(smem + kOffQpe + rq * 128, qp, rq);
+            tmem_wait_st();
+            tc_fence_before();
+            warp_arrive(&bars.q_full);
+          }
         }
+        if (it.J > 0) ++items;
       }
       if constexpr (kSparse) cp_async_wait_all();  // no copy into this CTA outlives it
     } else if (warp == 5 || warp == 6) {
@@ -687,6 +781,8 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
             mma_commit(&bars.s_full[b]);
             ++nb;
           }
+          if (!live) break;
+          if (!kDecode) mma_commit(&bars.q_free);  // arrives once this issuer's MMAs of the item (reading Q) are done
           ++i;
         }
       }
@@ -735,101 +831,34 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
       while (live && iter.next(it)) {
         if (it.J == 0) continue;  // no key: the O-CTA writes these rows on its own
         // this row's query and the keys it sees from the item's first tile on
-        bool row_ok;
-        const __nv_bfloat16* qrow = nullptr;  // the latent part (512 columns)
-        const __nv_bfloat16* qpe = nullptr;   // the RoPE part (64 columns)
-        int64_t nkeys = 0;
-        if constexpr (decode) {
-          row_ok = r < p.H;
-          if (row_ok) {
-            qrow = p.q + ((int64_t)it.id * p.H + r) * kDk;
-            nkeys = it.k1 - it.k0;
-          }
-        } else if constexpr (kSparse) {  // q_lift and q_pe rows of head r of token it.id
-          row_ok = r < p.H;
-          if (row_ok) {
-            qrow = p.q + ((int64_t)it.id * p.H + r) * kLatent;
-            qpe = p.q_pe + ((int64_t)it.id * p.H + r) * kRope;
-          }
-        } else {
-          const int64_t f = (int64_t)it.id * kRows + r;
-          row_ok = f < (int64_t)p.T * p.H;
-          if (row_ok) {
-            const int64_t tt = f / p.H, hh = f - tt * p.H;
-            qrow = p.q + tt * p.q_stride_t + hh * p.q_stride_h;
-            nkeys = keys_for_token(p, tt);
-          }
+        const __nv_bfloat16 *qrow, *qpe;
+        q_row_ptrs(it, r, qrow, qpe);
+        const bool row_ok = qrow != nullptr;
+        int64_t nkeys = 0;  // keys the row sees from the item's first tile on (prefill, decode)
+        if (row_ok) {
+          if constexpr (decode) nkeys = it.k1 - it.k0;
+          else if constexpr (!kSparse) nkeys = keys_for_token(p, ((int64_t)it.id * kRows + r) / p.H);
         }
-        if (!kSparse && row_ok) qpe = qrow + kLatent;
         // warm L2 with the next item's query row while this item runs (its Q load then
         // does not wait on HBM at the item boundary)
         {
           ItemIterT<kDecode, kSparse> peek = iter;
           ItemT nx;
           if (peek.next(nx) && nx.J > 0) {
-            const __nv_bfloat16* nq = nullptr;
-            if constexpr (decode) {
-              if (r < p.H) nq = p.q + ((int64_t)nx.id * p.H + r) * kDk;
-            } else if constexpr (kSparse) {
-              if (r < p.H) {
-                const char* b = reinterpret_cast<const char*>(p.q + ((int64_t)nx.id * p.H + r) * kLatent);
-                for (int o = 0; o < kLatent * 2; o += 128) prefetch_l2(b + o);
-                prefetch_l2(p.q_pe + ((int64_t)nx.id * p.H + r) * kRope);
-              }
-            } else {
-              const int64_t fn = (int64_t)nx.id * kRows + r;
-              if (fn < (int64_t)p.T * p.H) {
-                const int64_t tn = fn / p.H, hn = fn - tn * p.H;
-                nq = p.q + tn * p.q_stride_t + hn * p.q_stride_h;
-              }
-            }
+            const __nv_bfloat16 *nq, *np;
+            q_row_ptrs(nx, r, nq, np);
             if (nq) {
               const char* b = reinterpret_cast<const char*>(nq);
-              for (int o = 0; o < kDk * 2; o += 128) prefetch_l2(b + o);
+              for (int o = 0; o < kLatent * 2; o += 128) prefetch_l2(b + o);
+              prefetch_l2(np);
             }
           }
         }
         MLA_TRACE_ONLY(long long tq = clock64();)
         // ---- Q: latent part -> TMEM (256 columns), RoPE part -> smem (SW128 K-major) ----
         if (i > 0 && !waitb(&bars.q_taken, (i - 1) & 1, X_Q_TAKEN, false)) break;
-#pragma unroll 1
-        for (int c0 = 0; c0 < 8; c0 += 2) {
-          uint4 x[2][8];
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const uint4* src = row_ok ? reinterpret_cast<const uint4*>(qrow + 64 * (c0 + cc)) : nullptr;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) x[cc][u] = src ? __ldg(src + u) : make_uint4(0, 0, 0, 0);
-          }
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            uint32_t v[32];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              v[4 * u + 0] = x[cc][u].x;
-              v[4 * u + 1] = x[cc][u].y;
-              v[4 * u + 2] = x[cc][u].z;
-              v[4 * u + 3] = x[cc][u].w;
-            }
-            if constexpr (kFp8) {  // the MMAs take f16 operands
-#pragma unroll
-              for (int u = 0; u < 32; ++u) v[u] = bf16x2_to_f16x2(v[u]);
-            }
-            tmem_st32(tbase + lane_base + kTmemQ + 32 * (c0 + cc), v);
-          }
-        }
-        {
-          uint8_t* qpe_row = smem + kOffQpe + r * 128;
-          const uint4* src = row_ok ? reinterpret_cast<const uint4*>(qpe) : nullptr;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint4 v = src ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-            if constexpr (kFp8)
-              v = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
-            *reinterpret_cast<uint4*>(qpe_row + ((c ^ (r & 7)) << 4)) = v;
-          }
-          fence_proxy_async_smem();  // read by the MMA through the async proxy
-        }
+        load_q_pieces<kFp8>(tbase + lane_base + kTmemQ, row_ok ? qrow : nullptr, 0, kDecode ? 8 : kQRowPieces);
+        if constexpr (kDecode) load_q_rope<kFp8>(smem + kOffQpe + r * 128, row_ok ? qpe : nullptr, r);
         tmem_wait_st();
         tc_fence_before();
         warp_arrive(&bars.q_full);

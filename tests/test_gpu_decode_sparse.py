@@ -116,6 +116,8 @@ def _sparse(SI, lse=None):
     (9, 5000, 128, 512, 4990),     # H = 128: rows staged and stored by TMA
     (21, 3000, 64, 384, 2900),     # H = 64: rows stored by the row threads
     (1, 700, 100, 200, 650),       # one token, H not a multiple of 32
+    (300, 4000, 128, 256, 3900),   # several items per CTA pair (Q handed from item to item)
+    (200, 1000, 16, 384, 900),
 ])
 def test_sparse_parity(S, S_kv, H, K, pos0, sparse_engine):
     SI = gen.sparse_inputs(S, S_kv, H, K, pos0, seed=S + K)
