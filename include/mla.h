@@ -66,7 +66,10 @@ const char* mla_status_string(mla_status s);
  * Reads and clears the device status word in `workspace` (any workspace that
  * a call of this library was given).  Synchronises `stream` first.  Returns
  * MLA_OK, MLA_ERR_TIMEOUT or MLA_ERR_DEVICE_RANGE; `detail` (nullable)
- * receives the raw word (wait or check site id).
+ * receives the raw word (wait or check site id): 0x1000 | wait site for a timeout,
+ * 0x2000 | check site for an out-of-range page id or length, and, in the guarded build
+ * (libmla_guard.so, compiled with MLA_GUARD), 0x3000 | site for a plain load or store of a
+ * kernel that would have left its buffer (the access was skipped).
  */
 mla_status mla_check_device_status(void* workspace, void* stream, uint32_t* detail);
 

@@ -3,6 +3,11 @@
 Each translation unit is compiled in parallel, then linked into
 mla_attention_gb300/libmla.so against the shared CUDA runtime (the same one
 PyTorch loads).  Objects go to mla_attention_gb300/_build/.
+
+build(guard=True) makes the guarded library instead (libmla_guard.so, objects in
+_build_guard/): compiled with -DMLA_GUARD, every plain global load and store of the
+kernels is checked against the extent of its buffer, skipped when outside it, and
+the first such access is recorded in the status word (mla_check_device_status).
 """
 from __future__ import annotations
 
@@ -16,6 +21,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmla.so")
+OBJ_GUARD = os.path.join(PKG, "_build_guard")
+LIB_GUARD = os.path.join(PKG, "libmla_guard.so")
 ROOT = os.path.dirname(PKG)
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -34,26 +41,28 @@ def sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def _needs_rebuild(objs) -> bool:
-    if not os.path.exists(LIB):
+def _needs_rebuild(lib) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = sources() + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     deps.append(os.path.join(ROOT, "include", "mla.h"))
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, guard: bool = False) -> str:
     nvcc = _nvcc()
-    os.makedirs(OBJ, exist_ok=True)
+    obj_dir, lib = (OBJ_GUARD, LIB_GUARD) if guard else (OBJ, LIB)
+    flags = NVCC_FLAGS + (["-DMLA_GUARD"] if guard else [])
+    os.makedirs(obj_dir, exist_ok=True)
     srcs = sources()
-    objs = [os.path.join(OBJ, os.path.basename(s)[:-3] + ".o") for s in srcs]
-    if not force and not _needs_rebuild(objs):
-        return LIB
+    objs = [os.path.join(obj_dir, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    if not force and not _needs_rebuild(lib):
+        return lib
 
     def compile_one(src_obj):
         src, obj = src_obj
-        cmd = [nvcc] + NVCC_FLAGS + ["-c", src, "-o", obj]
+        cmd = [nvcc] + flags + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         return src, r.returncode, r.stdout + r.stderr
 
@@ -64,16 +73,16 @@ def build(force: bool = False, verbose: bool = False) -> str:
             sys.stderr.write(f"[libmla] {os.path.basename(src)}:\n{log}")
         if rc != 0:
             raise RuntimeError(f"nvcc failed on {src}")
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "shared",
                                                            "-Xlinker", "-rpath,/usr/local/cuda/lib64"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(r.stdout + r.stderr)
         raise RuntimeError("linking libmla.so failed")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, guard="--guard" in sys.argv))

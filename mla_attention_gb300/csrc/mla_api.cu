@@ -243,6 +243,14 @@ mla_status prefill_one(const void* q, int64_t q_stride_t, int64_t q_stride_h, co
   p.out = reinterpret_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.lse_stride = lse_stride;
+  {
+    const uint64_t hs = (uint64_t)(lse_stride ? lse_stride : (int64_t)T);  // head stride of lse / prev_lse
+    p.ext_q = ((uint64_t)(T - 1) * (uint64_t)q_stride_t + (uint64_t)(H - 1) * (uint64_t)q_stride_h + kDk) * 2;
+    p.ext_out = (uint64_t)T * H * kLatent * 2;
+    p.ext_prev_out = prev_out ? p.ext_out : 0;
+    p.ext_lse = ((uint64_t)(H - 1) * hs + (uint64_t)T) * 4;
+    p.ext_prev_lse = prev_lse ? p.ext_lse : 0;
+  }
   const int64_t items = ((int64_t)T * H + kRows - 1) / kRows;
   if (items < p.num_pairs) p.num_pairs = (int)items;
   cudaError_t e = tile128 ? launch_prefill128(p, maps, st) : launch_core(p, maps, st);
@@ -311,6 +319,16 @@ mla_status decode_impl(const void* q, int q_per_req, const void* kv_cache, bool 
   p.part_lse = reinterpret_cast<float*>(w);
   w += align_up(sizeof(float) * slots * (size_t)H, 256);
   p.part_o = reinterpret_cast<float*>(w);
+  p.ext_q = (uint64_t)G * H * kDk * 2;
+  p.ext_out = (uint64_t)G * H * kLatent * 2;
+  p.ext_lse = lse ? (uint64_t)G * H * 4 : 0;
+  p.ext_block_table = (uint64_t)B * max_pages * 4;
+  p.ext_lens = (uint64_t)B * 4;
+  p.ext_cache8 = fp8 ? rows * kDk : 0;
+  p.ext_sinks = sinks ? (uint64_t)H * 4 : 0;
+  p.ext_tile_prefix = ((uint64_t)G + 1) * 4;
+  p.ext_part_lse = slots * H * 4;
+  p.ext_part_o = slots * H * kLatent * 4;
   // FP8 runs on the 128-key engine only
   cudaError_t e = (fp8 || g_decode_keys.load() == 128) ? launch_prefill128(p, maps, st) : launch_core(p, maps, st);
   if (e != cudaSuccess) return cuda_fail(e, "mla_decode launch");
@@ -363,6 +381,8 @@ mla_status mla_check_device_status(void* workspace, void* stream, uint32_t* deta
   if (word == 0) return ok();
   if ((word & 0xF000u) == DEV_TIMEOUT_BASE)
     return fail(MLA_ERR_TIMEOUT, "a device wait ran out of its spin bound (site 0x%x)", word & 0xFFFu);
+  if ((word & 0xF000u) == DEV_GUARD_BASE)
+    return fail(MLA_ERR_DEVICE_RANGE, "guarded build: an access left its buffer (site %u)", word & 0xFFFu);
   return fail(MLA_ERR_DEVICE_RANGE, "a kernel met an out-of-range index (site 0x%x)", word & 0xFFFu);
 }
 
@@ -511,6 +531,13 @@ mla_status mla_sparse(const void* q_lift, const void* q_pe, const void* c_kv, co
   p.k_pe = reinterpret_cast<const __nv_bfloat16*>(k_pe);
   p.K = K;
   p.S_kv = S_kv;
+  p.ext_q = (uint64_t)S * H * kLatent * 2;
+  p.ext_q_pe = (uint64_t)S * H * kRope * 2;
+  p.ext_out = (uint64_t)S * H * kLatent * 2;
+  p.ext_lse = lse ? (uint64_t)S * H * 4 : 0;
+  p.ext_topk = (uint64_t)S * K * 4;
+  p.ext_c_kv = (uint64_t)S_kv * kLatent * 2;
+  p.ext_k_pe = (uint64_t)S_kv * kRope * 2;
   // the prefill engine choice applies to sparse as well (both are context-phase attention)
   cudaError_t e = g_prefill_keys.load() == 128 ? launch_prefill128(p, maps, st) : launch_core(p, maps, st);
   if (e != cudaSuccess) return cuda_fail(e, "mla_sparse launch");

@@ -279,8 +279,8 @@ __device__ __forceinline__ void sparse_tile_idx(const CoreParams& p, int id, int
   const int lane = threadIdx.x & 31;
   const int32_t* tk = p.topk + (int64_t)id * p.K;
   const int c0 = j * kKeys + 2 * lane;
-  re = (c0 < p.K) ? __ldg(tk + c0) : -1;
-  ro = (c0 + 1 < p.K) ? __ldg(tk + c0 + 1) : -1;
+  re = (c0 < p.K && guard_span(p.err, G_TOPK, tk + c0, 4, p.topk, p.ext_topk)) ? __ldg(tk + c0) : -1;
+  ro = (c0 + 1 < p.K && guard_span(p.err, G_TOPK, tk + c0 + 1, 4, p.topk, p.ext_topk)) ? __ldg(tk + c0 + 1) : -1;
 }
 
 // A top-k entry outside [0, S_kv) is padding: no row (-1 gathers zeros).
@@ -297,7 +297,8 @@ __device__ __forceinline__ int32_t sparse_row(const CoreParams& p, int32_t r) {
 // arrives on `bar` (noinc) once its copies have landed; the reader of the stage orders them
 // before its async-proxy reads with a proxy fence.
 __device__ __forceinline__ void lsu_gather_rows(uint32_t dst, const __nv_bfloat16* c_kv, const __nv_bfloat16* k_pe,
-                                                int32_t r_even, int32_t r_odd, uint64_t* bar, int q0, int q1) {
+                                                int32_t r_even, int32_t r_odd, uint64_t* bar, int q0, int q1,
+                                                const CoreParams& p) {
   const int lane = threadIdx.x & 31;
   // latent: lane copies pieces `lane` and `lane + 32` of each 1024-byte row: boxes lane/8 and
   // lane/8 + 4, 16-byte column lane % 8 (XOR the row's swizzle phase)
@@ -309,7 +310,8 @@ __device__ __forceinline__ void lsu_gather_rows(uint32_t dst, const __nv_bfloat1
     const uint32_t rb = dst + (uint32_t)q * 1024u;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const int32_t ri = __shfl_sync(0xffffffffu, (k & 1) ? r_odd : r_even, 4 * q + (k >> 1));
+      int32_t ri = __shfl_sync(0xffffffffu, (k & 1) ? r_odd : r_even, 4 * q + (k >> 1));
+      if (ri >= 0 && !guard_span(p.err, G_C_KV, c_kv + (int64_t)ri * kLatent, kLatent * 2, p.c_kv, p.ext_c_kv)) ri = -1;
       const uint32_t n = ri >= 0 ? 16u : 0u;
       const char* src = base + (int64_t)(ri >= 0 ? ri : 0) * (kLatent * 2);
       cp_async16_zfill(rb + k * 128 + (lp0 ^ ((uint32_t)k << 4)), src, n);
@@ -326,7 +328,8 @@ __device__ __forceinline__ void lsu_gather_rows(uint32_t dst, const __nv_bfloat1
       const int row = 4 * i + rr;
       const int32_t ae = __shfl_sync(0xffffffffu, r_even, 2 * i + (rr >> 1));
       const int32_t ao = __shfl_sync(0xffffffffu, r_odd, 2 * i + (rr >> 1));
-      const int32_t ri = (rr & 1) ? ao : ae;
+      int32_t ri = (rr & 1) ? ao : ae;
+      if (ri >= 0 && !guard_span(p.err, G_K_PE, k_pe + (int64_t)ri * kRope, kRope * 2, p.k_pe, p.ext_k_pe)) ri = -1;
       cp_async16_zfill(box + (uint32_t)row * 128u + ((uint32_t)(c ^ (row & 7)) << 4),
                        pbase + (int64_t)(ri >= 0 ? ri : 0) * (kRope * 2), ri >= 0 ? 16u : 0u);
     }
@@ -421,7 +424,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
       const int b = b0 + lane;
       int n = 0;
       if (b < p.B) {
-        const int raw = p.lens[decode_request(p, b)];
+        const int32_t* lp = p.lens + decode_request(p, b);
+        const int raw = guard_span(err, G_LENS, lp, 4, p.lens, p.ext_lens) ? *lp : 0;
         const int64_t cap = (int64_t)p.max_pages * p.page_size;
         if (raw < 0 || raw > cap) record_error(err, DEV_RANGE_BASE | R_LEN);
         n = (decode_len(p, b) + kKeys - 1) / kKeys;
@@ -432,10 +436,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
         const int v = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += v;
       }
-      if (b < p.B) p.tile_prefix[b] = (int32_t)(run + incl - n);
+      if (b < p.B && guard_span(err, G_TILE_PREFIX, p.tile_prefix + b, 4, p.tile_prefix, p.ext_tile_prefix))
+        p.tile_prefix[b] = (int32_t)(run + incl - n);
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) p.tile_prefix[p.B] = (int32_t)run;
+    if (lane == 0 && guard_span(err, G_TILE_PREFIX, p.tile_prefix + p.B, 4, p.tile_prefix, p.ext_tile_prefix))
+      p.tile_prefix[p.B] = (int32_t)run;
   }
   tc_fence_before();
   cluster_sync();  // barriers of both CTAs initialised before any remote arrive
@@ -473,7 +479,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
         // decode with pages of whole tiles: block-table entry of the next tile, loaded a tile ahead
         const bool whole_pages = !kSparse && p.mode == MODE_DECODE && p.page_size % kKeys == 0;
         int32_t npg = -1;
-        if (whole_pages && it.J > 0) npg = p.block_table[(int64_t)decode_request(p, it.id) * p.max_pages + it.k0 / p.page_size];
+        if (whole_pages && it.J > 0)
+          npg = bt_entry(p, p.block_table + (int64_t)decode_request(p, it.id) * p.max_pages + it.k0 / p.page_size);
         for (int j = 0; j < it.J && live; ++j, ++g) {
           const int s = g & 1;
           // stage s was last read by the S MMA of tile g-2
@@ -497,7 +504,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
               const int32_t* bt = p.block_table + (int64_t)decode_request(p, it.id) * p.max_pages;
               auto row_of = [&](int64_t key) -> int32_t {
                 if (key >= len) return -1;
-                const int32_t pg = bt[key / p.page_size];
+                const int32_t pg = bt_entry(p, bt + key / p.page_size);
                 if (pg < 0 || pg >= p.num_pages) {
                   record_error(err, DEV_RANGE_BASE | R_PAGE);
                   return -1;
@@ -506,7 +513,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
               };
               // pages that hold whole tiles: this tile's entry was loaded a tile ago
               const int32_t pg = npg;
-              if (whole_pages && j + 1 < it.J) npg = bt[(kb + kKeys) / p.page_size];
+              if (whole_pages && j + 1 < it.J) npg = bt_entry(p, bt + (kb + kKeys) / p.page_size);
               if (whole_pages && kb + kKeys <= len && pg >= 0 && pg < p.num_pages) {
                 tiled = true;
                 ytile = (int32_t)(pg * (int64_t)p.page_size + kb % p.page_size);
@@ -522,7 +529,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
             if constexpr (kSparse) {
               // all 576 columns by 16-byte copies: warp 4 copies rows 0-31, warp 9 rows 32-63
               const int q0 = (warp == 4) ? 0 : kKeys / 16;
-              lsu_gather_rows(dst, p.c_kv, p.k_pe, re, ro, &bars.s_go[s], q0, q0 + kKeys / 16);
+              lsu_gather_rows(dst, p.c_kv, p.k_pe, re, ro, &bars.s_go[s], q0, q0 + kKeys / 16, p);
             } else {
               if (lane == 0) mbar_arrive_expect_tx(&bars.s_go[s], kStageBytesS);
               __syncwarp();
@@ -677,6 +684,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
                 src = (c < 8) ? reinterpret_cast<const uint4*>(qrow + c * 64) : reinterpret_cast<const uint4*>(qpe);
               else
                 src = reinterpret_cast<const uint4*>(qrow + c * 64);
+              const bool pe_part = kSparse && c >= 8;
+              if (!guard_span(err, pe_part ? G_Q_PE : G_Q, src, 128, pe_part ? (const void*)p.q_pe : (const void*)p.q,
+                              pe_part ? p.ext_q_pe : p.ext_q))
+                src = nullptr;
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u) x[cc][u] = src ? __ldg(src + u) : make_uint4(0, 0, 0, 0);
@@ -715,8 +726,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
           } else {
             const int32_t* tk = p.topk + (int64_t)it.id * p.K;
             const int c0 = j * kKeys + lane, c1 = c0 + 32;
-            const int32_t i0 = (c0 < p.K) ? tk[c0] : -1;
-            const int32_t i1 = (c1 < p.K) ? tk[c1] : -1;
+            const int32_t i0 = (c0 < p.K && guard_span(err, G_TOPK, tk + c0, 4, p.topk, p.ext_topk)) ? tk[c0] : -1;
+            const int32_t i1 = (c1 < p.K && guard_span(err, G_TOPK, tk + c1, 4, p.topk, p.ext_topk)) ? tk[c1] : -1;
             const uint32_t lo = __ballot_sync(0xffffffffu, i0 >= 0 && i0 < p.S_kv);
             const uint32_t hi = __ballot_sync(0xffffffffu, i1 >= 0 && i1 < p.S_kv);
             vmask = ((uint64_t)hi << 32) | lo;
@@ -819,7 +830,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
         // decode with pages of whole tiles: block-table entry of the next tile, loaded a tile ahead
         const bool whole_pages = !kSparse && p.mode == MODE_DECODE && p.page_size % kKeys == 0;
         int32_t npg = -1;
-        if (whole_pages && it.J > 0) npg = p.block_table[(int64_t)decode_request(p, it.id) * p.max_pages + it.k0 / p.page_size];
+        if (whole_pages && it.J > 0)
+          npg = bt_entry(p, p.block_table + (int64_t)decode_request(p, it.id) * p.max_pages + it.k0 / p.page_size);
         for (int j = 0; j < it.J && live; ++j, ++g) {
           const int s = g % kStagesO;
           if (!waitb(&bars.o_kv_empty[s], ((g / kStagesO) & 1) ^ 1, W_O_KV_EMPTY, false)) { live = false; break; }
@@ -842,13 +854,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
               const int32_t* bt = p.block_table + (int64_t)decode_request(p, it.id) * p.max_pages;
               auto row_of = [&](int64_t key) -> int32_t {
                 if (key >= len) return -1;
-                const int32_t pg = bt[key / p.page_size];
+                const int32_t pg = bt_entry(p, bt + key / p.page_size);
                 if (pg < 0 || pg >= p.num_pages) return -1;
                 return (int32_t)(pg * (int64_t)p.page_size + key % p.page_size);
               };
               // pages that hold whole tiles: this tile's entry was loaded a tile ago
               const int32_t pg = npg;
-              if (whole_pages && j + 1 < it.J) npg = bt[(kb + kKeys) / p.page_size];
+              if (whole_pages && j + 1 < it.J) npg = bt_entry(p, bt + (kb + kKeys) / p.page_size);
               if (whole_pages && kb + kKeys <= len && pg >= 0 && pg < p.num_pages) {
                 tiled = true;
                 ytile = (int32_t)(pg * (int64_t)p.page_size + kb % p.page_size);
@@ -863,7 +875,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
             }
             if constexpr (kSparse) {
               if (lane == 0) mbar_arrive(&bars.o_kv_full[s]);
-              lsu_gather_rows(dst, p.c_kv, nullptr, re, ro, &bars.o_kv_full[s], 0, kKeys / 8);
+              lsu_gather_rows(dst, p.c_kv, nullptr, re, ro, &bars.o_kv_full[s], 0, kKeys / 8, p);
             } else {
               if (lane == 0) mbar_arrive_expect_tx(&bars.o_kv_full[s], kStageBytesO);
               __syncwarp();
@@ -966,7 +978,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
             lse_dst = p.lse + h * (p.lse_stride ? p.lse_stride : (int64_t)p.T) + t;
             if (p.prev_out) {
               prev_row = p.prev_out + f * kLatent;
-              prev_l = p.prev_lse[h * (p.lse_stride ? p.lse_stride : (int64_t)p.T) + t];
+              const float* pl = p.prev_lse + h * (p.lse_stride ? p.lse_stride : (int64_t)p.T) + t;
+              prev_l = guard_span(err, G_PREV_LSE, pl, 4, p.prev_lse, p.ext_prev_lse) ? *pl : -CUDART_INF_F;
             }
           }
         } else if (!kSparse) {
@@ -983,6 +996,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
           }
         }
 
+        // guarded build: a row outside its buffer is not written (or read) at all
+        if (orow && !guard_span(err, G_OUT, orow, kLatent * 2, p.out, p.ext_out)) orow = nullptr;
+        if (orow_f && !guard_span(err, G_PART_O, orow_f, kLatent * 4, p.part_o, p.ext_part_o)) orow_f = nullptr;
+        if (prev_row && !guard_span(err, G_PREV_OUT, prev_row, kLatent * 2, p.prev_out, p.ext_prev_out)) prev_row = nullptr;
+        if (lse_dst) {
+          const bool part = !kSparse && p.mode != MODE_PREFILL;
+          if (!guard_span(err, part ? G_PART_LSE : G_LSE, lse_dst, 4, part ? (const void*)p.part_lse : (const void*)p.lse,
+                          part ? p.ext_part_lse : p.ext_lse))
+            lse_dst = nullptr;
+        }
         if (it.J == 0) {
           // no key reaches these rows: out = prev (or 0), lse = prev_lse (or -inf).
           // Only prefill and sparse produce such items; decode segments always hold keys.
@@ -1129,7 +1152,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSp
               for (int u = 0; u < 8; ++u)
                 dst[u] = make_float4(__uint_as_float(v[4 * u]) * cn, __uint_as_float(v[4 * u + 1]) * cn,
                                      __uint_as_float(v[4 * u + 2]) * cn, __uint_as_float(v[4 * u + 3]) * cn);
-            } else {
+            } else if (orow) {
               uint4* dst = reinterpret_cast<uint4*>(orow + c0);
 #pragma unroll
               for (int u = 0; u < 4; ++u) {

@@ -85,6 +85,13 @@ struct CoreParams {
   const __nv_bfloat16* k_pe;     // [S_kv, 64] rows, read with 16-byte copies
   int K;
   int S_kv;
+
+  // ---- byte extents of the buffers above from their base pointers (the guarded build checks
+  // every plain access against them; 0 where a buffer is unused) ----
+  uint64_t ext_q, ext_q_pe, ext_out, ext_prev_out, ext_lse, ext_prev_lse;
+  uint64_t ext_block_table, ext_lens, ext_cache8, ext_sinks;
+  uint64_t ext_tile_prefix, ext_part_o, ext_part_lse;
+  uint64_t ext_topk, ext_c_kv, ext_k_pe;
 };
 
 // Decode query groups: group g is query token g % q_per_req of request g / q_per_req.  Token i of a
@@ -97,16 +104,22 @@ __device__ __forceinline__ int decode_group_len(const CoreParams& p, int g) {
   const int64_t cap = (int64_t)p.max_pages * p.page_size;
   int64_t n;
   if (p.q_per_req <= 1) {  // one token per request: it sees all len keys
-    n = p.lens[g];
+    n = guard_span(p.err, G_LENS, p.lens + g, 4, p.lens, p.ext_lens) ? p.lens[g] : 0;
     if (n > cap) n = cap;
   } else {
     const int s = p.q_per_req;
     const int b = g / s;
-    int64_t len = p.lens[b];
+    int64_t len = guard_span(p.err, G_LENS, p.lens + b, 4, p.lens, p.ext_lens) ? p.lens[b] : 0;
     if (len > cap) len = cap;
     n = len - s + 1 + (g - (int64_t)b * s);
   }
   return (int)(n < 0 ? 0 : n);
+}
+
+// An entry of the block table (guarded build: an entry outside the table's extent reads as -1, an
+// invalid page, and is recorded).
+__device__ __forceinline__ int32_t bt_entry(const CoreParams& p, const int32_t* e) {
+  return guard_span(p.err, G_BLOCK_TABLE, e, 4, p.block_table, p.ext_block_table) ? *e : -1;
 }
 
 // TMA descriptors of one launch of the absorbed engine

@@ -81,25 +81,37 @@ __global__ void __launch_bounds__(256) merge_kernel(const __nv_bfloat16* out_a, 
 // logit joins the softmax denominator as one more term that carries no value (Modular Mojo
 // "mha_single_batch_pipelined", sink / sink_weights): out = sum_j e^{s_j} v_j / (e^{sink_h} +
 // sum_j e^{s_j}), lse = ln(e^{sink_h} + sum_j e^{s_j}).
-__global__ void __launch_bounds__(256) decode_reduce_kernel(const float* __restrict__ part_o,
-                                                            const float* __restrict__ part_lse,
-                                                            const int32_t* __restrict__ tile_prefix, int B, int H,
-                                                            int num_pairs, const float* __restrict__ sinks,
-                                                            __nv_bfloat16* out, float* lse) {
+__global__ void __launch_bounds__(256) decode_reduce_kernel(const __grid_constant__ CoreParams prm, __nv_bfloat16* out,
+                                                            float* lse) {
+  const float* __restrict__ part_o = prm.part_o;
+  const float* __restrict__ part_lse = prm.part_lse;
+  const int32_t* __restrict__ tile_prefix = prm.tile_prefix;
+  const float* __restrict__ sinks = prm.sinks;
+  const int B = prm.B, H = prm.H, num_pairs = prm.num_pairs;
+  uint32_t* err = prm.err;
+  // guarded build: every plain access below is checked against its buffer (see guard_span)
+  auto prefix = [&](int64_t i) -> int64_t {
+    return guard_span(err, G_TILE_PREFIX, tile_prefix + i, 4, tile_prefix, prm.ext_tile_prefix) ? tile_prefix[i] : 0;
+  };
+  auto plse = [&](int64_t slot) -> float {
+    return guard_span(err, G_PART_LSE, part_lse + slot, 4, part_lse, prm.ext_part_lse) ? part_lse[slot] : -CUDART_INF_F;
+  };
   const int lane = threadIdx.x & 31;
   const int64_t nitems = (int64_t)B * H;
   const int64_t warp0 = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  const int64_t total = tile_prefix[B];
+  const int64_t total = prefix(B);
   for (int64_t it = warp0; it < nitems; it += nwarps) {
     const int b = (int)(it / H);
     const int h = (int)(it - (int64_t)b * H);
-    const int64_t t0 = tile_prefix[b], t1 = tile_prefix[b + 1];
+    const int64_t t0 = prefix(b), t1 = prefix(b + 1);
     __nv_bfloat16* orow = out + it * kLatent;
-    const float sink = sinks ? sinks[h] : -CUDART_INF_F;
+    if (!guard_span(err, G_OUT, orow, kLatent * 2, out, prm.ext_out)) continue;
+    float* lse_it = (lse && guard_span(err, G_LSE, lse + it, 4, lse, prm.ext_lse)) ? lse + it : nullptr;
+    const float sink = (sinks && guard_span(err, G_SINKS, sinks + h, 4, sinks, prm.ext_sinks)) ? sinks[h] : -CUDART_INF_F;
     if (t1 <= t0) {  // no key: out = 0, lse = -inf (or the sink's logit)
       for (int c = lane; c < kLatent / 8; c += 32) reinterpret_cast<uint4*>(orow)[c] = make_uint4(0, 0, 0, 0);
-      if (lane == 0 && lse) lse[it] = sink;
+      if (lane == 0 && lse_it) *lse_it = sink;
       continue;
     }
     // pair owning tile t: the largest p with floor(p * total / P) <= t
@@ -109,7 +121,7 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const float* __restr
     auto owns = [&](int p) { return (int64_t)p * total / num_pairs < (int64_t)(p + 1) * total / num_pairs; };
     float m = sink;
     for (int p = p_first; p <= p_last; ++p)
-      if (owns(p)) m = fmaxf(m, part_lse[(int64_t)(b + p) * H + h]);
+      if (owns(p)) m = fmaxf(m, plse((int64_t)(b + p) * H + h));
     float acc[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i] = 0.f;
@@ -118,8 +130,9 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const float* __restr
       for (int p = p_first; p <= p_last; ++p) {
         if (!owns(p)) continue;
         const int64_t slot = (int64_t)(b + p) * H + h;
-        const float l = part_lse[slot];
+        const float l = plse(slot);
         if (l == -CUDART_INF_F) continue;
+        if (!guard_span(err, G_PART_O, part_o + slot * kLatent, kLatent * 4, part_o, prm.ext_part_o)) continue;
         const float w = expf(l - m);
         wsum += w;
         const float4* src = reinterpret_cast<const float4*>(part_o + slot * kLatent);
@@ -143,7 +156,7 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const float* __restr
       pk.y = *reinterpret_cast<uint32_t*>(&hi);
       reinterpret_cast<uint2*>(orow)[lane + 32 * k] = pk;
     }
-    if (lane == 0 && lse) lse[it] = (wsum > 0.f) ? m + logf(wsum) : -CUDART_INF_F;
+    if (lane == 0 && lse_it) *lse_it = (wsum > 0.f) ? m + logf(wsum) : -CUDART_INF_F;
   }
 }
 
@@ -170,8 +183,7 @@ cudaError_t launch_merge(const __nv_bfloat16* out_a, const float* lse_a, const _
 cudaError_t launch_decode_reduce(const CoreParams& p, __nv_bfloat16* out, float* lse, cudaStream_t stream) {
   const int64_t items = (int64_t)p.B * p.H;
   if (items == 0) return cudaSuccess;
-  decode_reduce_kernel<<<grid_for(items), 256, 0, stream>>>(p.part_o, p.part_lse, p.tile_prefix, p.B, p.H,
-                                                           p.num_pairs, p.sinks, out, lse);
+  decode_reduce_kernel<<<grid_for(items), 256, 0, stream>>>(p, out, lse);
   return cudaGetLastError();
 }
 

@@ -238,8 +238,10 @@ __device__ __forceinline__ HalfIds load_half_ids(const CoreParams& p, int req, i
   const int32_t* bt = p.block_table + (int64_t)decode_request(p, req) * p.max_pages;
   const int64_t ke = kh + 2 * lane, ko = ke + 1;
   HalfIds ids;
-  ids.pe = ke < len ? __ldg(bt + ke / p.page_size) : 0;
-  ids.po = ko < len ? __ldg(bt + ko / p.page_size) : 0;
+  const int32_t* be = bt + ke / p.page_size;
+  const int32_t* bo = bt + ko / p.page_size;
+  ids.pe = (ke < len && guard_span(p.err, G_BLOCK_TABLE, be, 4, p.block_table, p.ext_block_table)) ? __ldg(be) : 0;
+  ids.po = (ko < len && guard_span(p.err, G_BLOCK_TABLE, bo, 4, p.block_table, p.ext_block_table)) ? __ldg(bo) : 0;
   return ids;
 }
 // Rows of a half that is not one tiled box per column block (the last half of a request,
@@ -297,8 +299,8 @@ __device__ __forceinline__ HalfIds sparse_half_ids(const CoreParams& p, int id, 
   const int32_t* tk = p.topk + (int64_t)id * p.K;
   const int64_t c0 = kh + 2 * lane;
   HalfIds ids;
-  ids.pe = c0 < p.K ? __ldg(tk + c0) : -1;
-  ids.po = c0 + 1 < p.K ? __ldg(tk + c0 + 1) : -1;
+  ids.pe = (c0 < p.K && guard_span(p.err, G_TOPK, tk + c0, 4, p.topk, p.ext_topk)) ? __ldg(tk + c0) : -1;
+  ids.po = (c0 + 1 < p.K && guard_span(p.err, G_TOPK, tk + c0 + 1, 4, p.topk, p.ext_topk)) ? __ldg(tk + c0 + 1) : -1;
   return ids;
 }
 // Gathers the 64 rows of a tile half listed in ids, column boxes cb0 .. cb0 + kBox - 1 (boxes 0-7
@@ -311,6 +313,7 @@ __device__ __forceinline__ HalfIds sparse_half_ids(const CoreParams& p, int id, 
 template <int kBox>
 __device__ __forceinline__ void gather_half_sparse(uint32_t dst, uint32_t box_stride, int cb0, const CoreParams& p,
                                                    const HalfIds& ids, uint64_t* bar) {
+  uint32_t* err = p.err;
   const int lane = threadIdx.x & 31;
   const int rq = lane >> 3, c = lane & 7;
 #pragma unroll 2
@@ -327,7 +330,9 @@ __device__ __forceinline__ void gather_half_sparse(uint32_t dst, uint32_t box_st
       const int gb = cb0 + b;
       const __nv_bfloat16* src = (gb < kVBoxes) ? p.c_kv + row * kLatent + gb * kBoxCols + c * 8
                                                 : p.k_pe + row * kRope + c * 8;
-      cp_async16_zfill(line + b * box_stride, src, ok ? 16u : 0u);
+      const bool in = ok && ((gb < kVBoxes) ? guard_span(err, G_C_KV, src, 16, p.c_kv, p.ext_c_kv)
+                                            : guard_span(err, G_K_PE, src, 16, p.k_pe, p.ext_k_pe));
+      cp_async16_zfill(line + b * box_stride, (kGuarded && !in) ? p.c_kv : src, in ? 16u : 0u);
     }
   }
   cp_async_arrive_noinc(bar);
@@ -362,8 +367,9 @@ __device__ __forceinline__ void fill_half_fp8(uint8_t* dst, uint32_t box_stride,
       if (in_len && !ok) record_error(err, DEV_RANGE_BASE | X_PAGE);
       const uint4* src = reinterpret_cast<const uint4*>(
           p.cache8 + ((int64_t)pg * p.page_size + key % p.page_size) * kDk + (cb0 + b) * 64);
+      const bool in = ok && guard_span(err, G_CACHE8, src, 64, p.cache8, p.ext_cache8);
 #pragma unroll
-      for (int w = 0; w < 4; ++w) v[i][w] = ok ? __ldg(src + w) : make_uint4(0, 0, 0, 0);
+      for (int w = 0; w < 4; ++w) v[i][w] = in ? __ldg(src + w) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int i = 0; i < kBlk; ++i) {
@@ -389,7 +395,8 @@ __device__ __forceinline__ void fill_half_fp8(uint8_t* dst, uint32_t box_stride,
 // and four producer warps (one per TMEM lane quadrant) split the pieces, so the next item's
 // Q is in place sooner.  FP8 decode: the MMAs take f16 operands.
 template <bool kF16>
-__device__ __forceinline__ void load_q_pieces(uint32_t tq, const __nv_bfloat16* qrow, int c_begin, int c_end) {
+__device__ __forceinline__ void load_q_pieces(uint32_t tq, const __nv_bfloat16* qrow, int c_begin, int c_end,
+                                              const CoreParams& p) {
 #pragma unroll 1
   for (int c0 = c_begin; c0 < c_end; c0 += 2) {
     const bool two = c0 + 1 < c_end;
@@ -397,6 +404,7 @@ __device__ __forceinline__ void load_q_pieces(uint32_t tq, const __nv_bfloat16* 
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
       const uint4* src = (qrow && (cc == 0 || two)) ? reinterpret_cast<const uint4*>(qrow + 64 * (c0 + cc)) : nullptr;
+      if (src && !guard_span(p.err, G_Q, src, 128, p.q, p.ext_q)) src = nullptr;
 #pragma unroll
       for (int u = 0; u < 8; ++u) x[cc][u] = src ? __ldg(src + u) : make_uint4(0, 0, 0, 0);
     }
@@ -420,8 +428,10 @@ __device__ __forceinline__ void load_q_pieces(uint32_t tq, const __nv_bfloat16* 
   }
 }
 template <bool kF16>
-__device__ __forceinline__ void load_q_rope(uint8_t* qpe_row, const __nv_bfloat16* qpe, int r) {
+__device__ __forceinline__ void load_q_rope(uint8_t* qpe_row, const __nv_bfloat16* qpe, int r, uint32_t* err,
+                                            const void* base, uint64_t extent) {
   const uint4* src = reinterpret_cast<const uint4*>(qpe);
+  if (src && !guard_span(err, G_Q_PE, src, 128, base, extent)) src = nullptr;
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     uint4 v = src ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
@@ -462,7 +472,7 @@ __device__ __forceinline__ void sparse_tile_entries(const CoreParams& p, int id,
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int c = j * kKeysT + 32 * q + lane;
-    e[q] = c < p.K ? __ldg(tk + c) : -1;
+    e[q] = (c < p.K && guard_span(p.err, G_TOPK, tk + c, 4, p.topk, p.ext_topk)) ? __ldg(tk + c) : -1;
   }
 }
 template <bool kUp>
@@ -589,7 +599,8 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
       const int b = b0 + lane;
       int n = 0;
       if (b < p.B) {
-        const int raw = p.lens[decode_request(p, b)];
+        const int32_t* lp = p.lens + decode_request(p, b);
+        const int raw = guard_span(err, G_LENS, lp, 4, p.lens, p.ext_lens) ? *lp : 0;
         const int64_t cap = (int64_t)p.max_pages * p.page_size;
         if (raw < 0 || raw > cap) record_error(err, DEV_RANGE_BASE | X_LEN);
         n = (decode_len_t(p, b) + kKeysT - 1) / kKeysT;
@@ -600,10 +611,12 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
         const int v = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += v;
       }
-      if (b < p.B) p.tile_prefix[b] = (int32_t)(run + incl - n);
+      if (b < p.B && guard_span(err, G_TILE_PREFIX, p.tile_prefix + b, 4, p.tile_prefix, p.ext_tile_prefix))
+        p.tile_prefix[b] = (int32_t)(run + incl - n);
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) p.tile_prefix[p.B] = (int32_t)run;
+    if (lane == 0 && guard_span(err, G_TILE_PREFIX, p.tile_prefix + p.B, 4, p.tile_prefix, p.ext_tile_prefix))
+      p.tile_prefix[p.B] = (int32_t)run;
   }
   tc_fence_before();
   cluster_sync();
@@ -726,8 +739,9 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
             const int rq = (warp & 3) * 32 + lane;
             const __nv_bfloat16 *qr, *qp;
             q_row_ptrs(it, rq, qr, qp);
-            load_q_pieces<kFp8>(tbase + ((uint32_t)((warp & 3) * 32) << 16) + kTmemQ, qr, kQRowPieces, 8);
-            load_q_rope<kFp8>(smem + kOffQpe + rq * 128, qp, rq);
+            load_q_pieces<kFp8>(tbase + ((uint32_t)((warp & 3) * 32) << 16) + kTmemQ, qr, kQRowPieces, 8, p);
+            load_q_rope<kFp8>(smem + kOffQpe + rq * 128, qp, rq, err, kSparse ? (const void*)p.q_pe : (const void*)p.q,
+                              kSparse ? p.ext_q_pe : p.ext_q);
             tmem_wait_st();
             tc_fence_before();
             warp_arrive(&bars.q_full);
@@ -857,8 +871,8 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
         MLA_TRACE_ONLY(long long tq = clock64();)
         // ---- Q: latent part -> TMEM (256 columns), RoPE part -> smem (SW128 K-major) ----
         if (i > 0 && !waitb(&bars.q_taken, (i - 1) & 1, X_Q_TAKEN, false)) break;
-        load_q_pieces<kFp8>(tbase + lane_base + kTmemQ, row_ok ? qrow : nullptr, 0, kDecode ? 8 : kQRowPieces);
-        if constexpr (kDecode) load_q_rope<kFp8>(smem + kOffQpe + r * 128, row_ok ? qpe : nullptr, r);
+        load_q_pieces<kFp8>(tbase + lane_base + kTmemQ, row_ok ? qrow : nullptr, 0, kDecode ? 8 : kQRowPieces, p);
+        if constexpr (kDecode) load_q_rope<kFp8>(smem + kOffQpe + r * 128, row_ok ? qpe : nullptr, r, err, p.q, p.ext_q);
         tmem_wait_st();
         tc_fence_before();
         warp_arrive(&bars.q_full);
@@ -1010,7 +1024,9 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
         if constexpr (decode) {
           ids = load_half_ids(p, it.id, len, it.k0 + 64 * h);
           const int64_t kp = it.k0 + (int64_t)kPrefetchTiles * kKeysT + 64 * h;
-          if (pf_ok && kp + 64 <= len) pf_pg = __ldg(bt + kp / p.page_size);
+          if (pf_ok && kp + 64 <= len && guard_span(err, G_BLOCK_TABLE, bt + kp / p.page_size, 4, p.block_table,
+                                                    p.ext_block_table))
+            pf_pg = __ldg(bt + kp / p.page_size);
         }
         if constexpr (kSparse) ids = sparse_half_ids(p, it.id, 64 * h);
         for (int j = 0; j < it.J && live; ++j, ++m) {
@@ -1029,7 +1045,11 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
               if constexpr (kFp8) bulk_prefetch_l2_hint<kHintPf>(p.cache8 + row * kDk, 64 * kDk);
               else bulk_prefetch_l2_hint<kHintPf>(p.cache + row * kDk, 64 * kDk * 2);
             }
-            pf_pg = (pf_ok && kp + kKeysT + 64 <= len) ? __ldg(bt + (kp + kKeysT) / p.page_size) : -1;
+            pf_pg = (pf_ok && kp + kKeysT + 64 <= len &&
+                     guard_span(err, G_BLOCK_TABLE, bt + (kp + kKeysT) / p.page_size, 4, p.block_table,
+                                p.ext_block_table))
+                        ? __ldg(bt + (kp + kKeysT) / p.page_size)
+                        : -1;
           }
           if (!waitb(&bars.vempty[h], (m & 1) ^ 1, X_V_EMPTY, false)) { live = false; break; }
           if constexpr (kSparse) {  // each lane arrives (noinc) once its row copies land
@@ -1150,10 +1170,18 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
             lse_dst = p.lse + hh * (p.lse_stride ? p.lse_stride : (int64_t)p.T) + tt;
             if (p.prev_out) {
               prev_row = p.prev_out + f * kLatent;
-              prev_l = p.prev_lse[hh * (p.lse_stride ? p.lse_stride : (int64_t)p.T) + tt];
+              const float* pl = p.prev_lse + hh * (p.lse_stride ? p.lse_stride : (int64_t)p.T) + tt;
+              prev_l = guard_span(err, G_PREV_LSE, pl, 4, p.prev_lse, p.ext_prev_lse) ? *pl : -CUDART_INF_F;
             }
           }
         }
+        // guarded build: a row outside its buffer is not written (or read) at all
+        if (orow && !guard_span(err, G_OUT, orow, kLatent * 2, p.out, p.ext_out)) orow = nullptr;
+        if (orow_f && !guard_span(err, G_PART_O, orow_f, kLatent * 4, p.part_o, p.ext_part_o)) orow_f = nullptr;
+        if (prev_row && !guard_span(err, G_PREV_OUT, prev_row, kLatent * 2, p.prev_out, p.ext_prev_out)) prev_row = nullptr;
+        if (lse_dst && !guard_span(err, decode ? G_PART_LSE : G_LSE, lse_dst, 4, decode ? (const void*)p.part_lse : (const void*)p.lse,
+                                   decode ? p.ext_part_lse : p.ext_lse))
+          lse_dst = nullptr;
         if (it.J == 0) {
           // no key reaches these rows: out = prev (or 0), lse = prev_lse (or -inf); only
           // prefill has such items (decode segments always hold keys)
@@ -1162,7 +1190,7 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
               uint4 v = prev_row ? *reinterpret_cast<const uint4*>(prev_row + c) : make_uint4(0, 0, 0, 0);
               *reinterpret_cast<uint4*>(orow + c) = v;
             }
-            *lse_dst = prev_row ? prev_l : -CUDART_INF_F;
+            if (lse_dst) *lse_dst = prev_row ? prev_l : -CUDART_INF_F;
           }
           continue;
         }
@@ -1225,7 +1253,7 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
             uint32_t v[32];
             tmem_ld32(tbase + lane_base + c0, v);
             tmem_wait_ld();
-            if (row_ok) {
+            if (row_ok && orow_f) {
               float4* dst = reinterpret_cast<float4*>(orow_f + c0);
 #pragma unroll
               for (int q = 0; q < 8; ++q)
@@ -1235,7 +1263,7 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
           }
           tc_fence_before();
           warp_arrive(&bars.o_free);  // O has been read: the next item's P V may start
-          if (row_ok) *lse_dst = lse_out;
+          if (row_ok && lse_dst) *lse_dst = lse_out;
           ++i;
           continue;
         }
@@ -1246,7 +1274,7 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
             uint32_t v[32];
             tmem_ld32(tbase + lane_base + c0, v);
             tmem_wait_ld();
-            if (row_ok) {
+            if (row_ok && orow) {
               uint4* dst = reinterpret_cast<uint4*>(orow + c0);
 #pragma unroll
               for (int q = 0; q < 4; ++q)

@@ -71,39 +71,53 @@ __global__ void __launch_bounds__(256) rope_append_kernel(const RopeAppendParams
   const int b = blockIdx.x;
   __shared__ float cs[kR];
   __shared__ int64_t row_s;
-  __shared__ int ok_s;
+  __shared__ int ok_s, pos_s;
+  // guarded build: every plain access is checked against the extent its sizes give (guard_span)
+  const uint64_t ext_cache = (uint64_t)p.num_pages * p.page_size * kDk * 2;
   if (threadIdx.x == 0) {
-    const int pos = p.positions[b];
+    const int pos = guard_span(p.err, G_POS, p.positions + b, 4, p.positions, (uint64_t)p.B * 4) ? p.positions[b] : -1;
     const int64_t cap = (int64_t)p.max_pages * p.page_size;
     bool ok = pos >= 0 && pos < p.max_pos && pos < cap;
     int64_t row = 0;
     if (ok) {
-      const int32_t pg = p.block_table[(int64_t)b * p.max_pages + pos / p.page_size];
+      const int32_t* e = p.block_table + (int64_t)b * p.max_pages + pos / p.page_size;
+      const int32_t pg =
+          guard_span(p.err, G_BLOCK_TABLE, e, 4, p.block_table, (uint64_t)p.B * p.max_pages * 4) ? *e : -1;
       ok = pg >= 0 && pg < p.num_pages;
       row = (int64_t)pg * p.page_size + pos % p.page_size;
     }
     if (!ok) record_error(p.err, DEV_RANGE_BASE | 0x60);
-    ok_s = ok;
+    ok_s = ok && guard_span(p.err, G_ROPE_OUT, p.cache + row * kDk, kDk * 2, p.cache, ext_cache) &&
+           guard_span(p.err, G_ROPE_IN, p.cos_sin + (int64_t)pos * kR, kR * 4, p.cos_sin, (uint64_t)p.max_pos * kR * 4);
     row_s = row;
+    pos_s = pos;
   }
   __syncthreads();
   if (!ok_s) return;
-  if (threadIdx.x < kR) cs[threadIdx.x] = p.cos_sin[(int64_t)p.positions[b] * kR + threadIdx.x];
+  if (threadIdx.x < kR) cs[threadIdx.x] = p.cos_sin[(int64_t)pos_s * kR + threadIdx.x];
   __syncthreads();
   const bool neox = p.is_neox != 0;
   // q: H rows of 64 values, 8 units each
   for (int u = threadIdx.x; u < p.H * 8; u += blockDim.x) {
     const int h = u >> 3;
-    rotate_unit(p.q_pe + ((int64_t)b * p.H + h) * kR, p.q_out + ((int64_t)b * p.H + h) * kDk + kLatent, u & 7, neox,
-                cs);
+    const __nv_bfloat16* src = p.q_pe + ((int64_t)b * p.H + h) * kR;
+    __nv_bfloat16* dst = p.q_out + ((int64_t)b * p.H + h) * kDk + kLatent;
+    if (guard_span(p.err, G_ROPE_IN, src, kR * 2, p.q_pe, (uint64_t)p.B * p.H * kR * 2) &&
+        guard_span(p.err, G_ROPE_OUT, dst, kR * 2, p.q_out, (uint64_t)p.B * p.H * kDk * 2))
+      rotate_unit(src, dst, u & 7, neox, cs);
   }
   // the cache row: 512 latent values copied, 64 RoPE values rotated
   __nv_bfloat16* crow = p.cache + row_s * kDk;
   const int t = threadIdx.x;
-  if (t < kLatent / 8)
-    reinterpret_cast<uint4*>(crow)[t] = reinterpret_cast<const uint4*>(p.c_kv + (int64_t)b * kLatent)[t];
-  else if (t < kLatent / 8 + 8)
-    rotate_unit(p.k_pe + (int64_t)b * kR, crow + kLatent, t - kLatent / 8, neox, cs);
+  if (t < kLatent / 8) {
+    const __nv_bfloat16* src = p.c_kv + (int64_t)b * kLatent;
+    if (guard_span(p.err, G_ROPE_IN, src, kLatent * 2, p.c_kv, (uint64_t)p.B * kLatent * 2))
+      reinterpret_cast<uint4*>(crow)[t] = reinterpret_cast<const uint4*>(src)[t];
+  } else if (t < kLatent / 8 + 8) {
+    const __nv_bfloat16* src = p.k_pe + (int64_t)b * kR;
+    if (guard_span(p.err, G_ROPE_IN, src, kR * 2, p.k_pe, (uint64_t)p.B * kR * 2))
+      rotate_unit(src, crow + kLatent, t - kLatent / 8, neox, cs);
+  }
 }
 
 }  // namespace

@@ -316,7 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float lse_new = has ? (m_used + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
       float wn = has ? 1.f : 0.f, wp = 0.f, lse_out = lse_new;
       const __nv_bfloat16* prow = nullptr;
-      if (p.prev_out && row_ok) {
+      // guarded build: rows checked against the [Nq, H, 128] / [H, Nq] extents (guard_span)
+      const uint64_t ext_rows = (uint64_t)p.Nq * p.H * 128 * 2, ext_lse = (uint64_t)p.H * p.Nq * 4;
+      if (p.prev_out && row_ok && guard_span(p.err, G_PREV_OUT, p.prev_out + (tok * p.H + ti.h) * 128, 256, p.prev_out, ext_rows) &&
+          guard_span(p.err, G_PREV_LSE, p.prev_lse + (int64_t)ti.h * p.Nq + tok, 4, p.prev_lse, ext_lse)) {
         prow = p.prev_out + (tok * p.H + ti.h) * 128;
         const float pl = p.prev_lse[(int64_t)ti.h * p.Nq + tok];
         const float m = fmaxf(pl, lse_new);
@@ -334,6 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float cn = has ? wn / l : 0.f;
       __nv_bfloat16* orow = p.out + (tok * p.H + ti.h) * 128;
+      const bool out_ok = guard_span(p.err, G_OUT, orow, 256, p.out, ext_rows) &&
+                          guard_span(p.err, G_LSE, p.lse + (int64_t)ti.h * p.Nq + tok, 4, p.lse, ext_lse);
 #pragma unroll 1
       for (int c0 = 0; c0 < 128; c0 += 32) {
         float o[32];
@@ -347,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 32; ++c) o[c] = 0.f;
         }
-        if (!row_ok) continue;
+        if (!row_ok || !out_ok) continue;
         if (prow && wp > 0.f) {
           const uint4* pr = reinterpret_cast<const uint4*>(prow + c0);
 #pragma unroll
@@ -368,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           dst[u] = make_uint4(pack_bf16x2(o[8 * u], o[8 * u + 1]), pack_bf16x2(o[8 * u + 2], o[8 * u + 3]),
                               pack_bf16x2(o[8 * u + 4], o[8 * u + 5]), pack_bf16x2(o[8 * u + 6], o[8 * u + 7]));
       }
-      if (row_ok) p.lse[(int64_t)ti.h * p.Nq + tok] = lse_out;
+      if (row_ok && out_ok) p.lse[(int64_t)ti.h * p.Nq + tok] = lse_out;
     }
   }
 

@@ -18,9 +18,7 @@ namespace mla {
 // device error word (one per launch, lives in the caller's workspace)
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ void record_error(uint32_t* err, uint32_t code) {
-  if (err) atomicCAS(err, 0u, code);
-}
+// record_error and guard_span live in mla_device_status.h.
 
 __device__ __forceinline__ bool error_raised(const uint32_t* err) {
   return err && *((volatile const uint32_t*)err) != 0u;
