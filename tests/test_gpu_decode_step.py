@@ -113,7 +113,7 @@ def _gemm_close(gpu, ref, what, k):
     assert (err <= bound).all(), f"{what}: worst excess {float((err - bound).max()):.3e}"
 
 
-@pytest.mark.parametrize("T,H", [(300, 16), (128, 128), (1, 3)])
+@pytest.mark.parametrize("T,H", [(300, 16), (128, 128), (1, 3), (2048, 32)])   # the last: several items per CTA
 def test_absorb_q_parity_strided_input(T, H):
     from mla_attention_gb300 import mla_absorb_q
     g = torch.Generator().manual_seed(40 + T)
@@ -129,7 +129,7 @@ def test_absorb_q_parity_strided_input(T, H):
     assert (fused[:, :, 512:] == 7.0).all()       # the RoPE columns are not written
 
 
-@pytest.mark.parametrize("T,H", [(300, 16), (129, 128)])
+@pytest.mark.parametrize("T,H", [(300, 16), (129, 128), (1500, 64)])
 def test_project_out_parity(T, H):
     from mla_attention_gb300 import mla_project_out
     g = torch.Generator().manual_seed(50 + T)
