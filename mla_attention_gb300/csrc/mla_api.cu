@@ -284,12 +284,21 @@ mla_status decode_impl(const void* q, int q_per_req, const void* kv_cache, bool 
   CoreMaps maps;
   memset(&maps, 0, sizeof(maps));
   const uint64_t rows = (uint64_t)num_pages * (uint64_t)page_size;
-  if (!fp8) {  // FP8 decode reads the cache with ordinary loads
+  if (!fp8) {
     mla_status s = map2d(&maps.kv, kv_cache, kDk, rows, kDk, page_size >= kKeys ? kKeys : (uint32_t)page_size, "cache");
     if (s != MLA_OK) return s;
     s = map2d(&maps.row, kv_cache, kDk, rows, kDk, 1, "cache rows");
     if (s != MLA_OK) return s;
     maps.pe = maps.row;
+  } else {
+    // the e4m3 cache as bytes [rows, 576], boxes of 64 bytes x 64 rows with no swizzle: the kernel
+    // stages them and converts in place (ordinary loads where a 64-key half spans pages)
+    const uint64_t dims[2] = {(uint64_t)kDk, rows};
+    const uint64_t strides[1] = {(uint64_t)kDk};
+    const uint32_t box[2] = {64, 64};
+    CUresult r = encode_tiled(&maps.kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, kv_cache, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (r != CUDA_SUCCESS) return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled(e4m3 cache) failed: %d", (int)r);
   }
   CoreParams p;
   memset(&p, 0, sizeof(p));

@@ -124,7 +124,8 @@ __device__ __forceinline__ int32_t bt_entry(const CoreParams& p, const int32_t* 
 
 // TMA descriptors of one launch of the absorbed engine
 struct CoreMaps {
-  CUtensorMap kv;    // K/V rows [rows, 576] (prefill: the chunk; decode: the cache), box {64, 64 or page}
+  CUtensorMap kv;    // K/V rows [rows, 576] (prefill: the chunk; decode: the cache), box {64, 64 or page};
+                     // FP8 decode: the e4m3 cache as bytes, box {64 bytes, 64 rows}, no swizzle
   CUtensorMap row;   // gather rows, box {64, 1} (decode: the cache; sparse: c_kv [S_kv, 512])
   CUtensorMap pe;    // sparse: k_pe [S_kv, 64], box {64, 1}
   CUtensorMap out;   // prefill / sparse output rows [rows, 512], box {64, 64}

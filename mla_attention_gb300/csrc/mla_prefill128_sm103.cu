@@ -98,6 +98,7 @@ struct BarsT {
   uint64_t pb_free[2];         // P V of O-CTA buffer b done (multicast commit)
   uint64_t stall;              // fault injection: never arrived on
   uint64_t drain[2];           // abort: one commit of each MMA issuer lands here
+  uint64_t raw[16];            // FP8: producer warp q's staged e4m3 boxes landed (S-CTA: q < 6, O-CTA: 8 + q)
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
@@ -106,7 +107,7 @@ static_assert(sizeof(BarsT) <= 512, "barrier block too large");
 enum : uint32_t {
   X_K_EMPTY = 0x40, X_K_FULL, X_S_FREE, X_S_FULL, X_Q_FULL, X_Q_TAKEN, X_P_WRITTEN, X_PBUF_FREE, X_PB_FREE,
   X_STATS_FREE, X_V_EMPTY, X_V_FULL, X_P_FULL, X_P_READY, X_PV_DONE, X_STATS_FULL, X_O_FREE, X_STALL, X_EP_HALF,
-  X_Q_FREE,
+  X_Q_FREE, X_RAW,
   X_ALIGN = 0x4F, X_PAGE = 0x50, X_LEN = 0x51,
 };
 
@@ -443,6 +444,33 @@ __device__ __forceinline__ void load_q_rope(uint8_t* qpe_row, const __nv_bfloat1
 }
 constexpr int kQRowPieces = 3;  // latent pieces the row warps load; the producers load the rest and the RoPE part
 
+// FP8 decode, staged path: a 64-row box of the e4m3 cache (64 bytes a row) that TMA wrote into
+// the upper half of its own 8 KB f16 chunk is converted in place into 64 SW128 rows of 128 B.
+// Rows 0-31 land below the staged bytes; rows 32-63 overwrite them, so every lane loads its
+// staged row before any lane stores (the warp synchronises in between).  The caller fences the
+// async proxy and arrives once every lane has stored.
+__device__ __forceinline__ void convert_box_in_place(uint8_t* chunk) {
+  const int lane = threadIdx.x & 31;
+  const uint8_t* raw = chunk + 4096;
+#pragma unroll 1
+  for (int half = 0; half < 2; ++half) {
+    const int r = 32 * half + lane;
+    uint4 v[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) v[w] = reinterpret_cast<const uint4*>(raw + r * 64)[w];
+    __syncwarp();
+    uint8_t* line = chunk + r * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {  // chunk c: values 8c .. 8c + 7
+      const uint4& q = v[c >> 1];
+      const uint32_t w0 = (c & 1) ? q.z : q.x, w1 = (c & 1) ? q.w : q.y;
+      *reinterpret_cast<uint4*>(line + ((c ^ (r & 7)) << 4)) =
+          make_uint4(e4m3x2_to_f16x2((uint16_t)(w0 & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(w0 >> 16)),
+                     e4m3x2_to_f16x2((uint16_t)(w1 & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(w1 >> 16)));
+    }
+  }
+}
+
 // ---- softmax rows: one 32-column piece of a score row ----
 // Keys of a piece past lim (the visible keys in it) get the score -inf (+inf when the scale
 // is negative), so one mask-free body serves every piece: the extreme ignores them and
@@ -575,6 +603,7 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
       mbar_init(&bars.ep_half[1], 2);
     }
     mbar_init(&bars.stall, 1);
+    for (int q = 0; q < 16; ++q) mbar_init(&bars.raw[q], 1);
     mbar_init(&bars.drain[0], 1);
     mbar_init(&bars.drain[1], 1);
     bars.abort_flag = 0;
@@ -691,7 +720,7 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
       // prefill and sparse: one per TMEM lane quadrant, they load most of each item's Q (decode has
       // few, long items: its rows load Q alone)
       const bool q_helper = !kDecode && warp >= 8 && warp <= 11;
-      uint32_t t = 0, items = 0;
+      uint32_t t = 0, items = 0, n_raw = 0;
       bool live = true;
       while (live && iter.next(it)) {
         const int len = decode ? decode_len_t(p, it.id) : 0;
@@ -714,8 +743,27 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
           uint64_t* fb = &bars.kfull[k][par];
           if constexpr (kSparse) {  // the listed rows by cp.async; each lane arrives (noinc) once they land
             gather_half_sparse<3>(dst, kBoxBytesK, 3 * k, p, cur, fb);
-          } else if constexpr (kFp8) {  // ordinary loads, converted into the slot, then one arrival
-            fill_half_fp8<3>(smem + kOffK + k * kGroupBytes + h * kBoxBytesV, kBoxBytesK, 3 * k, p, len, kh, cur, err);
+          } else if constexpr (kFp8) {
+            // a half inside one valid page: its three e4m3 boxes by TMA into the upper halves of their
+            // f16 chunks, converted in place; else ordinary loads converted into the slot
+            uint8_t* chunk0 = smem + kOffK + k * kGroupBytes + h * kBoxBytesV;
+            const int32_t pg0 = __shfl_sync(0xffffffffu, cur.pe, 0);
+            if (p.page_size % 64 == 0 && kh + 64 <= len && pg0 >= 0 && pg0 < p.num_pages) {
+              uint64_t* rb = &bars.raw[q];
+              if (lane == 0) mbar_arrive_expect_tx(rb, 3 * 4096);
+              __syncwarp();
+              const int32_t y = (int32_t)(pg0 * (int64_t)p.page_size + kh % p.page_size);
+              if (lane < 3)
+                tma_load_2d_hint<kHintK>(smem_u32(chunk0 + lane * kBoxBytesK + 4096), &maps.kv, (3 * k + lane) * 64, y, rb);
+              drain_bar = rb;
+              drain_par = n_raw & 1;
+              if (!waitb(rb, n_raw & 1, X_RAW, false)) { live = false; break; }
+              ++n_raw;
+#pragma unroll 1
+              for (int b = 0; b < 3; ++b) convert_box_in_place(chunk0 + b * kBoxBytesK);
+            } else {
+              fill_half_fp8<3>(chunk0, kBoxBytesK, 3 * k, p, len, kh, cur, err);
+            }
             fence_proxy_async_smem();  // the MMA reads the slot through the async proxy
             __syncwarp();
             if (lane == 0) mbar_arrive(fb);
@@ -1013,7 +1061,8 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
       const int h = kEight ? (vq >> 2) : ((warp == 4) ? 0 : 1);
       const int qq = kEight ? (vq & 3) : 0;
       const uint32_t dst = smem_u32(smem + kOffV + h * kHalfBytesV);
-      uint32_t m = 0;  // uses of this slot
+      uint32_t m = 0;      // uses of this slot
+      uint32_t n_raw = 0;  // FP8: staged loads of this warp
       bool live = true;
       while (live && iter.next(it)) {
         const int len = decode ? decode_len_t(p, it.id) : 0;
@@ -1057,8 +1106,26 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
             continue;
           }
           if constexpr (kFp8) {
-            fill_half_fp8<2>(smem + kOffV + h * kHalfBytesV + 2 * qq * kBoxBytesV, kBoxBytesV, 2 * qq, p, len, kh, cur,
-                             err);
+            // as the K producers: two staged e4m3 boxes converted in place, or ordinary loads
+            uint8_t* chunk0 = smem + kOffV + h * kHalfBytesV + 2 * qq * kBoxBytesV;
+            const int32_t pg0 = __shfl_sync(0xffffffffu, cur.pe, 0);
+            if (p.page_size % 64 == 0 && kh + 64 <= len && pg0 >= 0 && pg0 < p.num_pages) {
+              uint64_t* rb = &bars.raw[8 + vq];
+              if (lane == 0) mbar_arrive_expect_tx(rb, 2 * 4096);
+              __syncwarp();
+              const int32_t y = (int32_t)(pg0 * (int64_t)p.page_size + kh % p.page_size);
+              if (lane < 2)
+                tma_load_2d_hint<kHintV>(smem_u32(chunk0 + lane * kBoxBytesV + 4096), &maps.kv, (2 * qq + lane) * 64, y,
+                                         rb);
+              drain_bar = rb;
+              drain_par = n_raw & 1;
+              if (!waitb(rb, n_raw & 1, X_RAW, false)) { live = false; break; }
+              ++n_raw;
+#pragma unroll 1
+              for (int b = 0; b < 2; ++b) convert_box_in_place(chunk0 + b * kBoxBytesV);
+            } else {
+              fill_half_fp8<2>(chunk0, kBoxBytesV, 2 * qq, p, len, kh, cur, err);
+            }
             fence_proxy_async_smem();  // the MMA reads the slot through the async proxy
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars.vfull[h]);
