@@ -81,7 +81,8 @@ struct BarsT {
   uint64_t kempty[kGroups];    // the MMAs of group k of the last tile are done
   uint64_t s_full[2];          // S tile of issuer b done
   uint64_t s_free[2];          // every row warp read S buffer b
-  uint64_t q_full;             // Q of the item in TMEM / smem
+  uint64_t q_full;             // Q of the item in TMEM / smem (prefill, sparse: latent pieces 0-5, the producers' part)
+  uint64_t q_tail;             // prefill, sparse: latent pieces 6-7 and the RoPE part (the rows' part)
   uint64_t q_taken;            // both issuers passed q_full (count 2)
   uint64_t q_free;             // every S MMA of the item is done: Q may be replaced (one commit per issuer)
   uint64_t pwritten[2];        // rows wrote local P buffer b
@@ -442,7 +443,11 @@ __device__ __forceinline__ void load_q_rope(uint8_t* qpe_row, const __nv_bfloat1
   }
   fence_proxy_async_smem();  // read by the MMA through the async proxy
 }
-constexpr int kQRowPieces = 3;  // latent pieces the row warps load; the producers load the rest and the RoPE part
+// Prefill and sparse: producer warps 8-11 load latent pieces 0-5 of the next item's Q (K groups 0
+// and 1 of the S MMA) as soon as the previous item's MMAs are done; the row warps, which first
+// finish the previous item's last softmax, load pieces 6-7 and the RoPE part (group 2).  The
+// first tile's groups 0-1 run on the producers' part while the rows load theirs.
+constexpr int kQProdPieces = 6;
 
 // FP8 decode, staged path: a 64-row box of the e4m3 cache (64 bytes a row) that TMA wrote into
 // the upper half of its own 8 KB f16 chunk is converted in place into 64 SW128 rows of 128 B.
@@ -584,7 +589,8 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
         mbar_init(&bars.pbuf_free[b], 1);
         mbar_init(&bars.pb_free[b], 1);
       }
-      mbar_init(&bars.q_full, kRowWarpsS + (kDecode ? 0 : 4));  // the row warps (and producer warps 8-11)
+      mbar_init(&bars.q_full, 4);  // decode: the row warps; prefill, sparse: producer warps 8-11
+      mbar_init(&bars.q_tail, kRowWarpsS);
       mbar_init(&bars.q_taken, 2);
       mbar_init(&bars.q_free, 2);
       mbar_init(&bars.stats_free, kRowWarpsO);
@@ -780,16 +786,14 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
             __syncwarp();
           }
           if (q_helper && j == 0) {
-            // This item's Q: latent pieces kQRowPieces.. and the RoPE part of the rows of this warp's
-            // TMEM lane quadrant, once every S MMA of the previous item is done (both issuers commit
-            // to q_free after their last tile of an item), so the Q region and the RoPE box are free.
+            // This item's Q: latent pieces 0 .. kQProdPieces - 1 of the rows of this warp's TMEM lane
+            // quadrant, once every S MMA of the previous item is done (both issuers commit to q_free
+            // after their last tile of an item), so the Q region and the RoPE box are free.
             if (items > 0 && !waitb(&bars.q_free, (items - 1) & 1, X_Q_FREE, false)) { live = false; break; }
             const int rq = (warp & 3) * 32 + lane;
             const __nv_bfloat16 *qr, *qp;
             q_row_ptrs(it, rq, qr, qp);
-            load_q_pieces<kFp8>(tbase + ((uint32_t)((warp & 3) * 32) << 16) + kTmemQ, qr, kQRowPieces, 8, p);
-            load_q_rope<kFp8>(smem + kOffQpe + rq * 128, qp, rq, err, kSparse ? (const void*)p.q_pe : (const void*)p.q,
-                              kSparse ? p.ext_q_pe : p.ext_q);
+            load_q_pieces<kFp8>(tbase + ((uint32_t)((warp & 3) * 32) << 16) + kTmemQ, qr, 0, kQProdPieces, p);
             tmem_wait_st();
             tc_fence_before();
             warp_arrive(&bars.q_full);
@@ -812,7 +816,16 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
         while (live && iter.next(it)) {
           if (it.J == 0) continue;
           if (!wait1(&bars.q_full, i & 1, X_Q_FULL, false)) break;
-          mbar_arrive(&bars.q_taken);
+          // prefill, sparse: group 2 of the first tile waits for the rows' part of Q (q_tail)
+          bool tail = kDecode;
+          auto take_tail = [&]() -> bool {
+            if (tail) return true;
+            if (!wait1(&bars.q_tail, i & 1, X_Q_FULL, false)) return false;
+            tail = true;
+            mbar_arrive(&bars.q_taken);
+            return true;
+          };
+          if (kDecode) mbar_arrive(&bars.q_taken);
           for (int j = 0; j < it.J && live; ++j, ++t) {
             if ((t & 1u) != b) continue;
             // S buffer b was read by the rows (this issuer's previous tile)
@@ -821,7 +834,7 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
             // when all three have landed the tile goes out as one block of 36 MMAs; otherwise
             // group by group, waiting for each.
             if (!wait1(&bars.kfull[0][b], nb & 1, X_K_FULL, false)) { live = false; break; }
-            const bool all = mbar_try_wait(smem_u32(&bars.kfull[1][b]), nb & 1) &&
+            const bool all = tail && mbar_try_wait(smem_u32(&bars.kfull[1][b]), nb & 1) &&
                              mbar_try_wait(smem_u32(&bars.kfull[2][b]), nb & 1);
             if (all) {
               tc_fence_after();
@@ -831,6 +844,7 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
             } else {
               for (int k = 0; k < kGroups; ++k) {
                 if (k > 0 && !wait1(&bars.kfull[k][b], nb & 1, X_K_FULL, false)) { live = false; break; }
+                if (k == 2 && !take_tail()) { live = false; break; }
                 tc_fence_after();
                 if constexpr (kSparse) fence_proxy_async_smem();
                 const uint64_t bd = sdesc_sw128(smem_u32(smem + kOffK + k * kGroupBytes), 16, 1024);
@@ -843,7 +857,7 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
             mma_commit(&bars.s_full[b]);
             ++nb;
           }
-          if (!live) break;
+          if (!live || !take_tail()) break;  // an issuer with no tile in the item consumes q_tail too
           if (!kDecode) mma_commit(&bars.q_free);  // arrives once this issuer's MMAs of the item (reading Q) are done
           ++i;
         }
@@ -919,11 +933,12 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
         MLA_TRACE_ONLY(long long tq = clock64();)
         // ---- Q: latent part -> TMEM (256 columns), RoPE part -> smem (SW128 K-major) ----
         if (i > 0 && !waitb(&bars.q_taken, (i - 1) & 1, X_Q_TAKEN, false)) break;
-        load_q_pieces<kFp8>(tbase + lane_base + kTmemQ, row_ok ? qrow : nullptr, 0, kDecode ? 8 : kQRowPieces, p);
-        if constexpr (kDecode) load_q_rope<kFp8>(smem + kOffQpe + r * 128, row_ok ? qpe : nullptr, r, err, p.q, p.ext_q);
+        load_q_pieces<kFp8>(tbase + lane_base + kTmemQ, row_ok ? qrow : nullptr, kDecode ? 0 : kQProdPieces, 8, p);
+        load_q_rope<kFp8>(smem + kOffQpe + r * 128, row_ok ? qpe : nullptr, r, err,
+                          kSparse ? (const void*)p.q_pe : (const void*)p.q, kSparse ? p.ext_q_pe : p.ext_q);
         tmem_wait_st();
         tc_fence_before();
-        warp_arrive(&bars.q_full);
+        warp_arrive(kDecode ? &bars.q_full : &bars.q_tail);
 
         MLA_TRACE_ONLY(trace_wait[24] += clock64() - tq;)
         float m_used = -CUDART_INF_F;  // log2-domain offset of the exponentials
