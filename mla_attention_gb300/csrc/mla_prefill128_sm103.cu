@@ -30,6 +30,7 @@
 #include "mla_internal.h"
 #include "mma_seq.cuh"
 #include "sm103_ptx.cuh"
+#include "softmax_rows.cuh"
 
 namespace mla {
 namespace {
@@ -477,27 +478,6 @@ __device__ __forceinline__ void convert_box_in_place(uint8_t* chunk) {
 }
 
 // ---- softmax rows: one 32-column piece of a score row ----
-// Keys of a piece past lim (the visible keys in it) get the score -inf (+inf when the scale
-// is negative), so one mask-free body serves every piece: the extreme ignores them and
-// 2^(s * scale_log2 - m) is 0 for them.  (A zero scale is run as a tiny positive one, so
-// no infinite score is ever multiplied by 0.)
-template <bool kUp>
-__device__ __forceinline__ void mask_piece(uint32_t (&sr)[32], int lim) {
-  if (lim < 32) {
-    const uint32_t hide = __float_as_uint(kUp ? -CUDART_INF_F : CUDART_INF_F);
-#pragma unroll
-    for (int c = 0; c < 32; ++c) sr[c] = (c < lim) ? sr[c] : hide;
-  }
-}
-// Sparse: the same with the piece's visible keys given as bits (bit c: key c is listed).
-template <bool kUp>
-__device__ __forceinline__ void mask_bits(uint32_t (&sr)[32], uint32_t bits) {
-  if (bits != 0xffffffffu) {
-    const uint32_t hide = __float_as_uint(kUp ? -CUDART_INF_F : CUDART_INF_F);
-#pragma unroll
-    for (int c = 0; c < 32; ++c) sr[c] = ((bits >> c) & 1u) ? sr[c] : hide;
-  }
-}
 // Sparse: raw top-k entries of tile j of token id, key 32 q + lane in e[q] (-1 past K).
 __device__ __forceinline__ void sparse_tile_entries(const CoreParams& p, int id, int j, int32_t (&e)[4]) {
   const int lane = threadIdx.x & 31;
@@ -506,14 +486,6 @@ __device__ __forceinline__ void sparse_tile_entries(const CoreParams& p, int id,
   for (int q = 0; q < 4; ++q) {
     const int c = j * kKeysT + 32 * q + lane;
     e[q] = (c < p.K && guard_span(p.err, G_TOPK, tk + c, 4, p.topk, p.ext_topk)) ? __ldg(tk + c) : -1;
-  }
-}
-template <bool kUp>
-__device__ __forceinline__ void row_extreme(const uint32_t (&sr)[32], float (&eq)[4]) {
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float v0 = __uint_as_float(sr[2 * i]), v1 = __uint_as_float(sr[2 * i + 1]);
-    eq[i & 3] = kUp ? max3f(eq[i & 3], v0, v1) : min3f(eq[i & 3], v0, v1);
   }
 }
 // p = 2^(s * scale_log2 - msub) of a piece as bf16 into four 16-byte chunks (chunk0 .. chunk0 + 3
@@ -972,9 +944,7 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
           // no key yet finds the extreme first.
           const uint32_t scol = tbase + lane_base + kTmemS + sb * kKeysT;
           auto tile_offset = [&](const float (&eq)[4]) -> float {
-            const float e = kUp ? fmaxf(fmaxf(eq[0], eq[1]), fmaxf(eq[2], eq[3]))
-                               : fminf(fminf(eq[0], eq[1]), fminf(eq[2], eq[3]));
-            return (nv == 0) ? -CUDART_INF_F : e * sl2;
+            return (nv == 0) ? -CUDART_INF_F : extreme4<kUp>(eq) * sl2;
           };
           float a = 1.f;  // factor on the O accumulated so far
           // (tcgen05.ld is warp-collective: every branch around one is taken by the whole warp;

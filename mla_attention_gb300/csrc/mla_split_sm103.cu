@@ -4,17 +4,28 @@
 // seqLen [batch] or [2, batch], kvHeadNum for grouped heads, qkScale,
 // maskType NO_MASK / TRIU, prevOut / prevLse merged into the output).
 //
-// One CTA per (128-query tile of one sequence, head).  The scores use both
-// column groups: S = Q_nope K_nope^T + Q_pe K_pe^T, one contraction of depth
-// 192 over the two tensors' boxes.  Tensor memory holds two S buffers (128
-// columns each) and O (128 x 128 fp32).  P is written back over its own S
-// buffer as bf16 and consumed from tensor memory by the P V MMA, so shared
-// memory only holds Q and the K/V stages.
+// Work items are (128-query tile of one sequence, head) pairs, in head-major order (the
+// items running at one time share one or a few heads, whose K/V stays in L2) and longest
+// first within a head.  The kernel is persistent: one CTA per SM takes items blockIdx.x,
+// blockIdx.x + gridDim.x, ...  The scores use both column groups: S = Q_nope K_nope^T +
+// Q_pe K_pe^T, one contraction of depth 192 over the two tensors' boxes.  Tensor memory
+// holds two S buffers (128 columns each) and two O buffers (128 x 128 fp32 each, one per
+// item in flight).  P is written back over its own S buffer as bf16 and consumed from
+// tensor memory by the P V MMA, so shared memory only holds Q and the K/V stages.
 //
-//   warp 4: TMA (Q once; K_nope, K_pe, V per 128-key tile, two stages)
-//   warp 5: MMA issue in the order S0, S1, PV0, S2, PV1, ...
-//   warps 0-3: one query row per thread: mask, online softmax with lazy
-//              rescale (threshold 2^8), P -> TMEM, epilogue with prev merge
+//   warp 4: TMA (Q per item once the previous item's S MMAs are done; K_nope, K_pe, V per
+//           128-key tile, two stages; an L2 prefetch of the next item's Q)
+//   warp 5: MMA issue in the order S0, S1, PV0, S2, PV1, ... across items (the first S of
+//           an item goes out before the last P V of the previous one)
+//   warps 0-3: one query row per thread: mask, online softmax with lazy rescale (threshold
+//           2^8), P -> TMEM; an item's epilogue (O / l, prev merge, store) runs in four
+//           32-column pieces, one after each of the next item's first tiles, so the tensor
+//           pipe keeps working through it
+//
+// A row's 128 scores of a tile are read from tensor memory in one go (four 32-column loads,
+// one wait); its extreme is taken on the raw scores and 2^(s * scale_log2 - m) with one
+// packed two-wide FMA per pair of scores (the sign of the scale picks the instantiation:
+// the extreme of the raw scores is their maximum for a scale >= 0, their minimum below).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -22,6 +33,7 @@
 #include "mla_internal.h"
 #include "mma_seq.cuh"
 #include "sm103_ptx.cuh"
+#include "softmax_rows.cuh"
 
 namespace mla {
 namespace {
@@ -41,16 +53,19 @@ constexpr int kSmemAlloc = kOffBars + 256 + 1024;
 static_assert(kSmemAlloc <= 232448, "shared memory over the sm_103a limit");
 
 constexpr uint32_t kTmemS = 0;     // two S buffers: [0,128), [128,256)
-constexpr uint32_t kTmemO = 256;   // O: [256, 384)
+constexpr uint32_t kTmemO = 256;   // two O buffers: [256,384), [384,512)
 constexpr float kRescaleLog2 = 8.0f;
+constexpr int kEpiPieces = 4;      // 32-column pieces of an item's epilogue
 
 struct Bars {
   uint64_t q_full;
+  uint64_t q_empty;  // every S MMA of the item that holds Q is done (one commit per item)
   uint64_t k_full[kStages], k_empty[kStages];  // K part of stage s (freed by the S MMA)
   uint64_t v_full[kStages], v_empty[kStages];  // V part of stage s (freed by the P V MMA)
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t pv_done[2];  // pv_done[b]: the P V that read P from S buffer b is complete
+  uint64_t o_free[2];   // the rows read O buffer b out (its item's epilogue is done)
   uint64_t stall;  // fault injection: never arrived on
   uint64_t drain;  // abort: one commit of the MMA issuer lands here
   uint32_t tmem_base;
@@ -59,7 +74,7 @@ struct Bars {
 
 static_assert(sizeof(Bars) <= 256, "barrier block larger than its shared-memory slot");
 
-enum : uint32_t { W_QFULL = 0x20, W_KVEMPTY, W_KVFULL, W_SFULL, W_PFULL, W_ODONE, W_STALL };
+enum : uint32_t { W_QFULL = 0x20, W_KVEMPTY, W_KVFULL, W_SFULL, W_PFULL, W_ODONE, W_STALL, W_QEMPTY, W_OFREE };
 
 struct TileInfo {
   int seq, tile, h, hk;
@@ -74,18 +89,25 @@ __device__ __forceinline__ int keys_for_query(const SplitParams& p, int ql, int 
   return n < 0 ? 0 : n;
 }
 
-__device__ __forceinline__ TileInfo tile_info(const SplitParams& p, int block) {
+__device__ __forceinline__ TileInfo tile_info(const SplitParams& p, int64_t item) {
   TileInfo t;
   // Head-major: the CTAs running at one time work on one or a few heads, so those heads' K/V
   // stay in L2 while every query tile of the head reads them (head-minor order had ~150 heads'
   // K/V in flight at once and re-read them from HBM for every query tile).  Within a head the
   // tiles go longest first.
   const int per_head = p.total_q_tiles;
-  const int gt = per_head - 1 - block % per_head;
-  t.h = block / per_head;
+  const int gt = per_head - 1 - (int)(item % per_head);
+  t.h = (int)(item / per_head);
   t.hk = t.h / (p.H / p.Hkv);
-  int s = 0;
-  while (s + 1 < p.batch && p.tile_off[s + 1] <= gt) ++s;
+  // the sequence: the largest s with tile_off[s] <= gt (a sequence without query tiles shares
+  // its offset with the next one and is passed over)
+  int lo = 0, hi = p.batch - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.tile_off[mid] <= gt) lo = mid;
+    else hi = mid - 1;
+  }
+  const int s = lo;
   t.seq = s;
   t.tile = gt - p.tile_off[s];
   t.q0 = p.q_off[s];
@@ -99,6 +121,24 @@ __device__ __forceinline__ TileInfo tile_info(const SplitParams& p, int block) {
   return t;
 }
 
+// One row's epilogue still to write: its item's output row, the softmax statistics and the
+// merge with the previous output, written out in 32-column pieces.
+struct RowEpilogue {
+  int64_t tok;        // the row's token (the sequence's first when the row is past its end)
+  int h;
+  bool row_ok;        // the row is a query of the sequence
+  bool tm;            // O is in tensor memory (the item has KV tiles)
+  uint32_t item;      // the item's O buffer is item & 1
+  uint32_t g_last;    // the item's last KV tile: its P V completes O
+  float m_used, l;    // log2-domain offset and row sum
+  // set by the first piece
+  const __nv_bfloat16* prow;
+  __nv_bfloat16* orow;
+  float cn, wp, lse_out;
+  int piece;          // next piece to write; kEpiPieces: nothing pending
+};
+
+template <bool kUp>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_split_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUtensorMap mq_nope,
                      const __grid_constant__ CUtensorMap mq_pe, const __grid_constant__ CUtensorMap mk_nope,
@@ -109,10 +149,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t lim = p.spin_limit;
   uint32_t* err = p.err;
-  const TileInfo ti = tile_info(p, blockIdx.x);
+  const int64_t n_items = (int64_t)p.total_q_tiles * p.H;
+  const int64_t step = gridDim.x;
 
   if (tid == 0) {
     mbar_init(&bars.q_full, 1);
+    mbar_init(&bars.q_empty, 1);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&bars.k_full[i], 1);
       mbar_init(&bars.k_empty[i], 1);
@@ -121,10 +163,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.s_full[i], 1);
-      mbar_init(&bars.p_full[i], kTile);
+      mbar_init(&bars.p_full[i], 4);  // one arrival per row warp
+      mbar_init(&bars.pv_done[i], 1);
+      mbar_init(&bars.o_free[i], 4);
     }
-    mbar_init(&bars.pv_done[0], 1);
-    mbar_init(&bars.pv_done[1], 1);
     mbar_init(&bars.stall, 1);
     mbar_init(&bars.drain, 1);
     bars.abort_flag = 0;
@@ -147,7 +189,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) *abort_flag = 1;
     return ok;
   };
-  const int qz = ti.q0 + ti.tile * kTile;  // first query token of the tile
   if (p.debug_stall && warp == 5) waitb(&bars.stall, 0, W_STALL);  // runs out: injected fault
 
   // abort drain: the last barrier phase this thread's TMA loads were counted on
@@ -155,206 +196,197 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t drain_par = 0;
   if (warp == 4) {
     // ---------------- TMA producer ----------------
-    if (ti.J > 0) {
-      drain_bar = &bars.q_full;
-      drain_par = 0;
-    }
-    if (ti.J > 0) {
-      const uint32_t sq = smem_u32(smem + kOffQ);
-      if (lane == 0) mbar_arrive_expect_tx(&bars.q_full, kQBytes);
-      __syncwarp();
-      if (lane < 3) tma_load_3d(sq + lane * kBox, lane < 2 ? &mq_nope : &mq_pe, lane == 1 ? 64 : 0, ti.h, qz, &bars.q_full);
-    }
     // K of a stage goes back to the producer once its S MMA is done, V once its P V MMA is done,
     // so K runs one tile ahead of V.  The boxes of a part go out from separate lanes at once: one
     // thread issues a TMA box only every few hundred cycles, lanes of a warp overlap theirs.
-    auto load_k = [&](int j) -> bool {
-      const int s = j % kStages;
-      if (!waitb(&bars.k_empty[s], ((j / kStages) & 1) ^ 1, W_KVEMPTY)) return false;
+    // Counters run over the CTA's items: gk / gv KV tiles whose K / V went out, nq Q loads.
+    uint32_t gk = 0, gv = 0, nq = 0;
+    auto load_k = [&](const TileInfo& ti, int j) -> bool {
+      const int s = gk % kStages;
+      if (!waitb(&bars.k_empty[s], ((gk / kStages) & 1) ^ 1, W_KVEMPTY)) return false;
       const uint32_t st = smem_u32(smem + kOffStage + s * kStageBytes);
       if (lane == 0) mbar_arrive_expect_tx(&bars.k_full[s], kKBytes);
       __syncwarp();
       if (lane < 3) tma_load_3d(st + lane * kBox, lane < 2 ? &mk_nope : &mk_pe, lane == 1 ? 64 : 0, ti.hk,
                                 ti.kv0 + j * kTile, &bars.k_full[s]);
       drain_bar = &bars.k_full[s];
-      drain_par = (j / kStages) & 1;
+      drain_par = (gk / kStages) & 1;
+      ++gk;
       __syncwarp();
       return true;
     };
-    auto load_v = [&](int j) -> bool {
-      const int s = j % kStages;
-      if (!waitb(&bars.v_empty[s], ((j / kStages) & 1) ^ 1, W_KVEMPTY)) return false;
+    auto load_v = [&](const TileInfo& ti, int j) -> bool {
+      const int s = gv % kStages;
+      if (!waitb(&bars.v_empty[s], ((gv / kStages) & 1) ^ 1, W_KVEMPTY)) return false;
       const uint32_t st = smem_u32(smem + kOffStage + s * kStageBytes + kKBytes);
       if (lane == 0) mbar_arrive_expect_tx(&bars.v_full[s], kVBytes);
       __syncwarp();
       if (lane < 2) tma_load_3d(st + lane * kBox, &mv, 64 * lane, ti.hk, ti.kv0 + j * kTile, &bars.v_full[s]);
       drain_bar = &bars.v_full[s];
-      drain_par = (j / kStages) & 1;
+      drain_par = (gv / kStages) & 1;
+      ++gv;
       __syncwarp();
       return true;
     };
-    bool ok = ti.J == 0 || load_k(0);
-    for (int j = 0; ok && j < ti.J; ++j) {
-      if (j + 1 < ti.J && !load_k(j + 1)) break;
-      ok = load_v(j);
+    bool ok = true;
+    for (int64_t w = blockIdx.x; ok && w < n_items; w += step) {
+      const TileInfo ti = tile_info(p, w);
+      if (ti.J == 0) continue;
+      // Q: the single buffer is free once every S MMA of the previous item is done
+      if (nq > 0 && !waitb(&bars.q_empty, (nq - 1) & 1, W_QEMPTY)) break;
+      const int qz = ti.q0 + ti.tile * kTile;  // first query token of the tile
+      const uint32_t sq = smem_u32(smem + kOffQ);
+      if (lane == 0) mbar_arrive_expect_tx(&bars.q_full, kQBytes);
+      __syncwarp();
+      if (lane < 3) tma_load_3d(sq + lane * kBox, lane < 2 ? &mq_nope : &mq_pe, lane == 1 ? 64 : 0, ti.h, qz, &bars.q_full);
+      drain_bar = &bars.q_full;
+      drain_par = nq & 1;
+      ++nq;
+      // the next item's Q into L2 while this item runs (its load then waits on L2, not HBM)
+      if (w + step < n_items) {
+        const TileInfo tn = tile_info(p, w + step);
+        const int qn = tn.q0 + tn.tile * kTile;
+        if (lane < 3) tma_prefetch_3d(lane < 2 ? &mq_nope : &mq_pe, lane == 1 ? 64 : 0, tn.h, qn);
+      }
+      __syncwarp();
+      ok = load_k(ti, 0);
+      for (int j = 0; ok && j < ti.J; ++j) {
+        if (j + 1 < ti.J && !load_k(ti, j + 1)) { ok = false; break; }
+        ok = load_v(ti, j);
+      }
     }
   } else if (warp == 5) {
     // ---------------- MMA issuer ----------------
+    // S(g) goes out as soon as K(g) has landed; the P V of the tile before it then waits for
+    // its P.  Across items the order is the same: the next item's first S is issued before the
+    // last P V of the previous item, so the tensor pipe works while the rows finish that P.
     const uint32_t idesc_s = idesc_bf16_f32(kTile, kTile, false, false);
     const uint32_t idesc_o = idesc_bf16_f32(kTile, 128, false, true);
     const uint32_t sq = smem_u32(smem + kOffQ);
-    auto issue_s = [&](int j) -> bool {
-      const int s = j % kStages;
-      if (!waitb(&bars.k_full[s], (j / kStages) & 1, W_KVFULL)) return false;
+    uint32_t g = 0;      // KV tiles whose S went out
+    uint32_t items = 0;  // items with KV tiles started
+    // the P V still to issue: its tile, its item (O buffer item & 1), first of its item
+    bool pend = false, pfirst = false;
+    uint32_t pg = 0, pitem = 0;
+    auto issue_pv = [&]() -> bool {
+      if (!waitb(&bars.p_full[pg & 1], (pg >> 1) & 1, W_PFULL)) return false;
+      const int s = pg % kStages;
+      if (!waitb(&bars.v_full[s], (pg / kStages) & 1, W_KVFULL)) return false;
+      // the first P V of an item overwrites its O buffer: the rows must have read out the item
+      // that used the buffer before (item - 2)
+      if (pfirst && pitem >= 2 && !waitb(&bars.o_free[pitem & 1], ((pitem >> 1) & 1) ^ 1, W_OFREE)) return false;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t st = smem_u32(smem + kOffStage + s * kStageBytes);
-        mma_s_k192_n128(tbase + kTmemS + (j & 1) * kTile, sdesc_sw128(sq, 16, 1024), sdesc_sw128(st, 16, 1024),
-                        idesc_s);
-        mma_commit(&bars.k_empty[s]);
-        mma_commit(&bars.s_full[j & 1]);
+        const uint32_t vst = smem_u32(smem + kOffStage + s * kStageBytes + kKBytes);
+        mma_pv_tmem_k128_n128(tbase + kTmemO + (pitem & 1) * 128, tbase + kTmemS + (pg & 1) * kTile,
+                              sdesc_sw128(vst, kBox, 1024), idesc_o, pfirst ? 0u : 1u);
+        mma_commit(&bars.v_empty[s]);
+        mma_commit(&bars.pv_done[pg & 1]);
       }
       __syncwarp();
+      pend = false;
       return true;
     };
-    bool live = ti.J == 0 ? true : waitb(&bars.q_full, 0, W_QFULL);
-    if (live && ti.J > 0) live = issue_s(0);
-    for (int j = 0; live && j < ti.J; ++j) {
-      if (j + 1 < ti.J && !issue_s(j + 1)) break;
-      if (!waitb(&bars.p_full[j & 1], (j >> 1) & 1, W_PFULL)) break;
-      if (!waitb(&bars.v_full[j % kStages], (j / kStages) & 1, W_KVFULL)) break;
-      tc_fence_after();
-      if (lane == 0) {
-        const int s = j % kStages;
-        const uint32_t vst = smem_u32(smem + kOffStage + s * kStageBytes + kKBytes);
-        mma_pv_tmem_k128_n128(tbase + kTmemO, tbase + kTmemS + (j & 1) * kTile, sdesc_sw128(vst, kBox, 1024), idesc_o,
-                              j > 0 ? 1u : 0u);
-        mma_commit(&bars.v_empty[s]);
-        mma_commit(&bars.pv_done[j & 1]);
+    bool live = true;
+    for (int64_t w = blockIdx.x; live && w < n_items; w += step) {
+      const TileInfo ti = tile_info(p, w);
+      if (ti.J == 0) continue;
+      if (!waitb(&bars.q_full, items & 1, W_QFULL)) { live = false; break; }
+      for (int j = 0; j < ti.J; ++j, ++g) {
+        const int s = g % kStages;
+        if (!waitb(&bars.k_full[s], (g / kStages) & 1, W_KVFULL)) { live = false; break; }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t st = smem_u32(smem + kOffStage + s * kStageBytes);
+          mma_s_k192_n128(tbase + kTmemS + (g & 1) * kTile, sdesc_sw128(sq, 16, 1024), sdesc_sw128(st, 16, 1024),
+                          idesc_s);
+          mma_commit(&bars.k_empty[s]);
+          mma_commit(&bars.s_full[g & 1]);
+          if (j + 1 == ti.J) mma_commit(&bars.q_empty);  // the item's last read of Q
+        }
+        __syncwarp();
+        if (pend && !issue_pv()) { live = false; break; }
+        pend = true;
+        pg = g;
+        pitem = items;
+        pfirst = (j == 0);
       }
-      __syncwarp();
+      ++items;
     }
+    if (live && pend) issue_pv();
   } else {
     // ---------------- rows: softmax and epilogue ----------------
     const int r = tid;
-    const int i = ti.tile * kTile + r;  // query index within the sequence
-    const bool row_ok = i < ti.ql;
-    const int nkeys = row_ok ? keys_for_query(p, ti.ql, ti.kl, i) : 0;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    float m_used = -CUDART_INF_F, l = 0.f;
-    bool live = true;
-    for (int j = 0; j < ti.J; ++j) {
-      const int sb = j & 1;
-      if (!waitb(&bars.s_full[sb], (j >> 1) & 1, W_SFULL)) { live = false; break; }
-      tc_fence_after();
-      const uint32_t sa = tbase + lane_base + kTmemS + sb * kTile;
-      float x[128];
-      float mt = -CUDART_INF_F;
-      int nv = nkeys - j * kTile;
-      nv = nv < 0 ? 0 : (nv > kTile ? kTile : nv);
-#pragma unroll
-      for (int c0 = 0; c0 < kTile; c0 += 32) {
+    const float sl2 = (p.scale_log2 == 0.f) ? 1e-30f : p.scale_log2;  // see softmax_rows.cuh
+    const uint64_t sl2x2 = f32x2(sl2, sl2);
+    // guarded build: rows checked against the [Nq, H, 128] / [H, Nq] extents (guard_span)
+    const uint64_t ext_rows = (uint64_t)p.Nq * p.H * 128 * 2, ext_lse = (uint64_t)p.H * p.Nq * 4;
+    auto epi_begin = [&](RowEpilogue& e, int64_t tok, int h, bool row_ok, bool tm, uint32_t item, uint32_t g_last,
+                         float m_used, float l) {
+      e.tok = tok;
+      e.h = h;
+      e.row_ok = row_ok;
+      e.tm = tm;
+      e.item = item;
+      e.g_last = g_last;
+      e.m_used = m_used;
+      e.l = l;
+      e.piece = 0;
+    };
+    // One 32-column piece of an epilogue; the first waits for the item's last P V and works
+    // out the weights.  The TMEM load is warp-collective: e.tm is uniform over the CTA.
+    auto epi_piece = [&](RowEpilogue& e) -> bool {
+      const int c0 = 32 * e.piece;
+      if (e.piece == 0) {
+        if (e.tm) {
+          if (!waitb(&bars.pv_done[e.g_last & 1], (e.g_last >> 1) & 1, W_ODONE)) return false;
+          tc_fence_after();
+        }
+        const bool has = e.tm && (e.l > 0.f);
+        const float lse_new = has ? (e.m_used + log2f(e.l)) * 0.69314718055994531f : -CUDART_INF_F;
+        float wn = has ? 1.f : 0.f, wp = 0.f, lse_out = lse_new;
+        e.prow = nullptr;
+        if (p.prev_out && e.row_ok &&
+            guard_span(p.err, G_PREV_OUT, p.prev_out + (e.tok * p.H + e.h) * 128, 256, p.prev_out, ext_rows) &&
+            guard_span(p.err, G_PREV_LSE, p.prev_lse + (int64_t)e.h * p.Nq + e.tok, 4, p.prev_lse, ext_lse)) {
+          e.prow = p.prev_out + (e.tok * p.H + e.h) * 128;
+          const float pl = p.prev_lse[(int64_t)e.h * p.Nq + e.tok];
+          const float m = fmaxf(pl, lse_new);
+          if (m == -CUDART_INF_F) {
+            wn = wp = 0.f;
+            lse_out = -CUDART_INF_F;
+          } else {
+            wp = (pl == -CUDART_INF_F) ? 0.f : expf(pl - m);
+            wn = has ? expf(lse_new - m) : 0.f;
+            const float ws = wp + wn;
+            lse_out = m + logf(ws);
+            wp /= ws;
+            wn /= ws;
+          }
+        }
+        e.cn = has ? wn / e.l : 0.f;
+        e.wp = wp;
+        e.lse_out = lse_out;
+        __nv_bfloat16* orow = p.out + (e.tok * p.H + e.h) * 128;
+        const bool out_ok = e.row_ok && guard_span(p.err, G_OUT, orow, 256, p.out, ext_rows) &&
+                            guard_span(p.err, G_LSE, p.lse + (int64_t)e.h * p.Nq + e.tok, 4, p.lse, ext_lse);
+        e.orow = out_ok ? orow : nullptr;
+      }
+      float o[32];
+      if (e.tm) {
         uint32_t v[32];
-        tmem_ld32(sa + c0, v);
+        tmem_ld32(tbase + lane_base + kTmemO + (e.item & 1) * 128 + c0, v);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          x[c0 + c] = (c0 + c < nv) ? __uint_as_float(v[c]) * p.scale_log2 : -CUDART_INF_F;
-          mt = fmaxf(mt, x[c0 + c]);
-        }
-      }
-      float a = 1.f;
-      if (mt > m_used + kRescaleLog2) {
-        if (l > 0.f) a = ex2_approx(m_used - mt);
-        l *= a;
-        m_used = mt;
-      }
-      // tcgen05.ld/st are warp-collective: rescale when any row of the warp needs it
-      if (__any_sync(0xffffffffu, a != 1.f)) {
-        // O must hold P V of every earlier tile before it is rescaled: PV(j-1) is
-        // use (j-1)/2 of buffer (j-1)%2 and the next use of that buffer needs P(j+1)
-        if (!waitb(&bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, W_ODONE)) { live = false; break; }
-        tc_fence_after();
-        const uint32_t oa = tbase + lane_base + kTmemO;
-#pragma unroll 1
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(oa + c0, v);
-          tmem_wait_ld();
+        for (int c = 0; c < 32; ++c) o[c] = __uint_as_float(v[c]) * e.cn;
+      } else {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * a);
-          tmem_st32(oa + c0, v);
-        }
+        for (int c = 0; c < 32; ++c) o[c] = 0.f;
       }
-      const float msub = (m_used == -CUDART_INF_F) ? 0.f : m_used;
-      float rs = 0.f;
-#pragma unroll
-      for (int c0 = 0; c0 < kTile; c0 += 32) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float e0 = ex2_approx(x[c0 + 2 * c] - msub);
-          const float e1 = ex2_approx(x[c0 + 2 * c + 1] - msub);
-          rs += e0 + e1;
-          pk[c] = pack_bf16x2(e0, e1);
-        }
-        tmem_st16(sa + (c0 >> 1), pk);  // P (bf16 pairs) over the first 64 columns of S
-      }
-      l += rs;
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars.p_full[sb]);
-    }
-    // ---- epilogue ----
-    if (live && ti.J > 0) {
-      live = waitb(&bars.pv_done[(ti.J - 1) & 1], ((ti.J - 1) >> 1) & 1, W_ODONE);
-      tc_fence_after();
-    }
-    if (live) {
-      const int64_t tok = (int64_t)ti.q0 + (row_ok ? i : 0);
-      const bool has = (ti.J > 0) && (l > 0.f);
-      const float lse_new = has ? (m_used + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
-      float wn = has ? 1.f : 0.f, wp = 0.f, lse_out = lse_new;
-      const __nv_bfloat16* prow = nullptr;
-      // guarded build: rows checked against the [Nq, H, 128] / [H, Nq] extents (guard_span)
-      const uint64_t ext_rows = (uint64_t)p.Nq * p.H * 128 * 2, ext_lse = (uint64_t)p.H * p.Nq * 4;
-      if (p.prev_out && row_ok && guard_span(p.err, G_PREV_OUT, p.prev_out + (tok * p.H + ti.h) * 128, 256, p.prev_out, ext_rows) &&
-          guard_span(p.err, G_PREV_LSE, p.prev_lse + (int64_t)ti.h * p.Nq + tok, 4, p.prev_lse, ext_lse)) {
-        prow = p.prev_out + (tok * p.H + ti.h) * 128;
-        const float pl = p.prev_lse[(int64_t)ti.h * p.Nq + tok];
-        const float m = fmaxf(pl, lse_new);
-        if (m == -CUDART_INF_F) {
-          wn = wp = 0.f;
-          lse_out = -CUDART_INF_F;
-        } else {
-          wp = (pl == -CUDART_INF_F) ? 0.f : expf(pl - m);
-          wn = has ? expf(lse_new - m) : 0.f;
-          const float ws = wp + wn;
-          lse_out = m + logf(ws);
-          wp /= ws;
-          wn /= ws;
-        }
-      }
-      const float cn = has ? wn / l : 0.f;
-      __nv_bfloat16* orow = p.out + (tok * p.H + ti.h) * 128;
-      const bool out_ok = guard_span(p.err, G_OUT, orow, 256, p.out, ext_rows) &&
-                          guard_span(p.err, G_LSE, p.lse + (int64_t)ti.h * p.Nq + tok, 4, p.lse, ext_lse);
-#pragma unroll 1
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        float o[32];
-        if (ti.J > 0) {  // uniform over the CTA: every lane takes part in the TMEM load
-          uint32_t v[32];
-          tmem_ld32(tbase + lane_base + kTmemO + c0, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = __uint_as_float(v[c]) * cn;
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = 0.f;
-        }
-        if (!row_ok || !out_ok) continue;
-        if (prow && wp > 0.f) {
-          const uint4* pr = reinterpret_cast<const uint4*>(prow + c0);
+      if (e.orow) {
+        if (e.prow && e.wp > 0.f) {
+          const uint4* pr = reinterpret_cast<const uint4*>(e.prow + c0);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             uint4 xv = pr[u];
@@ -362,19 +394,132 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               float2 f2 = __bfloat1622float2(hx[k]);
-              o[8 * u + 2 * k] += wp * f2.x;
-              o[8 * u + 2 * k + 1] += wp * f2.y;
+              o[8 * u + 2 * k] += e.wp * f2.x;
+              o[8 * u + 2 * k + 1] += e.wp * f2.y;
             }
           }
         }
-        uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+        uint4* dst = reinterpret_cast<uint4*>(e.orow + c0);
 #pragma unroll
         for (int u = 0; u < 4; ++u)
           dst[u] = make_uint4(pack_bf16x2(o[8 * u], o[8 * u + 1]), pack_bf16x2(o[8 * u + 2], o[8 * u + 3]),
                               pack_bf16x2(o[8 * u + 4], o[8 * u + 5]), pack_bf16x2(o[8 * u + 6], o[8 * u + 7]));
       }
-      if (row_ok && out_ok) p.lse[(int64_t)ti.h * p.Nq + tok] = lse_out;
+      if (++e.piece == kEpiPieces) {
+        if (e.orow) p.lse[(int64_t)e.h * p.Nq + e.tok] = e.lse_out;
+        if (e.tm) {  // O buffer item & 1 is read out: the item two on may overwrite it
+          tc_fence_before();
+          warp_arrive(&bars.o_free[e.item & 1]);
+        }
+      }
+      return true;
+    };
+
+    RowEpilogue ep;  // the previous item's epilogue, written during this item's first tiles
+    ep.piece = kEpiPieces;
+    uint32_t g = 0, items = 0;  // KV tiles and items with KV tiles so far (as the MMA warp counts)
+    bool live = true;
+    for (int64_t w = blockIdx.x; live && w < n_items; w += step) {
+      const TileInfo ti = tile_info(p, w);
+      const int i = ti.tile * kTile + r;  // query index within the sequence
+      const bool row_ok = i < ti.ql;
+      const int nkeys = row_ok ? keys_for_query(p, ti.ql, ti.kl, i) : 0;
+      const int64_t tok = (int64_t)ti.q0 + (row_ok ? i : 0);
+      if (p.prev_out && row_ok) {  // the previous output row into L2 for this item's epilogue
+        const __nv_bfloat16* pr = p.prev_out + (tok * p.H + ti.h) * 128;
+        if (guard_span(p.err, G_PREV_OUT, pr, 256, p.prev_out, ext_rows)) {
+          prefetch_l2(pr);
+          prefetch_l2(pr + 64);
+        }
+      }
+      if (ti.J == 0) {  // no key: O is zero and the previous output passes through
+        RowEpilogue z;
+        epi_begin(z, tok, ti.h, row_ok, false, 0, 0, -CUDART_INF_F, 0.f);
+        while (z.piece < kEpiPieces) epi_piece(z);  // no wait without TMEM
+        continue;
+      }
+      float m_used = -CUDART_INF_F, l = 0.f;
+      for (int j = 0; j < ti.J; ++j, ++g) {
+        const int sb = g & 1;
+        if (!waitb(&bars.s_full[sb], (g >> 1) & 1, W_SFULL)) { live = false; break; }
+        tc_fence_after();
+        const uint32_t sa = tbase + lane_base + kTmemS + sb * kTile;
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld32(sa + 32 * q, sr[q]);
+        tmem_wait_ld();
+        int nv = nkeys - j * kTile;
+        nv = nv < 0 ? 0 : (nv > kTile ? kTile : nv);
+        float eq[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) eq[k] = kUp ? -CUDART_INF_F : CUDART_INF_F;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          mask_piece<kUp>(sr[q], nv - 32 * q);
+          row_extreme<kUp>(sr[q], eq);
+        }
+        const float mt = (nv == 0) ? -CUDART_INF_F : extreme4<kUp>(eq) * sl2;
+        float a = 1.f;
+        if (mt > m_used + kRescaleLog2) {
+          if (l > 0.f) a = ex2_approx(m_used - mt);
+          l *= a;
+          m_used = mt;
+        }
+        // tcgen05.ld/st are warp-collective: rescale when any row of the warp needs it (never on
+        // an item's first tile, where l is 0 and the first P V overwrites O)
+        if (__any_sync(0xffffffffu, a != 1.f)) {
+          // O must hold P V of every earlier tile of the item before it is rescaled
+          if (!waitb(&bars.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, W_ODONE)) { live = false; break; }
+          tc_fence_after();
+          const uint32_t oa = tbase + lane_base + kTmemO + (items & 1) * 128;
+#pragma unroll 1
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(oa + c0, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * a);
+            tmem_st32(oa + c0, v);
+          }
+        }
+        const float msub = (m_used == -CUDART_INF_F) ? 0.f : m_used;
+        const uint64_t nmsub2 = f32x2(-msub, -msub);
+        uint64_t rsq[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            float x0, x1;
+            f32x2_split(fma_f32x2(f32x2(__uint_as_float(sr[q][2 * u]), __uint_as_float(sr[q][2 * u + 1])), sl2x2,
+                                  nmsub2),
+                        x0, x1);
+            const float e0 = ex2_approx(x0);
+            const float e1 = ex2_approx(x1);
+            rsq[u & 1] = add_f32x2(rsq[u & 1], f32x2(e0, e1));
+            pk[u] = pack_bf16x2(e0, e1);
+          }
+          tmem_st16(sa + 16 * q, pk);  // P (bf16 pairs) over the first 64 columns of S
+        }
+        {
+          float q0, q1, q2, q3;
+          f32x2_split(rsq[0], q0, q1);
+          f32x2_split(rsq[1], q2, q3);
+          l += (q0 + q1) + (q2 + q3);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        warp_arrive(&bars.p_full[sb]);
+        // a piece of the previous item's epilogue while the tensor pipe runs this tile's P V
+        if (ep.piece < kEpiPieces && !epi_piece(ep)) { live = false; break; }
+      }
+      if (!live) break;
+      while (live && ep.piece < kEpiPieces) live = epi_piece(ep);  // the item had fewer tiles than pieces
+      if (!live) break;
+      epi_begin(ep, tok, ti.h, row_ok, true, items, g - 1, m_used, l);
+      ++items;
     }
+    while (live && ep.piece < kEpiPieces) live = epi_piece(ep);
   }
 
   __syncwarp();
@@ -398,13 +543,18 @@ cudaError_t launch_split(const SplitParams& p, const CUtensorMap& mq_nope, const
                          const CUtensorMap& mk_nope, const CUtensorMap& mk_pe, const CUtensorMap& mv,
                          cudaStream_t stream) {
   static PerDeviceOnce attrs;
-  cudaError_t e = attrs.run(
-      [] { return cudaFuncSetAttribute(mla_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc); });
+  cudaError_t e = attrs.run([] {
+    cudaError_t r = cudaFuncSetAttribute(mla_split_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    if (r != cudaSuccess) return r;
+    return cudaFuncSetAttribute(mla_split_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+  });
   if (e != cudaSuccess) return e;
-  const int64_t blocks = (int64_t)p.total_q_tiles * p.H;
-  if (blocks == 0) return cudaSuccess;
-  mla_split_kernel<<<dim3((unsigned)blocks), dim3(kThreads), kSmemAlloc, stream>>>(p, mq_nope, mq_pe, mk_nope, mk_pe,
-                                                                                   mv);
+  const int64_t items = (int64_t)p.total_q_tiles * p.H;
+  if (items == 0) return cudaSuccess;
+  const int64_t sms = device_sm_count();
+  const int64_t blocks = items < sms ? items : sms;
+  auto kern = p.scale_log2 >= 0.f ? mla_split_kernel<true> : mla_split_kernel<false>;
+  kern<<<dim3((unsigned)blocks), dim3(kThreads), kSmemAlloc, stream>>>(p, mq_nope, mq_pe, mk_nope, mk_pe, mv);
   return cudaGetLastError();
 }
 

@@ -41,6 +41,18 @@ def test_split_parity(qlens, kvlens, H, Hkv, mt, prev):
     assert_lse_close(lse, rl)
 
 
+@pytest.mark.parametrize("scale", [-0.09, 0.0, -0.0])
+def test_split_negative_and_zero_scale(scale):
+    """A negative scale runs the instantiation whose row extreme is the minimum of the raw scores;
+    a zero scale (either sign) gives every visible key the same weight."""
+    si = gen.split_inputs([70, 200], [70, 260], 4, 2, seed=17, scale=scale, with_prev=True, prev_lse_range=(2.0, 5.0))
+    out, lse = _split(si, 1, with_prev=True)
+    ro, rl = mo.mla_prefill_split(si.q_nope, si.q_pe, si.k_nope, si.k_pe, si.v, si.seq_len, 4, 2, scale, 1,
+                                  prev_out=si.prev_out, prev_lse=si.prev_lse)
+    assert_out_close(out, ro)
+    assert_lse_close(lse, rl)
+
+
 def test_split_seq_len_one_row_and_kv_head_zero():
     si = gen.split_inputs([40, 90], [40, 90], 4, 4, seed=3)
     out1, lse1 = _split(si, 1)
