@@ -168,6 +168,9 @@ mla_status mla_prefill_varlen(const void* q, int64_t q_stride_t, int64_t q_strid
  * out bf16 [Nq, H, 128] (may alias prev_out); lse fp32 [H, Nq] (may alias prev_lse).
  * The [512, 512] mask tensor, kernelType (high precision only), inputLayout
  * (BSND only) and calcType of the page are fixed by these arguments.
+ * workspace: device memory of mla_prefill_split_workspace_size bytes; besides the status
+ *   word it holds the counter the kernel's CTAs claim work items from (reset on `stream`
+ *   before the launch), so two calls in flight at once need two workspaces.
  */
 size_t mla_prefill_split_workspace_size(int Nq, int H);
 mla_status mla_prefill_split(const void* q_nope, const void* q_pe, const void* k_nope, const void* k_pe,

@@ -590,6 +590,7 @@ mla_status mla_prefill_split(const void* q_nope, const void* q_pe, const void* k
     tiles += (ql + kRows - 1) / kRows;
     MLA_REQUIRE(nq < (1ll << 31) && nkv < (1ll << 31), "mla_prefill_split: too many tokens");
   }
+  MLA_REQUIRE(tiles * head_num < (1ll << 31), "mla_prefill_split: too many (query tile, head) items");
   p.q_off[batch] = (int)nq;
   p.kv_off[batch] = (int)nkv;
   p.tile_off[batch] = (int)tiles;
@@ -638,7 +639,10 @@ mla_status mla_prefill_split(const void* q_nope, const void* q_pe, const void* k
   p.prev_lse = prev_lse;
   p.out = reinterpret_cast<__nv_bfloat16*>(out);
   p.lse = lse;
-  cudaError_t e = launch_split(p, m[0], m[1], m[2], m[3], m[4], st);
+  p.ticket = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(workspace) + kWsTicket);
+  cudaError_t e = cudaMemsetAsync(p.ticket, 0, sizeof(uint32_t), st);  // the kernel's CTAs claim items from 0
+  if (e != cudaSuccess) return cuda_fail(e, "mla_prefill_split ticket reset");
+  e = launch_split(p, m[0], m[1], m[2], m[3], m[4], st);
   if (e != cudaSuccess) return cuda_fail(e, "mla_prefill_split launch");
   return ok();
 }

@@ -29,6 +29,7 @@ constexpr int kVBoxes = kLatent / kBoxCols;   // 8 column boxes for V (512 colum
 // workspace layout (shared by every call): a 256-byte header first
 // ---------------------------------------------------------------------------
 constexpr size_t kWsHeader = 256;       // [0]: device status word
+constexpr size_t kWsTicket = 64;        // split kernel: next work item to claim (zeroed before each launch)
 constexpr uint32_t kDefaultSpinLimit = 1u << 25;
 
 uint32_t spin_limit();                  // process-wide bound for device waits
@@ -213,6 +214,7 @@ struct SplitParams {
   uint32_t debug_stall;
   uint32_t* err;
   int total_q_tiles;           // sum over sequences of ceil(q_len / 128)
+  uint32_t* ticket;            // ws: work items claimed so far (0 at launch)
   const __nv_bfloat16* prev_out;
   const float* prev_lse;
   __nv_bfloat16* out;

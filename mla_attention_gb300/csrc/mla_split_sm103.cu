@@ -6,15 +6,18 @@
 //
 // Work items are (128-query tile of one sequence, head) pairs, in head-major order (the
 // items running at one time share one or a few heads, whose K/V stays in L2) and longest
-// first within a head.  The kernel is persistent: one CTA per SM takes items blockIdx.x,
-// blockIdx.x + gridDim.x, ...  The scores use both column groups: S = Q_nope K_nope^T +
+// first within a head.  The kernel is persistent: one CTA per SM claims the next item from a
+// counter in the workspace whenever it starts one, so the items in flight stay a window of
+// consecutive items (a fixed share per CTA lets CTAs drift apart by many heads and their K/V
+// out of L2); the claiming warp hands the item to the others through a small queue in
+// shared memory.  The scores use both column groups: S = Q_nope K_nope^T +
 // Q_pe K_pe^T, one contraction of depth 192 over the two tensors' boxes.  Tensor memory
 // holds two S buffers (128 columns each) and two O buffers (128 x 128 fp32 each, one per
 // item in flight).  P is written back over its own S buffer as bf16 and consumed from
 // tensor memory by the P V MMA, so shared memory only holds Q and the K/V stages.
 //
-//   warp 4: TMA (Q per item once the previous item's S MMAs are done; K_nope, K_pe, V per
-//           128-key tile, two stages; an L2 prefetch of the next item's Q)
+//   warp 4: claims items; TMA (Q per item once the previous item's S MMAs are done; K_nope,
+//           K_pe, V per 128-key tile, two stages; an L2 prefetch of the next item's Q)
 //   warp 5: MMA issue in the order S0, S1, PV0, S2, PV1, ... across items (the first S of
 //           an item goes out before the last P V of the previous one)
 //   warps 0-3: one query row per thread: mask, online softmax with lazy rescale (threshold
@@ -56,6 +59,7 @@ constexpr uint32_t kTmemS = 0;     // two S buffers: [0,128), [128,256)
 constexpr uint32_t kTmemO = 256;   // two O buffers: [256,384), [384,512)
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kEpiPieces = 4;      // 32-column pieces of an item's epilogue
+constexpr int kRing = 4;           // claimed items handed from the TMA warp to the others
 
 struct Bars {
   uint64_t q_full;
@@ -66,15 +70,17 @@ struct Bars {
   uint64_t p_full[2];
   uint64_t pv_done[2];  // pv_done[b]: the P V that read P from S buffer b is complete
   uint64_t o_free[2];   // the rows read O buffer b out (its item's epilogue is done)
+  uint64_t item_full[kRing], item_empty[kRing];  // the queue of claimed items (empty: 5 readers)
   uint64_t stall;  // fault injection: never arrived on
   uint64_t drain;  // abort: one commit of the MMA issuer lands here
   uint32_t tmem_base;
   uint32_t abort_flag;
+  int32_t ring[kRing];  // item index, -1: no item left
 };
 
 static_assert(sizeof(Bars) <= 256, "barrier block larger than its shared-memory slot");
 
-enum : uint32_t { W_QFULL = 0x20, W_KVEMPTY, W_KVFULL, W_SFULL, W_PFULL, W_ODONE, W_STALL, W_QEMPTY, W_OFREE };
+enum : uint32_t { W_QFULL = 0x20, W_KVEMPTY, W_KVFULL, W_SFULL, W_PFULL, W_ODONE, W_STALL, W_QEMPTY, W_OFREE, W_ITEM };
 
 struct TileInfo {
   int seq, tile, h, hk;
@@ -150,7 +156,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t lim = p.spin_limit;
   uint32_t* err = p.err;
   const int64_t n_items = (int64_t)p.total_q_tiles * p.H;
-  const int64_t step = gridDim.x;
 
   if (tid == 0) {
     mbar_init(&bars.q_full, 1);
@@ -166,6 +171,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.p_full[i], 4);  // one arrival per row warp
       mbar_init(&bars.pv_done[i], 1);
       mbar_init(&bars.o_free[i], 4);
+    }
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&bars.item_full[i], 1);
+      mbar_init(&bars.item_empty[i], 5);  // the MMA warp and the four row warps
     }
     mbar_init(&bars.stall, 1);
     mbar_init(&bars.drain, 1);
@@ -190,6 +199,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     return ok;
   };
   if (p.debug_stall && warp == 5) waitb(&bars.stall, 0, W_STALL);  // runs out: injected fault
+  // the next claimed item from the queue (warps 0-3 and 5); -1 once none is left
+  uint32_t n_popped = 0;
+  auto pop_item = [&](int64_t& w) -> bool {
+    const int k = n_popped % kRing;
+    if (!waitb(&bars.item_full[k], (n_popped / kRing) & 1, W_ITEM)) return false;
+    w = *reinterpret_cast<volatile int32_t*>(&bars.ring[k]);
+    warp_arrive(&bars.item_empty[k]);
+    ++n_popped;
+    return true;
+  };
 
   // abort drain: the last barrier phase this thread's TMA loads were counted on
   uint64_t* drain_bar = nullptr;
@@ -228,9 +247,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       return true;
     };
+    auto claim = [&]() -> int64_t {
+      uint32_t v = 0;
+      if (lane == 0) v = atomicAdd(p.ticket, 1u);
+      v = __shfl_sync(0xffffffffu, v, 0);
+      return (int64_t)v < n_items ? (int64_t)v : -1;
+    };
+    uint32_t n_pushed = 0;
+    auto push_item = [&](int64_t w) -> bool {
+      const int k = n_pushed % kRing;
+      if (!waitb(&bars.item_empty[k], ((n_pushed / kRing) & 1) ^ 1, W_ITEM)) return false;
+      if (lane == 0) {
+        bars.ring[k] = (int32_t)w;
+        mbar_arrive(&bars.item_full[k]);  // release: the readers see the entry
+      }
+      __syncwarp();
+      ++n_pushed;
+      return true;
+    };
     bool ok = true;
-    for (int64_t w = blockIdx.x; ok && w < n_items; w += step) {
+    int64_t w = claim();
+    while (ok) {
+      if (!push_item(w) || w < 0) break;
+      const int64_t wn = claim();  // claimed now: its Q is prefetched while this item runs
       const TileInfo ti = tile_info(p, w);
+      w = wn;
       if (ti.J == 0) continue;
       // Q: the single buffer is free once every S MMA of the previous item is done
       if (nq > 0 && !waitb(&bars.q_empty, (nq - 1) & 1, W_QEMPTY)) break;
@@ -243,8 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_par = nq & 1;
       ++nq;
       // the next item's Q into L2 while this item runs (its load then waits on L2, not HBM)
-      if (w + step < n_items) {
-        const TileInfo tn = tile_info(p, w + step);
+      if (wn >= 0) {
+        const TileInfo tn = tile_info(p, wn);
         const int qn = tn.q0 + tn.tile * kTile;
         if (lane < 3) tma_prefetch_3d(lane < 2 ? &mq_nope : &mq_pe, lane == 1 ? 64 : 0, tn.h, qn);
       }
@@ -288,7 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     bool live = true;
-    for (int64_t w = blockIdx.x; live && w < n_items; w += step) {
+    while (live) {
+      int64_t w;
+      if (!pop_item(w)) { live = false; break; }
+      if (w < 0) break;
       const TileInfo ti = tile_info(p, w);
       if (ti.J == 0) continue;
       if (!waitb(&bars.q_full, items & 1, W_QFULL)) { live = false; break; }
@@ -419,7 +463,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     ep.piece = kEpiPieces;
     uint32_t g = 0, items = 0;  // KV tiles and items with KV tiles so far (as the MMA warp counts)
     bool live = true;
-    for (int64_t w = blockIdx.x; live && w < n_items; w += step) {
+    while (live) {
+      int64_t w;
+      if (!pop_item(w)) { live = false; break; }
+      if (w < 0) break;
       const TileInfo ti = tile_info(p, w);
       const int i = ti.tile * kTile + r;  // query index within the sequence
       const bool row_ok = i < ti.ql;
