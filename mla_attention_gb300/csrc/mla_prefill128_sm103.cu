@@ -91,7 +91,9 @@ struct BarsT {
   uint64_t stats_free;         // the O-CTA read the row statistics (remote)
   // O-CTA
   uint64_t vfull[2], vempty[2];
-  uint64_t p_full[2];          // P tile and factors landed (bulk copy with its tx bytes)
+  uint64_t p_full[2];          // P tile and factors landed (bulk copy with its tx bytes); sparse: box 0 of P
+                               // (keys 0-63) and the factors
+  uint64_t p_full1[2];         // sparse: box 1 of P tile b (keys 64-127) landed
   uint64_t p_ready[2];         // rows rescaled O for P tile b
   uint64_t stats_full;         // row statistics stored here by the S-CTA (remote)
   uint64_t o_free;             // the epilogue read O
@@ -572,6 +574,7 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
         mbar_init(&bars.vfull[b], kSparse ? 128 : (kFp8 ? 4 : 1));
         mbar_init(&bars.vempty[b], 1);
         mbar_init(&bars.p_full[b], 1);
+        mbar_init(&bars.p_full1[b], 1);
         mbar_init(&bars.p_ready[b], kRowWarpsO);
         mbar_init(&bars.pb_free[b], 1);
       }
@@ -841,6 +844,7 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
       const float* alpha = reinterpret_cast<const float*>(smem + kOffAlphaS);
       const uint32_t rem_p_full0 = map_to_rank(smem_u32(&bars.p_full[0]), peer);
       const uint32_t rem_p_full1 = map_to_rank(smem_u32(&bars.p_full[1]), peer);
+
       const uint32_t rem_p_o = map_to_rank(smem_u32(smem + kOffPO), peer);
       const uint32_t rem_alpha_o = map_to_rank(smem_u32(smem + kOffAlphaO), peer);
       uint32_t t = 0;
@@ -855,9 +859,20 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
           }
           if (lane == 0) {
             const uint32_t bar = sb ? rem_p_full1 : rem_p_full0;
-            mbar_arrive_expect_tx_remote(bar, kPBytesT + kRows * 4);
-            bulk_copy_to_peer(rem_p_o + sb * kPBytesT, smem_u32(pbuf + sb * kPBytesT), kPBytesT, bar);
-            bulk_copy_to_peer(rem_alpha_o + sb * kRows * 4, smem_u32(alpha + sb * kRows), kRows * 4, bar);
+            if constexpr (kSparse) {
+              // two boxes on two barriers: P V of keys 0-63 starts once the first has landed
+              mbar_arrive_expect_tx_remote(bar, kPBoxBytes + kRows * 4);
+              bulk_copy_to_peer(rem_alpha_o + sb * kRows * 4, smem_u32(alpha + sb * kRows), kRows * 4, bar);
+              bulk_copy_to_peer(rem_p_o + sb * kPBytesT, smem_u32(pbuf + sb * kPBytesT), kPBoxBytes, bar);
+              const uint32_t bar1 = map_to_rank(smem_u32(&bars.p_full1[sb]), peer);
+              mbar_arrive_expect_tx_remote(bar1, kPBoxBytes);
+              bulk_copy_to_peer(rem_p_o + sb * kPBytesT + kPBoxBytes, smem_u32(pbuf + sb * kPBytesT + kPBoxBytes),
+                                kPBoxBytes, bar1);
+            } else {
+              mbar_arrive_expect_tx_remote(bar, kPBytesT + kRows * 4);
+              bulk_copy_to_peer(rem_p_o + sb * kPBytesT, smem_u32(pbuf + sb * kPBytesT), kPBytesT, bar);
+              bulk_copy_to_peer(rem_alpha_o + sb * kRows * 4, smem_u32(alpha + sb * kRows), kRows * 4, bar);
+            }
             bulk_commit();
             bulk_wait_read_all();  // this copy has read local buffer sb: the rows may refill it
             mbar_arrive(&bars.pbuf_free[sb]);
@@ -1164,6 +1179,7 @@ __device__ __forceinline__ void prefill128_body(const CoreParams& p, const CoreM
             for (int h = 0; h < 2; ++h, ++u) {
               const int s = u & 1;
               if (!wait1(&bars.vfull[s], (u >> 1) & 1, X_V_FULL, false)) { live = false; break; }
+              if (kSparse && h == 1 && !wait1(&bars.p_full1[pb], (t >> 1) & 1, X_P_FULL, true)) { live = false; break; }
               tc_fence_after();
               if constexpr (kSparse) fence_proxy_async_smem();  // cp.async rows, read by the MMA
               const uint32_t vst = smem_u32(smem + kOffV + s * kHalfBytesV);
