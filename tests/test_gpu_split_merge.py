@@ -53,6 +53,31 @@ def test_split_negative_and_zero_scale(scale):
     assert_lse_close(lse, rl)
 
 
+def test_split_query_tiles_without_keys():
+    """KV shorter than the queries under TRIU (bottom-right): the first query tiles see no key and
+    keep the previous output; a sequence with no key at all keeps it entirely."""
+    si = gen.split_inputs([300, 5, 130], [50, 0, 200], 4, 4, seed=23, with_prev=True, prev_lse_range=(2.0, 5.0))
+    out, lse = _split(si, 1, with_prev=True)
+    ro, rl = mo.mla_prefill_split(si.q_nope, si.q_pe, si.k_nope, si.k_pe, si.v, si.seq_len, 4, 4, si.scale, 1,
+                                  prev_out=si.prev_out, prev_lse=si.prev_lse)
+    assert_out_close(out, ro)
+    assert_lse_close(lse, rl)
+
+
+def test_split_many_sequences():
+    """40 sequences of mixed lengths, some empty: every work item is claimed once and finds its
+    sequence (the per-CTA item claiming and the sequence search over the tile offsets)."""
+    g = np.random.default_rng(29)
+    qlens = [int(x) for x in g.integers(0, 200, size=40)]
+    qlens[3] = qlens[17] = 0
+    kvlens = [q + int(x) for q, x in zip(qlens, g.integers(0, 60, size=40))]
+    si = gen.split_inputs(qlens, kvlens, 2, 1, seed=31)
+    out, lse = _split(si, 1)
+    ro, rl = mo.mla_prefill_split(si.q_nope, si.q_pe, si.k_nope, si.k_pe, si.v, si.seq_len, 2, 1, si.scale, 1)
+    assert_out_close(out, ro)
+    assert_lse_close(lse, rl)
+
+
 def test_split_seq_len_one_row_and_kv_head_zero():
     si = gen.split_inputs([40, 90], [40, 90], 4, 4, seed=3)
     out1, lse1 = _split(si, 1)
