@@ -1,8 +1,8 @@
 """The guarded build: libmla compiled with MLA_GUARD checks every plain global load and store of its
 kernels against the extent of the buffer it belongs to and records the first access that would
-leave it (status word 0x3000 | site; the access is skipped).  compute-sanitizer is closed on this
-pool, so this build stands in for its out-of-bounds checks: small cases of every call run through
-it (a child process loads the guarded library) must match the oracle with no check firing."""
+leave it (status word 0x3000 | site; the access is skipped).  It serves as an out-of-bounds
+checker where no external memory checker can run: small cases of every call run through the
+guarded library (a child process loads it) must match the oracle with no check firing."""
 import os
 import subprocess
 import sys
