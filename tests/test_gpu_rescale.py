@@ -8,8 +8,8 @@ import torch
 
 import oracle.mla_oracle as mo
 from mla_attention_gb300 import inputs as gen
-from mla_attention_gb300 import (check_device_status, mla_decode, mla_prefill, mla_prefill_split, mla_sparse,
-                                 set_tile_keys)
+from mla_attention_gb300 import (check_device_status, mla_decode, mla_decode_ex, mla_prefill, mla_prefill_split,
+                                 mla_sparse, set_tile_keys)
 from tests.helpers import assert_lse_close, assert_out_close, dev
 
 pytestmark = pytest.mark.gpu
@@ -42,6 +42,44 @@ def test_prefill_climbing_scores(tile_keys, sign):
     torch.cuda.synchronize()
     check_device_status()
     ro, rl = mo.mla_prefill(P.q, P.kv, P.scale, **kw)
+    assert_out_close(out, ro)
+    assert_lse_close(lse, rl)
+
+
+def test_prefill_climbing_scores_with_prev(tile_keys):
+    """The same climb merged with a previous result whose LSEs are of the same size, so both sides
+    of the merge carry weight."""
+    P = gen.prefill_inputs(T=150, H=16, Tkv=900, seed=75)
+    P.kv[:, 512] = ramp(900, P.scale)
+    P.q[:, :, 512] = 1.0
+    po, pl = gen.prev_inputs(150, 16, 512, seed=76, lse_lo=95.0, lse_hi=125.0)
+    kw = dict(causal=True, q_pos0=740, kv_pos0=0)
+    out, lse = mla_prefill(P.q.to(dev()), P.kv.to(dev()), P.scale, prev_out=po.to(dev()), prev_lse=pl.to(dev()), **kw)
+    torch.cuda.synchronize()
+    check_device_status()
+    ro, rl = mo.mla_prefill(P.q, P.kv, P.scale, prev_out=po, prev_lse=pl, **kw)
+    assert_out_close(out, ro)
+    assert_lse_close(lse, rl)
+
+
+def test_multi_token_decode_climbing_scores_with_sinks(tile_keys):
+    """Two query tokens per request (causal between them) and per-head sinks of the same size as
+    the climbing scores' LSEs."""
+    D = gen.decode_inputs([700, 1300, 260], H=16, seed=77, page_size=16)
+    bt = D.block_table.numpy()
+    for b, n in enumerate(D.lens.tolist()):
+        r = ramp(n, D.scale)
+        for j in range(n):
+            D.cache[int(bt[b, j // D.page_size]), j % D.page_size, 512] = r[j]
+    g = torch.Generator().manual_seed(78)
+    q2 = gen.randn_bf16((3, 2, 16, 576), g)
+    q2[..., 512] = 1.0
+    sinks = (90.0 + 40.0 * torch.rand((16,), generator=g)).float()
+    out, lse = mla_decode_ex(q2.to(dev()), D.cache.to(dev()), D.block_table.to(dev()), D.lens.to(dev()), D.scale,
+                             sinks=sinks.to(dev()), num_splits=4)
+    torch.cuda.synchronize()
+    check_device_status()
+    ro, rl = mo.mla_decode_ex(q2, D.cache, D.block_table, D.lens, D.scale, sinks=sinks)
     assert_out_close(out, ro)
     assert_lse_close(lse, rl)
 
