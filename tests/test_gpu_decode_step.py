@@ -224,6 +224,7 @@ def test_multi_token_decode_with_sinks(decode_engine, S, H, sinks, splits):
     ([1, 63, 64, 65, 200, 4100], 1, 128, 64, 0, False),
     ([3000, 17, 0, 129, 64], 2, 16, 64, 7, True),
     ([70, 5, 130, 300], 1, 128, 16, 0, False),
+    ([300, 129, 1000, 64], 1, 128, 128, 0, False),   # 128-token pages: halves at offsets 0 and 64 of a page
 ])
 def test_fp8_cache_decode(lens, S, H, page_size, splits, sinks):
     from mla_attention_gb300 import mla_decode_fp8
