@@ -120,7 +120,7 @@ void mla_debug_inject_stall(int enable);
  * scale    multiplies q.k (required; no default).
  * causal   1: key j is visible to token t iff kv_pos0 + j <= q_pos0 + t; 0: all valid keys.
  * prev_out bf16 [T, H, dv] contiguous, prev_lse fp32 [H, T]; both or neither.
- * out      bf16 [T, H, dv] contiguous; may be the same buffer as prev_out.
+ * out      bf16 [T, H, dv] contiguous (T * H below 2^31); may be the same buffer as prev_out.
  * lse      fp32 [H, T]; may be the same buffer as prev_lse.
  * workspace/_bytes  >= mla_prefill_workspace_size(T, H).
  */
@@ -191,7 +191,7 @@ mla_status mla_prefill_split(const void* q_nope, const void* q_pe, const void* k
  *
  * q           bf16 [B, H, 576] contiguous (H <= 128).
  * kv_cache    bf16 [num_pages, page_size, 576] contiguous; page_size in {16, 32, 64}
- *             or a multiple of 64.
+ *             or a multiple of 64; num_pages * page_size below 2^31.
  * block_table DEVICE int32 [B, max_pages]: token j of request b is row
  *             j % page_size of page block_table[b][j / page_size].
  * lens        DEVICE int32 [B]: keys of request b (0 allowed: out = 0, lse = -inf);

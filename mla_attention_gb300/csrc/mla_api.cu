@@ -216,7 +216,8 @@ mla_status prefill_one(const void* q, int64_t q_stride_t, int64_t q_stride_h, co
     if (s != MLA_OK) return s;
   }
   {
-    const uint64_t rows = (uint64_t)T * (uint64_t)H;
+    const uint64_t rows = (uint64_t)T * (uint64_t)H;  // output rows are 32-bit signed tensor-map coordinates
+    MLA_REQUIRE(rows <= (uint64_t)INT32_MAX, "mla_prefill: T * H must be below 2^31");
     mla_status s = map2d(&maps.out, out, kLatent, rows, kLatent, 64, "out");
     if (s == MLA_OK && prev_out) s = map2d(&maps.prev, prev_out, kLatent, rows, kLatent, 64, "prev_out");
     if (s != MLA_OK) return s;
@@ -284,6 +285,8 @@ mla_status decode_impl(const void* q, int q_per_req, const void* kv_cache, bool 
   CoreMaps maps;
   memset(&maps, 0, sizeof(maps));
   const uint64_t rows = (uint64_t)num_pages * (uint64_t)page_size;
+  // cache rows are 32-bit signed tensor-map coordinates
+  MLA_REQUIRE(rows <= (uint64_t)INT32_MAX, "mla_decode: num_pages * page_size must be below 2^31");
   if (!fp8) {
     mla_status s = map2d(&maps.kv, kv_cache, kDk, rows, kDk, page_size >= kKeys ? kKeys : (uint32_t)page_size, "cache");
     if (s != MLA_OK) return s;
