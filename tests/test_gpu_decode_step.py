@@ -142,6 +142,30 @@ def test_project_out_parity(T, H):
     _gemm_close(out, mo.project_out(o, wv), "projected out", 512)
 
 
+@pytest.mark.full
+def test_absorption_bmms_full_size_sampled_tokens():
+    """Both BMMs at the measured size (T = 8192 tokens, H = 128): every token is its own
+    per-head product, so sampled tokens against the oracle check the whole launch's indexing
+    (the q side reads a strided [T, H, 128] view of a [T, H, 192] projection)."""
+    from mla_attention_gb300 import mla_absorb_q, mla_project_out
+    T, H = 8192, 128
+    d = dev()
+    q = gen.randn_bf16_device((T, H, 192), 311, d)
+    o = gen.randn_bf16_device((T, H, 512), 312, d)
+    wk, wv = gen.absorb_weights(H, seed=313)
+    fused = torch.full((T, H, 576), 7.0, dtype=torch.bfloat16, device=d)
+    mla_absorb_q(q[:, :, :128], wk.to(d), q_out=fused)
+    out = mla_project_out(o, wv.to(d))
+    torch.cuda.synchronize()
+    check_device_status()
+    for t in gen.sample_rows(T, 8, seed=314, must=[0, 127, 128, T - 1]):
+        _gemm_close(fused[t:t + 1, :, :512], mo.absorb_q(q[t:t + 1, :, :128].cpu(), wk), f"q_lift[{t}]", 128)
+        _gemm_close(out[t:t + 1], mo.project_out(o[t:t + 1].cpu(), wv), f"projected out[{t}]", 512)
+    assert bool((fused[:, :, 512:] == 7.0).all())
+    del q, o, fused, out
+    torch.cuda.empty_cache()
+
+
 def test_absorbed_chain_equals_non_absorbed_attention():
     """q_nope -> q_lift (tensor cores) -> latent causal attention over [c_kv | k_pe] -> O x v_b_proj^T
     equals, within the parity tolerance, per-head attention over the explicitly up-projected
@@ -266,3 +290,37 @@ def test_fp8_cache_row_set_is_exact():
             row = int(D.block_table[b, j // 64]) * 64 + j % 64
             want[row % 512] += 1.0 / n
         np.testing.assert_allclose(to_np(out[b, 0]), want.numpy(), atol=2.0 ** -8)
+
+
+@pytest.mark.full
+@pytest.mark.parametrize("fp8", [False, True], ids=["bf16", "e4m3"])
+def test_decode_step_variants_full_size_sampled_requests(fp8):
+    """The measured decode-step variants at full size (B = 64, H = 128, lens U[4096, 32768],
+    64-token pages): bf16 with two query tokens per request and per-head sinks, and the e4m3
+    cache with one.  The GPU runs every request; the oracle checks 12 sampled ones (each
+    request's rows depend only on its own keys)."""
+    from mla_attention_gb300 import mla_decode_ex, mla_decode_fp8
+    lens = gen.decode_lens(64, 4096, 32768, seed=4)
+    D = gen.decode_inputs(lens, H=128, seed=315, page_size=64)
+    g = torch.Generator().manual_seed(316)
+    S = 1 if fp8 else 2
+    q = gen.randn_bf16((64, S, 128, 576), g)
+    d = dev()
+    if fp8:
+        kv_scale = 0.05
+        c8 = (D.cache.float() / kv_scale).to(torch.float8_e4m3fn)
+        out, lse = mla_decode_fp8(q.to(d), c8.to(d), kv_scale, D.block_table.to(d), D.lens.to(d), D.scale)
+    else:
+        sinks = (torch.randn((128,), generator=g) * 2.0).float()
+        out, lse = mla_decode_ex(q.to(d), D.cache.to(d), D.block_table.to(d), D.lens.to(d), D.scale,
+                                 sinks=sinks.to(d))
+    torch.cuda.synchronize()
+    check_device_status()
+    reqs = gen.sample_rows(64, 12, seed=317, must=[0, 63, int(np.argmax(lens)), int(np.argmin(lens))])
+    bt, ln = D.block_table[reqs], D.lens[reqs]
+    if fp8:
+        ro, rl = mo.mla_decode_fp8(q[reqs], c8, kv_scale, bt, ln, D.scale)
+    else:
+        ro, rl = mo.mla_decode_ex(q[reqs], D.cache, bt, ln, D.scale, sinks=sinks)
+    assert_out_close(out[reqs], ro)
+    assert_lse_close(lse[reqs], rl)
