@@ -454,27 +454,32 @@ constexpr int kQProdPieces = 6;
 
 // FP8 decode, staged path: a 64-row box of the e4m3 cache (64 bytes a row) that TMA wrote into
 // the upper half of its own 8 KB f16 chunk is converted in place into 64 SW128 rows of 128 B.
-// Rows 0-31 land below the staged bytes; rows 32-63 overwrite them, so every lane loads its
-// staged row before any lane stores (the warp synchronises in between).  The caller fences the
-// async proxy and arrives once every lane has stored.
+// Rows 0-31 land below the staged bytes; rows 32-63 overwrite them, so each half's staged
+// bytes are all loaded before any lane stores that half (the warp synchronises in between).
+// Each staged load covers 512 contiguous bytes (lane l: row 8 i + l / 4, bytes 16 (l % 4) ..),
+// so it has no bank conflict; the two 16-byte f16 chunks a lane then stores (chunks 2 (l % 4)
+// and the next, swizzled by row) fall in distinct banks across each quarter-warp.  The caller
+// fences the async proxy and arrives once every lane has stored.
 __device__ __forceinline__ void convert_box_in_place(uint8_t* chunk) {
   const int lane = threadIdx.x & 31;
   const uint8_t* raw = chunk + 4096;
+  const int c0 = 2 * (lane & 3);  // first f16 chunk of the lane's 16 values
 #pragma unroll 1
   for (int half = 0; half < 2; ++half) {
-    const int r = 32 * half + lane;
     uint4 v[4];
 #pragma unroll
-    for (int w = 0; w < 4; ++w) v[w] = reinterpret_cast<const uint4*>(raw + r * 64)[w];
+    for (int i = 0; i < 4; ++i) v[i] = reinterpret_cast<const uint4*>(raw + half * 2048 + i * 512)[lane];
     __syncwarp();
-    uint8_t* line = chunk + r * 128;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {  // chunk c: values 8c .. 8c + 7
-      const uint4& q = v[c >> 1];
-      const uint32_t w0 = (c & 1) ? q.z : q.x, w1 = (c & 1) ? q.w : q.y;
-      *reinterpret_cast<uint4*>(line + ((c ^ (r & 7)) << 4)) =
-          make_uint4(e4m3x2_to_f16x2((uint16_t)(w0 & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(w0 >> 16)),
-                     e4m3x2_to_f16x2((uint16_t)(w1 & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(w1 >> 16)));
+    for (int i = 0; i < 4; ++i) {
+      const int r = 32 * half + 8 * i + (lane >> 2);
+      uint8_t* line = chunk + r * 128;
+      *reinterpret_cast<uint4*>(line + ((c0 ^ (r & 7)) << 4)) =
+          make_uint4(e4m3x2_to_f16x2((uint16_t)(v[i].x & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(v[i].x >> 16)),
+                     e4m3x2_to_f16x2((uint16_t)(v[i].y & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(v[i].y >> 16)));
+      *reinterpret_cast<uint4*>(line + (((c0 + 1) ^ (r & 7)) << 4)) =
+          make_uint4(e4m3x2_to_f16x2((uint16_t)(v[i].z & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(v[i].z >> 16)),
+                     e4m3x2_to_f16x2((uint16_t)(v[i].w & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(v[i].w >> 16)));
     }
   }
 }
