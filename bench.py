@@ -628,6 +628,14 @@ def run_profile_case(kind: str):
     elif kind == "decode":
         measure_decode(lib, dev, load_peaks()[0], steps=1, warmup=1)
         return
+    elif kind == "fp8_decode":
+        lens, cache, bt = _decode_config4(dev)
+        c8 = (cache.float() / 0.05).to(torch.float8_e4m3fn)
+        del cache
+        torch.cuda.empty_cache()  # the device then holds the 0.68 GB e4m3 cache and little else
+        q1 = gen.randn_bf16_device((len(lens), H, DK), 41, dev)
+        lens_d = torch.tensor(lens, dtype=torch.int32, device=dev)
+        fn = lambda: lib.mla_decode_fp8(q1, c8, 0.05, bt, lens_d, SCALE)  # noqa: E731
     elif kind == "sparse":
         S, S_kv, K = 512, 32768, 2048
         q_lift = gen.randn_bf16_device((1, S, H, 512), 51, dev)
@@ -661,7 +669,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the decode/sparse/split lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
-    ap.add_argument("--profile", choices=["prefill", "decode", "sparse", "split"], default=None,
+    ap.add_argument("--profile", choices=["prefill", "decode", "fp8_decode", "sparse", "split"], default=None,
                     help="run one small case of a kernel for ncu and exit (prints no JSON)")
     args = ap.parse_args()
     if args.profile:
