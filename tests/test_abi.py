@@ -69,6 +69,9 @@ def test_prefill_validation(L):
     assert _prefill(L) == 6
     # kv_valid beyond Tkv
     assert _prefill(L, kvv=9, ws=fake, wsb=256) == 1
+    # T * H of 2^31 or more: output rows are signed 32-bit tensor-map coordinates
+    assert _prefill(L, T=1 << 24, Tkv=0, kvv=0, q=fake, out=fake, lse=fake, ws=fake, wsb=1 << 40) == 1
+    assert b"T * H" in L.mla_last_error_string()
     # T = 0 is a no-op (no launch, no CUDA call)
     assert _prefill(L, T=0, ws=fake, wsb=256) == 0
     assert L.mla_last_error_string() == b""  # a successful call leaves no error text
@@ -94,6 +97,9 @@ def test_decode_and_merge_validation(L):
     assert L.mla_decode(fake, fake, 8, 48, fake, 4, fake, 2, 128, 0.1, 0, fake, None, fake, 1 << 30, None) == 1
     assert L.mla_decode(fake, fake, 8, 64, fake, 4, fake, 2, 256, 0.1, 0, fake, None, fake, 1 << 30, None) == 2
     assert L.mla_decode(fake, fake, 8, 64, fake, 4, fake, 2, 128, 0.1, 0, fake, None, fake, 16, None) == 6
+    # num_pages * page_size of 2^31 or more: cache rows are signed 32-bit tensor-map coordinates
+    assert L.mla_decode(fake, fake, 1 << 25, 64, fake, 4, fake, 2, 128, 0.1, 0, fake, None, fake, 1 << 30, None) == 1
+    assert b"num_pages * page_size" in L.mla_last_error_string()
     assert L.mla_merge_lse(fake, fake, fake, fake, fake, fake, 4, 2, 12, None) == 1
     assert L.mla_merge_lse(None, None, None, None, None, None, 0, 2, 16, None) == 0
 
