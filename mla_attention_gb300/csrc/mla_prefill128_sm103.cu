@@ -360,8 +360,10 @@ __device__ __forceinline__ void fill_half_fp8(uint8_t* dst, uint32_t box_stride,
     int rows[kBlk];
 #pragma unroll
     for (int i = 0; i < kBlk; ++i) {
-      const int u = lane + 32 * (batch * kBlk + i);  // 64 * kBlk units, 2 * kBlk per lane
-      const int r = u / kBlk, b = u - r * kBlk;
+      // 64 * kBlk units (box b, row r), 2 * kBlk per lane; consecutive lanes take consecutive rows
+      // of one box, so each quarter-warp's swizzled 16-byte stores fall in distinct banks
+      const int u = lane + 32 * (batch * kBlk + i);
+      const int r = u & 63, b = u >> 6;
       rows[i] = r;
       const int32_t pe = __shfl_sync(0xffffffffu, ids.pe, r >> 1);
       const int32_t po = __shfl_sync(0xffffffffu, ids.po, r >> 1);
@@ -379,7 +381,7 @@ __device__ __forceinline__ void fill_half_fp8(uint8_t* dst, uint32_t box_stride,
 #pragma unroll
     for (int i = 0; i < kBlk; ++i) {
       const int u = lane + 32 * (batch * kBlk + i);
-      const int r = rows[i], b = u - r * kBlk;
+      const int r = rows[i], b = u >> 6;
       uint8_t* line = dst + b * box_stride + r * 128;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {  // chunk c: values 8c .. 8c + 7 = bytes 8c .. 8c + 7 of the piece
